@@ -1,0 +1,416 @@
+"""Benchmark: paged decode attention + paged cache write on GB300.
+
+One step = one decode step of the 1.1B edge model shape over all 24 layers:
+for every layer, write each sequence's new K/V row into its slot
+(pa_cache_write) and run paged decode attention over the layer's cache
+(pa_decode).  64 sequences, context lengths uniform in [16, 2048], 12 query /
+2 kv heads, head dim 128, fp16, 16-token blocks, a randomly permuted pool of
+1.2x the blocks needed, 24 distinct layer caches (about 1.6 GB, far above the
+129 MB L2, so every step reads its K/V from HBM).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  ``value`` is achieved HBM GB/s over the
+algorithmic bytes (K/V rows read, q read, out written, table and length reads,
+the cache write's rows read and written), whole job.  ``--impl reference``
+times the CPU oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s"
+SPEC_PEAK_GBS = 8000.0
+
+
+# ------------------------------------------------------------------------------------------
+# byte ledger of one step
+# ------------------------------------------------------------------------------------------
+
+def decode_bytes(wl) -> int:
+    """Algorithmic bytes of one pa_decode call: every context row of K and V, q read,
+    out written, the table entries and lengths read.  Split partials are not counted."""
+    e = 2
+    D = wl.head_dim
+    lens = wl.context_lens.to(torch.int64)
+    kv = int(lens.sum()) * wl.num_kv_heads * D * e * 2
+    qo = 2 * wl.num_seqs * wl.num_q_heads * D * e
+    table = 4 * int(((lens + wl.block_size - 1) // wl.block_size).sum())
+    return kv + qo + table + 4 * wl.num_seqs
+
+
+def cache_write_bytes(wl) -> int:
+    rows = wl.num_seqs * wl.num_kv_heads * wl.head_dim * 2 * 2   # K and V rows, 16-bit
+    return 2 * rows + 8 * wl.num_seqs                             # read + written, slots read
+
+
+# ------------------------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+class Step:
+    """All device buffers of one bench step plus the captured CUDA graph."""
+
+    def __init__(self, wl, device):
+        import paged_kv_cache_08_gb300 as pa
+        self.pa = pa
+        self.wl = wl
+        self.dev = device
+        L = wl.layers
+        self.bt = wl.block_tables.to(device)
+        self.lens = wl.context_lens.to(device)
+        slots = pa.build_slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)
+        self.slots = torch.from_numpy(slots).to(device)
+        self.out = [torch.empty_like(wl.q[i]) for i in range(L)]
+        S, Hq, D = wl.q[0].shape
+        ws = pa.decode_workspace_size(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.tps = pa.plan_tokens_per_split(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
+        self.graph = None
+        self.ev = None
+
+    def launch_layer(self, i, ev_pair=None):
+        wl, pa = self.wl, self.pa
+        pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
+        if ev_pair is not None:
+            ev_pair[0].record()
+        pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
+                  out=self.out[i], workspace=self.ws)
+        if ev_pair is not None:
+            ev_pair[1].record()
+
+    def eager(self):
+        for i in range(self.wl.layers):
+            self.launch_layer(i)
+
+    def capture(self):
+        self.eager()                       # warm every kernel / attribute outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.eager()
+        self.graph = g
+
+    def decode_launch_ms(self, rounds: int = 3):
+        """Duration of every pa_decode call of the step, from CUDA events recorded on the
+        launching stream around it.  The step is enqueued behind a spin kernel so that the
+        GPU runs it back to back and host launch gaps stay outside the events."""
+        times = []
+        for _ in range(rounds):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(self.wl.layers)]
+            torch.cuda._sleep(50_000_000)
+            for i in range(self.wl.layers):
+                self.launch_layer(i, evs[i])
+            torch.cuda.synchronize()
+            times += [a.elapsed_time(b) for a, b in evs]
+        return times
+
+    def replay(self):
+        self.graph.replay()
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch.distributed as dist
+    world, rank, local = _dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workloads.config(2, device=dev, layers=args.layers)
+    st = Step(wl, dev)
+    d_bytes = decode_bytes(wl)
+    c_bytes = cache_write_bytes(wl)
+    step_bytes = wl.layers * (d_bytes + c_bytes)
+    kv_tokens = wl.layers * wl.total_context_tokens()
+
+    st.capture()
+    launches_per_step = wl.layers * (1 + 1 + (1 if st.tps < wl.max_blocks_per_seq * wl.block_size else 0))
+
+    for _ in range(args.warmup):
+        st.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        start.record()
+        for _ in range(args.steps):
+            st.replay()
+        stop.record()
+        torch.cuda.synchronize()
+        decode_ms = st.decode_launch_ms()
+    total_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # per-launch decode time: events around every pa_decode call of the step
+    peak, peak_kind = measured_peak_gbs()
+    roof = None
+    if decode_ms:
+        avg_ms = statistics.mean(decode_ms)
+        achieved = d_bytes / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "pa_decode (split pass + combine)",
+                "avg_launch_us": round(avg_ms * 1e3, 2), "peak_source": f"{peak_kind} copy bandwidth",
+                "frac_of_8TBs_spec": round(achieved / SPEC_PEAK_GBS, 4)}
+
+    # e2e through the public API with host buffers: H2D of the step's inputs, D2H of its outputs
+    e2e = run_e2e(st, wl, args, step_bytes) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": wl.name, "seqs": wl.num_seqs, "layers": wl.layers,
+                       "context": "uniform [16, 2048]", "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+                       "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_blocks": wl.num_blocks,
+                       "tokens_per_split": st.tps,
+                       "l2": "inputs larger than L2: 24 distinct layer caches (%.2f GB) read once per step"
+                             % (2 * sum(t.numel() * 2 for t in wl.k_cache) / 1e9),
+                       "parallelism": f"replicas x{world}", "cuda_graph": True},
+            "pct_of_measured_peak": round(100 * value / world / peak, 2),
+            "pct_of_8TBs_spec": round(100 * value / world / SPEC_PEAK_GBS, 2),
+            "kv_tokens_per_s": round(world * kv_tokens / (ms_per_step * 1e-3), 1),
+            "bytes_per_step": step_bytes,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(st, wl, args, step_bytes):
+    """Same step through the public API with inputs in pinned host memory: every step
+    copies q, the new K/V rows, the tables, lengths and slots to the device, runs the
+    24 layers and copies the outputs back."""
+    dev = st.dev
+    host_in = {
+        "q": [t.cpu().pin_memory() for t in wl.q],
+        "k": [t.cpu().pin_memory() for t in wl.k_new],
+        "v": [t.cpu().pin_memory() for t in wl.v_new],
+        "bt": wl.block_tables.pin_memory(), "lens": wl.context_lens.pin_memory(),
+        "slots": st.slots.cpu().pin_memory(),
+    }
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st.out]
+    h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host_in[k])
+    h2d += sum(host_in[k].numel() * host_in[k].element_size() for k in ("bt", "lens", "slots"))
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for i in range(wl.layers):
+            wl.q[i].copy_(host_in["q"][i], non_blocking=True)
+            wl.k_new[i].copy_(host_in["k"][i], non_blocking=True)
+            wl.v_new[i].copy_(host_in["v"][i], non_blocking=True)
+        st.bt.copy_(host_in["bt"], non_blocking=True)
+        st.lens.copy_(host_in["lens"], non_blocking=True)
+        st.slots.copy_(host_in["slots"], non_blocking=True)
+        st.replay()
+        for i in range(wl.layers):
+            host_out[i].copy_(st.out[i], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ------------------------------------------------------------------------------------------
+
+def _oracle_layer(o, wl, i):
+    import oracle as oracle_pkg
+    kc = oracle_pkg.as_u16(wl.k_cache[i]).copy()
+    vc = oracle_pkg.as_u16(wl.v_cache[i]).copy()
+    t0 = time.perf_counter()
+    slots = o.slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)
+    o.cache_write(wl.k_new[i], wl.v_new[i], slots, kc, vc)
+    o.decode(wl.q[i], kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.num_kv_heads, wl.dtype == "bf16")
+    return time.perf_counter() - t0
+
+
+def _host_layer(wl, i):
+    """A host copy of layer i (structure shared)."""
+    sub = workloads.Workload(**{k: getattr(wl, k) for k in (
+        "name", "dtype", "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "block_size", "num_blocks",
+        "max_blocks_per_seq", "context_lens", "block_tables", "scale", "seed", "shared_prefix_blocks")})
+    for key in ("q", "k_cache", "v_cache", "k_new", "v_new"):
+        getattr(sub, key).append(getattr(wl, key)[i].cpu())
+    return sub
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle, as it stands, on the host cores: whole layers of the same workload until
+    about ``budget_s`` seconds of oracle time; GB/s over the same algorithmic bytes."""
+    import oracle as oracle_pkg
+    o = oracle_pkg.get()
+    spent, layers = 0.0, 0
+    for i in range(wl.layers):
+        sub = _host_layer(wl, i)
+        spent += _oracle_layer(o, sub, 0)
+        layers += 1
+        if spent >= budget_s:
+            break
+    byts = layers * (decode_bytes(wl) + cache_write_bytes(wl))
+    return {"value": round(byts / spent / 1e9, 4), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{layers} of {wl.layers} layers of the same workload (cache write + decode, fp64)",
+            "seconds": round(spent, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import oracle as oracle_pkg
+    o = oracle_pkg.get()
+    wl = workloads.config(2, layers=1)                     # one layer per step: a bounded sample
+    step_bytes = decode_bytes(wl) + cache_write_bytes(wl)
+    for _ in range(args.warmup):
+        _oracle_layer(o, wl, 0)
+    times = [_oracle_layer(o, wl, 0) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = step_bytes / (ms * 1e-3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name + " (one layer of 24 per step)", "seqs": wl.num_seqs,
+                       "block_size": wl.block_size, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                             "sample": "one layer of the 24-layer step per timed step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

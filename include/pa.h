@@ -1,0 +1,211 @@
+/*
+ * pa.h -- C ABI of libpa: paged KV-cache write and paged decode attention on
+ * one GB300 GPU (sm_103a), plus the untimed host block pool that builds the
+ * block tables and slot mappings those two calls consume.
+ *
+ * Sources for what each call computes (page title, then section):
+ *   [P1] "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块"
+ *        -- "注意力寻址：非连续物理块的间接寻址内核" (token t lives in logical block
+ *        t / B at offset t % B; physical block = block_table[t / B]);
+ *        "嵌入式轻量 Block 分配器设计" (free bitmap, lowest free block first,
+ *        -1 when the pool is exhausted); "共享前缀块（Prefix Caching）" (shared,
+ *        reference-counted prefix blocks).
+ *   [P4] "显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结"
+ *        -- §三 sequence diagram (append a token: write at the next offset of the last
+ *        block, or allocate and append a block when it is full; free all blocks at the end);
+ *        §三.1 (two pool tensors, one fixed stride per physical block);
+ *        §四 (copy-on-write of shared blocks, reference counts);
+ *        §五.1 (decode kernel: per sequence and head, loop over logical blocks through
+ *        block_tables [num_seqs, max_blocks_per_seq] and context_lens [num_seqs],
+ *        q.k, softmax with running rescale, weight V, normalise at the end).
+ *
+ * Conventions shared by every call:
+ *   - Device pointers are owned by the caller; the library never frees them, never
+ *     keeps them after the call returns and never allocates device memory for the
+ *     caller's data.
+ *   - Calls that take a `stream` are asynchronous on that stream (a cudaStream_t;
+ *     NULL is the legacy default stream).  Their return value reports host-side
+ *     argument checks and launch errors only.  Faults the kernels detect in the data
+ *     (a block id outside the pool, a slot outside the pool, a context longer than
+ *     the table) skip the offending access and set a bit in a per-device status word
+ *     read by pa_read_device_status; no kernel traps.
+ *   - Data layouts (row-major, element type pa_dtype, 16-byte aligned base pointers):
+ *       q, out           [num_seqs][num_q_heads][head_dim]
+ *       k, v (new rows)  [num_tokens][num_kv_heads][head_dim]
+ *       k_cache, v_cache [num_blocks][num_kv_heads][block_size][head_dim]
+ *                        (one (block, kv-head) tile is block_size*head_dim contiguous
+ *                        elements)
+ *       block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *       context_lens     int32 [num_seqs]; the length counts the newest token
+ *       slot_mapping     int64 [num_tokens]; slot = physical_block * block_size + offset
+ *   - Query head h attends with kv head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,     /* a null pointer, a negative size, a misaligned pointer */
+    PA_ERR_UNSUPPORTED = -2,     /* a valid but unimplemented shape (head_dim, block size) */
+    PA_ERR_CUDA = -3,            /* the CUDA runtime reported an error */
+    PA_ERR_POOL_EXHAUSTED = -4,  /* the host pool has no free block */
+    PA_ERR_DEVICE_TIMEOUT = -5,  /* reserved for waits that gave up (see status bits) */
+    PA_ERR_BOUNDS = -6,          /* a host-side index outside its range */
+    PA_ERR_WORKSPACE = -7        /* workspace missing or smaller than required */
+} pa_status;
+
+/* Bits of the per-device status word (pa_read_device_status). */
+#define PA_DEV_BAD_BLOCK_ID 0x1u /* a block-table entry outside [0, num_blocks) was skipped */
+#define PA_DEV_BAD_CONTEXT  0x2u /* a context length < 0 or > max_blocks_per_seq*block_size was clamped */
+#define PA_DEV_BAD_SLOT     0x4u /* a slot >= num_blocks*block_size was skipped */
+#define PA_DEV_TIMEOUT      0x8u /* a copy pipeline wait gave up after about one second */
+
+/* Math path of pa_decode_ex. */
+typedef enum {
+    PA_MATH_AUTO = 0,            /* the library's choice for the shape */
+    PA_MATH_FMA = 1,             /* CUDA-core fp32 FMAs with warp-shuffle reductions */
+    PA_MATH_MMA = 2              /* tensor-core (mma.sync m16n8k16) QK^T and PV products */
+} pa_math;
+
+typedef struct {
+    int tokens_per_split;        /* 0 = library's choice; else a multiple of max(block_size, 64) */
+    int math;                    /* a pa_math value */
+} pa_decode_options;
+
+/* ------------------------------------------------------------------------------------
+ * pa_cache_write  [P4 §三 sequence diagram; P1 address formula]
+ * For every token i with slot_mapping[i] >= 0 and every kv head h, copy the rows
+ *   k[i][h][:] -> k_cache[slot / block_size][h][slot % block_size][:]
+ *   v[i][h][:] -> v_cache[slot / block_size][h][slot % block_size][:]
+ * bit for bit.  A negative slot skips the token (padding).  A slot at or beyond
+ * num_blocks*block_size is skipped and sets PA_DEV_BAD_SLOT.
+ * head_dim must be a positive multiple of 8; all pointers 16-byte aligned.
+ * Returns PA_OK, PA_ERR_INVALID_ARG or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------------------- */
+int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                   void* k_cache, void* v_cache,
+                   int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * pa_decode  [P4 §五.1; P1 address formula]
+ * For every sequence s and query head h (kv head hk = h / (num_q_heads/num_kv_heads)),
+ * with L = context_lens[s] and the cached rows t = 0..L-1 found at
+ *   (block_tables[s][t / block_size], t % block_size):
+ *   out[s][h][:] = sum_t softmax_t(scale * q[s][h] . K[t]) * V[t][:]
+ * accumulated in fp32 and rounded to nearest into the output dtype.  L == 0 gives
+ * a zero row.  Supported: head_dim 128, block_size 16/32/64/128, num_q_heads a
+ * multiple of num_kv_heads.
+ *
+ * Work is split over (sequence, kv head, token range); all query heads of a GQA
+ * group share each K/V tile.  Partial results of split sequences go to
+ * `workspace` (device memory of at least pa_decode_workspace_size(...) bytes,
+ * owned by the caller, contents need no initialisation; NULL is allowed when
+ * that size is 0).  Two kernels run on `stream`: the split pass and, when any
+ * sequence can be split, a combine pass.  Calls that share a workspace must not
+ * overlap on the GPU.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------------------- */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens,
+              float scale, int num_kv_heads,
+              int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+              int max_blocks_per_seq, int dtype,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace pa_decode needs for this shape on the current device. */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq);
+
+/* pa_decode with explicit options (opts may be NULL = defaults). */
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens,
+                 float scale, int num_kv_heads,
+                 int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                 int max_blocks_per_seq, int dtype,
+                 void* workspace, size_t workspace_bytes, void* stream,
+                 const pa_decode_options* opts);
+
+size_t pa_decode_workspace_size_ex(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq,
+                                   const pa_decode_options* opts);
+
+/* The split length (tokens per split) pa_decode_ex would use; < 0 on invalid input. */
+int pa_decode_plan_tokens_per_split(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_blocks_per_seq,
+                                    const pa_decode_options* opts);
+
+/* Human-readable text of a pa_status value (static storage). */
+const char* pa_status_string(int status);
+
+/* Copy the current device's status word into *bits after all work on `stream`
+ * has finished (this call synchronises the stream); clear it when `clear` != 0. */
+int pa_read_device_status(void* stream, int clear, uint32_t* bits);
+
+/* Number of kernels the library launched in this process (all devices). */
+uint64_t pa_kernel_launch_count(void);
+
+/* ------------------------------------------------------------------------------------
+ * Host block pool  [P1 allocator section; P4 §三 lifecycle and §四 copy-on-write]
+ * Not thread-safe; one owner.  Block ids are 0..num_blocks-1.
+ * ---------------------------------------------------------------------------------- */
+typedef struct pa_pool pa_pool;
+
+/* A pool of num_blocks free blocks, or NULL if num_blocks <= 0 or memory is short. */
+pa_pool* pa_pool_create(int num_blocks);
+void pa_pool_destroy(pa_pool* pool);
+
+/* The lowest-numbered free block, now with reference count 1, or PA_ERR_POOL_EXHAUSTED. */
+int pa_pool_alloc(pa_pool* pool);
+/* Add one reference to an allocated block; returns the new count or PA_ERR_BOUNDS. */
+int pa_pool_incref(pa_pool* pool, int block_id);
+/* Drop one reference; the block returns to the free set at 0.  Returns the new
+ * count, or PA_ERR_BOUNDS for an id that is out of range or already free. */
+int pa_pool_decref(pa_pool* pool, int block_id);
+int pa_pool_refcount(const pa_pool* pool, int block_id);
+int pa_pool_num_free(const pa_pool* pool);
+int pa_pool_num_blocks(const pa_pool* pool);
+
+/* Give a sequence of context_len tokens its ceil(context_len / block_size) blocks:
+ * the first `shared_blocks` entries are copied from `shared_row` (each gains a
+ * reference), the rest are allocated.  table_row has max_blocks entries; unused
+ * ones are set to -1.  On PA_ERR_POOL_EXHAUSTED nothing stays allocated. */
+int pa_pool_assign(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                   int block_size, const int32_t* shared_row, int shared_blocks);
+
+/* Append one token to a sequence that holds context_len tokens (P4 §三): if its last
+ * block is full (or it has none) allocate a block and append it to the table; if the
+ * last block is shared (reference count > 1) and not full, copy-on-write: allocate a
+ * new block, drop one reference of the old one and point the table at the new one,
+ * reporting (*cow_src, *cow_dst) so that the caller copies the block's rows on the
+ * GPU (both -1 when no copy is needed).  *slot receives the new token's slot.
+ * Returns PA_OK, PA_ERR_POOL_EXHAUSTED or PA_ERR_BOUNDS (table full). */
+int pa_pool_append_token(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                         int block_size, int64_t* slot, int32_t* cow_src, int32_t* cow_dst);
+
+/* Drop one reference of each of the ceil(context_len / block_size) blocks of a
+ * sequence (P4 §三, end of request) and set the entries to -1. */
+int pa_pool_release(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                    int block_size);
+
+/* slots[s] = slot of token context_lens[s] - 1 (the newest one), or -1 when the
+ * context is empty; host arrays.  Returns PA_OK or PA_ERR_BOUNDS if a length
+ * exceeds max_blocks*block_size or a needed table entry is negative. */
+int pa_build_slot_mapping(const int32_t* block_tables, int max_blocks,
+                          const int32_t* context_lens, int num_seqs, int block_size,
+                          int64_t* slots);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,239 @@
+"""Paged KV-cache write and paged decode attention for GB300 (sm_103a).
+
+Thin Python layer over the C ABI of ``libpa.so`` (include/pa.h).  Every step
+of the path runs in the library's CUDA kernels; this module only checks tensor
+types and passes pointers, sizes and the current CUDA stream.  PyTorch serves
+as the device-memory and stream provider.
+
+    cache_write(k, v, slot_mapping, k_cache, v_cache)
+    decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads) -> out
+    BlockPool(num_blocks)                       # host block pool (untimed)
+    build_slot_mapping(block_tables, context_lens, block_size)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _native
+from ._native import PAError, DecodeOptions, MATH
+
+__all__ = ["cache_write", "decode", "decode_workspace_size", "plan_tokens_per_split", "BlockPool",
+           "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
+
+_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def lib() -> ctypes.CDLL:
+    return _native.load()
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _opts(tokens_per_split: int, math: str) -> DecodeOptions:
+    if math not in MATH:
+        raise ValueError(f"math must be one of {sorted(MATH)}")
+    return DecodeOptions(int(tokens_per_split), MATH[math])
+
+
+def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """k, v: [T, Hkv, D]; slot_mapping: int64 [T] (negative = skip); caches [NB, Hkv, B, D]."""
+    for n, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    if k.dtype not in _DTYPE:
+        raise TypeError("k must be float16 or bfloat16")
+    T, H, D = k.shape
+    NB, H2, B, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or H2 != H or D2 != D or slot_mapping.numel() != T:
+        raise ValueError("shape mismatch")
+    rc = lib().pa_cache_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+                              v_cache.data_ptr(), T, H, D, B, NB, _DTYPE[k.dtype], _stream_ptr(stream))
+    _native.check("pa_cache_write", rc)
+
+
+def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                          max_blocks_per_seq: int, tokens_per_split: int = 0, math: str = "auto") -> int:
+    o = _opts(tokens_per_split, math)
+    return int(lib().pa_decode_workspace_size_ex(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                                 max_blocks_per_seq, ctypes.byref(o)))
+
+
+def plan_tokens_per_split(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                          max_blocks_per_seq: int, tokens_per_split: int = 0, math: str = "auto") -> int:
+    o = _opts(tokens_per_split, math)
+    return _native.check("pa_decode_plan_tokens_per_split",
+                         lib().pa_decode_plan_tokens_per_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                               block_size, max_blocks_per_seq, ctypes.byref(o)))
+
+
+_workspaces: dict = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: float, num_kv_heads: int, out: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None, tokens_per_split: int = 0, math: str = "auto",
+           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Paged decode attention.  q: [S, Hq, D]; caches [NB, Hkv, B, D]; block_tables int32
+    [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype."""
+    _need_cuda("q", q)
+    if q.dtype not in _DTYPE:
+        raise TypeError("q must be float16 or bfloat16")
+    _need_cuda("k_cache", k_cache, q.dtype)
+    _need_cuda("v_cache", v_cache, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if Hkv != num_kv_heads or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape does not match q / num_kv_heads")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("block_tables / context_lens do not match q")
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    o = _opts(tokens_per_split, math)
+    need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_decode_ex(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                            block_tables.data_ptr(), context_lens.data_ptr(), float(scale), int(num_kv_heads),
+                            S, Hq, D, B, NB, max_blocks, _DTYPE[q.dtype], ws_ptr, ws_bytes, _stream_ptr(stream),
+                            ctypes.byref(o))
+    _native.check("pa_decode", rc)
+    return out
+
+
+def read_device_status(clear: bool = True, stream: Optional[torch.cuda.Stream] = None) -> int:
+    bits = ctypes.c_uint32(0)
+    _native.check("pa_read_device_status",
+                  lib().pa_read_device_status(_stream_ptr(stream), int(clear), ctypes.byref(bits)))
+    return int(bits.value)
+
+
+def kernel_launch_count() -> int:
+    return int(lib().pa_kernel_launch_count())
+
+
+# ------------------------------------------------------------------------------------------
+# host block pool
+# ------------------------------------------------------------------------------------------
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(_native.c_i32p)
+
+
+class BlockPool:
+    """Free-bitmap pool with reference counts (host, untimed).  See include/pa.h."""
+
+    def __init__(self, num_blocks: int):
+        self._lib = lib()
+        self._h = self._lib.pa_pool_create(int(num_blocks))
+        if not self._h:
+            raise ValueError("pa_pool_create failed")
+
+    def close(self):
+        if self._h:
+            self._lib.pa_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self) -> int:
+        return _native.check("pa_pool_alloc", self._lib.pa_pool_alloc(self._h))
+
+    def incref(self, block_id: int) -> int:
+        return _native.check("pa_pool_incref", self._lib.pa_pool_incref(self._h, int(block_id)))
+
+    def decref(self, block_id: int) -> int:
+        return _native.check("pa_pool_decref", self._lib.pa_pool_decref(self._h, int(block_id)))
+
+    def refcount(self, block_id: int) -> int:
+        return _native.check("pa_pool_refcount", self._lib.pa_pool_refcount(self._h, int(block_id)))
+
+    @property
+    def num_free(self) -> int:
+        return self._lib.pa_pool_num_free(self._h)
+
+    @property
+    def num_blocks(self) -> int:
+        return self._lib.pa_pool_num_blocks(self._h)
+
+    def assign(self, table_row: np.ndarray, context_len: int, block_size: int,
+               shared_row: Optional[np.ndarray] = None, shared_blocks: int = 0) -> None:
+        assert table_row.dtype == np.int32 and table_row.flags.c_contiguous
+        sr = None
+        if shared_blocks:
+            shared_row = np.ascontiguousarray(shared_row, dtype=np.int32)
+            sr = _i32p(shared_row)
+        _native.check("pa_pool_assign", self._lib.pa_pool_assign(self._h, _i32p(table_row), table_row.size,
+                                                                 int(context_len), int(block_size), sr,
+                                                                 int(shared_blocks)))
+
+    def append_token(self, table_row: np.ndarray, context_len: int, block_size: int):
+        """Returns (slot, cow_src, cow_dst) for a token appended after context_len tokens."""
+        assert table_row.dtype == np.int32 and table_row.flags.c_contiguous
+        slot = ctypes.c_int64(-1)
+        src = ctypes.c_int32(-1)
+        dst = ctypes.c_int32(-1)
+        _native.check("pa_pool_append_token",
+                      self._lib.pa_pool_append_token(self._h, _i32p(table_row), table_row.size, int(context_len),
+                                                     int(block_size), ctypes.byref(slot), ctypes.byref(src),
+                                                     ctypes.byref(dst)))
+        return int(slot.value), int(src.value), int(dst.value)
+
+    def release(self, table_row: np.ndarray, context_len: int, block_size: int) -> None:
+        assert table_row.dtype == np.int32 and table_row.flags.c_contiguous
+        _native.check("pa_pool_release", self._lib.pa_pool_release(self._h, _i32p(table_row), table_row.size,
+                                                                   int(context_len), int(block_size)))
+
+
+def build_slot_mapping(block_tables, context_lens, block_size: int) -> np.ndarray:
+    """Host: slot of each sequence's newest token (context_lens[s] - 1), -1 for empty contexts."""
+    bt = np.ascontiguousarray(np.asarray(block_tables.cpu() if isinstance(block_tables, torch.Tensor)
+                                         else block_tables, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(context_lens.cpu() if isinstance(context_lens, torch.Tensor)
+                                           else context_lens, dtype=np.int32))
+    S = lens.size
+    out = np.empty(S, dtype=np.int64)
+    _native.check("pa_build_slot_mapping",
+                  lib().pa_build_slot_mapping(_i32p(bt), bt.shape[1] if bt.ndim == 2 else 0, _i32p(lens), S,
+                                              int(block_size), out.ctypes.data_as(_native.c_i64p)))
+    return out

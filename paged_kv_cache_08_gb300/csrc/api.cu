@@ -1,0 +1,271 @@
+// libpa C ABI: argument checks, split planning, kernel dispatch, device status word.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+// Per-device status word (static device memory, no allocation).  Kernels atomicOr
+// PA_DEV_* bits into it when they skip an out-of-range access or give up a wait.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 152;  // no device visible: size plans for a GB300
+    int n = g_sm_count[dev].load();
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    g_sm_count[dev].store(n);
+    return n;
+}
+
+bool supported_block_size(int b) { return b == 16 || b == 32 || b == 64 || b == 128; }
+
+// Split plan.  Sequences are split into runs of `tps` tokens (a multiple of the stage and of
+// the block) so that about four CTAs per SM are available even when the batch is small; the
+// floor of 256 tokens keeps the fp32 partials a few percent of the K/V bytes they summarise.
+int plan_tps(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq,
+             const pa_decode_options* opts) {
+    const int unit = block_size > kStageTokens ? block_size : kStageTokens;
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    const long long cap_units = ((cap + unit - 1) / unit) * unit;
+    if (opts && opts->tokens_per_split > 0) {
+        if (opts->tokens_per_split % unit) return PA_ERR_INVALID_ARG;
+        return opts->tokens_per_split;
+    }
+    if (cap_units == 0) return unit;
+    const long long pairs = (long long)num_seqs * num_kv_heads;
+    const long long target = 4LL * sm_count();
+    long long splits = pairs > 0 ? (target + pairs - 1) / pairs : 1;
+    if (splits < 1) splits = 1;
+    long long tps = (cap + splits - 1) / splits;
+    if (tps < 256) tps = 256;
+    tps = ((tps + unit - 1) / unit) * unit;
+    if (tps > cap_units) tps = cap_units;
+    return (int)tps;
+}
+
+int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int max_blocks_per_seq) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim || !supported_block_size(block_size)) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * block_size > (1LL << 30)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+size_t workspace_bytes_for(int num_seqs, int num_q_heads, int max_splits) {
+    if (max_splits <= 1) return 0;
+    const size_t n = (size_t)num_seqs * num_q_heads * max_splits;
+    return n * (kHeadDim * sizeof(float) + sizeof(float2));
+}
+
+int max_splits_for(int block_size, int max_blocks_per_seq, int tps) {
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    long long n = (cap + tps - 1) / tps;
+    return n < 1 ? 1 : (int)n;
+}
+
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n); }
+
+unsigned int* device_status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    unsigned int* p = g_status_ptr[dev].load();
+    if (p) return p;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    p = static_cast<unsigned int*>(addr);
+    g_status_ptr[dev].store(p);
+    return p;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+        case PA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case PA_ERR_BOUNDS: return "index out of bounds";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+uint64_t pa_kernel_launch_count(void) { return g_launches.load(); }
+
+int pa_read_device_status(void* stream, int clear, uint32_t* bits) {
+    if (!bits) return PA_ERR_INVALID_ARG;
+    unsigned int* p = device_status_ptr();
+    if (!p) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    if (cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    *bits = v;
+    return PA_OK;
+}
+
+int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                   int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
+                   void* stream) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 || block_size <= 0 ||
+        num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    CacheWriteArgs a;
+    a.k = static_cast<const uint4*>(k);
+    a.v = static_cast<const uint4*>(v);
+    a.slots = slot_mapping;
+    a.k_cache = static_cast<uint4*>(k_cache);
+    a.v_cache = static_cast<uint4*>(v_cache);
+    a.status = device_status_ptr();
+    a.vecs_per_row = head_dim / 8;
+    a.total_vecs = (long long)num_tokens * num_kv_heads * a.vecs_per_row;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.pool_slots = (long long)num_blocks * block_size;
+    if ((a.total_vecs + 255) / 256 > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    cudaError_t e = launch_cache_write(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode_plan_tokens_per_split(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int max_blocks_per_seq, const pa_decode_options* opts) {
+    int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    return plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
+}
+
+size_t pa_decode_workspace_size_ex(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, const pa_decode_options* opts) {
+    int tps = pa_decode_plan_tokens_per_split(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                              max_blocks_per_seq, opts);
+    if (tps <= 0) return 0;
+    return workspace_bytes_for(num_seqs, num_q_heads, max_splits_for(block_size, max_blocks_per_seq, tps));
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq) {
+    return pa_decode_workspace_size_ex(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_blocks_per_seq, nullptr);
+}
+
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 const int32_t* context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                 int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
+                 size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    if (num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (opts && (opts->math < PA_MATH_AUTO || opts->math > PA_MATH_MMA)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (num_blocks > 0 && (!k_cache || !v_cache)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned4(block_tables) || !aligned4(context_lens))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    int math = opts ? opts->math : PA_MATH_AUTO;
+    if (math == PA_MATH_AUTO) math = (mma_supports_group(group) && num_blocks > 0) ? PA_MATH_MMA : PA_MATH_FMA;
+    if (math == PA_MATH_MMA && (!mma_supports_group(group) || num_blocks == 0)) return PA_ERR_UNSUPPORTED;
+    if (math == PA_MATH_FMA && !fma_supports_group(group)) return PA_ERR_UNSUPPORTED;
+    const int tps = plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
+    if (tps <= 0) return PA_ERR_INVALID_ARG;
+    const int max_splits = max_splits_for(block_size, max_blocks_per_seq, tps);
+    const size_t need = workspace_bytes_for(num_seqs, num_q_heads, max_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    const size_t n_part = (size_t)num_seqs * num_q_heads * max_splits;
+    a.part_o = need ? static_cast<float*>(workspace) : nullptr;
+    a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + n_part * kHeadDim * sizeof(float))
+                     : nullptr;
+    a.status = device_status_ptr();
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.tokens_per_split = tps;
+    a.max_splits = max_splits;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = math == PA_MATH_MMA ? launch_decode_split_mma(a, dtype, st)
+                                        : launch_decode_split_fma(a, dtype, group, st);
+    if (e == cudaSuccess && max_splits > 1) e = launch_decode_combine(a, dtype, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+              int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    return pa_decode_ex(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
+                        num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+// Internal declarations shared by the libpa translation units (device side).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kHeadDim = 128;           // the only head size the pages use
+constexpr int kStageTokens = 64;        // tokens of K (and of V) staged per pipeline step
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // give a copy wait ~1 s
+
+// ---------------------------------------------------------------------------------------
+// Arguments
+// ---------------------------------------------------------------------------------------
+struct CacheWriteArgs {
+    const uint4* k;           // [T][Hkv][D] as 16-byte vectors
+    const uint4* v;
+    const int64_t* slots;     // [T]
+    uint4* k_cache;           // [NB][Hkv][B][D]
+    uint4* v_cache;
+    unsigned int* status;
+    long long total_vecs;     // T * Hkv * (D / 8)
+    int num_kv_heads;
+    int vecs_per_row;         // D / 8
+    int block_size;
+    long long pool_slots;     // NB * B
+};
+
+struct DecodeArgs {
+    void* out;                // [S][Hq][D]
+    const void* q;            // [S][Hq][D]
+    const void* k_cache;      // [NB][Hkv][B][D]
+    const void* v_cache;
+    const int32_t* block_tables;  // [S][max_blocks]
+    const int32_t* context_lens;  // [S]
+    float* part_o;            // [S][Hq][max_splits][D]       (unnormalised partial outputs)
+    float2* part_ml;          // [S][Hq][max_splits] (m, l)   (running max in log2 units, sum)
+    unsigned int* status;
+    float scale_log2;         // scale * log2(e)
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int num_blocks;
+    int max_blocks_per_seq;
+    int tokens_per_split;     // multiple of max(block_size, kStageTokens)
+    int max_splits;
+};
+
+// ---------------------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__half> {
+    static __device__ __forceinline__ float2 to_float2(uint32_t u) {
+        __half2 h = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(h);
+    }
+    static __device__ __forceinline__ float to_float(uint16_t u) {
+        return __half2float(__ushort_as_half(u));
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 to_float2(uint32_t u) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+        return __bfloat1622float2(h);
+    }
+    static __device__ __forceinline__ float to_float(uint16_t u) {
+        return __bfloat162float(__ushort_as_bfloat16(u));
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    float2 a = Elem<T>::to_float2(u.x), b = Elem<T>::to_float2(u.y);
+    float2 c = Elem<T>::to_float2(u.z), d = Elem<T>::to_float2(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// ---------------------------------------------------------------------------------------
+// Shared-memory barriers and bulk (TMA) copies, inline PTX
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this CTA's earlier generic-proxy shared-memory accesses before later async-proxy ones
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar`; false if it has not completed after ~kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// One contiguous global -> shared bulk copy completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's results / let the next grid start.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void flag_status(unsigned int* status, unsigned int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// ---------------------------------------------------------------------------------------
+// Host-side launch helpers (defined in the .cu files)
+// ---------------------------------------------------------------------------------------
+cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
+
+// FMA (CUDA-core) split pass for group size G and element type; returns cudaErrorInvalidValue
+// when G has no instantiation.
+cudaError_t launch_decode_split_fma(const DecodeArgs& a, int dtype, int group, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t stream);
+bool fma_supports_group(int group);
+
+// Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.
+cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
+bool mma_supports_group(int group);
+
+// Launch-count bookkeeping (api.cu).
+void note_launches(int n);
+
+// Status word address on the current device (api.cu).
+unsigned int* device_status_ptr();
+
+}  // namespace pa

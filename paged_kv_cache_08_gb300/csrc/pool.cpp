@@ -1,0 +1,180 @@
+// Host block pool: the untimed bookkeeping that produces block tables and slot mappings.
+//
+// Free set: a bitmap of 32-bit words, bit = 1 when the block is free, lowest free block
+// first via count-trailing-zeros -- the allocator of "端侧 SLM 显存保活术：在 4GB 内存板卡上
+// 实现轻量 PagedAttention 与 KV 缓存分块", section "嵌入式轻量 Block 分配器设计".
+// Reference counts: shared prefix blocks ("共享前缀块（Prefix Caching）" on the same page)
+// and copy-on-write on append ("显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §四).
+// Token append and release follow the lifecycle diagram of that page's §三.
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+#include <vector>
+
+#include "../../include/pa.h"
+
+struct pa_pool {
+    int num_blocks;
+    std::vector<uint32_t> free_bits;  // bit set = free
+    std::vector<int32_t> refs;        // 0 = free
+    int num_free;
+};
+
+namespace {
+
+inline bool valid_id(const pa_pool* p, int id) { return p && id >= 0 && id < p->num_blocks; }
+
+inline void mark_used(pa_pool* p, int id) {
+    p->free_bits[id >> 5] &= ~(1u << (id & 31));
+    --p->num_free;
+}
+
+inline void mark_free(pa_pool* p, int id) {
+    p->free_bits[id >> 5] |= (1u << (id & 31));
+    ++p->num_free;
+}
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+pa_pool* pa_pool_create(int num_blocks) {
+    if (num_blocks <= 0) return nullptr;
+    pa_pool* p = new (std::nothrow) pa_pool;
+    if (!p) return nullptr;
+    try {
+        p->num_blocks = num_blocks;
+        p->free_bits.assign((size_t)ceil_div(num_blocks, 32), 0xFFFFFFFFu);
+        int tail = num_blocks & 31;  // bits past the last block never read as free
+        if (tail) p->free_bits.back() = (1u << tail) - 1u;
+        p->refs.assign((size_t)num_blocks, 0);
+        p->num_free = num_blocks;
+    } catch (...) {
+        delete p;
+        return nullptr;
+    }
+    return p;
+}
+
+void pa_pool_destroy(pa_pool* pool) { delete pool; }
+
+int pa_pool_alloc(pa_pool* pool) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    const size_t words = pool->free_bits.size();
+    for (size_t w = 0; w < words; ++w) {
+        uint32_t bits = pool->free_bits[w];
+        if (bits) {
+            int id = (int)(w * 32) + __builtin_ctz(bits);
+            mark_used(pool, id);
+            pool->refs[id] = 1;
+            return id;
+        }
+    }
+    return PA_ERR_POOL_EXHAUSTED;
+}
+
+int pa_pool_incref(pa_pool* pool, int block_id) {
+    if (!valid_id(pool, block_id) || pool->refs[block_id] <= 0) return PA_ERR_BOUNDS;
+    return ++pool->refs[block_id];
+}
+
+int pa_pool_decref(pa_pool* pool, int block_id) {
+    if (!valid_id(pool, block_id) || pool->refs[block_id] <= 0) return PA_ERR_BOUNDS;
+    int r = --pool->refs[block_id];
+    if (r == 0) mark_free(pool, block_id);
+    return r;
+}
+
+int pa_pool_refcount(const pa_pool* pool, int block_id) {
+    if (!valid_id(pool, block_id)) return PA_ERR_BOUNDS;
+    return pool->refs[block_id];
+}
+
+int pa_pool_num_free(const pa_pool* pool) { return pool ? pool->num_free : PA_ERR_INVALID_ARG; }
+
+int pa_pool_num_blocks(const pa_pool* pool) { return pool ? pool->num_blocks : PA_ERR_INVALID_ARG; }
+
+int pa_pool_assign(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                   int block_size, const int32_t* shared_row, int shared_blocks) {
+    if (!pool || !table_row || max_blocks < 0 || context_len < 0 || block_size <= 0 ||
+        shared_blocks < 0 || (shared_blocks > 0 && !shared_row))
+        return PA_ERR_INVALID_ARG;
+    const int need = ceil_div(context_len, block_size);
+    if (need > max_blocks || shared_blocks > need) return PA_ERR_BOUNDS;
+    for (int i = 0; i < shared_blocks; ++i)
+        if (!valid_id(pool, shared_row[i]) || pool->refs[shared_row[i]] <= 0) return PA_ERR_BOUNDS;
+    if (need - shared_blocks > pool->num_free) return PA_ERR_POOL_EXHAUSTED;
+    for (int i = 0; i < shared_blocks; ++i) {
+        table_row[i] = shared_row[i];
+        ++pool->refs[shared_row[i]];
+    }
+    for (int i = shared_blocks; i < need; ++i) table_row[i] = pa_pool_alloc(pool);
+    for (int i = need; i < max_blocks; ++i) table_row[i] = -1;
+    return PA_OK;
+}
+
+int pa_pool_append_token(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                         int block_size, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+    if (!pool || !table_row || !slot || max_blocks < 0 || context_len < 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (cow_src) *cow_src = -1;
+    if (cow_dst) *cow_dst = -1;
+    const int logical = context_len / block_size;  // block of the new token
+    const int offset = context_len % block_size;
+    if (logical >= max_blocks) return PA_ERR_BOUNDS;
+    if (offset == 0) {
+        // the last block is full (or the sequence is empty): take a fresh block
+        int id = pa_pool_alloc(pool);
+        if (id < 0) return id;
+        table_row[logical] = id;
+    } else {
+        int cur = table_row[logical];
+        if (!valid_id(pool, cur) || pool->refs[cur] <= 0) return PA_ERR_BOUNDS;
+        if (pool->refs[cur] > 1) {
+            // shared and not full: copy-on-write before the write lands in it
+            int id = pa_pool_alloc(pool);
+            if (id < 0) return id;
+            --pool->refs[cur];
+            table_row[logical] = id;
+            if (cow_src) *cow_src = cur;
+            if (cow_dst) *cow_dst = id;
+        }
+    }
+    *slot = (int64_t)table_row[logical] * block_size + offset;
+    return PA_OK;
+}
+
+int pa_pool_release(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
+                    int block_size) {
+    if (!pool || !table_row || context_len < 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
+    const int n = ceil_div(context_len, block_size);
+    if (n > max_blocks) return PA_ERR_BOUNDS;
+    for (int i = 0; i < n; ++i) {
+        if (pa_pool_decref(pool, table_row[i]) < 0) return PA_ERR_BOUNDS;
+        table_row[i] = -1;
+    }
+    return PA_OK;
+}
+
+int pa_build_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                          int num_seqs, int block_size, int64_t* slots) {
+    if (num_seqs < 0 || block_size <= 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!block_tables || !context_lens || !slots)) return PA_ERR_INVALID_ARG;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int L = context_lens[s];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size) return PA_ERR_BOUNDS;
+        if (L == 0) {
+            slots[s] = -1;
+            continue;
+        }
+        const int t = L - 1;
+        const int32_t phys = block_tables[(int64_t)s * max_blocks + t / block_size];
+        if (phys < 0) return PA_ERR_BOUNDS;
+        slots[s] = (int64_t)phys * block_size + t % block_size;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

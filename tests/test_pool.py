@@ -1,0 +1,141 @@
+"""Host block pool: allocator semantics, the lifecycle of the explainer page's
+sequence diagram, copy-on-write, shared prefixes, and slot mappings that match
+the oracle bit for bit on every configuration (no GPU needed)."""
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_08_gb300 as pa
+import workloads
+
+GOLDEN = Path(__file__).resolve().parent / "golden"
+
+
+def _golden():
+    kv = {}
+    for line in (GOLDEN / "address_worked_example.txt").read_text(encoding="utf-8").splitlines():
+        line = line.strip()
+        if line and not line.startswith("#") and not line.startswith("token"):
+            k, *rest = line.split()
+            kv[k] = [int(x) for x in rest]
+    return kv
+
+
+def test_lowest_free_first_and_exhaustion():
+    p = pa.BlockPool(40)
+    ids = [p.alloc() for _ in range(40)]
+    assert ids == list(range(40))
+    with pytest.raises(pa.PAError) as e:
+        p.alloc()
+    assert e.value.code == -4                      # PA_ERR_POOL_EXHAUSTED
+    assert p.decref(33) == 0 and p.decref(5) == 0
+    assert p.num_free == 2
+    assert p.alloc() == 5                          # lowest free bit wins
+    assert p.alloc() == 33
+    with pytest.raises(pa.PAError):
+        p.decref(40)                               # out of range
+    assert p.decref(7) == 0
+    with pytest.raises(pa.PAError):
+        p.decref(7)                                # already free
+
+
+def test_refcounts_free_at_zero():
+    p = pa.BlockPool(4)
+    b = p.alloc()
+    assert p.incref(b) == 2 and p.incref(b) == 3
+    assert p.decref(b) == 2 and p.decref(b) == 1
+    assert p.num_free == 3
+    assert p.decref(b) == 0
+    assert p.num_free == 4 and p.refcount(b) == 0
+
+
+def test_sequence_diagram_worked_example():
+    """38-token prompt in [7, 3, 12]; the next token lands in #12 at offset 6; once #12
+    is full the manager appends #25 and writes at its offset 0; EOS frees them all."""
+    g = _golden()
+    B = g["block_size"][0]
+    new_block = g["grown_table"][-1]
+    p = pa.BlockPool(32)
+    for _ in range(32):
+        p.alloc()                                   # every block taken ...
+    p.decref(new_block)                             # ... but #25, the next one handed out
+    row = np.full(8, -1, dtype=np.int32)
+    row[:3] = g["table"]
+    L, phys, off = g["new_token"]
+    slot, cs, cd = p.append_token(row, L - 1, B)    # context before the append = L - 1
+    assert (slot, cs, cd) == (phys * B + off, -1, -1)
+    L2, phys2, off2 = g["new_token_after_growth"]
+    slot, cs, cd = p.append_token(row, L2 - 1, B)
+    assert (slot, cs, cd) == (phys2 * B + off2, -1, -1)
+    assert list(row[:4]) == g["grown_table"]
+    assert p.num_free == 0
+    p.release(row, L2, B)
+    assert p.num_free == 4
+    assert list(row[:4]) == [-1] * 4
+
+
+def test_copy_on_write_fork():
+    """Two branches share a prompt (reference count 2).  Appending into a shared,
+    partly filled block copies it first; a full shared block is left alone."""
+    B = 16
+    p = pa.BlockPool(16)
+    a = np.full(4, -1, dtype=np.int32)
+    p.assign(a, 20, B)                             # blocks [0, 1], 4 tokens in block 1
+    b = np.full(4, -1, dtype=np.int32)
+    p.assign(b, 20, B, shared_row=a, shared_blocks=2)
+    assert list(b[:2]) == list(a[:2]) and p.refcount(a[0]) == 2 and p.refcount(a[1]) == 2
+    slot, src, dst = p.append_token(a, 20, B)
+    assert src == 1 and dst == a[1] and dst not in (0, 1)
+    assert slot == dst * B + 4
+    assert p.refcount(1) == 1 and p.refcount(dst) == 1
+    slot, src, dst = p.append_token(b, 20, B)      # now the sole owner: no copy
+    assert (src, dst) == (-1, -1) and slot == 1 * B + 4
+    # full shared prompt blocks ([10, 11] pattern): new tokens go to fresh blocks
+    c = np.full(4, -1, dtype=np.int32)
+    p.assign(c, 32, B)
+    d = np.full(4, -1, dtype=np.int32)
+    p.assign(d, 32, B, shared_row=c, shared_blocks=2)
+    _, s1, _ = p.append_token(c, 32, B)
+    _, s2, _ = p.append_token(d, 32, B)
+    assert s1 == -1 and s2 == -1 and c[2] != d[2]
+    assert p.refcount(c[0]) == 2 and p.refcount(c[1]) == 2
+
+
+def test_assign_failure_leaves_pool_unchanged():
+    p = pa.BlockPool(3)
+    row = np.full(8, -1, dtype=np.int32)
+    with pytest.raises(pa.PAError):
+        p.assign(row, 4 * 16, 16)
+    assert p.num_free == 3
+
+
+@pytest.mark.parametrize("cfg,B", [(1, None), (2, None), (3, None), (4, None), (5, 16), (5, 32), (5, 64),
+                                   (5, 128)])
+def test_slot_mapping_matches_oracle(oracle, cfg, B):
+    wl = workloads.config(cfg, block_size=B, values=False)
+    got = pa.build_slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)
+    want = oracle.slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)
+    assert np.array_equal(got, want)
+    assert (got >= 0).all()
+
+
+def test_pool_builds_config5_shared_prefix_tables():
+    """The pool reproduces config 5's structure: one set of prefix blocks with a
+    reference per sequence (plus the resident one), private tails."""
+    wl = workloads.config(5, block_size=32, values=False)
+    B, S = wl.block_size, wl.num_seqs
+    n_prefix = 1024 // B
+    p = pa.BlockPool(wl.num_blocks)
+    prefix = np.full(wl.max_blocks_per_seq, -1, dtype=np.int32)
+    p.assign(prefix, 1024, B)                       # resident prefix owner
+    rows = np.full((S, wl.max_blocks_per_seq), -1, dtype=np.int32)
+    for s in range(S):
+        p.assign(rows[s], int(wl.context_lens[s]), B, shared_row=prefix, shared_blocks=n_prefix)
+    for b in prefix[:n_prefix]:
+        assert p.refcount(int(b)) == S + 1
+    tails = rows[:, n_prefix:]
+    used = tails[tails >= 0]
+    assert len(set(used.tolist())) == used.size     # tail blocks are private
+    slots = pa.build_slot_mapping(rows, wl.context_lens, B)
+    assert not np.isin(slots // B, prefix[:n_prefix]).any()   # no write lands in the shared prefix

@@ -105,7 +105,7 @@ def make_workload(name: str, *, context_lens: Sequence[int], num_q_heads: int, n
                   num_blocks: Optional[int] = None, pool_factor: float = 1.2,
                   max_context: Optional[int] = None, layers: int = 1,
                   shared_prefix_tokens: int = 0, device="cpu", gen: Optional[torch.Generator] = None,
-                  scale: Optional[float] = None) -> Workload:
+                  scale: Optional[float] = None, values: bool = True) -> Workload:
     """Build one seeded workload.
 
     ``shared_prefix_tokens`` (a multiple of ``block_size``) makes the first
@@ -113,6 +113,7 @@ def make_workload(name: str, *, context_lens: Sequence[int], num_q_heads: int, n
     the same physical blocks; each ``context_lens`` entry then includes the
     prefix.  Physical ids come from a seeded random permutation of the pool,
     taken in order: the prefix first, then each sequence's private blocks.
+    ``values=False`` draws only the structure (lengths, tables), no tensors.
     """
     if gen is None:
         gen = torch.Generator().manual_seed(seed)
@@ -149,7 +150,7 @@ def make_workload(name: str, *, context_lens: Sequence[int], num_q_heads: int, n
     tdt = DTYPES[dtype]
     dev = torch.device(device)
     vgen = gen if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(seed)
-    for _ in range(layers):
+    for _ in range(layers if values else 0):
         wl.q.append(_fill_normal((S, num_q_heads, head_dim), tdt, vgen, dev))
         wl.k_cache.append(_fill_normal((num_blocks, num_kv_heads, B, head_dim), tdt, vgen, dev))
         wl.v_cache.append(_fill_normal((num_blocks, num_kv_heads, B, head_dim), tdt, vgen, dev))
@@ -185,7 +186,7 @@ def _lognormal_lens(S: int, gen: torch.Generator, p90: float = 287.0, sigma: flo
 
 
 def config(cfg: int, *, device="cpu", layers: Optional[int] = None, block_size: Optional[int] = None,
-           num_seqs: Optional[int] = None) -> Workload:
+           num_seqs: Optional[int] = None, values: bool = True) -> Workload:
     """The five seeded configurations.  ``layers``/``num_seqs`` may shrink a
     config for a bounded sample; ``block_size`` picks the config-5 sweep point."""
     if cfg == 1:
@@ -194,7 +195,7 @@ def config(cfg: int, *, device="cpu", layers: Optional[int] = None, block_size: 
         lens = [7, 16, 33, 64]
         return make_workload(CONFIG_NAMES[1], context_lens=lens, num_q_heads=12, num_kv_heads=2,
                              block_size=16, dtype="f16", seed=seed, num_blocks=32, max_context=64,
-                             layers=layers or 1, device=device, gen=gen)
+                             layers=layers or 1, device=device, gen=gen, values=values)
     if cfg == 2:
         seed = 1002
         gen = torch.Generator().manual_seed(seed)
@@ -204,7 +205,7 @@ def config(cfg: int, *, device="cpu", layers: Optional[int] = None, block_size: 
             lens = lens[:num_seqs]
         return make_workload(CONFIG_NAMES[2], context_lens=lens, num_q_heads=12, num_kv_heads=2,
                              block_size=16, dtype="f16", seed=seed, max_context=2048,
-                             layers=24 if layers is None else layers, device=device, gen=gen)
+                             layers=24 if layers is None else layers, device=device, gen=gen, values=values)
     if cfg == 3:
         seed = 1003
         gen = torch.Generator().manual_seed(seed)
@@ -213,14 +214,14 @@ def config(cfg: int, *, device="cpu", layers: Optional[int] = None, block_size: 
             lens = lens[:num_seqs]
         return make_workload(CONFIG_NAMES[3], context_lens=lens, num_q_heads=32, num_kv_heads=32,
                              block_size=32, dtype="f16", seed=seed, max_context=4096,
-                             layers=layers or 1, device=device, gen=gen)
+                             layers=layers or 1, device=device, gen=gen, values=values)
     if cfg == 4:
         seed = 1004
         gen = torch.Generator().manual_seed(seed)
         S = 16 if num_seqs is None else num_seqs
         return make_workload(CONFIG_NAMES[4], context_lens=[16384] * S, num_q_heads=32,
                              num_kv_heads=8, block_size=64, dtype="bf16", seed=seed,
-                             max_context=16384, layers=layers or 1, device=device, gen=gen)
+                             max_context=16384, layers=layers or 1, device=device, gen=gen, values=values)
     if cfg == 5:
         B = 16 if block_size is None else block_size
         if B not in (16, 32, 64, 128):
@@ -235,7 +236,7 @@ def config(cfg: int, *, device="cpu", layers: Optional[int] = None, block_size: 
         return make_workload(f"{CONFIG_NAMES[5]}_B{B}", context_lens=lens, num_q_heads=12,
                              num_kv_heads=2, block_size=B, dtype="f16", seed=seed,
                              max_context=1024 + 512, shared_prefix_tokens=1024,
-                             layers=layers or 1, device=device, gen=gen)
+                             layers=layers or 1, device=device, gen=gen, values=values)
     raise ValueError(f"unknown config {cfg}")
 
 
