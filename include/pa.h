@@ -69,16 +69,22 @@ typedef enum {
 #define PA_DEV_BAD_SLOT     0x4u /* a slot >= num_blocks*block_size was skipped */
 #define PA_DEV_TIMEOUT      0x8u /* a copy pipeline wait gave up after about one second */
 
-/* Math path of pa_decode_ex. */
+/* Kernel choice of pa_decode_ex. */
 typedef enum {
-    PA_MATH_AUTO = 0,            /* the library's choice for the shape */
-    PA_MATH_FMA = 1,             /* CUDA-core fp32 FMAs with warp-shuffle reductions */
-    PA_MATH_MMA = 2              /* tensor-core (mma.sync m16n8k16) QK^T and PV products */
+    PA_MATH_AUTO = 0,            /* the library's choice for the shape (PA_MATH_MMA when G <= 16) */
+    PA_MATH_FMA = 1,             /* split grid, CUDA-core fp32 FMAs with warp-shuffle reductions,
+                                    separate combine pass; G in {1, 2, 3, 4, 6, 8} */
+    PA_MATH_MMA = 2,             /* tensor-core (mma.sync m16n8k16) QK^T and PV products in one
+                                    persistent, load-balanced launch (num_seqs <= 1024; else the
+                                    split grid below); G <= 16 */
+    PA_MATH_MMA_SPLIT = 3        /* tensor-core products on the split grid with a combine pass */
 } pa_math;
 
 typedef struct {
-    int tokens_per_split;        /* 0 = library's choice; else a multiple of max(block_size, 64) */
+    int tokens_per_split;        /* split grids: 0 = library's choice; else a multiple of
+                                    max(block_size, 64), at most 1024 * block_size */
     int math;                    /* a pa_math value */
+    int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once */
 } pa_decode_options;
 
 /* ------------------------------------------------------------------------------------
@@ -106,13 +112,17 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
  * a zero row.  Supported: head_dim 128, block_size 16/32/64/128, num_q_heads a
  * multiple of num_kv_heads.
  *
- * Work is split over (sequence, kv head, token range); all query heads of a GQA
- * group share each K/V tile.  Partial results of split sequences go to
- * `workspace` (device memory of at least pa_decode_workspace_size(...) bytes,
- * owned by the caller, contents need no initialisation; NULL is allowed when
- * that size is 0).  Two kernels run on `stream`: the split pass and, when any
- * sequence can be split, a combine pass.  Calls that share a workspace must not
- * overlap on the GPU.
+ * All query heads of a GQA group share each K/V tile.  The default kernel is one
+ * persistent launch in which every CTA streams an equal share of all 64-token
+ * chunks of all (sequence, kv head) pairs; pairs cut by share boundaries leave
+ * partial results in `workspace` that the last CTA to finish merges.
+ * `workspace`: device memory of at least pa_decode_workspace_size(...) bytes,
+ * owned by the caller, 16-byte aligned, ZERO-FILLED before its first use (see
+ * pa_decode_workspace_init); every completed call leaves it ready for the next
+ * one of any shape that runs the same kernel kind (pa_decode_kernel_kind) with the
+ * same CTA count.  NULL is allowed when the size is 0.  Calls that share a
+ * workspace must not overlap on the GPU.  After a call that set PA_DEV_TIMEOUT, or
+ * before switching kernel kind or CTA count, zero it again.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or PA_ERR_CUDA.
  * ---------------------------------------------------------------------------------- */
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -138,6 +148,17 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                    int block_size, int max_blocks_per_seq,
                                    const pa_decode_options* opts);
+
+/* Which kernel pa_decode_ex runs for this shape: PA_KERNEL_* below, or < 0 (a pa_status)
+ * when no kernel serves it.  A workspace must stay with one kind: the persistent kernel
+ * keeps arrival counters in it that split-grid partials would overwrite. */
+#define PA_KERNEL_SPLIT_FMA 1
+#define PA_KERNEL_PERSISTENT_MMA 2
+#define PA_KERNEL_SPLIT_MMA 3
+int pa_decode_kernel_kind(int num_seqs, int num_q_heads, int num_kv_heads, const pa_decode_options* opts);
+
+/* Zero-fill `bytes` of workspace on `stream` (cudaMemsetAsync). */
+int pa_decode_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* The split length (tokens per split) pa_decode_ex would use; < 0 on invalid input. */
 int pa_decode_plan_tokens_per_split(int num_seqs, int num_q_heads, int num_kv_heads,

@@ -21,7 +21,8 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "decode", "decode_workspace_size", "plan_tokens_per_split", "BlockPool",
+__all__ = ["cache_write", "decode", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
+           "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -45,10 +46,10 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def _opts(tokens_per_split: int, math: str) -> DecodeOptions:
+def _opts(tokens_per_split: int, math: str, num_ctas: int = 0) -> DecodeOptions:
     if math not in MATH:
         raise ValueError(f"math must be one of {sorted(MATH)}")
-    return DecodeOptions(int(tokens_per_split), MATH[math])
+    return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas))
 
 
 def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
@@ -69,8 +70,9 @@ def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_
 
 
 def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
-                          max_blocks_per_seq: int, tokens_per_split: int = 0, math: str = "auto") -> int:
-    o = _opts(tokens_per_split, math)
+                          max_blocks_per_seq: int, tokens_per_split: int = 0, math: str = "auto",
+                          num_ctas: int = 0) -> int:
+    o = _opts(tokens_per_split, math, num_ctas)
     return int(lib().pa_decode_workspace_size_ex(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                                  max_blocks_per_seq, ctypes.byref(o)))
 
@@ -83,16 +85,30 @@ def plan_tokens_per_split(num_seqs: int, num_q_heads: int, num_kv_heads: int, he
                                                                block_size, max_blocks_per_seq, ctypes.byref(o)))
 
 
+def kernel_kind(num_seqs: int, num_q_heads: int, num_kv_heads: int, math: str = "auto") -> int:
+    """1 = split grid (CUDA cores), 2 = persistent (tensor cores), 3 = split grid (tensor cores)."""
+    o = _opts(0, math)
+    return _native.check("pa_decode_kernel_kind",
+                         lib().pa_decode_kernel_kind(num_seqs, num_q_heads, num_kv_heads, ctypes.byref(o)))
+
+
 _workspaces: dict = {}
 
 
-def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled decode workspace (the persistent kernel expects zeroed counters)."""
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def _workspace(device: torch.device, nbytes: int, kind: int, num_ctas: int) -> Optional[torch.Tensor]:
+    """One zeroed workspace per (device, kernel kind, CTA count): the persistent kernel's
+    counters sit at an offset fixed by the CTA count and are left zero by every call."""
     if nbytes == 0:
         return None
-    key = device.index if device.index is not None else torch.cuda.current_device()
+    key = (device.index if device.index is not None else torch.cuda.current_device(), kind, num_ctas)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ws = new_workspace(nbytes, device)
         _workspaces[key] = ws
     return ws
 
@@ -100,7 +116,7 @@ def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, scale: float, num_kv_heads: int, out: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, tokens_per_split: int = 0, math: str = "auto",
-           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+           num_ctas: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Paged decode attention.  q: [S, Hq, D]; caches [NB, Hkv, B, D]; block_tables int32
     [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype."""
     _need_cuda("q", q)
@@ -123,10 +139,11 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(tokens_per_split, math)
+    o = _opts(tokens_per_split, math, num_ctas)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
-        workspace = _workspace(q.device, need)
+        kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))
+        workspace = _workspace(q.device, need, kind, int(num_ctas))
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().pa_decode_ex(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),

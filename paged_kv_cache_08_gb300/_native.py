@@ -22,7 +22,7 @@ c_u32p = ctypes.POINTER(ctypes.c_uint32)
 
 
 class DecodeOptions(ctypes.Structure):
-    _fields_ = [("tokens_per_split", c_int), ("math", c_int)]
+    _fields_ = [("tokens_per_split", c_int), ("math", c_int), ("num_ctas", c_int)]
 
 
 PA_OK = 0
@@ -30,7 +30,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "P
           -4: "PA_ERR_POOL_EXHAUSTED", -5: "PA_ERR_DEVICE_TIMEOUT", -6: "PA_ERR_BOUNDS",
           -7: "PA_ERR_WORKSPACE"}
 DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-MATH = {"auto": 0, "fma": 1, "mma": 2}
+MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 
 _SIGNATURES = {
     "pa_cache_write": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp]),
@@ -41,6 +41,8 @@ _SIGNATURES = {
     "pa_decode_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pa_decode_workspace_size_ex": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int,
                                              ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_workspace_init": (c_int, [c_vp, c_size, c_vp]),
+    "pa_decode_kernel_kind": (c_int, [c_int, c_int, c_int, ctypes.POINTER(DecodeOptions)]),
     "pa_decode_plan_tokens_per_split": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int,
                                                 ctypes.POINTER(DecodeOptions)]),
     "pa_status_string": (ctypes.c_char_p, [c_int]),

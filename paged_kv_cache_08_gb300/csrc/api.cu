@@ -53,8 +53,9 @@ int plan_tps(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_
     const int unit = block_size > kStageTokens ? block_size : kStageTokens;
     const long long cap = (long long)max_blocks_per_seq * block_size;
     const long long cap_units = ((cap + unit - 1) / unit) * unit;
+    const long long max_tps = (long long)kMaxTableSlice * block_size;  // table slice held in shared memory
     if (opts && opts->tokens_per_split > 0) {
-        if (opts->tokens_per_split % unit) return PA_ERR_INVALID_ARG;
+        if (opts->tokens_per_split % unit || opts->tokens_per_split > max_tps) return PA_ERR_INVALID_ARG;
         return opts->tokens_per_split;
     }
     if (cap_units == 0) return unit;
@@ -66,6 +67,7 @@ int plan_tps(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_
     if (tps < 256) tps = 256;
     tps = ((tps + unit - 1) / unit) * unit;
     if (tps > cap_units) tps = cap_units;
+    if (tps > max_tps) tps = max_tps;
     return (int)tps;
 }
 
@@ -84,6 +86,47 @@ size_t workspace_bytes_for(int num_seqs, int num_q_heads, int max_splits) {
     if (max_splits <= 1) return 0;
     const size_t n = (size_t)num_seqs * num_q_heads * max_splits;
     return n * (kHeadDim * sizeof(float) + sizeof(float2));
+}
+
+enum Path { kPathFma, kPathMmaSplit, kPathPersist };
+
+// Which kernel serves (num_seqs, group, math); PA_ERR_UNSUPPORTED when none does.
+int choose_path(int num_seqs, int group, int math, Path* path) {
+    if (math == PA_MATH_AUTO) math = mma_supports_group(group) ? PA_MATH_MMA : PA_MATH_FMA;
+    switch (math) {
+        case PA_MATH_FMA:
+            if (!fma_supports_group(group)) return PA_ERR_UNSUPPORTED;
+            *path = kPathFma;
+            return PA_OK;
+        case PA_MATH_MMA:
+            if (!mma_supports_group(group)) return PA_ERR_UNSUPPORTED;
+            *path = num_seqs <= kPersistMaxSeqs ? kPathPersist : kPathMmaSplit;
+            return PA_OK;
+        case PA_MATH_MMA_SPLIT:
+            if (!mma_supports_group(group)) return PA_ERR_UNSUPPORTED;
+            *path = kPathMmaSplit;
+            return PA_OK;
+        default:
+            return PA_ERR_INVALID_ARG;
+    }
+}
+
+inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+int persist_ctas(int group, const pa_decode_options* opts) {
+    if (opts && opts->num_ctas > 0) return opts->num_ctas;
+    return persist_ctas_per_sm(group) * sm_count();
+}
+
+// Persistent-path workspace: [C][2][16][D] fp32 partial outputs, [C][2][16] (m, l), then one
+// arrival counter per (sequence, kv head).  Pieces are sized for the largest group so that the
+// counters start at an offset that depends on the CTA count alone: a workspace keeps its zeroed
+// counters across calls of any shape that use the same CTA count.
+size_t persist_workspace_bytes(int num_seqs, int num_kv_heads, int group, int ctas) {
+    (void)group;
+    const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+    return align256(pieces * kHeadDim * sizeof(float)) + align256(pieces * sizeof(float2)) +
+           align256((size_t)num_seqs * num_kv_heads * sizeof(int));
 }
 
 int max_splits_for(int block_size, int max_blocks_per_seq, int tps) {
@@ -188,10 +231,35 @@ int pa_decode_plan_tokens_per_split(int num_seqs, int num_q_heads, int num_kv_he
 
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                    int max_blocks_per_seq, const pa_decode_options* opts) {
-    int tps = pa_decode_plan_tokens_per_split(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                              max_blocks_per_seq, opts);
+    if (check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) != PA_OK)
+        return 0;
+    const int group = num_q_heads / num_kv_heads;
+    Path path;
+    if (choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path) != PA_OK) return 0;
+    if (path == kPathPersist)
+        return persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_ctas(group, opts));
+    int tps = plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
     if (tps <= 0) return 0;
     return workspace_bytes_for(num_seqs, num_q_heads, max_splits_for(block_size, max_blocks_per_seq, tps));
+}
+
+int pa_decode_kernel_kind(int num_seqs, int num_q_heads, int num_kv_heads, const pa_decode_options* opts) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    Path path;
+    int rc = choose_path(num_seqs, num_q_heads / num_kv_heads, opts ? opts->math : PA_MATH_AUTO, &path);
+    if (rc != PA_OK) return rc;
+    return path == kPathFma ? PA_KERNEL_SPLIT_FMA : (path == kPathPersist ? PA_KERNEL_PERSISTENT_MMA
+                                                                          : PA_KERNEL_SPLIT_MMA);
+}
+
+int pa_decode_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (bytes == 0) return PA_OK;
+    if (!workspace) return PA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -207,37 +275,28 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
     if (rc != PA_OK) return rc;
-    if (num_blocks < 0) return PA_ERR_INVALID_ARG;
-    if (opts && (opts->math < PA_MATH_AUTO || opts->math > PA_MATH_MMA)) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (opts && (opts->math < PA_MATH_AUTO || opts->math > PA_MATH_MMA_SPLIT || opts->num_ctas < 0))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
-    if (!out || !q || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
-    if (num_blocks > 0 && (!k_cache || !v_cache)) return PA_ERR_INVALID_ARG;
+    if (!out || !q || !block_tables || !context_lens || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
         !aligned4(block_tables) || !aligned4(context_lens))
         return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    int math = opts ? opts->math : PA_MATH_AUTO;
-    if (math == PA_MATH_AUTO) math = (mma_supports_group(group) && num_blocks > 0) ? PA_MATH_MMA : PA_MATH_FMA;
-    if (math == PA_MATH_MMA && (!mma_supports_group(group) || num_blocks == 0)) return PA_ERR_UNSUPPORTED;
-    if (math == PA_MATH_FMA && !fma_supports_group(group)) return PA_ERR_UNSUPPORTED;
-    const int tps = plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
-    if (tps <= 0) return PA_ERR_INVALID_ARG;
-    const int max_splits = max_splits_for(block_size, max_blocks_per_seq, tps);
-    const size_t need = workspace_bytes_for(num_seqs, num_q_heads, max_splits);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+    Path path;
+    rc = choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path);
+    if (rc != PA_OK) return rc;
 
     DecodeArgs a;
+    std::memset(&a, 0, sizeof(a));
     a.out = out;
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
-    const size_t n_part = (size_t)num_seqs * num_q_heads * max_splits;
-    a.part_o = need ? static_cast<float*>(workspace) : nullptr;
-    a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + n_part * kHeadDim * sizeof(float))
-                     : nullptr;
-    a.status = device_status_ptr();
     a.scale_log2 = scale * 1.4426950408889634f;
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
@@ -245,13 +304,42 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     a.block_size = block_size;
     a.num_blocks = num_blocks;
     a.max_blocks_per_seq = max_blocks_per_seq;
-    a.tokens_per_split = tps;
-    a.max_splits = max_splits;
-
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = math == PA_MATH_MMA ? launch_decode_split_mma(a, dtype, st)
-                                        : launch_decode_split_fma(a, dtype, group, st);
-    if (e == cudaSuccess && max_splits > 1) e = launch_decode_combine(a, dtype, st);
+    cudaError_t e;
+
+    if (path == kPathPersist) {
+        const int ctas = persist_ctas(group, opts);
+        const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, ctas);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+        const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+        char* w = static_cast<char*>(workspace);
+        a.part_o = reinterpret_cast<float*>(w);
+        a.part_ml = reinterpret_cast<float2*>(w + align256(pieces * kHeadDim * sizeof(float)));
+        a.seg_counters = reinterpret_cast<int*>(w + align256(pieces * kHeadDim * sizeof(float)) +
+                                                align256(pieces * sizeof(float2)));
+        a.num_ctas = ctas;
+        a.tokens_per_split = 0;
+        a.max_splits = 1;
+        a.status = device_status_ptr();
+        e = launch_decode_persist(a, dtype, st);
+    } else {
+        const int tps = plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
+        if (tps <= 0) return PA_ERR_INVALID_ARG;
+        const int max_splits = max_splits_for(block_size, max_blocks_per_seq, tps);
+        const size_t need = workspace_bytes_for(num_seqs, num_q_heads, max_splits);
+        if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+        const size_t n_part = (size_t)num_seqs * num_q_heads * max_splits;
+        a.part_o = need ? static_cast<float*>(workspace) : nullptr;
+        a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                                     n_part * kHeadDim * sizeof(float))
+                         : nullptr;
+        a.tokens_per_split = tps;
+        a.max_splits = max_splits;
+        a.status = device_status_ptr();
+        e = path == kPathMmaSplit ? launch_decode_split_mma(a, dtype, st)
+                                  : launch_decode_split_fma(a, dtype, group, st);
+        if (e == cudaSuccess && max_splits > 1) e = launch_decode_combine(a, dtype, st);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;

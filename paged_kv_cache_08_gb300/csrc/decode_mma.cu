@@ -30,11 +30,19 @@ namespace pa {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;          // + one TMA producer warp
 constexpr int kStages = 3;
 constexpr int kStageKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kStageBytes = 2 * kStageKBytes;
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 /*align*/ + 64 /*barriers*/;
+constexpr size_t kRingBytes = (size_t)kStages * kStageBytes;
+constexpr size_t kBarOff = kRingBytes;                        // full[kStages], empty[kStages]
+constexpr size_t kFlagOff = kBarOff + 2 * kStages * sizeof(uint64_t);  // abort flag, issued count
+constexpr size_t kTblOff = kFlagOff + 16;                     // block-table slice of the split
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kTblOff + kMaxTableSlice * sizeof(int32_t);
+constexpr int kRedStride = kHeadDim + 8;                      // padded rows of the warp-merge buffer
+static_assert((size_t)kConsumerWarps * 16 * kRedStride * 4 + kConsumerWarps * 16 * 8 <= kRingBytes,
+              "merge buffers must fit in the ring");
 
 struct MmaMaps {
     CUtensorMap k;
@@ -119,8 +127,9 @@ __device__ __forceinline__ uint16_t out_bits<__nv_bfloat16>(float x) {
 }
 
 // Issue the TMA loads of one stage: tokens [base, min(base + 64, tok_end)).
-__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const MmaMaps& maps, const int32_t* table, int hk,
-                                            int base, int tok_end, uint32_t kdst, uint64_t* bar, int R_log2) {
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const MmaMaps& maps, const int32_t* tbl, int tbl0,
+                                            int hk, int base, int tok_end, uint32_t kdst, uint64_t* bar,
+                                            int R_log2) {
     const int B = a.block_size;
     const int R = 1 << R_log2;                   // rows per box: min(B, 64)
     const int first = base / B;
@@ -132,7 +141,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const MmaMaps& 
     for (int j = 0; j < 4; ++j) {
         phys[j] = -1;
         if (first + j <= last) {
-            const int p = table[first + j];
+            const int p = tbl[first + j - tbl0];
             if (p >= 0 && p < a.num_blocks) {
                 phys[j] = p;
                 bytes += 2u * 2u * (uint32_t)R * 128u;   // K and V, two 64-column halves
@@ -161,33 +170,51 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t ring = (raw + 1023u) & ~1023u;                  // 1024-aligned for the swizzle
-    unsigned char* ring_ptr = smem_raw + (ring - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + (size_t)kStages * kStageBytes);
+    unsigned char* base_ptr = smem_raw + (ring - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + kBarOff);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kFlagOff);
+    volatile int* issued_count = abort_flag + 1;
+    int32_t* tbl = reinterpret_cast<int32_t*>(base_ptr + kTblOff);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
     const int Hq = a.num_q_heads;
     const int G = Hq / a.num_kv_heads;
+    const int B = a.block_size;
 
     if (tid == 0) {
         prefetch_map(&maps.k);
         prefetch_map(&maps.v);
 #pragma unroll
-        for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *issued_count = 0;
         fence_mbar_init();
     }
     grid_dependency_wait();
 
+    // the split's slice of the block table and the context length, loaded together
+    const int tps = a.tokens_per_split;
+    const int tok0 = split * tps;
+    const int tbl0 = tok0 / B;
+    const int ntbl = min(tps / B, a.max_blocks_per_seq - tbl0);
+    {
+        const int32_t* row = a.block_tables + (size_t)s * a.max_blocks_per_seq + tbl0;
+        for (int j = tid; j < ntbl; j += kThreads) tbl[j] = row[j];
+    }
     int Lctx = a.context_lens[s];
-    const int cap = a.max_blocks_per_seq * a.block_size;
+    const int cap = a.max_blocks_per_seq * B;
     if (Lctx < 0 || Lctx > cap) {
         if (tid == 0 && split == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
         Lctx = Lctx < 0 ? 0 : cap;
     }
-    const int tps = a.tokens_per_split;
-    const int tok0 = split * tps;
+    __syncthreads();
     if (Lctx == 0) {
-        if (split == 0) {
+        if (split == 0 && tid < kHeadDim) {
             uint16_t* out = static_cast<uint16_t*>(a.out);
             for (int g = 0; g < G; ++g) out[((size_t)s * Hq + hk * G + g) * kHeadDim + tid] = 0;
         }
@@ -197,183 +224,197 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tok1 = min(Lctx, tok0 + tps);
     const int nsplit_s = (Lctx + tps - 1) / tps;
     const int nst = (tok1 - tok0 + kStageTokens - 1) / kStageTokens;
-    const int32_t* table = a.block_tables + (size_t)s * a.max_blocks_per_seq;
-
-    __syncthreads();
-    if (tid == 0) {
-        const int pre = min(kStages, nst);
-        for (int i = 0; i < pre; ++i)
-            issue_stage(a, maps, table, hk, tok0 + i * kStageTokens, tok1, ring + (uint32_t)i * kStageBytes,
-                        &bars[i], R_log2);
-    }
     grid_launch_dependents();
 
-    // ---- Q fragments (A operand, rows = query heads of the group, zero padded to 16) ----
     const int qr = lane >> 2, qc = (lane & 3) * 2;
-    uint32_t qa[8][4];
-    {
-        const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
-        const size_t row0 = ((size_t)s * Hq + hk * G + qr) * kHeadDim;
-        const size_t row1 = row0 + 8 * kHeadDim;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int d = ks * 16 + qc;
-            qa[ks][0] = (qr < G) ? q32[(row0 + d) >> 1] : 0u;
-            qa[ks][1] = (qr + 8 < G) ? q32[(row1 + d) >> 1] : 0u;
-            qa[ks][2] = (qr < G) ? q32[(row0 + d + 8) >> 1] : 0u;
-            qa[ks][3] = (qr + 8 < G) ? q32[(row1 + d + 8) >> 1] : 0u;
-        }
-    }
-
+    float m_run[2] = {-INFINITY, -INFINITY};   // rows qr and qr + 8, log2 units
+    float l_run[2] = {0.f, 0.f};               // this thread's columns only
     float o[16][4];
 #pragma unroll
     for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};   // rows qr and qr + 8, log2 units
-    float l_run[2] = {0.f, 0.f};               // this thread's columns only
 
-    const int t_warp = warp * 16;
-    // ldmatrix row providers: K (non-transposed) and V (transposed) tiles
-    const int tk = t_warp + (lane & 7) + ((lane >> 4) << 3);
-    const int ck = (lane >> 3) & 1;
-    const int tv = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
-    const int cv = lane >> 4;
-
-    int i = 0;
-    bool timed_out = false;
-    for (; i < nst; ++i) {
-        const int st = i % kStages;
-        const uint32_t parity = (uint32_t)(i / kStages) & 1u;
-        const bool ok = mbar_wait_bounded(&bars[st], parity);
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        const uint32_t kbase = ring + (uint32_t)st * kStageBytes;
-        const uint32_t vbase = kbase + kStageKBytes;
-        const int sbase = tok0 + i * kStageTokens;
-        const int nvalid = min(kStageTokens, tok1 - sbase);
-
-        if (nvalid < kStageTokens) {
-            // rows past the context may hold stale or unwritten data: zero V there so that
-            // P = 0 never meets a non-finite value in the P.V product
-            uint4* vz = reinterpret_cast<uint4*>(ring_ptr + (size_t)st * kStageBytes + kStageKBytes);
-            for (int idx = tid; idx < (kStageTokens - nvalid) * 16; idx += kThreads) {
-                const int t = nvalid + (idx >> 4);
-                const int c = idx & 15;
-                vz[line_of(t, c >> 3, R_log2) * 8 + (c & 7)] = make_uint4(0, 0, 0, 0);
+    if (warp == kConsumerWarps) {
+        // ---------------- producer warp: one lane keeps the ring full ----------------
+        if (lane == 0) {
+            int i = 0;
+            for (; i < nst; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages) {
+                    if (!mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u)) {
+                        flag_status(a.status, PA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    fence_proxy_async_smem();   // consumers' reads of this buffer precede the overwrite
+                }
+                if (*abort_flag) break;
+                issue_stage(a, maps, tbl, tbl0, hk, tok0 + i * kStageTokens, tok1, ring + (uint32_t)st * kStageBytes,
+                            &full[st], R_log2);
             }
-            __syncthreads();
+            *issued_count = i;
         }
-
-        if (t_warp < nvalid) {
-            // ---- S = Q K^T for this warp's 16 tokens ----
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    } else {
+        // ---------------- consumer warps: tokens [16w, 16w + 16) of every stage ----------------
+        uint32_t qa[8][4];
+        {
+            const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
+            const size_t row0 = ((size_t)s * Hq + hk * G + qr) * kHeadDim;
+            const size_t row1 = row0 + 8 * kHeadDim;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(chunk_addr(kbase, tk, 2 * ks + ck, R_log2), b0, b1, b2, b3);
-                mma16816<T>(sc[0], qa[ks], b0, b1);
-                mma16816<T>(sc[1], qa[ks], b2, b3);
-            }
-            // ---- online softmax over the 16 columns, rows qr and qr + 8 ----
-            float p[2][4];
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = t_warp + n * 8 + qc + (e & 1);
-                    const float x = sc[n][e] * a.scale_log2;
-                    p[n][e] = (col < nvalid) ? x : -INFINITY;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], p[n][e]);
-                }
-            float alpha[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float m_new = fmaxf(m_run[r], mx[r]);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[r] = exp2f(m_run[r] - m_use);
-                m_run[r] = m_new;
-                mx[r] = m_use;
-            }
-            float rs[2] = {0.f, 0.f};
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    p[n][e] = exp2f(p[n][e] - mx[e >> 1]);
-                    rs[e >> 1] += p[n][e];
-                }
-            l_run[0] = l_run[0] * alpha[0] + rs[0];
-            l_run[1] = l_run[1] * alpha[1] + rs[1];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                o[j][0] *= alpha[0];
-                o[j][1] *= alpha[0];
-                o[j][2] *= alpha[1];
-                o[j][3] *= alpha[1];
-            }
-            // ---- O += P V ----
-            uint32_t pa_[4];
-            pa_[0] = pack_pair<T>(p[0][0], p[0][1]);
-            pa_[1] = pack_pair<T>(p[0][2], p[0][3]);
-            pa_[2] = pack_pair<T>(p[1][0], p[1][1]);
-            pa_[3] = pack_pair<T>(p[1][2], p[1][3]);
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(chunk_addr(vbase, tv, 2 * np + cv, R_log2), b0, b1, b2, b3);
-                mma16816<T>(o[2 * np], pa_, b0, b1);
-                mma16816<T>(o[2 * np + 1], pa_, b2, b3);
+                const int d = ks * 16 + qc;
+                qa[ks][0] = (qr < G) ? q32[(row0 + d) >> 1] : 0u;
+                qa[ks][1] = (qr + 8 < G) ? q32[(row1 + d) >> 1] : 0u;
+                qa[ks][2] = (qr < G) ? q32[(row0 + d + 8) >> 1] : 0u;
+                qa[ks][3] = (qr + 8 < G) ? q32[(row1 + d + 8) >> 1] : 0u;
             }
         }
-        __syncthreads();   // every warp is done with this stage's buffers
-        if (tid == 0 && i + kStages < nst) {
-            fence_proxy_async_smem();
-            issue_stage(a, maps, table, hk, tok0 + (i + kStages) * kStageTokens, tok1,
-                        ring + (uint32_t)st * kStageBytes, &bars[st], R_log2);
+        const int t_warp = warp * 16;
+        const int tk = t_warp + (lane & 7) + ((lane >> 4) << 3);   // ldmatrix rows: K tile
+        const int ck = (lane >> 3) & 1;
+        const int tv = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);   // V tile (transposed)
+        const int cv = lane >> 4;
+
+        for (int i = 0; i < nst; ++i) {
+            const int st = i % kStages;
+            if (!mbar_wait_bounded(&full[st], (uint32_t)(i / kStages) & 1u)) {
+                flag_status(a.status, PA_DEV_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            const uint32_t kbase = ring + (uint32_t)st * kStageBytes;
+            const uint32_t vbase = kbase + kStageKBytes;
+            const int nvalid = min(kStageTokens, tok1 - (tok0 + i * kStageTokens));
+
+            if (t_warp < nvalid) {
+                if (nvalid < t_warp + 16) {
+                    // rows past the context may hold stale or unwritten data: zero this warp's
+                    // V rows there so that P = 0 never meets a non-finite value in P.V
+                    uint4* vz = reinterpret_cast<uint4*>(base_ptr + (size_t)st * kStageBytes + kStageKBytes);
+                    for (int idx = lane; idx < (t_warp + 16 - nvalid) * 16; idx += 32) {
+                        const int t = nvalid + (idx >> 4);
+                        const int c = idx & 15;
+                        vz[line_of(t, c >> 3, R_log2) * 8 + (c & 7)] = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+                // ---- S = Q K^T for this warp's 16 tokens ----
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(chunk_addr(kbase, tk, 2 * ks + ck, R_log2), b0, b1, b2, b3);
+                    mma16816<T>(sc[0], qa[ks], b0, b1);
+                    mma16816<T>(sc[1], qa[ks], b2, b3);
+                }
+                // ---- online softmax over the 16 columns, rows qr and qr + 8 ----
+                float p[2][4];
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = t_warp + n * 8 + qc + (e & 1);
+                        const float x = sc[n][e] * a.scale_log2;
+                        p[n][e] = (col < nvalid) ? x : -INFINITY;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], p[n][e]);
+                    }
+                float alpha[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                    const float m_new = fmaxf(m_run[r], mx[r]);
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    alpha[r] = exp2f(m_run[r] - m_use);
+                    m_run[r] = m_new;
+                    mx[r] = m_use;
+                }
+                float rs[2] = {0.f, 0.f};
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p[n][e] = exp2f(p[n][e] - mx[e >> 1]);
+                        rs[e >> 1] += p[n][e];
+                    }
+                l_run[0] = l_run[0] * alpha[0] + rs[0];
+                l_run[1] = l_run[1] * alpha[1] + rs[1];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    o[j][0] *= alpha[0];
+                    o[j][1] *= alpha[0];
+                    o[j][2] *= alpha[1];
+                    o[j][3] *= alpha[1];
+                }
+                // ---- O += P V ----
+                uint32_t pa_[4];
+                pa_[0] = pack_pair<T>(p[0][0], p[0][1]);
+                pa_[1] = pack_pair<T>(p[0][2], p[0][3]);
+                pa_[2] = pack_pair<T>(p[1][0], p[1][1]);
+                pa_[3] = pack_pair<T>(p[1][2], p[1][3]);
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(chunk_addr(vbase, tv, 2 * np + cv, R_log2), b0, b1, b2, b3);
+                    mma16816<T>(o[2 * np], pa_, b0, b1);
+                    mma16816<T>(o[2 * np + 1], pa_, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the stage's buffers
         }
     }
 
-    if (timed_out) {
-        if (tid == 0) flag_status(a.status, PA_DEV_TIMEOUT);
-        for (int j = i; j < min(nst, i + kStages); ++j)
-            (void)mbar_wait_bounded(&bars[j % kStages], (uint32_t)(j / kStages) & 1u);
+    __syncthreads();
+    if (*abort_flag) {
+        if (tid == 0) {
+            // let every copy still in flight land before the CTA's shared memory is released
+            const int n = *issued_count;
+            for (int st = 0; st < kStages; ++st) {
+                int last = -1;
+                for (int i = st; i < n; i += kStages) last = i;
+                if (last >= 0) (void)mbar_wait_bounded(&full[st], (uint32_t)(last / kStages) & 1u);
+            }
+        }
         return;
     }
 
-    // ---- merge the four warps: per row, M = max m_w, o = sum 2^(m_w - M) o_w ----
+    // ---- merge the four consumer warps: per row, M = max m_w, o = sum 2^(m_w - M) o_w ----
+    float* red_o = reinterpret_cast<float*>(base_ptr);        // [4][16][kRedStride]
+    float2* red_ml = reinterpret_cast<float2*>(base_ptr + (size_t)kConsumerWarps * 16 * kRedStride * 4);
+    if (warp < kConsumerWarps) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-    }
-    float* red_o = reinterpret_cast<float*>(ring_ptr);                  // [4][16][128]
-    float2* red_ml = reinterpret_cast<float2*>(ring_ptr + 4 * 16 * kHeadDim * sizeof(float));  // [4][16]
+        for (int r = 0; r < 2; ++r) {
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+        }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int d = j * 8 + qc;
-        *reinterpret_cast<float2*>(&red_o[(warp * 16 + qr) * kHeadDim + d]) = make_float2(o[j][0], o[j][1]);
-        *reinterpret_cast<float2*>(&red_o[(warp * 16 + qr + 8) * kHeadDim + d]) = make_float2(o[j][2], o[j][3]);
-    }
-    if ((lane & 3) == 0) {
-        red_ml[warp * 16 + qr] = make_float2(m_run[0], l_run[0]);
-        red_ml[warp * 16 + qr + 8] = make_float2(m_run[1], l_run[1]);
+        for (int j = 0; j < 16; ++j) {
+            const int d = j * 8 + qc;
+            *reinterpret_cast<float2*>(&red_o[(warp * 16 + qr) * kRedStride + d]) = make_float2(o[j][0], o[j][1]);
+            *reinterpret_cast<float2*>(&red_o[(warp * 16 + qr + 8) * kRedStride + d]) =
+                make_float2(o[j][2], o[j][3]);
+        }
+        if ((lane & 3) == 0) {
+            red_ml[warp * 16 + qr] = make_float2(m_run[0], l_run[0]);
+            red_ml[warp * 16 + qr + 8] = make_float2(m_run[1], l_run[1]);
+        }
     }
     __syncthreads();
+    if (tid >= kHeadDim) return;
     const int d = tid;
     for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, red_ml[w * 16 + g].x);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[w * 16 + g].x);
         float num = 0.f, den = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < kConsumerWarps; ++w) {
             const float2 ml = red_ml[w * 16 + g];
             const float sc = exp2f(ml.x - M);   // warps without a valid token: 2^-inf = 0
-            num = fmaf(sc, red_o[(w * 16 + g) * kHeadDim + d], num);
+            num = fmaf(sc, red_o[(w * 16 + g) * kRedStride + d], num);
             den = fmaf(sc, ml.y, den);
         }
         const int h = hk * G + g;

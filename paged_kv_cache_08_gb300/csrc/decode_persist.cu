@@ -1,0 +1,730 @@
+// Paged decode attention: persistent, load-balanced, tensor-core kernel (one launch per call).
+//
+// What it computes ("显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §五.1): for every
+// sequence and query head, walk the sequence's logical blocks through its block-table row,
+// q.k for every cached token, softmax with a running maximum, weight V, normalise at the end.
+// Address rule: "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块",
+// section "注意力寻址：非连续物理块的间接寻址内核".
+//
+// Work decomposition.  A segment is one (sequence, kv head); it is cut into 64-token chunks.
+// All chunks of all segments form one list of N chunks (sequence-major); the grid holds as many
+// CTAs as can be resident at once, and CTA c streams the contiguous chunk range
+// [N c / C, N (c + 1) / C).  Every CTA therefore moves the same number of bytes, and its TMA
+// ring stays full across segment boundaries.  A segment that lies inside one CTA's range is
+// finished there; a segment cut by range boundaries leaves one partial (m, l, o) per CTA and
+// the last CTA to finish its piece (a per-segment arrival counter) merges the pieces.
+//
+// Inside a CTA: one producer warp issues, per chunk, the 2-D TMA tensor loads of the K and V
+// rows (128-byte swizzle) and, at the first chunk of a segment, a bulk copy of the segment's
+// query rows; four consumer warps each own 16 of the chunk's 64 tokens and run
+//   S = Q K^T and O += P V  with mma.sync m16n8k16 (fp32 accumulation),
+// keeping a running max / sum per query row.  At a segment's last chunk the four warps merge
+// through the stage buffer they just consumed.  Full / empty mbarriers per stage connect the
+// producer and the consumers; every wait is bounded.
+#include "pa_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+namespace pa {
+
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
+constexpr int kKVBytes = 2 * kKBytes;
+constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
+
+template <bool kG16>
+struct PLayout {
+    static constexpr int kQRows = kG16 ? 16 : 8;
+    static constexpr int kStageBytes = kKVBytes + kQRows * kHeadDim * 2;  // multiple of 1024
+    static constexpr size_t kRing = (size_t)kStages * kStageBytes;
+    static constexpr size_t kBars = kRing;            // full[kStages], empty[kStages], consumer barrier
+    static constexpr size_t kFlags = kBars + (2 * kStages + 1) * sizeof(uint64_t);
+    static constexpr size_t kPrefix = kFlags + 16;                 // int P[S + 1], then int L[S]
+    static size_t total(int num_seqs) {
+        return 1024 /*alignment slack*/ + kPrefix + (size_t)(2 * num_seqs + 1) * sizeof(int32_t);
+    }
+    static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-aligned");
+};
+static_assert(kConsumerWarps * 8 * kRedStride * 4 + kConsumerWarps * 8 * 8 <= kKVBytes, "merge scratch");
+
+struct MmaMaps {
+    CUtensorMap k;
+    CUtensorMap v;
+};
+
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+
+// Barrier of the 128 consumer threads on an mbarrier (every thread arrives, bounded wait), so
+// that a warp that gave up on a copy cannot leave the others waiting forever.  `phase` counts
+// completed barrier phases and is the same in every consumer thread.
+__device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase) {
+    mbar_arrive(bar);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase & 1u));
+    ++phase;
+    return ok;
+}
+
+__device__ __forceinline__ float ld_cg(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_cg2(const float2* p) {
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
+// Shared-memory line (128 bytes) of token t (0..63 of the chunk), column half h: a chunk holds
+// 64 / R boxes of [2 halves][R rows][64 columns], R = min(block_size, 64).
+__device__ __forceinline__ uint32_t line_of(int t, int h, int R_log2) {
+    const int R = 1 << R_log2;
+    return (uint32_t)(((t >> R_log2) << (R_log2 + 1)) + h * R + (t & (R - 1)));
+}
+
+// Byte address of 16-byte chunk c (0..15 over the 128 columns) of token t, 128-byte swizzle.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int t, int c, int R_log2) {
+    return base + line_of(t, c >> 3, R_log2) * 128u + ((uint32_t)((c & 7) ^ (t & 7)) << 4);
+}
+
+// CTA whose chunk range holds global chunk g: the largest c with floor(N c / C) <= g.
+__device__ __forceinline__ int cta_of(long long g, long long N, int C) {
+    return (int)(((g + 1) * (long long)C - 1) / N);
+}
+
+__device__ __forceinline__ long long range_begin(int c, long long N, int C) { return (N * c) / C; }
+
+// Largest s in [0, S) with P[s] <= g (skips empty sequences because P repeats for them).
+__device__ __forceinline__ int seq_of(const int32_t* P, int S, long long g) {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)P[mid] <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct SegPos {
+    int s, h, k, n, L;  // sequence, kv head, chunk within the segment, chunks per segment, length
+};
+
+__device__ __forceinline__ SegPos locate(const int32_t* P, const int32_t* Lc, int S, int Hkv, long long g) {
+    SegPos p;
+    p.s = seq_of(P, S, g);
+    p.n = (P[p.s + 1] - P[p.s]) / Hkv;
+    const int r = (int)(g - P[p.s]);
+    p.h = r / p.n;
+    p.k = r - p.h * p.n;
+    p.L = Lc[p.s];
+    return p;
+}
+
+__device__ __forceinline__ void advance(SegPos& p, const int32_t* P, const int32_t* Lc, int S, int Hkv) {
+    if (++p.k < p.n) return;
+    p.k = 0;
+    if (++p.h < Hkv) return;
+    p.h = 0;
+    do {
+        ++p.s;
+    } while (p.s < S && P[p.s + 1] == P[p.s]);
+    if (p.s >= S) {   // past the last chunk: nothing left to read
+        p.n = 0;
+        p.L = 0;
+        return;
+    }
+    p.n = (P[p.s + 1] - P[p.s]) / Hkv;
+    p.L = Lc[p.s];
+}
+
+// Finish one segment piece at its last chunk in this CTA's range: merge the four consumer warps
+// through the stage buffer they have just consumed (`scratch`, 32 KB), then write the normalised
+// output (whole segment) or this CTA's partial (m, l, o); for a cut segment, the last CTA to
+// arrive merges all pieces.  Returns false if a barrier wait gave up.
+template <typename T, bool kG16>
+__device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
+                                              const int32_t* P, long long b_c, long long b_e, long long N, int C,
+                                              int c, const float (&o)[16][4], const float (&m_run)[2],
+                                              const float (&l_run)[2], uint64_t* cbar, uint32_t& cphase,
+                                              volatile int* last_flag) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
+    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
+    const long long Pseg = (long long)P[pos.s] + (long long)pos.h * pos.n;
+    const bool whole = (Pseg >= b_c) && (Pseg + pos.n <= b_e);
+    float lr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        lr[r] = l_run[r];
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
+    }
+    float* red_o = reinterpret_cast<float*>(scratch);                             // [4][8][kRedStride]
+    float2* red_ml = reinterpret_cast<float2*>(red_o + kConsumerWarps * 8 * kRedStride);  // [4][8]
+    const size_t piece = (size_t)c * 2 + ((Pseg <= b_c) ? 0 : 1);
+    if (!consumers_sync(cbar, cphase)) return false;   // every warp is past its reads of the stage
+    for (int rg = 0; rg < G; rg += 8) {
+        const bool hi = rg >= 8;   // rows 0..7 live in (c0, c1), rows 8..15 in (c2, c3)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float v0 = hi ? o[j][2] : o[j][0];
+            const float v1 = hi ? o[j][3] : o[j][1];
+            *reinterpret_cast<float2*>(&red_o[(warp * 8 + qr) * kRedStride + j * 8 + qc]) = make_float2(v0, v1);
+        }
+        if ((lane & 3) == 0)
+            red_ml[warp * 8 + qr] = hi ? make_float2(m_run[1], lr[1]) : make_float2(m_run[0], lr[0]);
+        if (!consumers_sync(cbar, cphase)) return false;
+        const int r = tid >> 4;            // row within the group of 8
+        const int d0 = (tid & 15) * 8;     // 8 columns per thread
+        const int row = rg + r;
+        if (row < G) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, red_ml[w2 * 8 + r].x);
+            float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float den = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+                const float2 ml = red_ml[w2 * 8 + r];
+                const float f = exp2f(ml.x - M);   // a warp without a valid token: 2^-inf = 0
+                den = fmaf(f, ml.y, den);
+                const float4 x0 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0]);
+                const float4 x1 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0 + 4]);
+                num[0] = fmaf(f, x0.x, num[0]);
+                num[1] = fmaf(f, x0.y, num[1]);
+                num[2] = fmaf(f, x0.z, num[2]);
+                num[3] = fmaf(f, x0.w, num[3]);
+                num[4] = fmaf(f, x1.x, num[4]);
+                num[5] = fmaf(f, x1.y, num[5]);
+                num[6] = fmaf(f, x1.z, num[6]);
+                num[7] = fmaf(f, x1.w, num[7]);
+            }
+            if (whole) {
+                const float inv = 1.f / den;
+                uint4 packed;
+                packed.x = Elem<T>::pack2(num[0] * inv, num[1] * inv);
+                packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
+                packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
+                packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
+                *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)pos.s * Hq + pos.h * G + row) * kHeadDim +
+                                          d0) = packed;
+            } else {
+                float* dst = a.part_o + (piece * kPieceRows + row) * kHeadDim + d0;
+                *reinterpret_cast<float4*>(dst) = make_float4(num[0], num[1], num[2], num[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(num[4], num[5], num[6], num[7]);
+                if ((tid & 15) == 0) a.part_ml[piece * kPieceRows + row] = make_float2(M, den);
+            }
+        }
+        if (!consumers_sync(cbar, cphase)) return false;   // the scratch is rewritten next
+    }
+    if (!whole) {
+        // ---- pieces of a cut segment: the last CTA to arrive merges them ----
+        __threadfence();
+        if (!consumers_sync(cbar, cphase)) return false;
+        const int sigma = pos.s * Hkv + pos.h;
+        const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + pos.n - 1, N, C);
+        if (tid == 0) {
+            const int prev = atomicAdd(&a.seg_counters[sigma], 1);
+            *last_flag = (prev == c_last - c_first) ? 1 : 0;
+        }
+        if (!consumers_sync(cbar, cphase)) return false;
+        const bool last = *last_flag != 0;
+        if (last) {
+            __threadfence();
+            for (int e = tid; e < G * 16; e += kConsumerThreads) {
+                const int row = e >> 4, d0 = (e & 15) * 8;
+                float M = -INFINITY;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
+                    M = fmaxf(M, ld_cg2(&a.part_ml[pc * kPieceRows + row]).x);
+                }
+                float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float den = 0.f;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
+                    const float2 ml = ld_cg2(&a.part_ml[pc * kPieceRows + row]);
+                    const float f = exp2f(ml.x - M);
+                    den = fmaf(f, ml.y, den);
+                    const float* src = a.part_o + (pc * kPieceRows + row) * kHeadDim + d0;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) num[q] = fmaf(f, ld_cg(src + q), num[q]);
+                }
+                const float inv = 1.f / den;
+                uint4 packed;
+                packed.x = Elem<T>::pack2(num[0] * inv, num[1] * inv);
+                packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
+                packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
+                packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
+                *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)pos.s * Hq + pos.h * G + row) * kHeadDim +
+                                          d0) = packed;
+            }
+            if (tid == 0) a.seg_counters[sigma] = 0;   // ready for the next call
+        }
+    }
+    fence_proxy_async_smem();   // generic writes to the stage precede its next TMA fill
+    return true;
+}
+
+template <typename T, bool kG16>
+__global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
+    decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
+    using Lay = PLayout<kG16>;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t ring = (raw + 1023u) & ~1023u;
+    unsigned char* base_ptr = smem_raw + (ring - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + Lay::kBars);
+    uint64_t* empty = full + kStages;
+    uint64_t* cbar = empty + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Lay::kFlags);
+    volatile int* issued_count = abort_flag + 1;
+    volatile int* last_flag = abort_flag + 2;
+    int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
+    const int S = a.num_seqs;
+    int32_t* Lc = P + S + 1;                                              // [S], clamped lengths
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv, B = a.block_size;
+    const int cap = a.max_blocks_per_seq * B;
+
+    if (tid == 0) {
+        prefetch_map(&maps.k);
+        prefetch_map(&maps.v);
+#pragma unroll
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerThreads);
+        }
+        mbar_init(cbar, kConsumerThreads);
+        *abort_flag = 0;
+        *issued_count = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    grid_dependency_wait();
+
+    // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) ----
+    {
+        const int per = (S + kThreads - 1) / kThreads;
+        const int lo = min(S, tid * per), hi = min(S, lo + per);
+        int local = 0;
+        for (int s = lo; s < hi; ++s) {
+            int L = a.context_lens[s];
+            if (L < 0 || L > cap) {
+                flag_status(a.status, PA_DEV_BAD_CONTEXT);
+                L = L < 0 ? 0 : cap;
+            }
+            Lc[s] = L;
+            local += (L + kStageTokens - 1) / kStageTokens;
+        }
+        // exclusive scan of `local` over the CTA
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        __shared__ int warp_tot[kThreads / 32];
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        int run = before + incl - local;
+        for (int s = lo; s < hi; ++s) {
+            P[s] = run * Hkv;
+            run += (Lc[s] + kStageTokens - 1) / kStageTokens;
+        }
+        if (tid == kThreads - 1) {
+            int tot = 0;
+            for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
+            P[S] = tot * Hkv;
+        }
+    }
+    __syncthreads();
+
+    // ---- empty sequences produce zero rows (no chunk covers them) ----
+    for (int s = c; s < S; s += (int)gridDim.x) {
+        if (P[s + 1] == P[s]) {
+            uint16_t* out = static_cast<uint16_t*>(a.out) + (size_t)s * Hq * kHeadDim;
+            for (int e = tid; e < Hq * kHeadDim; e += kThreads) out[e] = 0;
+        }
+    }
+
+    const long long N = P[S];
+    if (N == 0) return;
+    // C <= N CTAs take part, so that every one of them owns at least one chunk
+    const int C = (int)min((long long)gridDim.x, N);
+    if (c >= C) return;
+    const long long b_c = range_begin(c, N, C), b_e = range_begin(c + 1, N, C);
+    if (b_c >= b_e) return;
+    grid_launch_dependents();
+
+    if (warp == kConsumerWarps) {
+        // ================= producer warp =================
+        SegPos pos = locate(P, Lc, S, Hkv, b_c);
+        int i = 0;
+        bool ok = true;
+        for (long long g = b_c; g < b_e && ok; ++g, ++i) {
+            const int st = i % kStages;
+            if (i >= kStages) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    if (lane == 0) {
+                        flag_status(a.status, PA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+            }
+            // block ids of this chunk: lanes 0..3 fetch one entry each
+            const int t0 = pos.k * kStageTokens;
+            const int t1 = min(t0 + kStageTokens, pos.L);
+            const int first = t0 / B;
+            const int nblk = (t1 - 1) / B - first + 1;   // <= 64 / 16
+            int phys = -1;
+            if (lane < nblk) {
+                phys = a.block_tables[(size_t)pos.s * a.max_blocks_per_seq + first + lane];
+                if (phys < 0 || phys >= a.num_blocks) {
+                    flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                    phys = -1;
+                }
+            }
+            const unsigned valid = __ballot_sync(0xffffffffu, phys >= 0);
+            const bool load_q = (pos.k == 0) || (g == b_c);
+            int ids[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ids[j] = __shfl_sync(0xffffffffu, phys, j);
+            if (lane == 0) {
+                if (*abort_flag) {
+                    ok = false;
+                } else {
+                    const int R = 1 << R_log2;
+                    const uint32_t dst = ring + (uint32_t)st * Lay::kStageBytes;
+                    const int within = (B > kStageTokens) ? (t0 % B) : 0;
+                    uint32_t bytes = (uint32_t)__popc(valid) * 4u * (uint32_t)R * 128u;
+                    if (load_q) bytes += (uint32_t)G * kHeadDim * 2u;
+                    if (i >= kStages) fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (j < nblk && ids[j] >= 0) {
+                            const int row = (ids[j] * Hkv + pos.h) * B + within;
+                            const uint32_t box = dst + (uint32_t)(j * 2 * R) * 128u;
+                            tma_load_2d(box, &maps.k, 0, row, &full[st]);
+                            tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &full[st]);
+                            tma_load_2d(box + kKBytes, &maps.v, 0, row, &full[st]);
+                            tma_load_2d(box + kKBytes + (uint32_t)R * 128u, &maps.v, 64, row, &full[st]);
+                        }
+                    }
+                    if (load_q) {
+                        const T* qsrc = static_cast<const T*>(a.q) + ((size_t)pos.s * Hq + pos.h * G) * kHeadDim;
+                        bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            advance(pos, P, Lc, S, Hkv);
+        }
+        if (lane == 0) *issued_count = i;
+    } else {
+        // ================= consumer warps =================
+        const int qr = lane >> 2, qc = (lane & 3) * 2;
+        const int t_warp = warp * 16;
+        const int tk = t_warp + (lane & 7) + ((lane >> 4) << 3);
+        const int ck = (lane >> 3) & 1;
+        const int tv = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int cv = lane >> 4;
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};
+        float o[16][4];
+        uint32_t qa[8][4];
+        SegPos pos = locate(P, Lc, S, Hkv, b_c);
+        uint32_t cphase = 0;
+        int i = 0;
+        for (long long g = b_c; g < b_e; ++g, ++i) {
+            const int st = i % kStages;
+            const bool w = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (uint32_t)(i / kStages) & 1u));
+            if (!w) {
+                if (lane == 0) {
+                    flag_status(a.status, PA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            __syncwarp();
+            if (*abort_flag) break;
+            const uint32_t kbase = ring + (uint32_t)st * Lay::kStageBytes;
+            const uint32_t vbase = kbase + kKBytes;
+            const bool seg_begin = (pos.k == 0) || (g == b_c);
+            const bool seg_end = (pos.k == pos.n - 1) || (g == b_e - 1);
+            if (seg_begin) {
+                // query rows of the segment's G heads, as mma A fragments (rows >= G are zero)
+                const uint32_t* qs = reinterpret_cast<const uint32_t*>(base_ptr + (size_t)st * Lay::kStageBytes +
+                                                                       kKVBytes);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int wcol = (ks * 16 + qc) >> 1;
+                    qa[ks][0] = (qr < G) ? qs[qr * 64 + wcol] : 0u;
+                    qa[ks][2] = (qr < G) ? qs[qr * 64 + wcol + 4] : 0u;
+                    if (kG16) {
+                        qa[ks][1] = (qr + 8 < G) ? qs[(qr + 8) * 64 + wcol] : 0u;
+                        qa[ks][3] = (qr + 8 < G) ? qs[(qr + 8) * 64 + wcol + 4] : 0u;
+                    } else {
+                        qa[ks][1] = 0u;
+                        qa[ks][3] = 0u;
+                    }
+                }
+                m_run[0] = m_run[1] = -INFINITY;
+                l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+            }
+            const int nvalid = min(kStageTokens, pos.L - pos.k * kStageTokens);
+
+            if (t_warp < nvalid) {
+                if (nvalid < t_warp + 16) {
+                    uint4* vz = reinterpret_cast<uint4*>(base_ptr + (size_t)st * Lay::kStageBytes + kKBytes);
+                    for (int idx = lane; idx < (t_warp + 16 - nvalid) * 16; idx += 32) {
+                        const int t = nvalid + (idx >> 4);
+                        const int cc = idx & 15;
+                        vz[line_of(t, cc >> 3, R_log2) * 8 + (cc & 7)] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(chunk_addr(kbase, tk, 2 * ks + ck, R_log2), b0, b1, b2, b3);
+                    mma16816<T>(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                    mma16816<T>(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+                }
+                float p[2][4];
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = t_warp + n * 8 + qc + (e & 1);
+                        const float x = sc[n][e] * a.scale_log2;
+                        p[n][e] = (col < nvalid) ? x : -INFINITY;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], p[n][e]);
+                    }
+                float alpha[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                    const float m_new = fmaxf(m_run[r], mx[r]);
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    alpha[r] = exp2f(m_run[r] - m_use);
+                    m_run[r] = m_new;
+                    mx[r] = m_use;
+                }
+                float rs[2] = {0.f, 0.f};
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p[n][e] = exp2f(p[n][e] - mx[e >> 1]);
+                        rs[e >> 1] += p[n][e];
+                    }
+                l_run[0] = l_run[0] * alpha[0] + rs[0];
+                l_run[1] = l_run[1] * alpha[1] + rs[1];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    o[j][0] *= alpha[0];
+                    o[j][1] *= alpha[0];
+                    o[j][2] *= alpha[1];
+                    o[j][3] *= alpha[1];
+                }
+                const uint32_t pa0 = Elem<T>::pack2(p[0][0], p[0][1]);
+                const uint32_t pa1 = Elem<T>::pack2(p[0][2], p[0][3]);
+                const uint32_t pa2 = Elem<T>::pack2(p[1][0], p[1][1]);
+                const uint32_t pa3 = Elem<T>::pack2(p[1][2], p[1][3]);
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(chunk_addr(vbase, tv, 2 * np + cv, R_log2), b0, b1, b2, b3);
+                    mma16816<T>(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+                    mma16816<T>(o[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                }
+            }
+
+            if (seg_end && !flush_segment<T, kG16>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
+                                                      N, C, c, o, m_run, l_run, cbar, cphase, last_flag)) {
+                if (lane == 0) {
+                    flag_status(a.status, PA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            mbar_arrive(&empty[st]);   // this thread is done with the stage's buffers
+            advance(pos, P, Lc, S, Hkv);
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && tid == 0) {
+        // let every copy still in flight land before the CTA's shared memory is released
+        const int n = *issued_count;
+        for (int st = 0; st < kStages; ++st) {
+            int last = -1;
+            for (int i = st; i < n; i += kStages) last = i;
+            if (last >= 0) (void)mbar_wait_bounded(&full[st], (uint32_t)(last / kStages) & 1u);
+        }
+    }
+}
+
+// ---- host side ----
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::atomic<int> state{0};
+    if (state.load() == 0) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+        state.store(1);
+    }
+    return fn;
+}
+
+bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtensorMap* out) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, bool kG16>
+cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
+    static std::atomic<unsigned long long> configured{0};
+    auto kernel = decode_persist_kernel<T, kG16>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PLayout<kG16>::total(kPersistMaxSeqs));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PLayout<kG16>::total(a.num_seqs);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a, maps, R_log2);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
+
+}  // namespace
+
+int persist_ctas_per_sm(int group) { return group <= 8 ? 2 : 1; }
+
+cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t stream) {
+    const int R = a.block_size < kStageTokens ? a.block_size : kStageTokens;
+    int R_log2 = 0;
+    while ((1 << R_log2) < R) ++R_log2;
+    const unsigned long long rows = (unsigned long long)a.num_blocks * a.num_kv_heads * a.block_size;
+    if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
+    MmaMaps maps;
+    if (!encode_map(a.k_cache, rows, R, &maps.k) || !encode_map(a.v_cache, rows, R, &maps.v))
+        return cudaErrorInvalidValue;
+    const bool g16 = (a.num_q_heads / a.num_kv_heads) > 8;
+    if (dtype == PA_BF16)
+        return g16 ? launch_impl<__nv_bfloat16, true>(a, maps, R_log2, stream)
+                   : launch_impl<__nv_bfloat16, false>(a, maps, R_log2, stream);
+    return g16 ? launch_impl<__half, true>(a, maps, R_log2, stream)
+               : launch_impl<__half, false>(a, maps, R_log2, stream);
+}
+
+}  // namespace pa

@@ -13,6 +13,9 @@ namespace pa {
 constexpr int kHeadDim = 128;           // the only head size the pages use
 constexpr int kStageTokens = 64;        // tokens of K (and of V) staged per pipeline step
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // give a copy wait ~1 s
+constexpr int kMaxTableSlice = 1024;    // block-table entries of one split staged in shared memory
+constexpr int kPersistMaxSeqs = 1024;   // sequences whose prefix sums the persistent kernel keeps on chip
+constexpr int kPieceRows = 16;          // query rows per partial piece (the largest group), any G
 
 // ---------------------------------------------------------------------------------------
 // Arguments
@@ -50,6 +53,8 @@ struct DecodeArgs {
     int max_blocks_per_seq;
     int tokens_per_split;     // multiple of max(block_size, kStageTokens)
     int max_splits;
+    int* seg_counters;        // persistent path: per-(sequence, kv head) arrival counters, zero between calls
+    int num_ctas;             // persistent path: grid size
 };
 
 // ---------------------------------------------------------------------------------------
@@ -114,6 +119,10 @@ __device__ __forceinline__ void fence_mbar_init() {
 // order this CTA's earlier generic-proxy shared-memory accesses before later async-proxy ones
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -190,6 +199,10 @@ cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split_fma(const DecodeArgs& a, int dtype, int group, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t stream);
 bool fma_supports_group(int group);
+
+// Persistent load-balanced tensor-core kernel (G <= 16, num_seqs <= kPersistMaxSeqs); one launch.
+cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t stream);
+int persist_ctas_per_sm(int group);
 
 // Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.
 cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);

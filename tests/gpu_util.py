@@ -13,7 +13,7 @@ import paged_kv_cache_08_gb300 as pa
 TOL = 2e-3
 
 
-def run_cuda(wl, layer=0, tokens_per_split=0, math="auto", stream=None):
+def run_cuda(wl, layer=0, tokens_per_split=0, math="auto", stream=None, num_ctas=0):
     dev = torch.device("cuda")
     kc = wl.k_cache[layer].to(dev).clone()
     vc = wl.v_cache[layer].to(dev).clone()
@@ -22,7 +22,7 @@ def run_cuda(wl, layer=0, tokens_per_split=0, math="auto", stream=None):
     slots = torch.from_numpy(pa.build_slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)).to(dev)
     pa.cache_write(wl.k_new[layer].to(dev), wl.v_new[layer].to(dev), slots, kc, vc, stream=stream)
     out = pa.decode(wl.q[layer].to(dev), kc, vc, bt, lens, wl.scale, wl.num_kv_heads,
-                    tokens_per_split=tokens_per_split, math=math, stream=stream)
+                    tokens_per_split=tokens_per_split, math=math, num_ctas=num_ctas, stream=stream)
     torch.cuda.synchronize()
     return kc, vc, out
 

@@ -45,7 +45,7 @@ def test_decode_rejects_before_launch(lib):
     assert _decode(lib, dtype=5) == E["PA_ERR_INVALID_ARG"]
     assert _decode(lib, out=None) == E["PA_ERR_INVALID_ARG"]      # null output
     assert _decode(lib, q=24) == E["PA_ERR_INVALID_ARG"]          # misaligned q
-    assert _decode(lib, hkv=1, hq=5) == E["PA_ERR_UNSUPPORTED"]   # no CUDA-core kernel for G=5
+    assert _decode(lib, hkv=1, hq=17) == E["PA_ERR_UNSUPPORTED"]  # G > 16: no kernel for that group
     assert _decode(lib, S=0) == 0                                 # empty batch: nothing to do
     # a long table needs a split workspace; none given
     assert _decode(lib, S=1, maxb=1024) == E["PA_ERR_WORKSPACE"]
@@ -72,5 +72,13 @@ def test_plan_and_workspace(lib):
     assert tps >= 128 * 32
     assert pa.decode_workspace_size(4096, 32, 32, 128, 32, 128) == 0
     # forced splits -> (S * Hq * splits) partial rows of 128 floats + (m, l)
-    ws = pa.decode_workspace_size(2, 4, 2, 128, 16, 64, tokens_per_split=256)
+    ws = pa.decode_workspace_size(2, 4, 2, 128, 16, 64, tokens_per_split=256, math="fma")
     assert ws == 2 * 4 * 4 * (128 * 4 + 8)
+    # persistent kernel: 2 pieces per CTA of G rows, (m, l) per row, one counter per (seq, kv head)
+    ws = pa.decode_workspace_size(3, 4, 2, 128, 16, 64, num_ctas=10)
+    a256 = lambda n: (n + 255) // 256 * 256
+    assert ws == a256(10 * 2 * 16 * 128 * 4) + a256(10 * 2 * 16 * 8) + a256(3 * 2 * 4)
+    assert pa.kernel_kind(3, 4, 2) == 2 and pa.kernel_kind(3, 4, 2, math="fma") == 1
+    assert pa.kernel_kind(2000, 4, 2) == 3           # too many sequences for the on-chip prefix sums
+    with pytest.raises(pa.PAError):
+        pa.kernel_kind(3, 17, 1)                     # G = 17: no kernel
