@@ -85,6 +85,11 @@ typedef struct {
                                     max(block_size, 64), at most 1024 * block_size */
     int math;                    /* a pa_math value */
     int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once */
+    unsigned long long* timeline;/* persistent kernel trace, NULL = off; else device memory of
+                                    num_ctas * 16 uint64: per CTA, (global ns, SM clock) pairs at
+                                    entry, after the dependency wait, after the prefix sums, first
+                                    copy issued, first chunk landed, last chunk done, exit; slot 14 =
+                                    chunks streamed.  Entries of CTAs that own no chunk stay as set. */
 } pa_decode_options;
 
 /* ------------------------------------------------------------------------------------

@@ -46,10 +46,11 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def _opts(tokens_per_split: int, math: str, num_ctas: int = 0) -> DecodeOptions:
+def _opts(tokens_per_split: int, math: str, num_ctas: int = 0, timeline: Optional[torch.Tensor] = None) -> DecodeOptions:
     if math not in MATH:
         raise ValueError(f"math must be one of {sorted(MATH)}")
-    return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas))
+    return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas),
+                         timeline.data_ptr() if timeline is not None else None)
 
 
 def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
@@ -116,9 +117,11 @@ def _workspace(device: torch.device, nbytes: int, kind: int, num_ctas: int) -> O
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, scale: float, num_kv_heads: int, out: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, tokens_per_split: int = 0, math: str = "auto",
-           num_ctas: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+           num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
+           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Paged decode attention.  q: [S, Hq, D]; caches [NB, Hkv, B, D]; block_tables int32
-    [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype."""
+    [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype.
+    ``timeline``: optional int64 CUDA tensor [num_ctas, 16] receiving the persistent kernel's trace."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -139,7 +142,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(tokens_per_split, math, num_ctas)
+    o = _opts(tokens_per_split, math, num_ctas, timeline)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))

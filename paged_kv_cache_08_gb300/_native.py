@@ -22,7 +22,7 @@ c_u32p = ctypes.POINTER(ctypes.c_uint32)
 
 
 class DecodeOptions(ctypes.Structure):
-    _fields_ = [("tokens_per_split", c_int), ("math", c_int), ("num_ctas", c_int)]
+    _fields_ = [("tokens_per_split", c_int), ("math", c_int), ("num_ctas", c_int), ("timeline", c_vp)]
 
 
 PA_OK = 0

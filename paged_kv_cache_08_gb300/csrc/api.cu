@@ -318,6 +318,7 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
         a.seg_counters = reinterpret_cast<int*>(w + align256(pieces * kHeadDim * sizeof(float)) +
                                                 align256(pieces * sizeof(float2)));
         a.num_ctas = ctas;
+        a.timeline = opts ? opts->timeline : nullptr;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();

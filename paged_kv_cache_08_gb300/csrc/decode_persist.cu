@@ -202,6 +202,46 @@ __device__ __forceinline__ void advance(SegPos& p, const int32_t* P, const int32
     p.L = Lc[p.s];
 }
 
+// What the producer needs to issue one chunk's copies.
+struct ChunkDesc {
+    int s, h, t0, nblk, load_q;
+    int ids[4];   // physical blocks of the chunk (-1: none or outside the pool)
+};
+
+__device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t* P, const int32_t* Lc, int S,
+                                              int Hkv, long long b_c, long long b_e, long long g) {
+    ChunkDesc d;
+    d.s = 0;
+    d.h = 0;
+    d.t0 = 0;
+    d.nblk = 0;
+    d.load_q = 0;
+    d.ids[0] = d.ids[1] = d.ids[2] = d.ids[3] = -1;
+    if (g >= b_e) return d;
+    const SegPos p = locate(P, Lc, S, Hkv, g);
+    const int B = a.block_size;
+    d.s = p.s;
+    d.h = p.h;
+    d.t0 = p.k * kStageTokens;
+    const int t1 = min(d.t0 + kStageTokens, p.L);
+    const int first = d.t0 / B;
+    d.nblk = (t1 - 1) / B - first + 1;   // <= 64 / 16
+    d.load_q = (p.k == 0) || (g == b_c);
+    const int32_t* row = a.block_tables + (size_t)p.s * a.max_blocks_per_seq + first;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (e < d.nblk) {
+            const int id = row[e];
+            if (id >= 0 && id < a.num_blocks) {
+                d.ids[e] = id;
+            } else {
+                flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            }
+        }
+    }
+    return d;
+}
+
 // Finish one segment piece at its last chunk in this CTA's range: merge the four consumer warps
 // through the stage buffer they have just consumed (`scratch`, 32 KB), then write the normalised
 // output (whole segment) or this CTA's partial (m, l, o); for a cut segment, the last CTA to
@@ -354,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
     const int cap = a.max_blocks_per_seq * B;
 
     if (tid == 0) {
+        trace(a.timeline, c, 0);
         prefetch_map(&maps.k);
         prefetch_map(&maps.v);
 #pragma unroll
@@ -368,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
         fence_mbar_init();
     }
     grid_dependency_wait();
+    if (tid == 0) trace(a.timeline, c, 1);
 
     // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) ----
     {
@@ -416,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
         }
     }
 
+    if (tid == 0) trace(a.timeline, c, 2);
     const long long N = P[S];
     if (N == 0) return;
     // C <= N CTAs take part, so that every one of them owns at least one chunk
@@ -427,72 +470,73 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
 
     if (warp == kConsumerWarps) {
         // ================= producer warp =================
-        SegPos pos = locate(P, Lc, S, Hkv, b_c);
+        // Lane j describes chunk gbase + j (segment position and physical block ids); the next
+        // group's descriptors are loaded while this group's copies are issued, so the ring is
+        // refilled as soon as a stage frees up.
+        ChunkDesc cur = describe(a, P, Lc, S, Hkv, b_c, b_e, b_c + lane);
         int i = 0;
         bool ok = true;
-        for (long long g = b_c; g < b_e && ok; ++g, ++i) {
-            const int st = i % kStages;
-            if (i >= kStages) {
-                bool w = true;
-                if (lane == 0) w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
-                w = __shfl_sync(0xffffffffu, w, 0);
-                if (!w) {
-                    if (lane == 0) {
-                        flag_status(a.status, PA_DEV_TIMEOUT);
-                        *abort_flag = 1;
+        for (long long gbase = b_c; gbase < b_e && ok; gbase += 32) {
+            const ChunkDesc nxt = describe(a, P, Lc, S, Hkv, b_c, b_e, gbase + 32 + lane);
+            const int cnt = (int)min(32LL, b_e - gbase);
+            for (int j = 0; j < cnt; ++j, ++i) {
+                const int st = i % kStages;
+                if (i >= kStages) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) {
+                        if (lane == 0) {
+                            flag_status(a.status, PA_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
                     }
-                    ok = false;
-                    break;
                 }
-            }
-            // block ids of this chunk: lanes 0..3 fetch one entry each
-            const int t0 = pos.k * kStageTokens;
-            const int t1 = min(t0 + kStageTokens, pos.L);
-            const int first = t0 / B;
-            const int nblk = (t1 - 1) / B - first + 1;   // <= 64 / 16
-            int phys = -1;
-            if (lane < nblk) {
-                phys = a.block_tables[(size_t)pos.s * a.max_blocks_per_seq + first + lane];
-                if (phys < 0 || phys >= a.num_blocks) {
-                    flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
-                    phys = -1;
-                }
-            }
-            const unsigned valid = __ballot_sync(0xffffffffu, phys >= 0);
-            const bool load_q = (pos.k == 0) || (g == b_c);
-            int ids[4];
+                const int s_j = __shfl_sync(0xffffffffu, cur.s, j);
+                const int h_j = __shfl_sync(0xffffffffu, cur.h, j);
+                const int t0_j = __shfl_sync(0xffffffffu, cur.t0, j);
+                const int nblk_j = __shfl_sync(0xffffffffu, cur.nblk, j);
+                const int loadq_j = __shfl_sync(0xffffffffu, cur.load_q, j);
+                int ids[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ids[j] = __shfl_sync(0xffffffffu, phys, j);
-            if (lane == 0) {
-                if (*abort_flag) {
-                    ok = false;
-                } else {
-                    const int R = 1 << R_log2;
-                    const uint32_t dst = ring + (uint32_t)st * Lay::kStageBytes;
-                    const int within = (B > kStageTokens) ? (t0 % B) : 0;
-                    uint32_t bytes = (uint32_t)__popc(valid) * 4u * (uint32_t)R * 128u;
-                    if (load_q) bytes += (uint32_t)G * kHeadDim * 2u;
-                    if (i >= kStages) fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&full[st], bytes);
+                for (int e = 0; e < 4; ++e) ids[e] = __shfl_sync(0xffffffffu, cur.ids[e], j);
+                if (lane == 0) {
+                    if (*abort_flag) {
+                        ok = false;
+                    } else {
+                        const int R = 1 << R_log2;
+                        const uint32_t dst = ring + (uint32_t)st * Lay::kStageBytes;
+                        const int within = (B > kStageTokens) ? (t0_j % B) : 0;
+                        uint32_t bytes = loadq_j ? (uint32_t)G * kHeadDim * 2u : 0u;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (j < nblk && ids[j] >= 0) {
-                            const int row = (ids[j] * Hkv + pos.h) * B + within;
-                            const uint32_t box = dst + (uint32_t)(j * 2 * R) * 128u;
-                            tma_load_2d(box, &maps.k, 0, row, &full[st]);
-                            tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &full[st]);
-                            tma_load_2d(box + kKBytes, &maps.v, 0, row, &full[st]);
-                            tma_load_2d(box + kKBytes + (uint32_t)R * 128u, &maps.v, 64, row, &full[st]);
+                        for (int e = 0; e < 4; ++e)
+                            if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
+                        if (i >= kStages) fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (e < nblk_j && ids[e] >= 0) {
+                                const int row = (ids[e] * Hkv + h_j) * B + within;
+                                const uint32_t box = dst + (uint32_t)(e * 2 * R) * 128u;
+                                tma_load_2d(box, &maps.k, 0, row, &full[st]);
+                                tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &full[st]);
+                                tma_load_2d(box + kKBytes, &maps.v, 0, row, &full[st]);
+                                tma_load_2d(box + kKBytes + (uint32_t)R * 128u, &maps.v, 64, row, &full[st]);
+                            }
+                        }
+                        if (i == 0) trace(a.timeline, c, 3);
+                        if (loadq_j) {
+                            const T* qsrc = static_cast<const T*>(a.q) + ((size_t)s_j * Hq + h_j * G) * kHeadDim;
+                            bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
                         }
                     }
-                    if (load_q) {
-                        const T* qsrc = static_cast<const T*>(a.q) + ((size_t)pos.s * Hq + pos.h * G) * kHeadDim;
-                        bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
-                    }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            advance(pos, P, Lc, S, Hkv);
+            cur = nxt;
         }
         if (lane == 0) *issued_count = i;
     } else {
@@ -521,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                 break;
             }
             __syncwarp();
+            if (i == 0 && tid == 0) trace(a.timeline, c, 4);
             if (*abort_flag) break;
             const uint32_t kbase = ring + (uint32_t)st * Lay::kStageBytes;
             const uint32_t vbase = kbase + kKBytes;
@@ -632,9 +677,14 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
             mbar_arrive(&empty[st]);   // this thread is done with the stage's buffers
             advance(pos, P, Lc, S, Hkv);
         }
+        if (tid == 0) trace(a.timeline, c, 5);
     }
 
     __syncthreads();
+    if (tid == 0) {
+        trace(a.timeline, c, 6);
+        if (a.timeline) a.timeline[(size_t)c * kTimelineSlots + 14] = (unsigned long long)(b_e - b_c);
+    }
     if (*abort_flag && tid == 0) {
         // let every copy still in flight land before the CTA's shared memory is released
         const int n = *issued_count;

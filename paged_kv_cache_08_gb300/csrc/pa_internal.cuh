@@ -55,7 +55,10 @@ struct DecodeArgs {
     int max_splits;
     int* seg_counters;        // persistent path: per-(sequence, kv head) arrival counters, zero between calls
     int num_ctas;             // persistent path: grid size
+    unsigned long long* timeline;  // optional trace: [num_ctas][kTimelineSlots] (see pa.h); null = off
 };
+
+constexpr int kTimelineSlots = 16;
 
 // ---------------------------------------------------------------------------------------
 // Element types
@@ -171,6 +174,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Trace point: global time (ns) and SM clock of event `ev` of CTA `cta`, when tracing is on.
+__device__ __forceinline__ void trace(unsigned long long* tl, int cta, int ev) {
+    if (tl) {
+        unsigned long long t, c;
+        asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+        asm volatile("mov.u64 %0, %clock64;" : "=l"(c));
+        tl[(size_t)cta * kTimelineSlots + 2 * ev] = t;
+        tl[(size_t)cta * kTimelineSlots + 2 * ev + 1] = c;
+    }
 }
 
 __device__ __forceinline__ void flag_status(unsigned int* status, unsigned int bits) {
