@@ -60,7 +60,8 @@ typedef enum {
     PA_ERR_POOL_EXHAUSTED = -4,  /* the host pool has no free block */
     PA_ERR_DEVICE_TIMEOUT = -5,  /* reserved for waits that gave up (see status bits) */
     PA_ERR_BOUNDS = -6,          /* a host-side index outside its range */
-    PA_ERR_WORKSPACE = -7        /* workspace missing or smaller than required */
+    PA_ERR_WORKSPACE = -7,       /* workspace missing or smaller than required */
+    PA_ERR_SCRATCH_LIMIT = -8    /* pa_decode_static: the problem needs more than its fixed scratch */
 } pa_status;
 
 /* Bits of the per-device status word (pa_read_device_status). */
@@ -136,6 +137,33 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
               int max_blocks_per_seq, int dtype,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * pa_decode_static  [no counterpart on the pages: an allocation-free calling form]
+ * pa_decode for callers that cannot allocate device memory: code that runs where it
+ * does not own an allocator (a plugin or custom op inside a host framework whose
+ * memory pool is reserved and managed by that framework), and real-time or
+ * certified deployments that forbid device allocation after start-up.  Same inputs,
+ * outputs and results as pa_decode; the scratch (partial results and arrival
+ * counters) lives in one file-scope device array of PA_DECODE_STATIC_SCRATCH_BYTES
+ * per GPU, held from the library's first use on that GPU until the process exits.
+ * No call allocates or frees memory.
+ *   - The first call on a device looks up that array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Problems whose scratch would not fit return PA_ERR_SCRATCH_LIMIT (see
+ *     pa_decode_workspace_size for the requirement).
+ *   - Every call shares the array and finds the previous call's contents; the call
+ *     clears what has to start at zero.  Calls that may overlap on the GPU (other
+ *     streams, other host threads) race on the array: serialise them.
+ * Returns the codes of pa_decode, or PA_ERR_SCRATCH_LIMIT.
+ * ---------------------------------------------------------------------------------- */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+int pa_decode_static(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     float scale, int num_kv_heads,
+                     int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                     int max_blocks_per_seq, int dtype, void* stream);
 
 /* Bytes of workspace pa_decode needs for this shape on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -28,7 +28,7 @@ class DecodeOptions(ctypes.Structure):
 PA_OK = 0
 STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "PA_ERR_CUDA",
           -4: "PA_ERR_POOL_EXHAUSTED", -5: "PA_ERR_DEVICE_TIMEOUT", -6: "PA_ERR_BOUNDS",
-          -7: "PA_ERR_WORKSPACE"}
+          -7: "PA_ERR_WORKSPACE", -8: "PA_ERR_SCRATCH_LIMIT"}
 DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 
@@ -38,6 +38,8 @@ _SIGNATURES = {
                           c_int, c_int, c_vp, c_size, c_vp]),
     "pa_decode_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int, c_int,
                              c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_static": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int,
+                                 c_int, c_int, c_int, c_vp]),
     "pa_decode_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pa_decode_workspace_size_ex": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int,
                                              ctypes.POINTER(DecodeOptions)]),

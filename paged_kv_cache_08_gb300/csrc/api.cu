@@ -139,6 +139,15 @@ int max_splits_for(int block_size, int max_blocks_per_seq, int tps) {
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 
+bool persist_counter_region(int num_seqs, int num_kv_heads, int group, const pa_decode_options* opts,
+                            size_t* offset, size_t* bytes) {
+    const int ctas = persist_ctas(group, opts);
+    const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+    *offset = align256(pieces * kHeadDim * sizeof(float)) + align256(pieces * sizeof(float2));
+    *bytes = (size_t)num_seqs * num_kv_heads * sizeof(int);
+    return true;
+}
+
 unsigned int* device_status_ptr() {
     const int dev = current_device();
     if (dev < 0) return nullptr;
@@ -170,6 +179,7 @@ const char* pa_status_string(int status) {
         case PA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case PA_ERR_BOUNDS: return "index out of bounds";
         case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than pa_decode_static's fixed array holds";
         default: return "unknown status";
     }
 }

@@ -222,6 +222,10 @@ int persist_ctas_per_sm(int group);
 cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
 bool mma_supports_group(int group);
 
+// Where the persistent kernel keeps its arrival counters inside a workspace (api.cu).
+bool persist_counter_region(int num_seqs, int num_kv_heads, int group, const pa_decode_options* opts,
+                            size_t* offset, size_t* bytes);
+
 // Launch-count bookkeeping (api.cu).
 void note_launches(int n);
 
