@@ -127,9 +127,13 @@ def measured_peak_gbs():
 # ------------------------------------------------------------------------------------------
 
 class Step:
-    """All device buffers of one bench step plus the captured CUDA graph."""
+    """All device buffers of one bench step plus the captured CUDA graph.
 
-    def __init__(self, wl, device):
+    ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
+    otherwise pa_cache_write followed by pa_decode."""
+
+    def __init__(self, wl, device, fused: bool = True):
+        self.fused = fused
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
         self.wl = wl
@@ -149,11 +153,16 @@ class Step:
 
     def launch_layer(self, i, ev_pair=None):
         wl, pa = self.wl, self.pa
-        pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
+        if not self.fused:
+            pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
         if ev_pair is not None:
             ev_pair[0].record()
-        pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
-                  out=self.out[i], workspace=self.ws)
+        if self.fused:
+            pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
+                             wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws)
+        else:
+            pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
+                      out=self.out[i], workspace=self.ws)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -203,17 +212,19 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workloads.config(2, device=dev, layers=args.layers)
-    st = Step(wl, dev)
+    import paged_kv_cache_08_gb300 as pa
+    kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
+    fused = args.path == "fused" and kind == 2
+    st = Step(wl, dev, fused=fused)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
     kv_tokens = wl.layers * wl.total_context_tokens()
 
     st.capture()
-    import paged_kv_cache_08_gb300 as pa
-    kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     split_combine = kind != 2 and st.tps < wl.max_blocks_per_seq * wl.block_size
-    launches_per_step = wl.layers * (2 + (1 if split_combine else 0))   # cache write + decode (+ combine)
+    # fused: one launch per layer; else cache write + decode (+ combine)
+    launches_per_step = wl.layers * (1 if fused else 2 + (1 if split_combine else 0))
 
     for _ in range(args.warmup):
         st.replay()
@@ -246,9 +257,11 @@ def run_ours(args):
     roof = None
     if decode_ms:
         avg_ms = statistics.mean(decode_ms)
-        achieved = d_bytes / (avg_ms * 1e-3) / 1e9
+        kernel_bytes = d_bytes + (c_bytes if fused else 0)   # the fused kernel also moves the new rows
+        achieved = kernel_bytes / (avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "pa_decode",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "pa_decode_append" if fused else "pa_decode",
                 "avg_launch_us": round(avg_ms * 1e3, 2), "peak_source": f"{peak_kind} copy bandwidth",
                 "frac_of_8TBs_spec": round(achieved / SPEC_PEAK_GBS, 4)}
 
@@ -269,6 +282,8 @@ def run_ours(args):
                        "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_blocks": wl.num_blocks,
                        "decode_kernel": {1: "split grid, CUDA cores", 2: "persistent, tensor cores",
                                          3: "split grid, tensor cores"}[kind],
+                       "step": ("pa_decode_append per layer (cache write fused)" if fused
+                                else "pa_cache_write + pa_decode per layer"),
                        "l2": "inputs larger than L2: 24 distinct layer caches (%.2f GB) read once per step"
                              % (2 * sum(t.numel() * 2 for t in wl.k_cache) / 1e9),
                        "parallelism": f"replicas x{world}", "cuda_graph": True},
@@ -407,6 +422,7 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -86,6 +86,8 @@ typedef struct {
                                     max(block_size, 64), at most 1024 * block_size */
     int math;                    /* a pa_math value */
     int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once */
+    int flags;                   /* PA_DECODE_NO_EARLY_READS: pa_decode_append reads nothing before
+                                    the preceding kernel in the stream has finished */
     unsigned long long* timeline;/* persistent kernel trace, NULL = off; else device memory of
                                     num_ctas * 16 uint64: per CTA, (global ns, SM clock) pairs at
                                     entry, after the dependency wait, after the prefix sums, first
@@ -164,6 +166,34 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
                      float scale, int num_kv_heads,
                      int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
                      int max_blocks_per_seq, int dtype, void* stream);
+
+#define PA_DECODE_NO_EARLY_READS 1
+
+/* ------------------------------------------------------------------------------------
+ * pa_decode_append  [P4 §三 sequence diagram + §五.1; P1 address formula]
+ * One decode step of one layer in a single launch: the cache write of the newest token
+ * followed by decode attention over the whole context, i.e. the effect of
+ *   pa_cache_write(k_new, v_new, slot(s) = block_tables[s][(L-1)/B]*B + (L-1)%B, ...)
+ *   pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, ...)
+ * with L = context_lens[s] (sequences with L == 0 write nothing and get zero rows).
+ * k_new, v_new: [num_seqs][num_kv_heads][head_dim].  Workspace as for pa_decode (same
+ * size query, persistent kind).  Supported: the persistent kernel's shapes
+ * (pa_decode_kernel_kind == PA_KERNEL_PERSISTENT_MMA); else PA_ERR_UNSUPPORTED.
+ * Early reads: unless opts->flags has PA_DECODE_NO_EARLY_READS, the kernel may read
+ * context_lens, block_tables and the cached rows of earlier tokens before the preceding
+ * kernel in the stream has finished (so that, launched back to back, one layer's start
+ * overlaps the previous layer's end); q, k_new and v_new are read, and out, the new slots
+ * and the workspace written, only after it has finished.  The caller guarantees that the
+ * preceding kernel does not write the caches, the tables or the lengths.
+ * ---------------------------------------------------------------------------------- */
+int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                     void* k_cache, void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     float scale, int num_kv_heads,
+                     int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                     int max_blocks_per_seq, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream,
+                     const pa_decode_options* opts);
 
 /* Bytes of workspace pa_decode needs for this shape on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

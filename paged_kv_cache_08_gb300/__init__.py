@@ -21,7 +21,7 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "decode", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
+__all__ = ["cache_write", "decode", "decode_append", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
 
@@ -46,10 +46,11 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def _opts(tokens_per_split: int, math: str, num_ctas: int = 0, timeline: Optional[torch.Tensor] = None) -> DecodeOptions:
+def _opts(tokens_per_split: int, math: str, num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
+          flags: int = 0) -> DecodeOptions:
     if math not in MATH:
         raise ValueError(f"math must be one of {sorted(MATH)}")
-    return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas),
+    return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas), int(flags),
                          timeline.data_ptr() if timeline is not None else None)
 
 
@@ -154,6 +155,49 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
                             S, Hq, D, B, NB, max_blocks, _DTYPE[q.dtype], ws_ptr, ws_bytes, _stream_ptr(stream),
                             ctypes.byref(o))
     _native.check("pa_decode", rc)
+    return out
+
+
+def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                  num_kv_heads: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  num_ctas: int = 0, early_reads: bool = True, timeline: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Cache write of each sequence's newest token (position context_lens[s] - 1) and decode
+    attention, in one launch.  k_new, v_new: [S, Hkv, D].  See pa_decode_append in include/pa.h
+    for the early-read contract (disable with early_reads=False)."""
+    _need_cuda("q", q)
+    if q.dtype not in _DTYPE:
+        raise TypeError("q must be float16 or bfloat16")
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if Hkv != num_kv_heads or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape does not match q / num_kv_heads")
+    if k_new.shape != (S, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [S, Hkv, D]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("block_tables / context_lens do not match q")
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+    o = _opts(0, "mma", num_ctas, timeline, 0 if early_reads else _native.NO_EARLY_READS)
+    need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
+    if workspace is None:
+        kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))
+        workspace = _workspace(q.device, need, kind, int(num_ctas))
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_decode_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                context_lens.data_ptr(), float(scale), int(num_kv_heads), S, Hq, D, B, NB,
+                                max_blocks, _DTYPE[q.dtype], ws_ptr, ws_bytes, _stream_ptr(stream), ctypes.byref(o))
+    _native.check("pa_decode_append", rc)
     return out
 
 

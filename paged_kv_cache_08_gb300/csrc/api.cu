@@ -139,6 +139,8 @@ int max_splits_for(int block_size, int max_blocks_per_seq, int tps) {
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 
+int sm_count_current() { return sm_count(); }
+
 bool persist_counter_region(int num_seqs, int num_kv_heads, int group, const pa_decode_options* opts,
                             size_t* offset, size_t* bytes) {
     const int ctas = persist_ctas(group, opts);
@@ -278,10 +280,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                        max_blocks_per_seq, nullptr);
 }
 
-int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                 const int32_t* context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
-                 int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
-                 size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
+static int decode_impl(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, const int32_t* context_lens, float scale,
+                       int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                       int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                       const pa_decode_options* opts) {
+    const bool append = k_new != nullptr;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
     if (rc != PA_OK) return rc;
@@ -298,6 +302,10 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     Path path;
     rc = choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path);
     if (rc != PA_OK) return rc;
+    if (append) {
+        if (path != kPathPersist) return PA_ERR_UNSUPPORTED;
+        if (!v_new || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    }
 
     DecodeArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -329,6 +337,9 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
                                                 align256(pieces * sizeof(float2)));
         a.num_ctas = ctas;
         a.timeline = opts ? opts->timeline : nullptr;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.early = (append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS))) ? 1 : 0;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();
@@ -356,6 +367,26 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
         return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 const int32_t* context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                 int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
+                 size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
+    return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
+                       workspace_bytes, stream, opts);
+}
+
+int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens, float scale, int num_kv_heads,
+                     int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                     int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                     const pa_decode_options* opts) {
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
+                       workspace_bytes, stream, opts);
 }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -34,22 +34,29 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 6;
 constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kKVBytes = 2 * kKBytes;
 constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
 
-template <bool kG16>
+// Shared-memory layout for a ring of kStages 64-token stages: 3 stages let two CTAs share an
+// SM, 6 stages give one CTA the whole SM.
+template <bool kG16, int kStages>
 struct PLayout {
     static constexpr int kQRows = kG16 ? 16 : 8;
     static constexpr int kStageBytes = kKVBytes + kQRows * kHeadDim * 2;  // multiple of 1024
     static constexpr size_t kRing = (size_t)kStages * kStageBytes;
-    static constexpr size_t kBars = kRing;            // full[kStages], empty[kStages], consumer barrier
-    static constexpr size_t kFlags = kBars + (2 * kStages + 1) * sizeof(uint64_t);
-    static constexpr size_t kPrefix = kFlags + 16;                 // int P[S + 1], then int L[S]
-    static size_t total(int num_seqs) {
+    static constexpr size_t kBars = kRing;   // full[kStages], empty[kStages], consumer barrier, q barrier
+    static constexpr size_t kFlags = kBars + (2 * kStages + 2) * sizeof(uint64_t);
+    static constexpr size_t kNewPhys = kFlags + 16;   // int [kStages] block of the new token, then
+                                                       // int [kStages] deferred q rows (s * Hkv + h)
+    static constexpr size_t kPrefix = kNewPhys + ((2 * kStages * sizeof(int32_t) + 15) & ~size_t(15));
+    // then int P[S + 1], int L[S]
+    static constexpr size_t total(int num_seqs) {
         return 1024 /*alignment slack*/ + kPrefix + (size_t)(2 * num_seqs + 1) * sizeof(int32_t);
     }
+    static_assert(1024 + kPrefix + (2 * kPersistMaxSeqs + 1) * sizeof(int32_t) <= 227 * 1024,
+                  "one CTA's shared memory must fit in 227 KB");
     static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-aligned");
 };
 static_assert(kConsumerWarps * 8 * kRedStride * 4 + kConsumerWarps * 8 * 8 <= kKVBytes, "merge scratch");
@@ -109,6 +116,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      dst),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
@@ -206,6 +218,7 @@ __device__ __forceinline__ void advance(SegPos& p, const int32_t* P, const int32
 struct ChunkDesc {
     int s, h, t0, nblk, load_q;
     int ids[4];   // physical blocks of the chunk (-1: none or outside the pool)
+    int newblk;   // physical block of token L - 1 when this chunk holds it, else -1
 };
 
 __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t* P, const int32_t* Lc, int S,
@@ -217,6 +230,7 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
     d.nblk = 0;
     d.load_q = 0;
     d.ids[0] = d.ids[1] = d.ids[2] = d.ids[3] = -1;
+    d.newblk = -1;
     if (g >= b_e) return d;
     const SegPos p = locate(P, Lc, S, Hkv, g);
     const int B = a.block_size;
@@ -239,14 +253,30 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
             }
         }
     }
+    if (t1 == p.L) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e == d.nblk - 1) d.newblk = d.ids[e];
+    }
     return d;
+}
+
+// Zero output rows of the empty sequences this CTA is responsible for (s = c, c + grid, ...).
+__device__ __forceinline__ void zero_empty_rows(const DecodeArgs& a, const int32_t* P, int c, int t, int nthreads) {
+    const int Hq = a.num_q_heads;
+    for (int s = c; s < a.num_seqs; s += (int)gridDim.x) {
+        if (P[s + 1] == P[s]) {
+            uint16_t* out = static_cast<uint16_t*>(a.out) + (size_t)s * Hq * kHeadDim;
+            for (int e = t; e < Hq * kHeadDim; e += nthreads) out[e] = 0;
+        }
+    }
 }
 
 // Finish one segment piece at its last chunk in this CTA's range: merge the four consumer warps
 // through the stage buffer they have just consumed (`scratch`, 32 KB), then write the normalised
 // output (whole segment) or this CTA's partial (m, l, o); for a cut segment, the last CTA to
 // arrive merges all pieces.  Returns false if a barrier wait gave up.
-template <typename T, bool kG16>
+template <typename T>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e, long long N, int C,
                                               int c, const float (&o)[16][4], const float (&m_run)[2],
@@ -370,10 +400,10 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     return true;
 }
 
-template <typename T, bool kG16>
-__global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
+template <typename T, bool kG16, int kStages>
+__global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
-    using Lay = PLayout<kG16>;
+    using Lay = PLayout<kG16, kStages>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -381,9 +411,11 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + Lay::kBars);
     uint64_t* empty = full + kStages;
     uint64_t* cbar = empty + kStages;
+    uint64_t* qbar = cbar + 1;   // q rows of the first kStages chunks (fetched after the dependency wait)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Lay::kFlags);
     volatile int* issued_count = abort_flag + 1;
     volatile int* last_flag = abort_flag + 2;
+    volatile int* new_phys = reinterpret_cast<volatile int*>(base_ptr + Lay::kNewPhys);
     int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
     const int S = a.num_seqs;
     int32_t* Lc = P + S + 1;                                              // [S], clamped lengths
@@ -403,12 +435,15 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
             mbar_init(&empty[i], kConsumerThreads);
         }
         mbar_init(cbar, kConsumerThreads);
+        mbar_init(qbar, 1);
         *abort_flag = 0;
         *issued_count = 0;
         *last_flag = 0;
         fence_mbar_init();
     }
-    grid_dependency_wait();
+    // Without the early contract every input may come from the preceding kernel: wait now.
+    // With it, lengths, tables and the cached rows are read first and the wait comes later.
+    if (!a.early) grid_dependency_wait();
     if (tid == 0) trace(a.timeline, c, 1);
 
     // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) ----
@@ -449,24 +484,19 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
         }
     }
     __syncthreads();
-
-    // ---- empty sequences produce zero rows (no chunk covers them) ----
-    for (int s = c; s < S; s += (int)gridDim.x) {
-        if (P[s + 1] == P[s]) {
-            uint16_t* out = static_cast<uint16_t*>(a.out) + (size_t)s * Hq * kHeadDim;
-            for (int e = tid; e < Hq * kHeadDim; e += kThreads) out[e] = 0;
-        }
-    }
-
     if (tid == 0) trace(a.timeline, c, 2);
+
     const long long N = P[S];
-    if (N == 0) return;
     // C <= N CTAs take part, so that every one of them owns at least one chunk
-    const int C = (int)min((long long)gridDim.x, N);
-    if (c >= C) return;
+    const int C = N > 0 ? (int)min((long long)gridDim.x, N) : 0;
+    if (c >= C) {
+        if (a.early) grid_dependency_wait();
+        grid_launch_dependents();
+        zero_empty_rows(a, P, c, tid, kThreads);
+        return;
+    }
     const long long b_c = range_begin(c, N, C), b_e = range_begin(c + 1, N, C);
-    if (b_c >= b_e) return;
-    grid_launch_dependents();
+    if (!a.early) grid_launch_dependents();
 
     if (warp == kConsumerWarps) {
         // ================= producer warp =================
@@ -474,6 +504,34 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
         // group's descriptors are loaded while this group's copies are issued, so the ring is
         // refilled as soon as a stage frees up.
         ChunkDesc cur = describe(a, P, Lc, S, Hkv, b_c, b_e, b_c + lane);
+        volatile int* qdef = new_phys + kStages;   // [kStages]: q rows the first stages still need
+        const bool append = a.k_new != nullptr;
+        bool deps_done = false;
+        // After the preceding kernel has finished (early mode), fetch the q rows of the first
+        // stages onto their own barrier: they may be that kernel's output.
+        auto dependency_point = [&](int issued) {
+            if (a.early) {
+                grid_dependency_wait();
+                grid_launch_dependents();
+            }
+            if (lane == 0) {
+                const int n = min(issued, kStages);
+                uint32_t bytes = 0;
+                for (int e = 0; e < n; ++e)
+                    if (qdef[e] >= 0) bytes += (uint32_t)G * kHeadDim * 2u;
+                mbar_arrive_expect_tx(qbar, bytes);
+                for (int e = 0; e < n; ++e) {
+                    const int sh = qdef[e];
+                    if (sh >= 0) {
+                        const T* qsrc = static_cast<const T*>(a.q) +
+                                        ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim;
+                        bulk_g2s(ring + (uint32_t)e * Lay::kStageBytes + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u,
+                                 qbar);
+                    }
+                }
+            }
+            __syncwarp();
+        };
         int i = 0;
         bool ok = true;
         for (long long gbase = b_c; gbase < b_e && ok; gbase += 32) {
@@ -481,6 +539,10 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
             const int cnt = (int)min(32LL, b_e - gbase);
             for (int j = 0; j < cnt; ++j, ++i) {
                 const int st = i % kStages;
+                if (i == kStages && !deps_done) {
+                    dependency_point(i);
+                    deps_done = true;
+                }
                 if (i >= kStages) {
                     bool w = true;
                     if (lane == 0) w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
@@ -499,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                 const int t0_j = __shfl_sync(0xffffffffu, cur.t0, j);
                 const int nblk_j = __shfl_sync(0xffffffffu, cur.nblk, j);
                 const int loadq_j = __shfl_sync(0xffffffffu, cur.load_q, j);
+                const int newblk_j = __shfl_sync(0xffffffffu, cur.newblk, j);
                 int ids[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ids[e] = __shfl_sync(0xffffffffu, cur.ids[e], j);
@@ -509,7 +572,10 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                         const int R = 1 << R_log2;
                         const uint32_t dst = ring + (uint32_t)st * Lay::kStageBytes;
                         const int within = (B > kStageTokens) ? (t0_j % B) : 0;
-                        uint32_t bytes = loadq_j ? (uint32_t)G * kHeadDim * 2u : 0u;
+                        const bool defer_q = i < kStages;   // fetched at the dependency point
+                        if (defer_q) qdef[i] = loadq_j ? s_j * Hkv + h_j : -1;
+                        new_phys[st] = append ? newblk_j : -1;
+                        uint32_t bytes = (loadq_j && !defer_q) ? (uint32_t)G * kHeadDim * 2u : 0u;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
@@ -527,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                             }
                         }
                         if (i == 0) trace(a.timeline, c, 3);
-                        if (loadq_j) {
+                        if (loadq_j && !defer_q) {
                             const T* qsrc = static_cast<const T*>(a.q) + ((size_t)s_j * Hq + h_j * G) * kHeadDim;
                             bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
                         }
@@ -538,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
             }
             cur = nxt;
         }
+        if (!deps_done) dependency_point(i);
         if (lane == 0) *issued_count = i;
     } else {
         // ================= consumer warps =================
@@ -551,6 +618,12 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
         float l_run[2] = {0.f, 0.f};
         float o[16][4];
         uint32_t qa[8][4];
+        if (a.early) {
+            grid_dependency_wait();   // q, the new rows and every output belong after this point
+            grid_launch_dependents();
+        }
+        zero_empty_rows(a, P, c, tid, kConsumerThreads);
+        const bool append = a.k_new != nullptr;
         SegPos pos = locate(P, Lc, S, Hkv, b_c);
         uint32_t cphase = 0;
         int i = 0;
@@ -571,6 +644,16 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
             const uint32_t vbase = kbase + kKBytes;
             const bool seg_begin = (pos.k == 0) || (g == b_c);
             const bool seg_end = (pos.k == pos.n - 1) || (g == b_e - 1);
+            if (seg_begin && i < kStages) {
+                // the first stages' q rows arrive on their own barrier
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(qbar, 0u))) {
+                    if (lane == 0) {
+                        flag_status(a.status, PA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+            }
             if (seg_begin) {
                 // query rows of the segment's G heads, as mma A fragments (rows >= G are zero)
                 const uint32_t* qs = reinterpret_cast<const uint32_t*>(base_ptr + (size_t)st * Lay::kStageBytes +
@@ -602,6 +685,24 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                         const int t = nvalid + (idx >> 4);
                         const int cc = idx & 15;
                         vz[line_of(t, cc >> 3, R_log2) * 8 + (cc & 7)] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const int tn = nvalid - 1;   // the newest token, when this is the segment's last chunk
+                if (append && pos.k == pos.n - 1 && (tn >> 4) == warp) {
+                    // append: the new K/V row goes into the staged tile and into its cache slot
+                    const int cc = lane & 15;
+                    const bool isv = lane >= 16;
+                    const size_t src_off = ((size_t)pos.s * Hkv + pos.h) * kHeadDim + cc * 8;
+                    const uint4 val = *reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) +
+                                                                      src_off);
+                    st_shared_v4(chunk_addr(isv ? vbase : kbase, tn, cc, R_log2), val);
+                    const int phys = new_phys[st];
+                    if (phys >= 0) {
+                        const size_t row = ((size_t)phys * Hkv + pos.h) * B + (size_t)((pos.L - 1) % B);
+                        T* cache = const_cast<T*>(static_cast<const T*>(isv ? a.v_cache : a.k_cache));
+                        *reinterpret_cast<uint4*>(cache + row * kHeadDim + cc * 8) = val;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -666,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, kG16 ? 1 : 2)
                 }
             }
 
-            if (seg_end && !flush_segment<T, kG16>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
+            if (seg_end && !flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
                                                       N, C, c, o, m_run, l_run, cbar, cphase, last_flag)) {
                 if (lane == 0) {
                     flag_status(a.status, PA_DEV_TIMEOUT);
@@ -727,24 +828,24 @@ bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtenso
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool kG16>
+template <typename T, bool kG16, int kStages>
 cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_persist_kernel<T, kG16>;
+    auto kernel = decode_persist_kernel<T, kG16, kStages>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)PLayout<kG16>::total(kPersistMaxSeqs));
+                                 (int)PLayout<kG16, kStages>::total(kPersistMaxSeqs));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = PLayout<kG16>::total(a.num_seqs);
+    cfg.dynamicSmemBytes = PLayout<kG16, kStages>::total(a.num_seqs);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -770,11 +871,18 @@ cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t s
     if (!encode_map(a.k_cache, rows, R, &maps.k) || !encode_map(a.v_cache, rows, R, &maps.v))
         return cudaErrorInvalidValue;
     const bool g16 = (a.num_q_heads / a.num_kv_heads) > 8;
-    if (dtype == PA_BF16)
-        return g16 ? launch_impl<__nv_bfloat16, true>(a, maps, R_log2, stream)
-                   : launch_impl<__nv_bfloat16, false>(a, maps, R_log2, stream);
-    return g16 ? launch_impl<__half, true>(a, maps, R_log2, stream)
-               : launch_impl<__half, false>(a, maps, R_log2, stream);
+    // as many CTAs as SMs (or fewer): one CTA per SM with the deep ring
+    const bool deep = a.num_ctas <= sm_count_current();
+    if (dtype == PA_BF16) {
+        if (g16) return deep ? launch_impl<__nv_bfloat16, true, 6>(a, maps, R_log2, stream)
+                             : launch_impl<__nv_bfloat16, true, 3>(a, maps, R_log2, stream);
+        return deep ? launch_impl<__nv_bfloat16, false, 6>(a, maps, R_log2, stream)
+                    : launch_impl<__nv_bfloat16, false, 3>(a, maps, R_log2, stream);
+    }
+    if (g16) return deep ? launch_impl<__half, true, 6>(a, maps, R_log2, stream)
+                         : launch_impl<__half, true, 3>(a, maps, R_log2, stream);
+    return deep ? launch_impl<__half, false, 6>(a, maps, R_log2, stream)
+                : launch_impl<__half, false, 3>(a, maps, R_log2, stream);
 }
 
 }  // namespace pa

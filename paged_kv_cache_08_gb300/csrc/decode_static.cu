@@ -44,7 +44,7 @@ extern "C" int pa_decode_static(void* out, const void* q, const void* k_cache, c
                                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                                 int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
                                 int num_blocks, int max_blocks_per_seq, int dtype, void* stream) {
-    pa_decode_options opts = {0, PA_MATH_AUTO, 0, nullptr};
+    pa_decode_options opts = {0, PA_MATH_AUTO, 0, 0, nullptr};
     const int kind = pa_decode_kernel_kind(num_seqs, num_q_heads, num_kv_heads, &opts);
     if (kind < 0) return kind;
     const size_t need = pa_decode_workspace_size_ex(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

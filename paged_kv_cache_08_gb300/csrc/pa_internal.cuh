@@ -56,6 +56,9 @@ struct DecodeArgs {
     int* seg_counters;        // persistent path: per-(sequence, kv head) arrival counters, zero between calls
     int num_ctas;             // persistent path: grid size
     unsigned long long* timeline;  // optional trace: [num_ctas][kTimelineSlots] (see pa.h); null = off
+    const void* k_new;        // append mode: the new token's K and V rows [S][Hkv][D], written at
+    const void* v_new;        //   position context_lens[s] - 1 before attention reads it; null = off
+    int early;                // K/V of the first stages may be fetched before the preceding kernel ends
 };
 
 constexpr int kTimelineSlots = 16;
@@ -228,6 +231,9 @@ bool persist_counter_region(int num_seqs, int num_kv_heads, int group, const pa_
 
 // Launch-count bookkeeping (api.cu).
 void note_launches(int n);
+
+// SM count of the current device (api.cu; 152 when no device is visible).
+int sm_count_current();
 
 // Status word address on the current device (api.cu).
 unsigned int* device_status_ptr();
