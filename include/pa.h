@@ -92,7 +92,7 @@ typedef struct {
                                     num_ctas * 16 uint64: per CTA, (global ns, SM clock) pairs at
                                     entry, after the dependency wait, after the prefix sums, first
                                     copy issued, first chunk landed, last chunk done, exit; slot 14 =
-                                    chunks streamed.  Entries of CTAs that own no chunk stay as set. */
+                                    chunks streamed, slot 15 = SM id.  Entries of CTAs that own no chunk stay as set. */
 } pa_decode_options;
 
 /* ------------------------------------------------------------------------------------
@@ -128,7 +128,7 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
  * owned by the caller, 16-byte aligned, ZERO-FILLED before its first use (see
  * pa_decode_workspace_init); every completed call leaves it ready for the next
  * one of any shape that runs the same kernel kind (pa_decode_kernel_kind) with the
- * same CTA count.  NULL is allowed when the size is 0.  Calls that share a
+ * same num_ctas option.  NULL is allowed when the size is 0.  Calls that share a
  * workspace must not overlap on the GPU.  After a call that set PA_DEV_TIMEOUT, or
  * before switching kernel kind or CTA count, zero it again.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or PA_ERR_CUDA.
@@ -160,7 +160,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *     streams, other host threads) race on the array: serialise them.
  * Returns the codes of pa_decode, or PA_ERR_SCRATCH_LIMIT.
  * ---------------------------------------------------------------------------------- */
-#define PA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+#define PA_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
 int pa_decode_static(void* out, const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_tables, const int32_t* context_lens,
                      float scale, int num_kv_heads,

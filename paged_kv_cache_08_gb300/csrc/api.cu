@@ -118,13 +118,23 @@ int persist_ctas(int group, const pa_decode_options* opts) {
     return persist_ctas_per_sm(group) * sm_count();
 }
 
+// CTA count the workspace layout is sized for: the requested count, or the largest default
+// grid (two CTAs per SM) whatever the group size, so that one workspace serves every shape.
+int persist_layout_ctas(const pa_decode_options* opts) {
+    if (opts && opts->num_ctas > 0) return opts->num_ctas;
+    return 2 * sm_count();
+}
+
 // Persistent-path workspace: [C][2][16][D] fp32 partial outputs, [C][2][16] (m, l), then one
 // arrival counter per (sequence, kv head).  Pieces are sized for the largest group so that the
 // counters start at an offset that depends on the CTA count alone: a workspace keeps its zeroed
 // counters across calls of any shape that use the same CTA count.
+// Pieces of the persistent kernel: at most two per CTA (its first and its last sequence).
+inline size_t persist_pieces(int ctas) { return (size_t)ctas * 2 * kPieceRows; }
+
 size_t persist_workspace_bytes(int num_seqs, int num_kv_heads, int group, int ctas) {
     (void)group;
-    const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+    const size_t pieces = persist_pieces(ctas);
     return align256(pieces * kHeadDim * sizeof(float)) + align256(pieces * sizeof(float2)) +
            align256((size_t)num_seqs * num_kv_heads * sizeof(int));
 }
@@ -143,8 +153,8 @@ int sm_count_current() { return sm_count(); }
 
 bool persist_counter_region(int num_seqs, int num_kv_heads, int group, const pa_decode_options* opts,
                             size_t* offset, size_t* bytes) {
-    const int ctas = persist_ctas(group, opts);
-    const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+    (void)group;
+    const size_t pieces = persist_pieces(persist_layout_ctas(opts));
     *offset = align256(pieces * kHeadDim * sizeof(float)) + align256(pieces * sizeof(float2));
     *bytes = (size_t)num_seqs * num_kv_heads * sizeof(int);
     return true;
@@ -249,7 +259,7 @@ size_t pa_decode_workspace_size_ex(int num_seqs, int num_q_heads, int num_kv_hea
     Path path;
     if (choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path) != PA_OK) return 0;
     if (path == kPathPersist)
-        return persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_ctas(group, opts));
+        return persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
     int tps = plan_tps(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, opts);
     if (tps <= 0) return 0;
     return workspace_bytes_for(num_seqs, num_q_heads, max_splits_for(block_size, max_blocks_per_seq, tps));
@@ -327,9 +337,9 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
 
     if (path == kPathPersist) {
         const int ctas = persist_ctas(group, opts);
-        const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, ctas);
+        const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-        const size_t pieces = (size_t)ctas * 2 * kPieceRows;
+        const size_t pieces = persist_pieces(persist_layout_ctas(opts));
         char* w = static_cast<char*>(workspace);
         a.part_o = reinterpret_cast<float*>(w);
         a.part_ml = reinterpret_cast<float2*>(w + align256(pieces * kHeadDim * sizeof(float)));

@@ -784,7 +784,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     __syncthreads();
     if (tid == 0) {
         trace(a.timeline, c, 6);
-        if (a.timeline) a.timeline[(size_t)c * kTimelineSlots + 14] = (unsigned long long)(b_e - b_c);
+        if (a.timeline) {
+            unsigned int smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            a.timeline[(size_t)c * kTimelineSlots + 14] = (unsigned long long)(b_e - b_c);
+            a.timeline[(size_t)c * kTimelineSlots + 15] = smid;
+        }
     }
     if (*abort_flag && tid == 0) {
         // let every copy still in flight land before the CTA's shared memory is released

@@ -70,12 +70,12 @@ def test_static_matches_workspace_entry_point_twice(dtype):
 def test_static_refuses_problems_beyond_its_scratch():
     dev = torch.device("cuda")
     lib = pa.lib()
-    # 1024 sequences x 1024 kv heads: the persistent kernel's pieces plus one arrival counter
+    # 1024 sequences x 4096 kv heads: the persistent kernel's pieces plus one arrival counter
     # per (sequence, kv head) need more than the fixed scratch; the call must refuse before
     # launching anything
-    S, Hq, Hkv, D, B, maxb = 1024, 1024, 1024, 128, 16, 4
+    S, Hq, Hkv, D, B, maxb = 1024, 4096, 4096, 128, 16, 4
     need = pa.decode_workspace_size(S, Hq, Hkv, D, B, maxb)
-    assert need > (8 << 20)
+    assert need > (16 << 20)
     dummy = torch.zeros(16, dtype=torch.float16, device=dev)
     tbl = torch.zeros(16, dtype=torch.int32, device=dev)
     before = pa.kernel_launch_count()
