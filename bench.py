@@ -156,8 +156,9 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0):
         self.fused = fused
+        self.num_ctas = num_ctas
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
         self.wl = wl
@@ -169,7 +170,8 @@ class Step:
         self.slots = torch.from_numpy(slots).to(device)
         self.out = [torch.empty_like(wl.q[i]) for i in range(L)]
         S, Hq, D = wl.q[0].shape
-        ws = pa.decode_workspace_size(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
+        ws = pa.decode_workspace_size(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq,
+                                      num_ctas=num_ctas)
         self.ws = pa.new_workspace(ws, device)
         self.tps = pa.plan_tokens_per_split(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
         self.graph = None
@@ -183,10 +185,10 @@ class Step:
             ev_pair[0].record()
         if self.fused:
             pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
-                             wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws)
+                             wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas)
         else:
             pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
-                      out=self.out[i], workspace=self.ws)
+                      out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -256,7 +258,7 @@ def run_ours(args):
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -462,6 +464,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused")
+    ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

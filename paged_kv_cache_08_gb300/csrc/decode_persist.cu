@@ -38,6 +38,7 @@ constexpr int kMaxStages = 6;
 constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kKVBytes = 2 * kKBytes;
 constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
+constexpr int kMergeBatch = 4;                          // pieces whose loads are in flight together
 
 // Shared-memory layout for a ring of kStages 64-token stages: 3 stages let two CTAs share an
 // SM, 6 stages give one CTA the whole SM.
@@ -140,9 +141,9 @@ __device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase) {
     return ok;
 }
 
-__device__ __forceinline__ float ld_cg(const float* p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+__device__ __forceinline__ float4 ld_cg4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
     return v;
 }
 
@@ -368,21 +369,47 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
             __threadfence();
             for (int e = tid; e < G * 16; e += kConsumerThreads) {
                 const int row = e >> 4, d0 = (e & 15) * 8;
-                float M = -INFINITY;
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
-                    M = fmaxf(M, ld_cg2(&a.part_ml[pc * kPieceRows + row]).x);
-                }
+                // one online pass over the pieces, a few at a time, every load of a batch in flight
+                float M = -INFINITY, den = 0.f;
                 float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                float den = 0.f;
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
-                    const float2 ml = ld_cg2(&a.part_ml[pc * kPieceRows + row]);
-                    const float f = exp2f(ml.x - M);
-                    den = fmaf(f, ml.y, den);
-                    const float* src = a.part_o + (pc * kPieceRows + row) * kHeadDim + d0;
+                for (int cc0 = c_first; cc0 <= c_last; cc0 += kMergeBatch) {
+                    float2 ml[kMergeBatch];
+                    float4 x0[kMergeBatch], x1[kMergeBatch];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) num[q] = fmaf(f, ld_cg(src + q), num[q]);
+                    for (int k = 0; k < kMergeBatch; ++k) {
+                        const int cc = cc0 + k;
+                        if (cc <= c_last) {
+                            const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
+                            const size_t row_idx = pc * kPieceRows + row;
+                            ml[k] = ld_cg2(&a.part_ml[row_idx]);
+                            x0[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0);
+                            x1[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0 + 4);
+                        } else {
+                            ml[k] = make_float2(-INFINITY, 0.f);
+                            x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    float bm = M;
+#pragma unroll
+                    for (int k = 0; k < kMergeBatch; ++k) bm = fmaxf(bm, ml[k].x);
+                    const float rescale = exp2f(M - bm);   // M = -inf before the first batch: 0
+                    den *= rescale;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) num[q] *= rescale;
+#pragma unroll
+                    for (int k = 0; k < kMergeBatch; ++k) {
+                        const float f = exp2f(ml[k].x - bm);   // absent pieces: 2^-inf = 0
+                        den = fmaf(f, ml[k].y, den);
+                        num[0] = fmaf(f, x0[k].x, num[0]);
+                        num[1] = fmaf(f, x0[k].y, num[1]);
+                        num[2] = fmaf(f, x0[k].z, num[2]);
+                        num[3] = fmaf(f, x0[k].w, num[3]);
+                        num[4] = fmaf(f, x1[k].x, num[4]);
+                        num[5] = fmaf(f, x1[k].y, num[5]);
+                        num[6] = fmaf(f, x1[k].z, num[6]);
+                        num[7] = fmaf(f, x1[k].w, num[7]);
+                    }
+                    M = bm;
                 }
                 const float inv = 1.f / den;
                 uint4 packed;
