@@ -34,7 +34,6 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxStages = 6;
 constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kKVBytes = 2 * kKBytes;
 constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
@@ -131,14 +130,11 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
-// Barrier of the 128 consumer threads on an mbarrier (every thread arrives, bounded wait), so
-// that a warp that gave up on a copy cannot leave the others waiting forever.  `phase` counts
-// completed barrier phases and is the same in every consumer thread.
-__device__ __forceinline__ bool consumers_sync(uint64_t* bar, uint32_t& phase) {
-    mbar_arrive(bar);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase & 1u));
-    ++phase;
-    return ok;
+// Barrier of the 128 consumer threads (hardware named barrier 1).  Every consumer warp walks
+// the same chunk sequence and reaches the same barriers, also after it gave up on a copy (it
+// then skips waits, math and global writes), so no warp can be left waiting here.
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
 __device__ __forceinline__ float4 ld_cg4(const float* p) {
@@ -281,8 +277,7 @@ template <typename T>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e, long long N, int C,
                                               int c, const float (&o)[16][4], const float (&m_run)[2],
-                                              const float (&l_run)[2], uint64_t* cbar, uint32_t& cphase,
-                                              volatile int* last_flag) {
+                                              const float (&l_run)[2], bool dead, volatile int* last_flag) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = lane >> 2, qc = (lane & 3) * 2;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
@@ -298,22 +293,24 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     float* red_o = reinterpret_cast<float*>(scratch);                             // [4][8][kRedStride]
     float2* red_ml = reinterpret_cast<float2*>(red_o + kConsumerWarps * 8 * kRedStride);  // [4][8]
     const size_t piece = (size_t)c * 2 + ((Pseg <= b_c) ? 0 : 1);
-    if (!consumers_sync(cbar, cphase)) return false;   // every warp is past its reads of the stage
+    consumers_sync();   // every warp is past its reads of the stage
     for (int rg = 0; rg < G; rg += 8) {
         const bool hi = rg >= 8;   // rows 0..7 live in (c0, c1), rows 8..15 in (c2, c3)
+        if (rg + qr < G) {   // only the group's real query rows
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float v0 = hi ? o[j][2] : o[j][0];
-            const float v1 = hi ? o[j][3] : o[j][1];
-            *reinterpret_cast<float2*>(&red_o[(warp * 8 + qr) * kRedStride + j * 8 + qc]) = make_float2(v0, v1);
+            for (int j = 0; j < 16; ++j) {
+                const float v0 = hi ? o[j][2] : o[j][0];
+                const float v1 = hi ? o[j][3] : o[j][1];
+                *reinterpret_cast<float2*>(&red_o[(warp * 8 + qr) * kRedStride + j * 8 + qc]) = make_float2(v0, v1);
+            }
+            if ((lane & 3) == 0)
+                red_ml[warp * 8 + qr] = hi ? make_float2(m_run[1], lr[1]) : make_float2(m_run[0], lr[0]);
         }
-        if ((lane & 3) == 0)
-            red_ml[warp * 8 + qr] = hi ? make_float2(m_run[1], lr[1]) : make_float2(m_run[0], lr[0]);
-        if (!consumers_sync(cbar, cphase)) return false;
+        consumers_sync();
         const int r = tid >> 4;            // row within the group of 8
         const int d0 = (tid & 15) * 8;     // 8 columns per thread
         const int row = rg + r;
-        if (row < G) {
+        if (row < G && !dead) {
             float M = -INFINITY;
 #pragma unroll
             for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, red_ml[w2 * 8 + r].x);
@@ -351,20 +348,23 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
                 if ((tid & 15) == 0) a.part_ml[piece * kPieceRows + row] = make_float2(M, den);
             }
         }
-        if (!consumers_sync(cbar, cphase)) return false;   // the scratch is rewritten next
+        consumers_sync();   // the scratch is rewritten next
     }
     if (!whole) {
         // ---- pieces of a cut segment: the last CTA to arrive merges them ----
         __threadfence();
-        if (!consumers_sync(cbar, cphase)) return false;
+        consumers_sync();
         const int sigma = pos.s * Hkv + pos.h;
         const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + pos.n - 1, N, C);
         if (tid == 0) {
-            const int prev = atomicAdd(&a.seg_counters[sigma], 1);
-            *last_flag = (prev == c_last - c_first) ? 1 : 0;
+            *last_flag = 0;
+            if (!dead) {
+                const int prev = atomicAdd(&a.seg_counters[sigma], 1);
+                *last_flag = (prev == c_last - c_first) ? 1 : 0;
+            }
         }
-        if (!consumers_sync(cbar, cphase)) return false;
-        const bool last = *last_flag != 0;
+        consumers_sync();
+        const bool last = *last_flag != 0 && !dead;
         if (last) {
             __threadfence();
             for (int e = tid; e < G * 16; e += kConsumerThreads) {
@@ -461,7 +461,6 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerThreads);
         }
-        mbar_init(cbar, kConsumerThreads);
         mbar_init(qbar, 1);
         *abort_flag = 0;
         *issued_count = 0;
@@ -652,36 +651,38 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         zero_empty_rows(a, P, c, tid, kConsumerThreads);
         const bool append = a.k_new != nullptr;
         SegPos pos = locate(P, Lc, S, Hkv, b_c);
-        uint32_t cphase = 0;
+        // A warp that gave up on a wait (or sees that another did) is "dead": it keeps walking
+        // the same chunk sequence, so that every consumer warp reaches the same barriers, but
+        // waits for nothing and writes no result.
+        bool dead = false;
         int i = 0;
         for (long long g = b_c; g < b_e; ++g, ++i) {
             const int st = i % kStages;
-            const bool w = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (uint32_t)(i / kStages) & 1u));
-            if (!w) {
+            dead = dead || __any_sync(0xffffffffu, *abort_flag != 0);
+            if (!dead && !__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (uint32_t)(i / kStages) & 1u))) {
                 if (lane == 0) {
                     flag_status(a.status, PA_DEV_TIMEOUT);
                     *abort_flag = 1;
                 }
-                break;
+                dead = true;
             }
             __syncwarp();
             if (i == 0 && tid == 0) trace(a.timeline, c, 4);
-            if (*abort_flag) break;
             const uint32_t kbase = ring + (uint32_t)st * Lay::kStageBytes;
             const uint32_t vbase = kbase + kKBytes;
             const bool seg_begin = (pos.k == 0) || (g == b_c);
             const bool seg_end = (pos.k == pos.n - 1) || (g == b_e - 1);
-            if (seg_begin && i < kStages) {
+            if (!dead && seg_begin && i < kStages) {
                 // the first stages' q rows arrive on their own barrier
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(qbar, 0u))) {
                     if (lane == 0) {
                         flag_status(a.status, PA_DEV_TIMEOUT);
                         *abort_flag = 1;
                     }
-                    break;
+                    dead = true;
                 }
             }
-            if (seg_begin) {
+            if (seg_begin && !dead) {
                 // query rows of the segment's G heads, as mma A fragments (rows >= G are zero)
                 const uint32_t* qs = reinterpret_cast<const uint32_t*>(base_ptr + (size_t)st * Lay::kStageBytes +
                                                                        kKVBytes);
@@ -705,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             }
             const int nvalid = min(kStageTokens, pos.L - pos.k * kStageTokens);
 
-            if (t_warp < nvalid) {
+            if (t_warp < nvalid && !dead) {
                 if (nvalid < t_warp + 16) {
                     uint4* vz = reinterpret_cast<uint4*>(base_ptr + (size_t)st * Lay::kStageBytes + kKBytes);
                     for (int idx = lane; idx < (t_warp + 16 - nvalid) * 16; idx += 32) {
@@ -794,14 +795,9 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 }
             }
 
-            if (seg_end && !flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
-                                                      N, C, c, o, m_run, l_run, cbar, cphase, last_flag)) {
-                if (lane == 0) {
-                    flag_status(a.status, PA_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
-            }
+            if (seg_end)
+                flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N, C, c, o, m_run,
+                                 l_run, dead, last_flag);
             mbar_arrive(&empty[st]);   // this thread is done with the stage's buffers
             advance(pos, P, Lc, S, Hkv);
         }
