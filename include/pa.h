@@ -89,10 +89,14 @@ typedef struct {
     int flags;                   /* PA_DECODE_NO_EARLY_READS: pa_decode_append reads nothing before
                                     the preceding kernel in the stream has finished */
     unsigned long long* timeline;/* persistent kernel trace, NULL = off; else device memory of
-                                    num_ctas * 16 uint64: per CTA, (global ns, SM clock) pairs at
-                                    entry, after the dependency wait, after the prefix sums, first
-                                    copy issued, first chunk landed, last chunk done, exit; slot 14 =
-                                    chunks streamed, slot 15 = SM id.  Entries of CTAs that own no chunk stay as set. */
+                                    num_ctas * 16 uint64 per CTA: global-timer ns at 0 entry,
+                                    1 dependency wait passed, 2 prefix sums done, 3 first block ids
+                                    read, 4 first copies issued, 5 first chunk landed, 6 last chunk
+                                    landed, 7 last chunk consumed, 8 exit; then 9 ns consumers waited
+                                    for chunks, 10 ns spent finishing segments, 11 ns the producer
+                                    waited for a free stage, 12 cut segments merged, 13 segment
+                                    pieces finished, 14 chunks streamed, 15 SM id.  Entries of CTAs
+                                    that own no chunk stay as set. */
 } pa_decode_options;
 
 /* ------------------------------------------------------------------------------------

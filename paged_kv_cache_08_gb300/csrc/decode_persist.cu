@@ -21,23 +21,53 @@
 // keeping a running max / sum per query row.  At a segment's last chunk the four warps merge
 // through the stage buffer they just consumed.  Full / empty mbarriers per stage connect the
 // producer and the consumers; every wait is bounded.
+//
+// Finishing a cut segment costs dependent round trips to L2 (publish the partial, count the
+// arrival, read the other pieces), slow while the copies of every CTA queue in front of them.
+// Only the first piece of a range can end before the range does; the consumers hand it to an
+// epilogue warp (publish on a shared-memory barrier, move on) which does the arrival and, if
+// last, the merge while the stream continues.  The range's final piece is finished by the
+// consumers themselves, with all their threads, when nothing is left to stream.
 #include "pa_internal.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <climits>
 
 namespace pa {
 
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;      // issues the copies
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // finishes the range's first piece off the stream
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kKVBytes = 2 * kKBytes;
 constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
 constexpr int kMergeBatch = 4;                          // pieces whose loads are in flight together
+
+// Trace slots of one CTA: event times (global ns), then accumulated times and counters.
+enum : int {
+    kTrEntry = 0,       // CTA starts
+    kTrDeps = 1,        // the dependency wait on the preceding kernel has passed
+    kTrScan = 2,        // prefix sums of the chunk counts are in shared memory
+    kTrIds = 3,         // producer: block ids of the first chunk have been read
+    kTrIssue = 4,       // producer: copies of the first chunk issued
+    kTrFirst = 5,       // consumers: first chunk landed
+    kTrLastLanded = 6,  // consumers: last chunk landed
+    kTrLoopEnd = 7,     // consumers: last chunk consumed and flushed
+    kTrExit = 8,        // CTA ends
+    kTrWaitFull = 9,    // consumer warp 0: ns spent waiting for chunks to land
+    kTrFlush = 10,      // consumer warp 0: ns spent finishing segments (merges included)
+    kTrWaitEmpty = 11,  // producer: ns spent waiting for a free stage
+    kTrMerges = 12,     // cut segments this CTA merged
+    kTrFlushes = 13,    // segment pieces this CTA finished
+    kTrChunks = 14,     // chunks streamed
+    kTrSm = 15          // SM the CTA ran on
+};
 
 // Shared-memory layout for a ring of kStages 64-token stages: 3 stages let two CTAs share an
 // SM, 6 stages give one CTA the whole SM.
@@ -46,7 +76,7 @@ struct PLayout {
     static constexpr int kQRows = kG16 ? 16 : 8;
     static constexpr int kStageBytes = kKVBytes + kQRows * kHeadDim * 2;  // multiple of 1024
     static constexpr size_t kRing = (size_t)kStages * kStageBytes;
-    static constexpr size_t kBars = kRing;   // full[kStages], empty[kStages], consumer barrier, q barrier
+    static constexpr size_t kBars = kRing;   // full[kStages], empty[kStages], q barrier, piece barrier
     static constexpr size_t kFlags = kBars + (2 * kStages + 2) * sizeof(uint64_t);
     static constexpr size_t kNewPhys = kFlags + 16;   // int [kStages] block of the new token, then
                                                        // int [kStages] deferred q rows (s * Hkv + h)
@@ -269,15 +299,80 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs& a, const int32
     }
 }
 
+// Merge every piece (m, l, o) of the cut segment (s, h) -- chunks [Pseg, Pseg + n) of the list,
+// cut by the CTA ranges -- into its normalised output rows.  Threads t = 0..nthreads-1 share the
+// G x 16 (row, 8-column) items; one online pass over the pieces, a batch of loads in flight.
+template <typename T>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, long long Pseg, int n, long long N,
+                                             int C, int t, int nthreads) {
+    const int Hq = a.num_q_heads, G = Hq / a.num_kv_heads;
+    const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + n - 1, N, C);
+    for (int e = t; e < G * 16; e += nthreads) {
+        const int row = e >> 4, d0 = (e & 15) * 8;
+        // one online pass over the pieces, a few at a time, every load of a batch in flight
+        float M = -INFINITY, den = 0.f;
+        float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int cc0 = c_first; cc0 <= c_last; cc0 += kMergeBatch) {
+            float2 ml[kMergeBatch];
+            float4 x0[kMergeBatch], x1[kMergeBatch];
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const int cc = cc0 + k;
+                if (cc <= c_last) {
+                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
+                    const size_t row_idx = pc * kPieceRows + row;
+                    ml[k] = ld_cg2(&a.part_ml[row_idx]);
+                    x0[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0);
+                    x1[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0 + 4);
+                } else {
+                    ml[k] = make_float2(-INFINITY, 0.f);
+                    x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float bm = M;
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) bm = fmaxf(bm, ml[k].x);
+            const float rescale = exp2f(M - bm);   // M = -inf before the first batch: 0
+            den *= rescale;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) num[q] *= rescale;
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                const float f = exp2f(ml[k].x - bm);   // absent pieces: 2^-inf = 0
+                den = fmaf(f, ml[k].y, den);
+                num[0] = fmaf(f, x0[k].x, num[0]);
+                num[1] = fmaf(f, x0[k].y, num[1]);
+                num[2] = fmaf(f, x0[k].z, num[2]);
+                num[3] = fmaf(f, x0[k].w, num[3]);
+                num[4] = fmaf(f, x1[k].x, num[4]);
+                num[5] = fmaf(f, x1[k].y, num[5]);
+                num[6] = fmaf(f, x1[k].z, num[6]);
+                num[7] = fmaf(f, x1[k].w, num[7]);
+            }
+            M = bm;
+        }
+        const float inv = 1.f / den;
+        uint4 packed;
+        packed.x = Elem<T>::pack2(num[0] * inv, num[1] * inv);
+        packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
+        packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
+        packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
+        *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)s * Hq + h * G + row) * kHeadDim + d0) = packed;
+    }
+}
+
 // Finish one segment piece at its last chunk in this CTA's range: merge the four consumer warps
 // through the stage buffer they have just consumed (`scratch`, 32 KB), then write the normalised
-// output (whole segment) or this CTA's partial (m, l, o); for a cut segment, the last CTA to
-// arrive merges all pieces.  Returns false if a barrier wait gave up.
+// output (whole segment) or this CTA's partial (m, l, o).  A cut piece is then either handed to
+// the epilogue warp (`handoff`: every consumer thread arrives on `pdone` after its stores) or
+// finished here: count the arrival and, as the last CTA of the segment to arrive, merge all
+// pieces.  Returns true if this call merged a cut segment.
 template <typename T>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e, long long N, int C,
                                               int c, const float (&o)[16][4], const float (&m_run)[2],
-                                              const float (&l_run)[2], bool dead, volatile int* last_flag) {
+                                              const float (&l_run)[2], bool dead, volatile int* last_flag,
+                                              bool handoff, uint64_t* pdone) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = lane >> 2, qc = (lane & 3) * 2;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
@@ -350,6 +445,11 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         }
         consumers_sync();   // the scratch is rewritten next
     }
+    if (!whole && handoff) {
+        mbar_arrive(pdone);   // release: this thread's partial stores precede the epilogue's arrival
+        fence_proxy_async_smem();
+        return false;
+    }
     if (!whole) {
         // ---- pieces of a cut segment: the last CTA to arrive merges them ----
         __threadfence();
@@ -367,64 +467,14 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         const bool last = *last_flag != 0 && !dead;
         if (last) {
             __threadfence();
-            for (int e = tid; e < G * 16; e += kConsumerThreads) {
-                const int row = e >> 4, d0 = (e & 15) * 8;
-                // one online pass over the pieces, a few at a time, every load of a batch in flight
-                float M = -INFINITY, den = 0.f;
-                float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int cc0 = c_first; cc0 <= c_last; cc0 += kMergeBatch) {
-                    float2 ml[kMergeBatch];
-                    float4 x0[kMergeBatch], x1[kMergeBatch];
-#pragma unroll
-                    for (int k = 0; k < kMergeBatch; ++k) {
-                        const int cc = cc0 + k;
-                        if (cc <= c_last) {
-                            const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
-                            const size_t row_idx = pc * kPieceRows + row;
-                            ml[k] = ld_cg2(&a.part_ml[row_idx]);
-                            x0[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0);
-                            x1[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0 + 4);
-                        } else {
-                            ml[k] = make_float2(-INFINITY, 0.f);
-                            x0[k] = x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                    }
-                    float bm = M;
-#pragma unroll
-                    for (int k = 0; k < kMergeBatch; ++k) bm = fmaxf(bm, ml[k].x);
-                    const float rescale = exp2f(M - bm);   // M = -inf before the first batch: 0
-                    den *= rescale;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) num[q] *= rescale;
-#pragma unroll
-                    for (int k = 0; k < kMergeBatch; ++k) {
-                        const float f = exp2f(ml[k].x - bm);   // absent pieces: 2^-inf = 0
-                        den = fmaf(f, ml[k].y, den);
-                        num[0] = fmaf(f, x0[k].x, num[0]);
-                        num[1] = fmaf(f, x0[k].y, num[1]);
-                        num[2] = fmaf(f, x0[k].z, num[2]);
-                        num[3] = fmaf(f, x0[k].w, num[3]);
-                        num[4] = fmaf(f, x1[k].x, num[4]);
-                        num[5] = fmaf(f, x1[k].y, num[5]);
-                        num[6] = fmaf(f, x1[k].z, num[6]);
-                        num[7] = fmaf(f, x1[k].w, num[7]);
-                    }
-                    M = bm;
-                }
-                const float inv = 1.f / den;
-                uint4 packed;
-                packed.x = Elem<T>::pack2(num[0] * inv, num[1] * inv);
-                packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
-                packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
-                packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
-                *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)pos.s * Hq + pos.h * G + row) * kHeadDim +
-                                          d0) = packed;
-            }
+            merge_pieces<T>(a, pos.s, pos.h, Pseg, pos.n, N, C, tid, kConsumerThreads);
             if (tid == 0) a.seg_counters[sigma] = 0;   // ready for the next call
         }
+        fence_proxy_async_smem();   // generic writes to the stage precede its next TMA fill
+        return last;
     }
-    fence_proxy_async_smem();   // generic writes to the stage precede its next TMA fill
-    return true;
+    fence_proxy_async_smem();
+    return false;
 }
 
 template <typename T, bool kG16, int kStages>
@@ -437,11 +487,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     unsigned char* base_ptr = smem_raw + (ring - raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + Lay::kBars);
     uint64_t* empty = full + kStages;
-    uint64_t* cbar = empty + kStages;
-    uint64_t* qbar = cbar + 1;   // q rows of the first kStages chunks (fetched after the dependency wait)
+    uint64_t* qbar = empty + kStages;   // q rows of the first kStages chunks (fetched after the dependency wait)
+    uint64_t* pdone = qbar + 1;         // the consumers have published the piece the epilogue warp finishes
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Lay::kFlags);
     volatile int* issued_count = abort_flag + 1;
     volatile int* last_flag = abort_flag + 2;
+    volatile int* epi_merges = abort_flag + 3;
     volatile int* new_phys = reinterpret_cast<volatile int*>(base_ptr + Lay::kNewPhys);
     int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
     const int S = a.num_seqs;
@@ -453,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     const int cap = a.max_blocks_per_seq * B;
 
     if (tid == 0) {
-        trace(a.timeline, c, 0);
+        trace(a.timeline, c, kTrEntry);
         prefetch_map(&maps.k);
         prefetch_map(&maps.v);
 #pragma unroll
@@ -462,15 +513,19 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             mbar_init(&empty[i], kConsumerThreads);
         }
         mbar_init(qbar, 1);
+        mbar_init(pdone, kConsumerThreads);
         *abort_flag = 0;
         *issued_count = 0;
         *last_flag = 0;
+        *epi_merges = 0;
         fence_mbar_init();
     }
     // Without the early contract every input may come from the preceding kernel: wait now.
     // With it, lengths, tables and the cached rows are read first and the wait comes later.
-    if (!a.early) grid_dependency_wait();
-    if (tid == 0) trace(a.timeline, c, 1);
+    if (!a.early) {
+        grid_dependency_wait();
+        if (tid == 0) trace(a.timeline, c, kTrDeps);
+    }
 
     // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) ----
     {
@@ -510,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         }
     }
     __syncthreads();
-    if (tid == 0) trace(a.timeline, c, 2);
+    if (tid == 0) trace(a.timeline, c, kTrScan);
 
     const long long N = P[S];
     // C <= N CTAs take part, so that every one of them owns at least one chunk
@@ -524,12 +579,14 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     const long long b_c = range_begin(c, N, C), b_e = range_begin(c + 1, N, C);
     if (!a.early) grid_launch_dependents();
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ================= producer warp =================
         // Lane j describes chunk gbase + j (segment position and physical block ids); the next
         // group's descriptors are loaded while this group's copies are issued, so the ring is
         // refilled as soon as a stage frees up.
         ChunkDesc cur = describe(a, P, Lc, S, Hkv, b_c, b_e, b_c + lane);
+        unsigned long long wait_empty_ns = 0;
+        if (a.timeline && lane == 0 && cur.ids[0] != INT_MIN) trace(a.timeline, c, kTrIds);
         volatile int* qdef = new_phys + kStages;   // [kStages]: q rows the first stages still need
         const bool append = a.k_new != nullptr;
         bool deps_done = false;
@@ -571,7 +628,11 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 }
                 if (i >= kStages) {
                     bool w = true;
-                    if (lane == 0) w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
+                    if (lane == 0) {
+                        const unsigned long long t0 = a.timeline ? global_timer_ns() : 0ull;
+                        w = mbar_wait_bounded(&empty[st], (uint32_t)((i / kStages) - 1) & 1u);
+                        if (a.timeline) wait_empty_ns += global_timer_ns() - t0;
+                    }
                     w = __shfl_sync(0xffffffffu, w, 0);
                     if (!w) {
                         if (lane == 0) {
@@ -618,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                                 tma_load_2d(box + kKBytes + (uint32_t)R * 128u, &maps.v, 64, row, &full[st]);
                             }
                         }
-                        if (i == 0) trace(a.timeline, c, 3);
+                        if (i == 0) trace(a.timeline, c, kTrIssue);
                         if (loadq_j && !defer_q) {
                             const T* qsrc = static_cast<const T*>(a.q) + ((size_t)s_j * Hq + h_j * G) * kHeadDim;
                             bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
@@ -631,7 +692,46 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             cur = nxt;
         }
         if (!deps_done) dependency_point(i);
-        if (lane == 0) *issued_count = i;
+        if (lane == 0) {
+            *issued_count = i;
+            trace_put(a.timeline, c, kTrWaitEmpty, wait_empty_ns);
+        }
+    } else if (warp == kEpilogueWarp) {
+        // ================= epilogue warp =================
+        // The range's first segment, when it began in an earlier range and ends before this one
+        // does: count this CTA's arrival and, if it is the last, merge the segment's pieces.
+        const SegPos p0 = locate(P, Lc, S, Hkv, b_c);
+        const long long Pseg = (long long)P[p0.s] + (long long)p0.h * p0.n;
+        if (Pseg < b_c && Pseg + p0.n - 1 < b_e - 1) {
+            if (a.early) grid_dependency_wait();   // counters and outputs are written after it
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_bounded(pdone, 0u);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    flag_status(a.status, PA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+            } else if (*abort_flag == 0) {
+                // acquired through pdone: the consumers' partial stores; the fence publishes them
+                const int sigma = p0.s * Hkv + p0.h;
+                const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + p0.n - 1, N, C);
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    last = atomicAdd(&a.seg_counters[sigma], 1) == c_last - c_first;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    merge_pieces<T>(a, p0.s, p0.h, Pseg, p0.n, N, C, lane, 32);
+                    if (lane == 0) {
+                        a.seg_counters[sigma] = 0;   // ready for the next call
+                        *epi_merges = 1;
+                    }
+                }
+            }
+        }
     } else {
         // ================= consumer warps =================
         const int qr = lane >> 2, qc = (lane & 3) * 2;
@@ -647,7 +747,9 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         if (a.early) {
             grid_dependency_wait();   // q, the new rows and every output belong after this point
             grid_launch_dependents();
+            if (tid == 0) trace(a.timeline, c, kTrDeps);
         }
+        unsigned long long wait_full_ns = 0, flush_ns = 0, merges = 0, flushes = 0;
         zero_empty_rows(a, P, c, tid, kConsumerThreads);
         const bool append = a.k_new != nullptr;
         SegPos pos = locate(P, Lc, S, Hkv, b_c);
@@ -659,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         for (long long g = b_c; g < b_e; ++g, ++i) {
             const int st = i % kStages;
             dead = dead || __any_sync(0xffffffffu, *abort_flag != 0);
+            const unsigned long long tw = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
             if (!dead && !__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (uint32_t)(i / kStages) & 1u))) {
                 if (lane == 0) {
                     flag_status(a.status, PA_DEV_TIMEOUT);
@@ -667,7 +770,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 dead = true;
             }
             __syncwarp();
-            if (i == 0 && tid == 0) trace(a.timeline, c, 4);
+            if (a.timeline && tid == 0) {
+                const unsigned long long now = global_timer_ns();
+                wait_full_ns += now - tw;
+                if (i == 0) trace_put(a.timeline, c, kTrFirst, now);
+                if (g == b_e - 1) trace_put(a.timeline, c, kTrLastLanded, now);
+            }
             const uint32_t kbase = ring + (uint32_t)st * Lay::kStageBytes;
             const uint32_t vbase = kbase + kKBytes;
             const bool seg_begin = (pos.k == 0) || (g == b_c);
@@ -795,24 +903,36 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 }
             }
 
-            if (seg_end)
-                flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N, C, c, o, m_run,
-                                 l_run, dead, last_flag);
+            if (seg_end) {
+                const unsigned long long tf = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
+                const bool merged = flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
+                                                     C, c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone);
+                if (a.timeline && tid == 0) {
+                    flush_ns += global_timer_ns() - tf;
+                    merges += merged ? 1 : 0;
+                    ++flushes;
+                }
+            }
             mbar_arrive(&empty[st]);   // this thread is done with the stage's buffers
             advance(pos, P, Lc, S, Hkv);
         }
-        if (tid == 0) trace(a.timeline, c, 5);
+        if (tid == 0 && a.timeline) {
+            trace(a.timeline, c, kTrLoopEnd);
+            trace_put(a.timeline, c, kTrWaitFull, wait_full_ns);
+            trace_put(a.timeline, c, kTrFlush, flush_ns);
+            trace_put(a.timeline, c, kTrMerges, merges);   // the epilogue warp's merge is added at exit
+            trace_put(a.timeline, c, kTrFlushes, flushes);
+        }
     }
 
     __syncthreads();
-    if (tid == 0) {
-        trace(a.timeline, c, 6);
-        if (a.timeline) {
-            unsigned int smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            a.timeline[(size_t)c * kTimelineSlots + 14] = (unsigned long long)(b_e - b_c);
-            a.timeline[(size_t)c * kTimelineSlots + 15] = smid;
-        }
+    if (tid == 0 && a.timeline) {
+        trace(a.timeline, c, kTrExit);
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        trace_put(a.timeline, c, kTrChunks, (unsigned long long)(b_e - b_c));
+        trace_put(a.timeline, c, kTrSm, smid);
+        a.timeline[(size_t)c * kTimelineSlots + kTrMerges] += (unsigned long long)*epi_merges;
     }
     if (*abort_flag && tid == 0) {
         // let every copy still in flight land before the CTA's shared memory is released

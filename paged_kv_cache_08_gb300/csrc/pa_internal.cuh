@@ -179,15 +179,13 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Trace point: global time (ns) and SM clock of event `ev` of CTA `cta`, when tracing is on.
-__device__ __forceinline__ void trace(unsigned long long* tl, int cta, int ev) {
-    if (tl) {
-        unsigned long long t, c;
-        asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-        asm volatile("mov.u64 %0, %clock64;" : "=l"(c));
-        tl[(size_t)cta * kTimelineSlots + 2 * ev] = t;
-        tl[(size_t)cta * kTimelineSlots + 2 * ev + 1] = c;
-    }
+// Trace of the persistent kernel (slot layout documented with pa_decode_options in pa.h).
+// trace: global time (ns) of an event of CTA `cta`; trace_put: any value.  Both no-ops when off.
+__device__ __forceinline__ void trace_put(unsigned long long* tl, int cta, int slot, unsigned long long v) {
+    if (tl) tl[(size_t)cta * kTimelineSlots + slot] = v;
+}
+__device__ __forceinline__ void trace(unsigned long long* tl, int cta, int slot) {
+    if (tl) trace_put(tl, cta, slot, global_timer_ns());
 }
 
 __device__ __forceinline__ void flag_status(unsigned int* status, unsigned int bits) {
