@@ -10,11 +10,14 @@
  *        "嵌入式轻量 Block 分配器设计" (free bitmap, lowest free block first,
  *        -1 when the pool is exhausted); "共享前缀块（Prefix Caching）" (shared,
  *        reference-counted prefix blocks).
+ *   [P3] the KV Cache and BlockManager tutorial (hnwysp.cn) -- §3.4 (blocks swapped out to
+ *        a pinned host buffer of 0.3 x the pool).
  *   [P4] "显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结"
  *        -- §三 sequence diagram (append a token: write at the next offset of the last
  *        block, or allocate and append a block when it is full; free all blocks at the end);
  *        §三.1 (two pool tensors, one fixed stride per physical block);
  *        §四 (copy-on-write of shared blocks, reference counts);
+ *        FAQ on preemption (swap the blocks of a low-priority request to host memory);
  *        §五.1 (decode kernel: per sequence and head, loop over logical blocks through
  *        block_tables [num_seqs, max_blocks_per_seq] and context_lens [num_seqs],
  *        q.k, softmax with running rescale, weight V, normalise at the end).
@@ -113,6 +116,32 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
                    void* k_cache, void* v_cache,
                    int num_tokens, int num_kv_heads, int head_dim, int block_size,
                    int num_blocks, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * pa_copy_blocks  [P4 §四 copy-on-write; P4 FAQ on preemption (swap); P3 §3.4 pinned
+ *                  host swap buffer]
+ * For i = 0..num_pairs-1 copy every kv head's rows of block src_ids[i] of the source pool
+ * into block dst_ids[i] of the destination pool, bit for bit:
+ *   dst_k[dst_ids[i]][h][:][:] = src_k[src_ids[i]][h][:][:] for every h, and the same for V.
+ * Pools are [blocks][num_kv_heads][block_size][head_dim] (src_blocks, dst_blocks blocks).
+ * Source and destination may be the same pool (copy-on-write inside the cache) or two pools
+ * (swap out to, or in from, a pool in host memory).  Every pointer is device memory or
+ * pinned host memory (cudaHostAlloc / cudaHostRegister), passed by the address the caller
+ * holds; host memory that CUDA does not know as pinned is refused (PA_ERR_INVALID_ARG).
+ * src_ids, dst_ids: int32 [num_pairs], device or pinned host memory.
+ * A pair with an id outside its pool is skipped and sets PA_DEV_BAD_BLOCK_ID.  The
+ * destination blocks must be distinct and no destination may be the source of another pair
+ * (else which bytes land is unspecified).  Asynchronous on `stream`; pinned host memory
+ * must stay allocated, and host code must not touch it, until the copy has completed.
+ * A pa_decode_append launched right after it that reads the destination pool must not
+ * use early reads (PA_DECODE_NO_EARLY_READS).
+ * head_dim a positive multiple of 8; pools 16-byte aligned.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------------------- */
+int pa_copy_blocks(const void* src_k, const void* src_v, int src_blocks,
+                   void* dst_k, void* dst_v, int dst_blocks,
+                   const int32_t* src_ids, const int32_t* dst_ids, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------
  * pa_decode  [P4 §五.1; P1 address formula]
@@ -284,6 +313,16 @@ int pa_pool_append_token(pa_pool* pool, int32_t* table_row, int max_blocks, int 
  * sequence (P4 §三, end of request) and set the entries to -1. */
 int pa_pool_release(pa_pool* pool, int32_t* table_row, int max_blocks, int context_len,
                     int block_size);
+
+/* Move the first n blocks of a sequence from pool `from` to pool `to` (swap out: device pool
+ * to host pool; swap in: back), P4 FAQ on preemption: for each i < n allocate a block of
+ * `to`, record the pair (src_ids[i], dst_ids[i]) = (table_row[i], new id), drop one reference
+ * of the old block in `from` and point table_row[i] at the new one.  The caller then copies
+ * the pairs with pa_copy_blocks before anything reuses a freed block.  On
+ * PA_ERR_POOL_EXHAUSTED nothing has changed.  Returns n, PA_ERR_INVALID_ARG,
+ * PA_ERR_BOUNDS (a table entry not allocated in `from`) or PA_ERR_POOL_EXHAUSTED. */
+int pa_pool_move_blocks(pa_pool* from, pa_pool* to, int32_t* table_row, int n,
+                        int32_t* src_ids, int32_t* dst_ids);
 
 /* slots[s] = slot of token context_lens[s] - 1 (the newest one), or -1 when the
  * context is empty; host arrays.  Returns PA_OK or PA_ERR_BOUNDS if a length

@@ -87,6 +87,9 @@ class Oracle:
         L.pao_decode.restype = _c_int
         L.pao_decode.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _c_int, _ptr, ctypes.c_double,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]
+        L.pao_copy_blocks.restype = _c_int
+        L.pao_copy_blocks.argtypes = [_ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _c_int, _c_int,
+                                      _c_int]
         L.pao_num_threads.restype = _c_int
         L.pao_num_threads.argtypes = []
 
@@ -131,6 +134,20 @@ class Oracle:
         B = k_cache.shape[2]
         self._L.pao_cache_write(kk.ctypes.data, vv.ctypes.data, sl.ctypes.data,
                                 k_cache.ctypes.data, v_cache.ctypes.data, T, H, D, B)
+
+    def copy_blocks(self, src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray,
+                    src_ids, dst_ids) -> int:
+        """In place on the uint16 pools ``dst_k``/``dst_v`` [NB, Hkv, B, D] (they may be the
+        source arrays themselves); returns how many pairs had an id outside its pool."""
+        for a in (src_k, src_v, dst_k, dst_v):
+            assert a.dtype == np.uint16 and a.flags.c_contiguous
+        si = np.ascontiguousarray(np.asarray(src_ids, dtype=np.int32))
+        di = np.ascontiguousarray(np.asarray(dst_ids, dtype=np.int32))
+        assert si.shape == di.shape
+        NBs, H, B, D = src_k.shape
+        return int(self._L.pao_copy_blocks(src_k.ctypes.data, src_v.ctypes.data, NBs, dst_k.ctypes.data,
+                                           dst_v.ctypes.data, dst_k.shape[0], si.ctypes.data, di.ctypes.data,
+                                           si.size, H, B, D))
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                num_kv_heads: int, is_bf16: bool, num_threads: int = 0) -> np.ndarray:

@@ -17,6 +17,9 @@
  *       section 三 (sequence diagram of the decode loop): the new token is written at
  *       the next offset of the sequence's last block, or at offset 0 of a freshly
  *       appended block when the last one is full; then attention runs.
+ *       Section 四: a sequence about to write into a shared, unfilled block first gets a
+ *       deep copy of that block in a fresh one.  FAQ on preemption: a request's blocks move
+ *       to host memory and back (the same whole-block copy between two pools).
  *       Section 五.1 (kernel sketch): per (sequence, head) loop over the logical
  *       blocks, look up the physical block, take q.k for every cached token,
  *       softmax, weight V, normalise at the end.
@@ -147,6 +150,35 @@ void pao_cache_write(const uint16_t* k, const uint16_t* v, const int64_t* slots,
             memcpy(v_cache + dst, v + src, sizeof(uint16_t) * (size_t)head_dim);
         }
     }
+}
+
+/* ---- [B] section 四: copy-on-write deep copy of whole physical blocks; its FAQ on
+ * preemption: the same copy moves a request's blocks to a host pool and back ---- */
+
+/* For each pair i in order, every kv head's rows of block src_ids[i] of (src_k, src_v) are
+ * copied to block dst_ids[i] of (dst_k, dst_v).  A pair with an id outside its pool is left
+ * out.  Returns the number of pairs left out. */
+int pao_copy_blocks(const uint16_t* src_k, const uint16_t* src_v, int src_blocks,
+                    uint16_t* dst_k, uint16_t* dst_v, int dst_blocks,
+                    const int32_t* src_ids, const int32_t* dst_ids, int num_pairs,
+                    int num_kv_heads, int block_size, int head_dim) {
+    const int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;   /* elements */
+#if PAO_MUTANT == 8
+    const int64_t copied = (int64_t)block_size * head_dim;                      /* planted: kv head 0 only */
+#else
+    const int64_t copied = per_block;
+#endif
+    int left_out = 0;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int32_t s = src_ids[i], d = dst_ids[i];
+        if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+            ++left_out;
+            continue;
+        }
+        memcpy(dst_k + d * per_block, src_k + s * per_block, sizeof(uint16_t) * (size_t)copied);
+        memcpy(dst_v + d * per_block, src_v + s * per_block, sizeof(uint16_t) * (size_t)copied);
+    }
+    return left_out;
 }
 
 /* ---- [B] decode attention over the paged cache, fp64 ---- */

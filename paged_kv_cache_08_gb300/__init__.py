@@ -7,6 +7,7 @@ as the device-memory and stream provider.
 
     cache_write(k, v, slot_mapping, k_cache, v_cache)
     decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads) -> out
+    copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids)   # copy-on-write, swap out / in
     BlockPool(num_blocks)                       # host block pool (untimed)
     build_slot_mapping(block_tables, context_lens, block_size)
 """
@@ -21,7 +22,7 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "decode", "decode_append", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
 
@@ -69,6 +70,37 @@ def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_
     rc = lib().pa_cache_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
                               v_cache.data_ptr(), T, H, D, B, NB, _DTYPE[k.dtype], _stream_ptr(stream))
     _native.check("pa_cache_write", rc)
+
+
+def _pool_ptr(name: str, t: torch.Tensor, dtype=None):
+    """Device memory, or pinned host memory (the library reaches it through its device view)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def copy_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                src_ids: torch.Tensor, dst_ids: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy whole blocks: dst[dst_ids[i]] = src[src_ids[i]] for K and V (pools [NB, Hkv, B, D]).
+    Pools and ids live on the GPU or in pinned host memory; the ids are int32."""
+    if src_k.dtype not in _DTYPE:
+        raise TypeError("pools must be float16 or bfloat16")
+    ptrs = [_pool_ptr(n, t, src_k.dtype) for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k),
+                                                     ("dst_v", dst_v))]
+    sid = _pool_ptr("src_ids", src_ids, torch.int32)
+    did = _pool_ptr("dst_ids", dst_ids, torch.int32)
+    NBs, H, B, D = src_k.shape
+    NBd = dst_k.shape[0]
+    if (src_v.shape != src_k.shape or dst_k.shape[1:] != src_k.shape[1:] or dst_v.shape != dst_k.shape or
+            src_ids.numel() != dst_ids.numel()):
+        raise ValueError("shape mismatch")
+    rc = lib().pa_copy_blocks(ptrs[0], ptrs[1], NBs, ptrs[2], ptrs[3], NBd, sid, did, src_ids.numel(), H, D, B,
+                              _DTYPE[src_k.dtype], _stream_ptr(stream))
+    _native.check("pa_copy_blocks", rc)
 
 
 def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
@@ -282,6 +314,16 @@ class BlockPool:
                                                      int(block_size), ctypes.byref(slot), ctypes.byref(src),
                                                      ctypes.byref(dst)))
         return int(slot.value), int(src.value), int(dst.value)
+
+    def move_blocks(self, to: "BlockPool", table_row: np.ndarray, n: int):
+        """Move the first n blocks of a sequence to pool ``to`` (swap out / in); returns the
+        (src_ids, dst_ids) pairs that copy_blocks must then copy."""
+        assert table_row.dtype == np.int32 and table_row.flags.c_contiguous and n <= table_row.size
+        src = np.empty(max(n, 1), dtype=np.int32)
+        dst = np.empty(max(n, 1), dtype=np.int32)
+        _native.check("pa_pool_move_blocks", self._lib.pa_pool_move_blocks(self._h, to._h, _i32p(table_row), int(n),
+                                                                           _i32p(src), _i32p(dst)))
+        return src[:n], dst[:n]
 
     def release(self, table_row: np.ndarray, context_len: int, block_size: int) -> None:
         assert table_row.dtype == np.int32 and table_row.flags.c_contiguous

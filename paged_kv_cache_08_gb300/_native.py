@@ -36,6 +36,8 @@ NO_EARLY_READS = 1
 
 _SIGNATURES = {
     "pa_cache_write": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp]),
+    "pa_copy_blocks": (c_int, [c_vp, c_vp, c_int, c_vp, c_vp, c_int, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int,
+                               c_vp]),
     "pa_decode": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int, c_int,
                           c_int, c_int, c_vp, c_size, c_vp]),
     "pa_decode_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int, c_int,
@@ -65,6 +67,7 @@ _SIGNATURES = {
     "pa_pool_assign": (c_int, [c_vp, c_i32p, c_int, c_int, c_int, c_i32p, c_int]),
     "pa_pool_append_token": (c_int, [c_vp, c_i32p, c_int, c_int, c_int, c_i64p, c_i32p, c_i32p]),
     "pa_pool_release": (c_int, [c_vp, c_i32p, c_int, c_int, c_int]),
+    "pa_pool_move_blocks": (c_int, [c_vp, c_vp, c_i32p, c_int, c_i32p, c_i32p]),
     "pa_build_slot_mapping": (c_int, [c_i32p, c_int, c_i32p, c_int, c_int, c_i64p]),
 }
 

@@ -244,6 +244,59 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping, vo
     return PA_OK;
 }
 
+// Device address of memory the kernels may touch: device memory as it is, pinned (page-locked,
+// mapped) host memory translated to its device view; nullptr for pageable host memory.
+static const void* device_view(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeHost:
+            return at.devicePointer;
+        default:
+            return nullptr;
+    }
+}
+
+int pa_copy_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k, void* dst_v, int dst_blocks,
+                   const int32_t* src_ids, const int32_t* dst_ids, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int dtype, void* stream) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 || block_size <= 0 || src_blocks < 0 ||
+        dst_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_ids || !dst_ids) return PA_ERR_INVALID_ARG;
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) || !aligned4(src_ids) ||
+        !aligned4(dst_ids))
+        return PA_ERR_INVALID_ARG;
+    CopyBlocksArgs a;
+    a.src_k = static_cast<const uint4*>(device_view(src_k));
+    a.src_v = static_cast<const uint4*>(device_view(src_v));
+    a.dst_k = static_cast<uint4*>(const_cast<void*>(device_view(dst_k)));
+    a.dst_v = static_cast<uint4*>(const_cast<void*>(device_view(dst_v)));
+    a.src_ids = static_cast<const int32_t*>(device_view(src_ids));
+    a.dst_ids = static_cast<const int32_t*>(device_view(dst_ids));
+    if (!a.src_k || !a.src_v || !a.dst_k || !a.dst_v || !a.src_ids || !a.dst_ids) return PA_ERR_INVALID_ARG;
+    a.status = device_status_ptr();
+    a.vecs_per_block = (long long)num_kv_heads * block_size * (head_dim / 8);
+    a.num_pairs = num_pairs;
+    a.src_blocks = src_blocks;
+    a.dst_blocks = dst_blocks;
+    if (a.vecs_per_block > (1LL << 40) / num_pairs) return PA_ERR_UNSUPPORTED;
+    cudaError_t e = launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 int pa_decode_plan_tokens_per_split(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                     int block_size, int max_blocks_per_seq, const pa_decode_options* opts) {
     int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);

@@ -34,6 +34,20 @@ struct CacheWriteArgs {
     long long pool_slots;     // NB * B
 };
 
+struct CopyBlocksArgs {
+    const uint4* src_k;       // [src_blocks][Hkv][B][D] as 16-byte vectors (device or mapped host memory)
+    const uint4* src_v;
+    uint4* dst_k;             // [dst_blocks][Hkv][B][D]
+    uint4* dst_v;
+    const int32_t* src_ids;   // [num_pairs]
+    const int32_t* dst_ids;   // [num_pairs]
+    unsigned int* status;
+    long long vecs_per_block; // Hkv * B * D / 8
+    int num_pairs;
+    int src_blocks;
+    int dst_blocks;
+};
+
 struct DecodeArgs {
     void* out;                // [S][Hq][D]
     const void* q;            // [S][Hq][D]
@@ -208,6 +222,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Host-side launch helpers (defined in the .cu files)
 // ---------------------------------------------------------------------------------------
 cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 
 // FMA (CUDA-core) split pass for group size G and element type; returns cudaErrorInvalidValue
 // when G has no instantiation.

@@ -158,6 +158,22 @@ int pa_pool_release(pa_pool* pool, int32_t* table_row, int max_blocks, int conte
     return PA_OK;
 }
 
+int pa_pool_move_blocks(pa_pool* from, pa_pool* to, int32_t* table_row, int n, int32_t* src_ids,
+                        int32_t* dst_ids) {
+    if (!from || !to || n < 0 || (n > 0 && (!table_row || !src_ids || !dst_ids))) return PA_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!valid_id(from, table_row[i]) || from->refs[table_row[i]] <= 0) return PA_ERR_BOUNDS;
+    if (n > to->num_free) return PA_ERR_POOL_EXHAUSTED;
+    for (int i = 0; i < n; ++i) {
+        const int id = pa_pool_alloc(to);   // cannot fail: n blocks are free
+        src_ids[i] = table_row[i];
+        dst_ids[i] = id;
+        pa_pool_decref(from, table_row[i]);
+        table_row[i] = id;
+    }
+    return n;
+}
+
 int pa_build_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                           int num_seqs, int block_size, int64_t* slots) {
     if (num_seqs < 0 || block_size <= 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;

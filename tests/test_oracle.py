@@ -10,6 +10,10 @@
   forms (one token, zero query, equal keys, one dominant score, two tokens);
 * cache write: the worked example's slots, plus a canary fill showing that
   nothing but the addressed rows changes;
+* block copy: the copy-on-write fork of the PagedAttention explainer page
+  (tests/golden/cow_worked_example.txt) checked against torch's fp64 attention on
+  each branch's contiguous context, and a move to another pool and back that must
+  leave attention bit-identical;
 * planted mistakes (``PAO_MUTANT``): every one of them must fail some pin.
 """
 import math
@@ -261,8 +265,85 @@ def pin_cache_write(o):
     assert np.array_equal(kc2, canary) and np.array_equal(vc2, canary)
 
 
+def pin_copy_on_write_fork(o):
+    """The copy-on-write example of §四: a prompt in blocks #10 (full) and #11 (partial) shared by
+    branches A and B; A's append deep-copies #11 into #45 (tests/golden/cow_worked_example.txt),
+    B then writes into #11 in place.  Each branch's attention must equal torch's fp64 attention
+    on its own contiguous context (prompt + its token), and #45 must hold #11's rows."""
+    kv = {r[0]: [int(x) for x in r[1:]] for r in _read_golden("cow_worked_example.txt")}
+    b10, b11 = kv["prompt_blocks"]
+    new, = kv["cow_new_block"]
+    gen = torch.Generator().manual_seed(77)
+    B, Hkv, G, D = 16, 2, 3, 128
+    Hq = Hkv * G
+    NB = 96
+    P = B + 4                                   # #10 full, 4 rows in #11
+    kc = oracle_pkg.as_u16(_rand16((NB, Hkv, B, D), gen)).copy()
+    vc = oracle_pkg.as_u16(_rand16((NB, Hkv, B, D), gen)).copy()
+    Kp = _rand16((Hkv, P, D), gen)
+    Vp = _rand16((Hkv, P, D), gen)
+    kp, vp = oracle_pkg.as_u16(Kp), oracle_pkg.as_u16(Vp)
+    for t in range(P):
+        blk = b10 if t < B else b11
+        kc[blk, :, t % B, :] = kp[:, t, :]
+        vc[blk, :, t % B, :] = vp[:, t, :]
+    shared_k, shared_v = kc[b11].copy(), vc[b11].copy()
+    # A: copy-on-write, then its token lands in the copy; B: its token lands in #11 itself
+    assert o.copy_blocks(kc, vc, kc, vc, [b11], [new]) == 0
+    assert np.array_equal(kc[new], shared_k) and np.array_equal(vc[new], shared_v)
+    kn = _rand16((2, Hkv, D), gen)
+    vn = _rand16((2, Hkv, D), gen)
+    tables = np.array([[b10, new], [b10, b11]], np.int32)
+    lens = np.array([P + 1, P + 1], np.int32)
+    o.cache_write(kn, vn, o.slot_mapping(tables, lens, B), kc, vc)
+    q = _rand16((2, Hq, D), gen)
+    scale = 1.0 / math.sqrt(D)
+    got = o.decode(q, kc, vc, tables, lens, scale, Hkv, False)
+    Kc = [torch.cat([Kp, kn[i][:, None, :]], dim=1) for i in range(2)]
+    Vc = [torch.cat([Vp, vn[i][:, None, :]], dim=1) for i in range(2)]
+    want = _sdpa_fp64(q, Kc, Vc, Hkv, scale)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def pin_block_moves(o):
+    """Blocks moved to another pool and back to new ids (a swap out and in): the rows arrive
+    unchanged, nothing else changes, and attention through the rewritten table is bit-identical
+    to attention before the move (the permutation invariance of paging)."""
+    lens = [37, 64, 5]
+    B, Hkv, D = 16, 2, 128
+    q, Kc, Vc, kc, vc, tables = _paged_problem(lens, 4, Hkv, D, B, seed=91, pool_extra=12)
+    kc, vc = oracle_pkg.as_u16(kc).copy(), oracle_pkg.as_u16(vc).copy()
+    NB = kc.shape[0]
+    lens_np = np.array(lens, np.int32)
+    before = o.decode(q, kc, vc, tables, lens_np, 0.1, Hkv, False)
+    nb = (lens[1] + B - 1) // B
+    dev_ids = [int(x) for x in tables[1, :nb]]
+    host_k = np.zeros((8, Hkv, B, D), np.uint16)
+    host_v = np.zeros((8, Hkv, B, D), np.uint16)
+    host_ids = [5, 2, 7, 0][:nb]
+    assert o.copy_blocks(kc, vc, host_k, host_v, dev_ids, host_ids) == 0
+    for d, h in zip(dev_ids, host_ids):
+        assert np.array_equal(host_k[h], kc[d]) and np.array_equal(host_v[h], vc[d])
+    untouched = [i for i in range(8) if i not in host_ids]
+    assert not host_k[untouched].any() and not host_v[untouched].any()
+    used = set(int(x) for x in tables[tables >= 0].ravel())
+    free = [i for i in range(NB) if i not in used]
+    new_ids = free[:nb]
+    kc2, vc2 = kc.copy(), vc.copy()
+    assert o.copy_blocks(host_k, host_v, kc2, vc2, host_ids, new_ids) == 0
+    moved = tables.numpy().copy()
+    moved[1, :nb] = new_ids
+    after = o.decode(q, kc2, vc2, moved, lens_np, 0.1, Hkv, False)
+    assert np.array_equal(before, after)
+    # an id outside its pool leaves the pair out
+    kc3 = kc.copy()
+    assert o.copy_blocks(kc, vc, kc3, vc.copy(), [0, NB], [NB + 1, 1]) == 2
+    assert np.array_equal(kc3, kc)
+
+
 PINS = [pin_f16_exhaustive, pin_bf16_exhaustive, pin_address_worked_example, pin_byte_ledger,
-        pin_decode_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write]
+        pin_decode_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write,
+        pin_copy_on_write_fork, pin_block_moves]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -279,6 +360,7 @@ MUTANTS = {
     5: "softmax weights not normalised",
     6: "new token taken as position L instead of L - 1",
     7: "cache rows written with a [NB][B][H][D] layout",
+    8: "block copy moves kv head 0 only",
 }
 
 

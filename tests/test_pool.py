@@ -102,6 +102,90 @@ def test_copy_on_write_fork():
     assert p.refcount(c[0]) == 2 and p.refcount(c[1]) == 2
 
 
+def _cow_golden():
+    kv = {}
+    for line in (GOLDEN / "cow_worked_example.txt").read_text(encoding="utf-8").splitlines():
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, *rest = line.split()
+            kv[k] = [int(x) for x in rest]
+    return kv
+
+
+def _pool_with_prompt(prompt_len, B, keep_free):
+    """A pool in which other sequences hold every block below 96 except the prompt's two
+    blocks and `keep_free`, so that lowest-free allocation hands out the page's ids."""
+    g = _cow_golden()
+    b10, b11 = g["prompt_blocks"]
+    p = pa.BlockPool(128)
+    held = [p.alloc() for _ in range(96)]
+    for i in keep_free:
+        p.decref(i)
+    row = np.full(4, -1, dtype=np.int32)
+    row[:2] = [b10, b11]                               # the prompt owns #10 and #11 (count 1 each)
+    branch = np.full(4, -1, dtype=np.int32)
+    p.assign(branch, prompt_len, B, shared_row=row, shared_blocks=2)   # fork: count 2 each
+    return p, row, branch, held
+
+
+def test_copy_on_write_worked_example_ids():
+    """§四 of the PagedAttention explainer page, with its block numbers
+    (tests/golden/cow_worked_example.txt)."""
+    g = _cow_golden()
+    b10, b11 = g["prompt_blocks"]
+    B = 16
+    # the flowchart: the prompt fills #10 and #11, each branch's next token opens a block of its own
+    free = [g["figure_table_A"][2]] + list(range(g["figure_table_B"][2], 96))
+    p, A, Bt, _ = _pool_with_prompt(2 * B, B, free)
+    assert p.refcount(b10) == g["shared_refcount"][0] and p.refcount(b11) == g["shared_refcount"][0]
+    _, src, _ = p.append_token(A, 2 * B, B)
+    _, src2, _ = p.append_token(Bt, 2 * B, B)
+    assert (src, src2) == (-1, -1)
+    assert list(A[:3]) == g["figure_table_A"] and list(Bt[:3]) == g["figure_table_B"]
+    assert p.refcount(b10) == 2 and p.refcount(b11) == 2
+    # the numbered steps: #11 holds 4 tokens when A appends, so A copies it into #45 first
+    p, A, Bt, _ = _pool_with_prompt(B + 4, B, [g["cow_new_block"][0]])
+    slot, src, dst = p.append_token(A, B + 4, B)
+    assert (src, dst) == (b11, g["cow_new_block"][0])
+    assert list(A[:2]) == [b10, g["cow_new_block"][0]] and slot == dst * B + 4
+    assert p.refcount(b11) == g["refcount_after_cow"][0] and p.refcount(dst) == 1
+    slot, src, dst = p.append_token(Bt, B + 4, B)     # B is now #11's only owner: no copy
+    assert (src, dst) == (-1, -1) and slot == b11 * B + 4
+
+
+def test_move_blocks_swap_out_and_in():
+    """Swap a sequence out to a host pool of 0.3 x the device pool and back (the tutorial's
+    §3.4 sizing): pairs for the copy, freed and allocated blocks, shared blocks kept."""
+    dev = pa.BlockPool(40)
+    host = pa.BlockPool(12)                          # 0.3 x 40
+    B = 16
+    a = np.full(8, -1, dtype=np.int32)
+    dev.assign(a, 70, B)                             # 5 blocks: 0..4
+    b = np.full(8, -1, dtype=np.int32)
+    dev.assign(b, 40, B, shared_row=a, shared_blocks=2)   # shares 0, 1; owns 5
+    before = a.copy()
+    src, dst = dev.move_blocks(host, a, 5)
+    assert list(src) == list(before[:5]) and list(dst) == [0, 1, 2, 3, 4]
+    assert list(a[:5]) == list(dst)
+    assert dev.refcount(0) == 1 and dev.refcount(1) == 1      # still held by b
+    assert [dev.refcount(i) for i in (2, 3, 4)] == [0, 0, 0]
+    assert host.num_free == 7
+    src2, dst2 = host.move_blocks(dev, a, 5)          # swap in: lowest free device blocks
+    assert list(src2) == [0, 1, 2, 3, 4] and list(dst2) == [2, 3, 4, 6, 7]
+    assert host.num_free == 12
+    # too few free blocks: nothing changes
+    small = pa.BlockPool(2)
+    row = a.copy()
+    with pytest.raises(pa.PAError) as e:
+        dev.move_blocks(small, row, 5)
+    assert e.value.code == -4 and np.array_equal(row, a) and small.num_free == 2
+    # an entry that is not allocated in the source pool
+    bad = np.array([39, -1], dtype=np.int32)
+    with pytest.raises(pa.PAError) as e:
+        dev.move_blocks(host, bad, 1)
+    assert e.value.code == -6
+
+
 def test_assign_failure_leaves_pool_unchanged():
     p = pa.BlockPool(3)
     row = np.full(8, -1, dtype=np.int32)
