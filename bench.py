@@ -156,9 +156,10 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = True):
         self.fused = fused
         self.num_ctas = num_ctas
+        self.prefetch = prefetch
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
         self.wl = wl
@@ -183,12 +184,18 @@ class Step:
             pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
         if ev_pair is not None:
             ev_pair[0].record()
+        # the next layer's caches share this layer's block tables: their blocks are prefetched into
+        # L2 once this layer's copies are issued (the last layer of the step prefetches nothing)
+        nxt = (wl.k_cache[i + 1], wl.v_cache[i + 1]) if self.prefetch and i + 1 < wl.layers else None
         if self.fused:
             pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
-                             wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas)
+                             wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
+                             prefetch=nxt)
         else:
             pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
-                      out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas)
+                      out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
+                      prefetch=nxt if self.pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads) == 2
+                      else None)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -258,7 +265,7 @@ def run_ours(args):
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=not args.no_prefetch)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -602,6 +609,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
+    ap.add_argument("--no-prefetch", action="store_true", help="no L2 prefetch of the next layer's blocks")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
                     help="decode step (default), or the block-copy and swap benchmarks")
     args = ap.parse_args()

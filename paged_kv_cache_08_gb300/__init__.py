@@ -48,11 +48,19 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
 
 
 def _opts(tokens_per_split: int, math: str, num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
-          flags: int = 0) -> DecodeOptions:
+          flags: int = 0, prefetch=None, like: Optional[torch.Tensor] = None) -> DecodeOptions:
     if math not in MATH:
         raise ValueError(f"math must be one of {sorted(MATH)}")
+    pk = pv = None
+    if prefetch is not None:
+        pk_t, pv_t = prefetch
+        for n, t in (("prefetch k", pk_t), ("prefetch v", pv_t)):
+            _need_cuda(n, t, like.dtype)
+            if t.shape != like.shape:
+                raise ValueError(f"{n} pool must have the caches' shape")
+        pk, pv = pk_t.data_ptr(), pv_t.data_ptr()
     return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas), int(flags),
-                         timeline.data_ptr() if timeline is not None else None)
+                         timeline.data_ptr() if timeline is not None else None, pk, pv)
 
 
 def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
@@ -150,11 +158,13 @@ def _workspace(device: torch.device, nbytes: int, kind: int, num_ctas: int) -> O
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, scale: float, num_kv_heads: int, out: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, tokens_per_split: int = 0, math: str = "auto",
-           num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
+           num_ctas: int = 0, timeline: Optional[torch.Tensor] = None, prefetch=None,
            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Paged decode attention.  q: [S, Hq, D]; caches [NB, Hkv, B, D]; block_tables int32
     [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype.
-    ``timeline``: optional int64 CUDA tensor [num_ctas, 16] receiving the persistent kernel's trace."""
+    ``timeline``: optional int64 CUDA tensor [num_ctas, 16] receiving the persistent kernel's trace.
+    ``prefetch``: optional (k, v) pools of the caches' shape (the next layer's) whose blocks of
+    this call the persistent kernel asks the L2 to prefetch."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -175,7 +185,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(tokens_per_split, math, num_ctas, timeline)
+    o = _opts(tokens_per_split, math, num_ctas, timeline, prefetch=prefetch, like=k_cache)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))
@@ -194,10 +204,10 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                   num_kv_heads: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                   num_ctas: int = 0, early_reads: bool = True, timeline: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                  prefetch=None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Cache write of each sequence's newest token (position context_lens[s] - 1) and decode
     attention, in one launch.  k_new, v_new: [S, Hkv, D].  See pa_decode_append in include/pa.h
-    for the early-read contract (disable with early_reads=False)."""
+    for the early-read contract (disable with early_reads=False); ``prefetch`` as for decode."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -218,7 +228,8 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
         out = torch.empty_like(q)
     else:
         _need_cuda("out", out, q.dtype)
-    o = _opts(0, "mma", num_ctas, timeline, 0 if early_reads else _native.NO_EARLY_READS)
+    o = _opts(0, "mma", num_ctas, timeline, 0 if early_reads else _native.NO_EARLY_READS, prefetch=prefetch,
+              like=k_cache)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))

@@ -23,7 +23,7 @@ c_u32p = ctypes.POINTER(ctypes.c_uint32)
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("tokens_per_split", c_int), ("math", c_int), ("num_ctas", c_int), ("flags", c_int),
-                ("timeline", c_vp)]
+                ("timeline", c_vp), ("prefetch_k_cache", c_vp), ("prefetch_v_cache", c_vp)]
 
 
 PA_OK = 0

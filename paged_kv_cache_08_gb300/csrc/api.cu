@@ -355,6 +355,9 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (opts && (opts->math < PA_MATH_AUTO || opts->math > PA_MATH_MMA_SPLIT || opts->num_ctas < 0))
         return PA_ERR_INVALID_ARG;
+    if (opts && (!aligned16(opts->prefetch_k_cache) || !aligned16(opts->prefetch_v_cache) ||
+                 (opts->prefetch_k_cache == nullptr) != (opts->prefetch_v_cache == nullptr)))
+        return PA_ERR_INVALID_ARG;
     if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !block_tables || !context_lens || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
@@ -403,6 +406,8 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.k_new = k_new;
         a.v_new = v_new;
         a.early = (append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS))) ? 1 : 0;
+        a.pf_k = opts ? opts->prefetch_k_cache : nullptr;
+        a.pf_v = opts ? opts->prefetch_v_cache : nullptr;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();

@@ -154,6 +154,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -692,6 +696,24 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             cur = nxt;
         }
         if (!deps_done) dependency_point(i);
+        if (ok && a.pf_k != nullptr) {
+            // the same chunks' blocks in the prefetch pools (the next layer): lane j takes chunk
+            // gbase + j; each (block, kv head) run of rows is one L2 prefetch per pool
+            const int R = 1 << R_log2;
+            const uint32_t run = (uint32_t)R * kHeadDim * 2u;
+            for (long long gbase = b_c; gbase < b_e; gbase += 32) {
+                const ChunkDesc d = describe(a, P, Lc, S, Hkv, b_c, b_e, gbase + lane);
+                const int within = (B > kStageTokens) ? (d.t0 % B) : 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (e < d.nblk && d.ids[e] >= 0) {
+                        const size_t off = (((size_t)d.ids[e] * Hkv + d.h) * B + within) * kHeadDim * 2;
+                        prefetch_l2(static_cast<const char*>(a.pf_k) + off, run);
+                        prefetch_l2(static_cast<const char*>(a.pf_v) + off, run);
+                    }
+                }
+            }
+        }
         if (lane == 0) {
             *issued_count = i;
             trace_put(a.timeline, c, kTrWaitEmpty, wait_empty_ns);

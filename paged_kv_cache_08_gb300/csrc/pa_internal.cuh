@@ -73,6 +73,8 @@ struct DecodeArgs {
     const void* k_new;        // append mode: the new token's K and V rows [S][Hkv][D], written at
     const void* v_new;        //   position context_lens[s] - 1 before attention reads it; null = off
     int early;                // K/V of the first stages may be fetched before the preceding kernel ends
+    const void* pf_k;         // optional: pools whose blocks of this call's chunks are prefetched into L2
+    const void* pf_v;
 };
 
 constexpr int kTimelineSlots = 16;
