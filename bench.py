@@ -156,7 +156,7 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = True):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = False):
         self.fused = fused
         self.num_ctas = num_ctas
         self.prefetch = prefetch
@@ -265,7 +265,7 @@ def run_ours(args):
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=not args.no_prefetch)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=args.prefetch)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -609,7 +609,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
-    ap.add_argument("--no-prefetch", action="store_true", help="no L2 prefetch of the next layer's blocks")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
                     help="decode step (default), or the block-copy and swap benchmarks")
     args = ap.parse_args()
