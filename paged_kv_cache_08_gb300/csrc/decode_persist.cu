@@ -16,9 +16,12 @@
 //
 // Inside a CTA: one producer warp issues, per chunk, the 2-D TMA tensor loads of the K and V
 // rows (128-byte swizzle) and, at the first chunk of a segment, a bulk copy of the segment's
-// query rows; four consumer warps each own 16 of the chunk's 64 tokens and run
-//   S = Q K^T and O += P V  with mma.sync m16n8k16 (fp32 accumulation),
-// keeping a running max / sum per query row.  At a segment's last chunk the four warps merge
+// query rows; four consumer warps each own 16 of the chunk's 64 tokens and run the products
+// transposed, tokens and head dimensions on the 16-row side of mma.sync m16n8k16 and the GQA
+// group's query rows on its 8-column side:
+//   S^T = K Q^T  and  O^T += V^T P^T   (fp32 accumulation),
+// so that a group of up to 8 query rows fills every row of every product, keeping a running
+// max / sum per query row.  At a segment's last chunk the four warps merge
 // through the stage buffer they just consumed.  Full / empty mbarriers per stage connect the
 // producer and the consumers; every wait is bounded.
 //
@@ -46,7 +49,7 @@ constexpr int kEpilogueWarp = kConsumerWarps + 1;  // finishes the range's first
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
 constexpr int kKVBytes = 2 * kKBytes;
-constexpr int kRedStride = kHeadDim + 8;                // padded rows of the merge scratch
+constexpr int kRedStride = kHeadDim + 4;                // padded rows of the merge scratch (bank spread)
 constexpr int kMergeBatch = 4;                          // pieces whose loads are in flight together
 
 // Trace slots of one CTA: event times (global ns), then accumulated times and counters.
@@ -118,6 +121,13 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], uint32_t 
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as one mma fragment register per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -371,39 +381,51 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, 
 // the epilogue warp (`handoff`: every consumer thread arrives on `pdone` after its stores) or
 // finished here: count the arrival and, as the last CTA of the segment to arrive, merge all
 // pieces.  Returns true if this call merged a cut segment.
-template <typename T>
+template <typename T, int kNT>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e, long long N, int C,
-                                              int c, const float (&o)[16][4], const float (&m_run)[2],
-                                              const float (&l_run)[2], bool dead, volatile int* last_flag,
+                                              int c, const float (&o)[kNT][8][4], const float (&m_run)[kNT][2],
+                                              const float (&l_run)[kNT][2], bool dead, volatile int* last_flag,
                                               bool handoff, uint64_t* pdone) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qr = lane >> 2, qc = (lane & 3) * 2;
+    const int gid = lane >> 2, tig = lane & 3;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
     const long long Pseg = (long long)P[pos.s] + (long long)pos.h * pos.n;
     const bool whole = (Pseg >= b_c) && (Pseg + pos.n <= b_e);
-    float lr[2];
+    // row sums: each lane holds a partial over its own tokens; the 8 lanes of a row share tig
+    float lr[kNT][2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        lr[r] = l_run[r];
-        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
-        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
-    }
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v = l_run[nt][j];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            lr[nt][j] = v;
+        }
     float* red_o = reinterpret_cast<float*>(scratch);                             // [4][8][kRedStride]
     float2* red_ml = reinterpret_cast<float2*>(red_o + kConsumerWarps * 8 * kRedStride);  // [4][8]
     const size_t piece = (size_t)c * 2 + ((Pseg <= b_c) ? 0 : 1);
     consumers_sync();   // every warp is past its reads of the stage
-    for (int rg = 0; rg < G; rg += 8) {
-        const bool hi = rg >= 8;   // rows 0..7 live in (c0, c1), rows 8..15 in (c2, c3)
-        if (rg + qr < G) {   // only the group's real query rows
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float v0 = hi ? o[j][2] : o[j][0];
-                const float v1 = hi ? o[j][3] : o[j][1];
-                *reinterpret_cast<float2*>(&red_o[(warp * 8 + qr) * kRedStride + j * 8 + qc]) = make_float2(v0, v1);
+    for (int nt = 0; nt < kNT; ++nt) {
+        const int rg = nt * 8;   // query rows rg + 0..7 of the group
+        if (rg >= G) break;
+        // O^T fragment: o[nt][mt][j] = O[row tig*2 + j][dim mt*16 + gid], o[nt][mt][2 + j] the
+        // same row at dim + 8; only the group's real query rows are written
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int row = tig * 2 + j;
+            if (rg + row < G) {
+                float* dst = &red_o[(warp * 8 + row) * kRedStride + gid];
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    dst[mt * 16] = o[nt][mt][j];
+                    dst[mt * 16 + 8] = o[nt][mt][2 + j];
+                }
+                if (gid == 0) red_ml[warp * 8 + row] = make_float2(m_run[nt][j], lr[nt][j]);
             }
-            if ((lane & 3) == 0)
-                red_ml[warp * 8 + qr] = hi ? make_float2(m_run[1], lr[1]) : make_float2(m_run[0], lr[0]);
         }
         consumers_sync();
         const int r = tid >> 4;            // row within the group of 8
@@ -756,16 +778,23 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         }
     } else {
         // ================= consumer warps =================
-        const int qr = lane >> 2, qc = (lane & 3) * 2;
+        constexpr int kNT = kG16 ? 2 : 1;   // 8-row column tiles of the GQA group
+        const int gid = lane >> 2, tig = lane & 3;
         const int t_warp = warp * 16;
-        const int tk = t_warp + (lane & 7) + ((lane >> 4) << 3);
-        const int ck = (lane >> 3) & 1;
-        const int tv = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int cv = lane >> 4;
-        float m_run[2] = {-INFINITY, -INFINITY};
-        float l_run[2] = {0.f, 0.f};
-        float o[16][4];
-        uint32_t qa[8][4];
+        // ldmatrix row addresses: K tile as the A operand (tokens x dims), V tile transposed as
+        // the A operand (dims x tokens)
+        const int tokA = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int chA = lane >> 4;
+        const int tokV = t_warp + (lane & 7) + ((lane >> 4) << 3);
+        const int chV = (lane >> 3) & 1;
+        float m_run[kNT][2], l_run[kNT][2];
+        float o[kNT][8][4];
+        uint32_t qb[8][kNT][2];   // Q^T as the B operand: [k-step][column tile][2 registers]
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+            m_run[nt][0] = m_run[nt][1] = -INFINITY;
+            l_run[nt][0] = l_run[nt][1] = 0.f;
+        }
         if (a.early) {
             grid_dependency_wait();   // q, the new rows and every output belong after this point
             grid_launch_dependents();
@@ -813,26 +842,24 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 }
             }
             if (seg_begin && !dead) {
-                // query rows of the segment's G heads, as mma A fragments (rows >= G are zero)
+                // B fragments of Q^T: register 0 = Q[row][ks*16 + tig*2 + {0,1}], register 1 the
+                // same at + 8, row = nt*8 + gid; rows >= G are zero
                 const uint32_t* qs = reinterpret_cast<const uint32_t*>(base_ptr + (size_t)st * Lay::kStageBytes +
                                                                        kKVBytes);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int wcol = (ks * 16 + qc) >> 1;
-                    qa[ks][0] = (qr < G) ? qs[qr * 64 + wcol] : 0u;
-                    qa[ks][2] = (qr < G) ? qs[qr * 64 + wcol + 4] : 0u;
-                    if (kG16) {
-                        qa[ks][1] = (qr + 8 < G) ? qs[(qr + 8) * 64 + wcol] : 0u;
-                        qa[ks][3] = (qr + 8 < G) ? qs[(qr + 8) * 64 + wcol + 4] : 0u;
-                    } else {
-                        qa[ks][1] = 0u;
-                        qa[ks][3] = 0u;
-                    }
-                }
-                m_run[0] = m_run[1] = -INFINITY;
-                l_run[0] = l_run[1] = 0.f;
+                for (int nt = 0; nt < kNT; ++nt) {
+                    const int row = nt * 8 + gid;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int wcol = (ks * 16 + tig * 2) >> 1;
+                        qb[ks][nt][0] = (row < G) ? qs[row * 64 + wcol] : 0u;
+                        qb[ks][nt][1] = (row < G) ? qs[row * 64 + wcol + 4] : 0u;
+                    }
+                    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+                    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+                }
             }
             const int nvalid = min(kStageTokens, pos.L - pos.k * kStageTokens);
 
@@ -865,69 +892,77 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // S^T = K Q^T over the warp's 16 tokens: two accumulator chains (even / odd k-steps)
+                float sc[kNT][4], sc2[kNT][4];
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] = sc2[nt][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(chunk_addr(kbase, tk, 2 * ks + ck, R_log2), b0, b1, b2, b3);
-                    mma16816<T>(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                    mma16816<T>(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-                }
-                float p[2][4];
-                float mx[2] = {-INFINITY, -INFINITY};
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(chunk_addr(kbase, tokA, 2 * ks + chA, R_log2), a0, a1, a2, a3);
 #pragma unroll
-                for (int n = 0; n < 2; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = t_warp + n * 8 + qc + (e & 1);
-                        const float x = sc[n][e] * a.scale_log2;
-                        p[n][e] = (col < nvalid) ? x : -INFINITY;
-                        mx[e >> 1] = fmaxf(mx[e >> 1], p[n][e]);
+                    for (int nt = 0; nt < kNT; ++nt) {
+                        if (ks & 1) mma16816<T>(sc2[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+                        else mma16816<T>(sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
                     }
-                float alpha[2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                    const float m_new = fmaxf(m_run[r], mx[r]);
-                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    alpha[r] = exp2f(m_run[r] - m_use);
-                    m_run[r] = m_new;
-                    mx[r] = m_use;
                 }
-                float rs[2] = {0.f, 0.f};
+                // online softmax per query row: lane holds rows tig*2 + j at tokens gid and gid + 8;
+                // the 8 lanes of a row (same tig) reduce with xor 4, 8, 16
+                const bool tok0_ok = t_warp + gid < nvalid, tok1_ok = t_warp + gid + 8 < nvalid;
+                float alpha[kNT][2];
+                uint32_t pb[kNT][2];
 #pragma unroll
-                for (int n = 0; n < 2; ++n)
+                for (int nt = 0; nt < kNT; ++nt) {
+                    float pv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        p[n][e] = exp2f(p[n][e] - mx[e >> 1]);
-                        rs[e >> 1] += p[n][e];
+                    for (int j = 0; j < 2; ++j) {
+                        const float x0 = tok0_ok ? (sc[nt][j] + sc2[nt][j]) * a.scale_log2 : -INFINITY;
+                        const float x1 = tok1_ok ? (sc[nt][2 + j] + sc2[nt][2 + j]) * a.scale_log2 : -INFINITY;
+                        float mx = fmaxf(x0, x1);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[nt][j], mx);
+                        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                        alpha[nt][j] = exp2f(m_run[nt][j] - m_use);
+                        m_run[nt][j] = m_new;
+                        pv[j] = exp2f(x0 - m_use);
+                        pv[2 + j] = exp2f(x1 - m_use);
+                        l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + (pv[j] + pv[2 + j]);
                     }
-                l_run[0] = l_run[0] * alpha[0] + rs[0];
-                l_run[1] = l_run[1] * alpha[1] + rs[1];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    o[j][0] *= alpha[0];
-                    o[j][1] *= alpha[0];
-                    o[j][2] *= alpha[1];
-                    o[j][3] *= alpha[1];
+                    // P^T as the B operand: the C fragment (tokens x rows) transposed per 8x8 block
+                    pb[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0], pv[1]));
+                    pb[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2], pv[3]));
                 }
-                const uint32_t pa0 = Elem<T>::pack2(p[0][0], p[0][1]);
-                const uint32_t pa1 = Elem<T>::pack2(p[0][2], p[0][3]);
-                const uint32_t pa2 = Elem<T>::pack2(p[1][0], p[1][1]);
-                const uint32_t pa3 = Elem<T>::pack2(p[1][2], p[1][3]);
+                bool rescale = false;
 #pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(chunk_addr(vbase, tv, 2 * np + cv, R_log2), b0, b1, b2, b3);
-                    mma16816<T>(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
-                    mma16816<T>(o[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                for (int nt = 0; nt < kNT; ++nt) rescale = rescale || alpha[nt][0] != 1.f || alpha[nt][1] != 1.f;
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            o[nt][mt][0] *= alpha[nt][0];
+                            o[nt][mt][1] *= alpha[nt][1];
+                            o[nt][mt][2] *= alpha[nt][0];
+                            o[nt][mt][3] *= alpha[nt][1];
+                        }
+                }
+                // O^T += V^T P^T, one 16-dim tile of V^T at a time
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(chunk_addr(vbase, tokV, 2 * mt + chV, R_log2), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt) mma16816<T>(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
             }
 
             if (seg_end) {
                 const unsigned long long tf = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
-                const bool merged = flush_segment<T>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
+                const bool merged = flush_segment<T, kNT>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
                                                      C, c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone);
                 if (a.timeline && tid == 0) {
                     flush_ns += global_timer_ns() - tf;
