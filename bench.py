@@ -156,7 +156,9 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = False):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = False,
+                 prefetch_own: bool = False):
+        self.prefetch_own = prefetch_own
         self.fused = fused
         self.num_ctas = num_ctas
         self.prefetch = prefetch
@@ -190,7 +192,7 @@ class Step:
         if self.fused:
             pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
                              wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
-                             prefetch=nxt)
+                             prefetch=nxt, prefetch_own=self.prefetch_own)
         else:
             pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
                       out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
@@ -265,7 +267,7 @@ def run_ours(args):
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=args.prefetch)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=args.prefetch, prefetch_own=args.prefetch_own)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -611,6 +613,8 @@ def main():
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
     ap.add_argument("--prefetch", action="store_true",
                     help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
+    ap.add_argument("--prefetch-own", action="store_true",
+                    help="each layer prefetches its own chunks beyond the copy pipeline before its dependency wait")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
                     help="decode step (default), or the block-copy and swap benchmarks")
     args = ap.parse_args()

@@ -207,6 +207,9 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
                      int max_blocks_per_seq, int dtype, void* stream);
 
 #define PA_DECODE_NO_EARLY_READS 1
+/* pa_decode_append with early reads: before waiting for the preceding kernel, each CTA also
+ * asks the L2 to prefetch the blocks of its chunks that do not fit its copy pipeline. */
+#define PA_DECODE_PREFETCH_OWN 2
 
 /* ------------------------------------------------------------------------------------
  * pa_decode_append  [P4 §三 sequence diagram + §五.1; P1 address formula]

@@ -204,7 +204,8 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                   num_kv_heads: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                   num_ctas: int = 0, early_reads: bool = True, timeline: Optional[torch.Tensor] = None,
-                  prefetch=None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                  prefetch=None, prefetch_own: bool = False,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Cache write of each sequence's newest token (position context_lens[s] - 1) and decode
     attention, in one launch.  k_new, v_new: [S, Hkv, D].  See pa_decode_append in include/pa.h
     for the early-read contract (disable with early_reads=False); ``prefetch`` as for decode."""
@@ -228,8 +229,8 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
         out = torch.empty_like(q)
     else:
         _need_cuda("out", out, q.dtype)
-    o = _opts(0, "mma", num_ctas, timeline, 0 if early_reads else _native.NO_EARLY_READS, prefetch=prefetch,
-              like=k_cache)
+    flags = (0 if early_reads else _native.NO_EARLY_READS) | (_native.PREFETCH_OWN if prefetch_own else 0)
+    o = _opts(0, "mma", num_ctas, timeline, flags, prefetch=prefetch, like=k_cache)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))

@@ -33,6 +33,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "P
 DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 NO_EARLY_READS = 1
+PREFETCH_OWN = 2
 
 _SIGNATURES = {
     "pa_cache_write": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp]),

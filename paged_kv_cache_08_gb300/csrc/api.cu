@@ -408,6 +408,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.early = (append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS))) ? 1 : 0;
         a.pf_k = opts ? opts->prefetch_k_cache : nullptr;
         a.pf_v = opts ? opts->prefetch_v_cache : nullptr;
+        a.pf_own = (a.early && opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) ? 1 : 0;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();

@@ -181,6 +181,14 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
+// Arrival on a cut segment's counter: release publishes the partial stores that precede it (this
+// thread's, and the CTA's through the barrier before it); acquire orders the merge's reads after.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ float4 ld_cg4(const float* p) {
     float4 v;
     asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
@@ -478,21 +486,20 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     }
     if (!whole) {
         // ---- pieces of a cut segment: the last CTA to arrive merges them ----
-        __threadfence();
-        consumers_sync();
+        // (the barrier that closed the loop above orders every thread's partial stores before
+        // thread 0's release)
         const int sigma = pos.s * Hkv + pos.h;
         const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + pos.n - 1, N, C);
         if (tid == 0) {
             *last_flag = 0;
             if (!dead) {
-                const int prev = atomicAdd(&a.seg_counters[sigma], 1);
+                const int prev = atom_add_acq_rel_gpu(&a.seg_counters[sigma], 1);
                 *last_flag = (prev == c_last - c_first) ? 1 : 0;
             }
         }
         consumers_sync();
         const bool last = *last_flag != 0 && !dead;
         if (last) {
-            __threadfence();
             merge_pieces<T>(a, pos.s, pos.h, Pseg, pos.n, N, C, tid, kConsumerThreads);
             if (tid == 0) a.seg_counters[sigma] = 0;   // ready for the next call
         }
@@ -618,8 +625,28 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         bool deps_done = false;
         // After the preceding kernel has finished (early mode), fetch the q rows of the first
         // stages onto their own barrier: they may be that kernel's output.
+        // L2 prefetch of the blocks of chunks [g0, g1) of this range in the pools (pk, pv): lane j
+        // takes chunk g0 + j + 32 m; each (block, kv head) run of rows is one prefetch per pool
+        auto prefetch_chunks = [&](const void* pk, const void* pv, long long g0, long long g1) {
+            const int R = 1 << R_log2;
+            const uint32_t run = (uint32_t)R * kHeadDim * 2u;
+            for (long long gbase = g0; gbase < g1; gbase += 32) {
+                const ChunkDesc d = describe(a, P, Lc, S, Hkv, b_c, g1, gbase + lane);
+                const int within = (B > kStageTokens) ? (d.t0 % B) : 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (e < d.nblk && d.ids[e] >= 0) {
+                        const size_t off = (((size_t)d.ids[e] * Hkv + d.h) * B + within) * kHeadDim * 2;
+                        prefetch_l2(static_cast<const char*>(pk) + off, run);
+                        prefetch_l2(static_cast<const char*>(pv) + off, run);
+                    }
+                }
+            }
+        };
         auto dependency_point = [&](int issued) {
             if (a.early) {
+                // the rest of the range will find its rows in L2 once stages free up
+                if (a.pf_own && b_c + kStages < b_e) prefetch_chunks(a.k_cache, a.v_cache, b_c + kStages, b_e);
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
@@ -718,24 +745,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             cur = nxt;
         }
         if (!deps_done) dependency_point(i);
-        if (ok && a.pf_k != nullptr) {
-            // the same chunks' blocks in the prefetch pools (the next layer): lane j takes chunk
-            // gbase + j; each (block, kv head) run of rows is one L2 prefetch per pool
-            const int R = 1 << R_log2;
-            const uint32_t run = (uint32_t)R * kHeadDim * 2u;
-            for (long long gbase = b_c; gbase < b_e; gbase += 32) {
-                const ChunkDesc d = describe(a, P, Lc, S, Hkv, b_c, b_e, gbase + lane);
-                const int within = (B > kStageTokens) ? (d.t0 % B) : 0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (e < d.nblk && d.ids[e] >= 0) {
-                        const size_t off = (((size_t)d.ids[e] * Hkv + d.h) * B + within) * kHeadDim * 2;
-                        prefetch_l2(static_cast<const char*>(a.pf_k) + off, run);
-                        prefetch_l2(static_cast<const char*>(a.pf_v) + off, run);
-                    }
-                }
-            }
-        }
+        // the same chunks' blocks in the prefetch pools (the next layer)
+        if (ok && a.pf_k != nullptr) prefetch_chunks(a.pf_k, a.pf_v, b_c, b_e);
         if (lane == 0) {
             *issued_count = i;
             trace_put(a.timeline, c, kTrWaitEmpty, wait_empty_ns);
@@ -757,17 +768,14 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     *abort_flag = 1;
                 }
             } else if (*abort_flag == 0) {
-                // acquired through pdone: the consumers' partial stores; the fence publishes them
+                // acquired through pdone: the consumers' partial stores; the release publishes them
                 const int sigma = p0.s * Hkv + p0.h;
                 const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + p0.n - 1, N, C);
                 int last = 0;
-                if (lane == 0) {
-                    __threadfence();
-                    last = atomicAdd(&a.seg_counters[sigma], 1) == c_last - c_first;
-                }
+                if (lane == 0) last = atom_add_acq_rel_gpu(&a.seg_counters[sigma], 1) == c_last - c_first;
                 last = __shfl_sync(0xffffffffu, last, 0);
+                __syncwarp();   // the lanes' merge reads come after lane 0's acquire
                 if (last) {
-                    __threadfence();
                     merge_pieces<T>(a, p0.s, p0.h, Pseg, p0.n, N, C, lane, 32);
                     if (lane == 0) {
                         a.seg_counters[sigma] = 0;   // ready for the next call

@@ -75,6 +75,7 @@ struct DecodeArgs {
     int early;                // K/V of the first stages may be fetched before the preceding kernel ends
     const void* pf_k;         // optional: pools whose blocks of this call's chunks are prefetched into L2
     const void* pf_v;
+    int pf_own;               // early mode: prefetch this range's chunks beyond the ring into L2 before the wait
 };
 
 constexpr int kTimelineSlots = 16;

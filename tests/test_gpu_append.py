@@ -115,8 +115,9 @@ def test_append_rejects_shapes_outside_the_persistent_kernel():
 
 
 def test_append_with_next_layer_prefetch(oracle):
-    """The L2 prefetch of the next layer's blocks is a hint: results are bit-identical with and
-    without it, and match the oracle on both layers."""
+    """The L2 prefetches (the next layer's blocks; the range's own blocks beyond the copy
+    pipeline) are hints: results are bit-identical with and without them, and match the oracle
+    on both layers."""
     wl = workloads.config(2, layers=2)
     dev = torch.device("cuda")
     bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
@@ -128,7 +129,7 @@ def test_append_with_next_layer_prefetch(oracle):
         for i in range(2):
             nxt = (kcs[1], vcs[1]) if pf and i == 0 else None
             res.append(pa.decode_append(wl.q[i].to(dev), wl.k_new[i].to(dev), wl.v_new[i].to(dev), kcs[i], vcs[i],
-                                        bt, lens, wl.scale, wl.num_kv_heads, prefetch=nxt))
+                                        bt, lens, wl.scale, wl.num_kv_heads, prefetch=nxt, prefetch_own=pf))
         torch.cuda.synchronize()
         outs[pf] = (res, kcs, vcs)
     for i in range(2):
