@@ -18,6 +18,10 @@ it follows:
 * ``cache_write`` -- byte copy of each new (token, kv-head) row into its slot (§三 of the second page).
 * ``decode`` -- out = softmax(scale * q K^T) V over the rows gathered through the
   block table, in fp64 (§五.1 kernel sketch of the second page).
+* ``multi_query`` -- the same for several new query tokens per sequence, each attending
+  causally up to its own position (the chunked prefill the second page's closing section
+  points to).
+* ``copy_blocks`` -- whole-block deep copy (§四 copy-on-write of the second page).
 
 Pins (tests/test_oracle.py): exhaustive element decoding against numpy, the
 pages' worked address example and byte counts, torch's fp64
@@ -90,6 +94,9 @@ class Oracle:
         L.pao_copy_blocks.restype = _c_int
         L.pao_copy_blocks.argtypes = [_ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _c_int, _c_int,
                                       _c_int]
+        L.pao_multi_query.restype = _c_int
+        L.pao_multi_query.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _c_int, _ptr, _ptr, ctypes.c_double,
+                                      _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]
         L.pao_num_threads.restype = _c_int
         L.pao_num_threads.argtypes = []
 
@@ -163,6 +170,27 @@ class Oracle:
                                 int(num_kv_heads), D, B, int(is_bf16), int(num_threads))
         if rc != 0:
             raise ValueError("oracle: arguments do not describe a valid decode problem")
+        return out
+
+    def multi_query(self, q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+                    num_kv_heads: int, is_bf16: bool, num_threads: int = 0) -> np.ndarray:
+        """Several new query tokens per sequence, causal over the paged context: q [T, Hq, D]
+        with sequence s owning rows query_start[s] .. query_start[s+1]-1 (its newest tokens)."""
+        qq = as_u16(q)
+        kc, vc = as_u16(k_cache), as_u16(v_cache)
+        bt = as_i32(block_tables)
+        lens = as_i32(context_lens)
+        qs = as_i32(query_start)
+        T, Hq, D = qq.shape
+        S = lens.size
+        assert qs.size == S + 1 and int(qs[-1]) == T
+        B = kc.shape[2]
+        out = np.empty((T, Hq, D), dtype=np.float64)
+        rc = self._L.pao_multi_query(out.ctypes.data, qq.ctypes.data, kc.ctypes.data, vc.ctypes.data,
+                                     bt.ctypes.data, bt.shape[1], lens.ctypes.data, qs.ctypes.data, float(scale),
+                                     S, Hq, int(num_kv_heads), D, B, int(is_bf16), int(num_threads))
+        if rc != 0:
+            raise ValueError("oracle: arguments do not describe a valid multi-query problem")
         return out
 
     def num_threads(self) -> int:

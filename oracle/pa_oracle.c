@@ -271,6 +271,74 @@ int pao_decode(double* out, const uint16_t* q, const uint16_t* k_cache, const ui
     return bad ? -1 : 0;
 }
 
+/* ---- several new query tokens per sequence (chunked prefill, speculative verification) ----
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1: its n_s newest tokens,
+ * which are the last n_s of its context_lens[s] = L_s cached tokens.  Query token i sits at
+ * position L_s - n_s + i and attends causally, over the cached tokens t = 0 .. L_s - n_s + i.
+ * With n_s = 1 this is pao_decode.  q, out: [num_q_tokens][num_q_heads][head_dim].
+ * Returns 0, or -1 when the arguments cannot describe a valid problem (n_s < 0 or > L_s). */
+int pao_multi_query(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                    const int32_t* query_start, double scale, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, int is_bf16, int num_threads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0)
+        return -1;
+    const int G = num_q_heads / num_kv_heads;
+    const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : bad)
+#endif
+    for (int64_t pr = 0; pr < pairs; ++pr) {
+        const int s = (int)(pr / num_kv_heads);
+        const int hk = (int)(pr % num_kv_heads);
+        const int L = context_lens[s];
+        const int n = query_start[s + 1] - query_start[s];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size || n < 0 || n > L) { bad = 1; continue; }
+        const int32_t* row = block_tables + (int64_t)s * max_blocks;
+        double* K = (double*)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double* V = (double*)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double* z = (double*)malloc(sizeof(double) * ((size_t)L + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        gather(k_cache, row, L, hk, num_kv_heads, head_dim, block_size, is_bf16, K);
+        gather(v_cache, row, L, hk, num_kv_heads, head_dim, block_size, is_bf16, V);
+        for (int i = 0; i < n; ++i) {
+#if PAO_MUTANT == 9
+            const int last = L - n + i - 1;                      /* planted: a query misses itself */
+#else
+            const int last = L - n + i;                          /* newest position query i sees */
+#endif
+            const int64_t qrow = query_start[s] + i;
+            for (int g = 0; g < G; ++g) {
+                const int h = hk * G + g;
+                double* o = out + (qrow * num_q_heads + h) * head_dim;
+                const uint16_t* qr = q + (qrow * num_q_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d) qv[d] = elem(qr + d, is_bf16);
+                double zmax = -INFINITY;
+                for (int t = 0; t <= last; ++t) {
+                    double acc = 0.0;
+                    for (int d = 0; d < head_dim; ++d) acc += qv[d] * K[(int64_t)t * head_dim + d];
+                    z[t] = scale * acc;
+                    if (z[t] > zmax) zmax = z[t];
+                }
+                double denom = 0.0;
+                for (int t = 0; t <= last; ++t) {
+                    z[t] = exp(z[t] - zmax);
+                    denom += z[t];
+                }
+                for (int d = 0; d < head_dim; ++d) {
+                    double acc = 0.0;
+                    for (int t = 0; t <= last; ++t) acc += z[t] * V[(int64_t)t * head_dim + d];
+                    o[d] = (last >= 0) ? acc / denom : 0.0;
+                }
+            }
+        }
+        free(K); free(V); free(z); free(qv);
+    }
+    return bad ? -1 : 0;
+}
+
 int pao_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -10,6 +10,9 @@
   forms (one token, zero query, equal keys, one dominant score, two tokens);
 * cache write: the worked example's slots, plus a canary fill showing that
   nothing but the addressed rows changes;
+* several query tokens per sequence: torch's fp64 attention with an explicit causal mask on
+  the unpaged data (full causal prefill, one token, none), and bit-for-bit the decode at one
+  token per sequence;
 * block copy: the copy-on-write fork of the PagedAttention explainer page
   (tests/golden/cow_worked_example.txt) checked against torch's fp64 attention on
   each branch's contiguous context, and a move to another pool and back that must
@@ -341,9 +344,42 @@ def pin_block_moves(o):
     assert np.array_equal(kc3, kc)
 
 
+def pin_multi_query_vs_sdpa(o):
+    """Several new query tokens per sequence: each attends causally over the paged context up
+    to its own position.  Checked against torch's fp64 attention with an explicit mask on the
+    unpaged data: ragged contexts, a full causal prefill (n = L), one token (n = 1) and no new
+    token (n = 0); n = 1 must also reproduce the decode bit for bit."""
+    lens = [37, 16, 5, 64, 1, 20]
+    nq = [4, 16, 5, 1, 1, 0]
+    B, Hkv, G, D = 16, 2, 3, 128
+    Hq = Hkv * G
+    q1, Kc, Vc, kc, vc, tables = _paged_problem(lens, Hq, Hkv, D, B, seed=123)
+    gen = torch.Generator().manual_seed(321)
+    T = sum(nq)
+    q = _rand16((T, Hq, D), gen)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    scale = 1.0 / math.sqrt(D)
+    got = o.multi_query(q, kc, vc, tables, np.array(lens, np.int32), qs, scale, Hkv, False)
+    for s, (L, n) in enumerate(zip(lens, nq)):
+        if n == 0:
+            continue
+        qq = q[qs[s]:qs[s + 1]].to(torch.float64).permute(1, 0, 2)[None]          # [1, Hq, n, D]
+        kk = Kc[s].to(torch.float64).repeat_interleave(G, dim=0)[None]             # [1, Hq, L, D]
+        vv = Vc[s].to(torch.float64).repeat_interleave(G, dim=0)[None]
+        pos = torch.arange(L - n, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos                                      # [n, L]
+        want = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)[0].permute(1, 0, 2)
+        assert np.max(np.abs(got[qs[s]:qs[s + 1]] - want.numpy())) < 1e-12, s
+    # one new token per sequence is the decode
+    dec = o.decode(q1, kc, vc, tables, np.array(lens, np.int32), scale, Hkv, False)
+    one = o.multi_query(q1, kc, vc, tables, np.array(lens, np.int32), np.arange(len(lens) + 1, dtype=np.int32),
+                        scale, Hkv, False)
+    assert np.array_equal(dec, one)
+
+
 PINS = [pin_f16_exhaustive, pin_bf16_exhaustive, pin_address_worked_example, pin_byte_ledger,
         pin_decode_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write,
-        pin_copy_on_write_fork, pin_block_moves]
+        pin_copy_on_write_fork, pin_block_moves, pin_multi_query_vs_sdpa]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -361,6 +397,7 @@ MUTANTS = {
     6: "new token taken as position L instead of L - 1",
     7: "cache rows written with a [NB][B][H][D] layout",
     8: "block copy moves kv head 0 only",
+    9: "a query token does not attend to its own position",
 }
 
 
