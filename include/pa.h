@@ -237,6 +237,31 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
                      void* workspace, size_t workspace_bytes, void* stream,
                      const pa_decode_options* opts);
 
+/* ------------------------------------------------------------------------------------
+ * pa_multi_query  [P4 §五.1 attention over the paged cache; P4's closing section on
+ *                  chunked prefill: several new tokens of a sequence at once]
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1 of q and out
+ * ([num_q_tokens][num_q_heads][head_dim]): its n_s newest tokens, which are the last n_s of its
+ * L = context_lens[s] cached tokens (their K/V already written, e.g. by pa_cache_write).
+ * Query token i sits at position L - n_s + i and attends causally:
+ *   out[row][h][:] = sum_{t <= L - n_s + i} softmax_t(scale * q[row][h] . K[t]) * V[t][:]
+ * with row = query_start[s] + i and K/V of kv head h / (num_q_heads / num_kv_heads).
+ * n_s = 1 everywhere is pa_decode.  query_start: int32 [num_seqs + 1], non-decreasing,
+ * query_start[num_seqs] = num_q_tokens; max_q_per_seq bounds every n_s.  Counts outside
+ * [0, min(L, max_q_per_seq)] are clamped and set PA_DEV_BAD_CONTEXT.
+ * Runs the persistent kernel: supported while max_q_per_seq x (num_q_heads / num_kv_heads)
+ * <= 16 and num_seqs <= 1024, else PA_ERR_UNSUPPORTED.  Workspace as for pa_decode (same size
+ * query, persistent kind).  opts: num_ctas, timeline and the next-layer prefetch apply.
+ * Returns the codes of pa_decode.
+ * ---------------------------------------------------------------------------------- */
+int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start,
+                   float scale, int num_kv_heads,
+                   int num_seqs, int num_q_tokens, int max_q_per_seq, int num_q_heads, int head_dim,
+                   int block_size, int num_blocks, int max_blocks_per_seq, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream,
+                   const pa_decode_options* opts);
+
 /* Bytes of workspace pa_decode needs for this shape on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq);

@@ -7,6 +7,7 @@ as the device-memory and stream provider.
 
     cache_write(k, v, slot_mapping, k_cache, v_cache)
     decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads) -> out
+    multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, num_kv_heads, max_q)
     copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids)   # copy-on-write, swap out / in
     BlockPool(num_blocks)                       # host block pool (untimed)
     build_slot_mapping(block_tables, context_lens, block_size)
@@ -22,7 +23,7 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "multi_query", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
 
@@ -242,6 +243,50 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
                                 context_lens.data_ptr(), float(scale), int(num_kv_heads), S, Hq, D, B, NB,
                                 max_blocks, _DTYPE[q.dtype], ws_ptr, ws_bytes, _stream_ptr(stream), ctypes.byref(o))
     _native.check("pa_decode_append", rc)
+    return out
+
+
+def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                context_lens: torch.Tensor, query_start: torch.Tensor, scale: float, num_kv_heads: int,
+                max_q: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Several new query tokens per sequence attending causally over the paged cache.
+    q: [T, Hq, D]; sequence s owns rows query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its
+    newest tokens; at most ``max_q`` per sequence.  See pa_multi_query in include/pa.h."""
+    _need_cuda("q", q)
+    if q.dtype not in _DTYPE:
+        raise TypeError("q must be float16 or bfloat16")
+    _need_cuda("k_cache", k_cache, q.dtype)
+    _need_cuda("v_cache", v_cache, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("query_start", query_start, torch.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    S = context_lens.numel()
+    if Hkv != num_kv_heads or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape does not match q / num_kv_heads")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.numel() != S + 1:
+        raise ValueError("block_tables / query_start do not match context_lens")
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    o = _opts(0, "mma", num_ctas, timeline)
+    need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
+    if workspace is None:
+        workspace = _workspace(q.device, need, 2, int(num_ctas))
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_multi_query(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), float(scale),
+                              int(num_kv_heads), S, T, int(max_q), Hq, D, B, NB, max_blocks, _DTYPE[q.dtype], ws_ptr,
+                              ws_bytes, _stream_ptr(stream), ctypes.byref(o))
+    _native.check("pa_multi_query", rc)
     return out
 
 

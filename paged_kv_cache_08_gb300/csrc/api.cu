@@ -347,8 +347,9 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
                        const void* v_cache, const int32_t* block_tables, const int32_t* context_lens, float scale,
                        int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
                        int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes, void* stream,
-                       const pa_decode_options* opts) {
+                       const pa_decode_options* opts, const int32_t* q_start = nullptr, int max_q = 1) {
     const bool append = k_new != nullptr;
+    const bool multi = q_start != nullptr;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
     if (rc != PA_OK) return rc;
@@ -368,6 +369,12 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     Path path;
     rc = choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path);
     if (rc != PA_OK) return rc;
+    if (multi) {
+        // several query tokens per sequence: the persistent kernel, at most 16 query rows per
+        // (sequence, kv head)
+        if (append || max_q < 1 || !aligned4(q_start)) return PA_ERR_INVALID_ARG;
+        if (path != kPathPersist || (long long)max_q * group > kPieceRows) return PA_ERR_UNSUPPORTED;
+    }
     if (append) {
         if (path != kPathPersist) return PA_ERR_UNSUPPORTED;
         if (!v_new || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
@@ -392,7 +399,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     cudaError_t e;
 
     if (path == kPathPersist) {
-        const int ctas = persist_ctas(group, opts);
+        const int ctas = persist_ctas(multi ? max_q * group : group, opts);
         const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
         const size_t pieces = persist_pieces(persist_layout_ctas(opts));
@@ -409,6 +416,8 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.pf_k = opts ? opts->prefetch_k_cache : nullptr;
         a.pf_v = opts ? opts->prefetch_v_cache : nullptr;
         a.pf_own = (a.early && opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) ? 1 : 0;
+        a.q_start = q_start;
+        a.max_q = multi ? max_q : 1;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();
@@ -456,6 +465,19 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
     return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
                        workspace_bytes, stream, opts);
+}
+
+int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                   const int32_t* context_lens, const int32_t* query_start, float scale, int num_kv_heads,
+                   int num_seqs, int num_q_tokens, int max_q_per_seq, int num_q_heads, int head_dim, int block_size,
+                   int num_blocks, int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream, const pa_decode_options* opts) {
+    if (num_q_tokens < 0 || !query_start) return PA_ERR_INVALID_ARG;
+    if (num_q_tokens == 0) return num_seqs >= 0 ? PA_OK : PA_ERR_INVALID_ARG;
+    if (opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
+                       workspace_bytes, stream, opts, query_start, max_q_per_seq);
 }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -25,6 +25,10 @@
 // through the stage buffer they just consumed.  Full / empty mbarriers per stage connect the
 // producer and the consumers; every wait is bounded.
 //
+// Several query tokens per sequence (q_start): a segment's query rows are its new tokens x the
+// GQA group (at most 16), token i of n sitting at position L - n + i and attending causally up
+// to it; the per-row position limits enter the mask, the rest is unchanged.
+//
 // Finishing a cut segment costs dependent round trips to L2 (publish the partial, count the
 // arrival, read the other pieces), slow while the copies of every CTA queue in front of them.
 // Only the first piece of a range can end before the range does; the consumers hand it to an
@@ -38,6 +42,7 @@
 
 #include <atomic>
 #include <climits>
+#include <type_traits>
 
 namespace pa {
 
@@ -82,8 +87,10 @@ struct PLayout {
     static constexpr size_t kBars = kRing;   // full[kStages], empty[kStages], q barrier, piece barrier
     static constexpr size_t kFlags = kBars + (2 * kStages + 2) * sizeof(uint64_t);
     static constexpr size_t kNewPhys = kFlags + 16;   // int [kStages] block of the new token, then
-                                                       // int [kStages] deferred q rows (s * Hkv + h)
-    static constexpr size_t kPrefix = kNewPhys + ((2 * kStages * sizeof(int32_t) + 15) & ~size_t(15));
+                                                       // int [kStages] deferred q rows (s * Hkv + h), then
+                                                       // int [kStages] x 2 first q row / query tokens of
+                                                       // the segment a stage starts
+    static constexpr size_t kPrefix = kNewPhys + ((4 * kStages * sizeof(int32_t) + 15) & ~size_t(15));
     // then int P[S + 1], int L[S]
     static constexpr size_t total(int num_seqs) {
         return 1024 /*alignment slack*/ + kPrefix + (size_t)(2 * num_seqs + 1) * sizeof(int32_t);
@@ -263,13 +270,28 @@ __device__ __forceinline__ void advance(SegPos& p, const int32_t* P, const int32
     p.L = Lc[p.s];
 }
 
+// Query span and q / out offsets, fixed at compile time for one query token per sequence.
+template <bool kMulti>
+__device__ __forceinline__ QSpan span_of(const DecodeArgs& a, int s, int L) {
+    if constexpr (kMulti) return q_span(a, s, L);
+    else return QSpan{s, 1};
+}
+
+template <bool kMulti>
+__device__ __forceinline__ size_t out_offset(const DecodeArgs& a, const QSpan& q, int h, int G, int r) {
+    if constexpr (kMulti) return q_offset(a, q, h, G, r);
+    else return ((size_t)q.row0 * a.num_q_heads + (size_t)h * G + r) * kHeadDim;
+}
+
 // What the producer needs to issue one chunk's copies.
 struct ChunkDesc {
     int s, h, t0, nblk, load_q;
+    int q0, qn;   // the segment's query rows (first row, tokens), read when load_q
     int ids[4];   // physical blocks of the chunk (-1: none or outside the pool)
     int newblk;   // physical block of token L - 1 when this chunk holds it, else -1
 };
 
+template <bool kMulti>
 __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t* P, const int32_t* Lc, int S,
                                               int Hkv, long long b_c, long long b_e, long long g) {
     ChunkDesc d;
@@ -280,6 +302,8 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
     d.load_q = 0;
     d.ids[0] = d.ids[1] = d.ids[2] = d.ids[3] = -1;
     d.newblk = -1;
+    d.q0 = 0;
+    d.qn = 0;
     if (g >= b_e) return d;
     const SegPos p = locate(P, Lc, S, Hkv, g);
     const int B = a.block_size;
@@ -290,6 +314,11 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
     const int first = d.t0 / B;
     d.nblk = (t1 - 1) / B - first + 1;   // <= 64 / 16
     d.load_q = (p.k == 0) || (g == b_c);
+    if (d.load_q) {
+        const QSpan q = span_of<kMulti>(a, p.s, p.L);
+        d.q0 = q.row0;
+        d.qn = q.n;
+    }
     const int32_t* row = a.block_tables + (size_t)p.s * a.max_blocks_per_seq + first;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -310,8 +339,19 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
     return d;
 }
 
+// 64-token chunks of each kv head of sequence s: all of its L cached tokens, unless no query
+// token of it is new (several-token mode), then none.
+template <bool kMulti>
+__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int L) {
+    if (kMulti && span_of<kMulti>(a, s, L).n == 0) return 0;
+    return (L + kStageTokens - 1) / kStageTokens;
+}
+
 // Zero output rows of the empty sequences this CTA is responsible for (s = c, c + grid, ...).
+// (Several query tokens per sequence: a sequence without chunks has no new token, so no row.)
+template <bool kMulti>
 __device__ __forceinline__ void zero_empty_rows(const DecodeArgs& a, const int32_t* P, int c, int t, int nthreads) {
+    if (kMulti) return;
     const int Hq = a.num_q_heads;
     for (int s = c; s < a.num_seqs; s += (int)gridDim.x) {
         if (P[s + 1] == P[s]) {
@@ -324,12 +364,13 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs& a, const int32
 // Merge every piece (m, l, o) of the cut segment (s, h) -- chunks [Pseg, Pseg + n) of the list,
 // cut by the CTA ranges -- into its normalised output rows.  Threads t = 0..nthreads-1 share the
 // G x 16 (row, 8-column) items; one online pass over the pieces, a batch of loads in flight.
-template <typename T>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, long long Pseg, int n, long long N,
-                                             int C, int t, int nthreads) {
-    const int Hq = a.num_q_heads, G = Hq / a.num_kv_heads;
+template <typename T, bool kMulti>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& qsp, int h, long long Pseg, int n,
+                                             long long N, int C, int t, int nthreads) {
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int rows = qsp.n * G;
     const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + n - 1, N, C);
-    for (int e = t; e < G * 16; e += nthreads) {
+    for (int e = t; e < rows * 16; e += nthreads) {
         const int row = e >> 4, d0 = (e & 15) * 8;
         // one online pass over the pieces, a few at a time, every load of a batch in flight
         float M = -INFINITY, den = 0.f;
@@ -354,13 +395,15 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, 
             float bm = M;
 #pragma unroll
             for (int k = 0; k < kMergeBatch; ++k) bm = fmaxf(bm, ml[k].x);
-            const float rescale = exp2f(M - bm);   // M = -inf before the first batch: 0
+            // nothing seen yet (M = -inf): the running sums are 0 and stay so
+            const float rescale = (kMulti && M == -INFINITY) ? 0.f : exp2f(M - bm);
             den *= rescale;
 #pragma unroll
             for (int q = 0; q < 8; ++q) num[q] *= rescale;
 #pragma unroll
             for (int k = 0; k < kMergeBatch; ++k) {
-                const float f = exp2f(ml[k].x - bm);   // absent pieces: 2^-inf = 0
+                // absent pieces, and rows a piece saw no token of (causal limit): weight 0
+                const float f = (kMulti && ml[k].x == -INFINITY) ? 0.f : exp2f(ml[k].x - bm);
                 den = fmaf(f, ml[k].y, den);
                 num[0] = fmaf(f, x0[k].x, num[0]);
                 num[1] = fmaf(f, x0[k].y, num[1]);
@@ -379,7 +422,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, 
         packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
         packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
         packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
-        *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)s * Hq + h * G + row) * kHeadDim + d0) = packed;
+        *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + out_offset<kMulti>(a, qsp, h, G, row) + d0) = packed;
     }
 }
 
@@ -389,15 +432,16 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, int h, 
 // the epilogue warp (`handoff`: every consumer thread arrives on `pdone` after its stores) or
 // finished here: count the arrival and, as the last CTA of the segment to arrive, merge all
 // pieces.  Returns true if this call merged a cut segment.
-template <typename T, int kNT>
+template <typename T, int kNT, bool kMulti>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e, long long N, int C,
                                               int c, const float (&o)[kNT][8][4], const float (&m_run)[kNT][2],
                                               const float (&l_run)[kNT][2], bool dead, volatile int* last_flag,
-                                              bool handoff, uint64_t* pdone) {
+                                              bool handoff, uint64_t* pdone, const QSpan& qsp) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
+    const int Hkv = a.num_kv_heads, G = a.num_q_heads / Hkv;
+    const int rows = qsp.n * G;   // query rows of the segment
     const long long Pseg = (long long)P[pos.s] + (long long)pos.h * pos.n;
     const bool whole = (Pseg >= b_c) && (Pseg + pos.n <= b_e);
     // row sums: each lane holds a partial over its own tokens; the 8 lanes of a row share tig
@@ -418,14 +462,14 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     consumers_sync();   // every warp is past its reads of the stage
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
-        const int rg = nt * 8;   // query rows rg + 0..7 of the group
-        if (rg >= G) break;
+        const int rg = nt * 8;   // query rows rg + 0..7 of the segment
+        if (rg >= rows) break;
         // O^T fragment: o[nt][mt][j] = O[row tig*2 + j][dim mt*16 + gid], o[nt][mt][2 + j] the
         // same row at dim + 8; only the group's real query rows are written
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int row = tig * 2 + j;
-            if (rg + row < G) {
+            if (rg + row < rows) {
                 float* dst = &red_o[(warp * 8 + row) * kRedStride + gid];
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
@@ -439,7 +483,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         const int r = tid >> 4;            // row within the group of 8
         const int d0 = (tid & 15) * 8;     // 8 columns per thread
         const int row = rg + r;
-        if (row < G && !dead) {
+        if (row < rows && !dead) {
             float M = -INFINITY;
 #pragma unroll
             for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, red_ml[w2 * 8 + r].x);
@@ -448,7 +492,9 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
 #pragma unroll
             for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
                 const float2 ml = red_ml[w2 * 8 + r];
-                const float f = exp2f(ml.x - M);   // a warp without a valid token: 2^-inf = 0
+                // a warp without a valid token for the row: weight 0 (also when no warp has one,
+                // which a cut piece can meet under a causal limit; its den stays 0)
+                const float f = (kMulti && ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
                 den = fmaf(f, ml.y, den);
                 const float4 x0 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0]);
                 const float4 x1 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0 + 4]);
@@ -468,8 +514,8 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
                 packed.y = Elem<T>::pack2(num[2] * inv, num[3] * inv);
                 packed.z = Elem<T>::pack2(num[4] * inv, num[5] * inv);
                 packed.w = Elem<T>::pack2(num[6] * inv, num[7] * inv);
-                *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)pos.s * Hq + pos.h * G + row) * kHeadDim +
-                                          d0) = packed;
+                *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + out_offset<kMulti>(a, qsp, pos.h, G, row) + d0) =
+                    packed;
             } else {
                 float* dst = a.part_o + (piece * kPieceRows + row) * kHeadDim + d0;
                 *reinterpret_cast<float4*>(dst) = make_float4(num[0], num[1], num[2], num[3]);
@@ -500,7 +546,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         consumers_sync();
         const bool last = *last_flag != 0 && !dead;
         if (last) {
-            merge_pieces<T>(a, pos.s, pos.h, Pseg, pos.n, N, C, tid, kConsumerThreads);
+            merge_pieces<T, kMulti>(a, qsp, pos.h, Pseg, pos.n, N, C, tid, kConsumerThreads);
             if (tid == 0) a.seg_counters[sigma] = 0;   // ready for the next call
         }
         fence_proxy_async_smem();   // generic writes to the stage precede its next TMA fill
@@ -510,7 +556,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     return false;
 }
 
-template <typename T, bool kG16, int kStages>
+template <typename T, bool kG16, int kStages, bool kMulti>
 __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
     using Lay = PLayout<kG16, kStages>;
@@ -527,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     volatile int* last_flag = abort_flag + 2;
     volatile int* epi_merges = abort_flag + 3;
     volatile int* new_phys = reinterpret_cast<volatile int*>(base_ptr + Lay::kNewPhys);
+    volatile int* stage_q0 = new_phys + 2 * kStages;   // first q row of the segment a stage starts
+    volatile int* stage_qn = new_phys + 3 * kStages;   // and its query tokens
     int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
     const int S = a.num_seqs;
     int32_t* Lc = P + S + 1;                                              // [S], clamped lengths
@@ -572,7 +620,11 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 L = L < 0 ? 0 : cap;
             }
             Lc[s] = L;
-            local += (L + kStageTokens - 1) / kStageTokens;
+            if constexpr (kMulti) {
+                const int n = a.q_start[s + 1] - a.q_start[s];
+                if (n < 0 || n > L || n > a.max_q) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+            }
+            local += seq_chunks<kMulti>(a, s, L);
         }
         // exclusive scan of `local` over the CTA
         int incl = local;
@@ -589,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         int run = before + incl - local;
         for (int s = lo; s < hi; ++s) {
             P[s] = run * Hkv;
-            run += (Lc[s] + kStageTokens - 1) / kStageTokens;
+            run += seq_chunks<kMulti>(a, s, Lc[s]);
         }
         if (tid == kThreads - 1) {
             int tot = 0;
@@ -606,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     if (c >= C) {
         if (a.early) grid_dependency_wait();
         grid_launch_dependents();
-        zero_empty_rows(a, P, c, tid, kThreads);
+        zero_empty_rows<kMulti>(a, P, c, tid, kThreads);
         return;
     }
     const long long b_c = range_begin(c, N, C), b_e = range_begin(c + 1, N, C);
@@ -617,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         // Lane j describes chunk gbase + j (segment position and physical block ids); the next
         // group's descriptors are loaded while this group's copies are issued, so the ring is
         // refilled as soon as a stage frees up.
-        ChunkDesc cur = describe(a, P, Lc, S, Hkv, b_c, b_e, b_c + lane);
+        ChunkDesc cur = describe<kMulti>(a, P, Lc, S, Hkv, b_c, b_e, b_c + lane);
         unsigned long long wait_empty_ns = 0;
         if (a.timeline && lane == 0 && cur.ids[0] != INT_MIN) trace(a.timeline, c, kTrIds);
         volatile int* qdef = new_phys + kStages;   // [kStages]: q rows the first stages still need
@@ -631,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             const int R = 1 << R_log2;
             const uint32_t run = (uint32_t)R * kHeadDim * 2u;
             for (long long gbase = g0; gbase < g1; gbase += 32) {
-                const ChunkDesc d = describe(a, P, Lc, S, Hkv, b_c, g1, gbase + lane);
+                const ChunkDesc d = describe<kMulti>(a, P, Lc, S, Hkv, b_c, g1, gbase + lane);
                 const int within = (B > kStageTokens) ? (d.t0 % B) : 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -652,17 +704,25 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             }
             if (lane == 0) {
                 const int n = min(issued, kStages);
+                const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
                 uint32_t bytes = 0;
                 for (int e = 0; e < n; ++e)
-                    if (qdef[e] >= 0) bytes += (uint32_t)G * kHeadDim * 2u;
+                    if (qdef[e] >= 0) bytes += (uint32_t)(kMulti ? stage_qn[e] : 1) * group_bytes;
                 mbar_arrive_expect_tx(qbar, bytes);
                 for (int e = 0; e < n; ++e) {
                     const int sh = qdef[e];
                     if (sh >= 0) {
-                        const T* qsrc = static_cast<const T*>(a.q) +
-                                        ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim;
-                        bulk_g2s(ring + (uint32_t)e * Lay::kStageBytes + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u,
-                                 qbar);
+                        // query token r of the segment: its group's G rows, contiguous in q
+                        // the segment's query rows: its span (several tokens) or row s (one token;
+                        // the stage metadata is written in several-token mode only)
+                        const int nq = kMulti ? stage_qn[e] : 1;
+                        const int row0 = kMulti ? stage_q0[e] : sh / Hkv;
+                        for (int r = 0; r < nq; ++r) {
+                            const T* qsrc = static_cast<const T*>(a.q) +
+                                            ((size_t)(row0 + r) * Hq + (sh % Hkv) * G) * kHeadDim;
+                            bulk_g2s(ring + (uint32_t)e * Lay::kStageBytes + kKVBytes + (uint32_t)r * group_bytes, qsrc,
+                                     group_bytes, qbar);
+                        }
                     }
                 }
             }
@@ -671,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         int i = 0;
         bool ok = true;
         for (long long gbase = b_c; gbase < b_e && ok; gbase += 32) {
-            const ChunkDesc nxt = describe(a, P, Lc, S, Hkv, b_c, b_e, gbase + 32 + lane);
+            const ChunkDesc nxt = describe<kMulti>(a, P, Lc, S, Hkv, b_c, b_e, gbase + 32 + lane);
             const int cnt = (int)min(32LL, b_e - gbase);
             for (int j = 0; j < cnt; ++j, ++i) {
                 const int st = i % kStages;
@@ -702,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 const int nblk_j = __shfl_sync(0xffffffffu, cur.nblk, j);
                 const int loadq_j = __shfl_sync(0xffffffffu, cur.load_q, j);
                 const int newblk_j = __shfl_sync(0xffffffffu, cur.newblk, j);
+                const int q0_j = kMulti ? __shfl_sync(0xffffffffu, cur.q0, j) : s_j;
+                const int qn_j = kMulti ? __shfl_sync(0xffffffffu, cur.qn, j) : 1;
                 int ids[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ids[e] = __shfl_sync(0xffffffffu, cur.ids[e], j);
@@ -713,9 +775,15 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         const uint32_t dst = ring + (uint32_t)st * Lay::kStageBytes;
                         const int within = (B > kStageTokens) ? (t0_j % B) : 0;
                         const bool defer_q = i < kStages;   // fetched at the dependency point
+                        const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
                         if (defer_q) qdef[i] = loadq_j ? s_j * Hkv + h_j : -1;
                         new_phys[st] = append ? newblk_j : -1;
-                        uint32_t bytes = (loadq_j && !defer_q) ? (uint32_t)G * kHeadDim * 2u : 0u;
+                        if (kMulti) {
+                            stage_q0[st] = q0_j;
+                            stage_qn[st] = qn_j;
+                        }
+                        const int nq = kMulti ? qn_j : 1;
+                        uint32_t bytes = (loadq_j && !defer_q) ? (uint32_t)nq * group_bytes : 0u;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
@@ -734,8 +802,11 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         }
                         if (i == 0) trace(a.timeline, c, kTrIssue);
                         if (loadq_j && !defer_q) {
-                            const T* qsrc = static_cast<const T*>(a.q) + ((size_t)s_j * Hq + h_j * G) * kHeadDim;
-                            bulk_g2s(dst + kKVBytes, qsrc, (uint32_t)G * kHeadDim * 2u, &full[st]);
+                            for (int r = 0; r < nq; ++r) {
+                                const T* qsrc =
+                                    static_cast<const T*>(a.q) + ((size_t)(q0_j + r) * Hq + h_j * G) * kHeadDim;
+                                bulk_g2s(dst + kKVBytes + (uint32_t)r * group_bytes, qsrc, group_bytes, &full[st]);
+                            }
                         }
                     }
                 }
@@ -776,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 last = __shfl_sync(0xffffffffu, last, 0);
                 __syncwarp();   // the lanes' merge reads come after lane 0's acquire
                 if (last) {
-                    merge_pieces<T>(a, p0.s, p0.h, Pseg, p0.n, N, C, lane, 32);
+                    merge_pieces<T, kMulti>(a, span_of<kMulti>(a, p0.s, p0.L), p0.h, Pseg, p0.n, N, C, lane, 32);
                     if (lane == 0) {
                         a.seg_counters[sigma] = 0;   // ready for the next call
                         *epi_merges = 1;
@@ -798,6 +869,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         float m_run[kNT][2], l_run[kNT][2];
         float o[kNT][8][4];
         uint32_t qb[8][kNT][2];   // Q^T as the B operand: [k-step][column tile][2 registers]
+        int lim[kNT][2];          // newest position each of the lane's query rows attends to
+        QSpan qsp{0, 0};          // the current segment's query tokens
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
             m_run[nt][0] = m_run[nt][1] = -INFINITY;
@@ -809,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             if (tid == 0) trace(a.timeline, c, kTrDeps);
         }
         unsigned long long wait_full_ns = 0, flush_ns = 0, merges = 0, flushes = 0;
-        zero_empty_rows(a, P, c, tid, kConsumerThreads);
+        zero_empty_rows<kMulti>(a, P, c, tid, kConsumerThreads);
         const bool append = a.k_new != nullptr;
         SegPos pos = locate(P, Lc, S, Hkv, b_c);
         // A warp that gave up on a wait (or sees that another did) is "dead": it keeps walking
@@ -849,9 +922,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     dead = true;
                 }
             }
+            if (seg_begin) qsp = kMulti ? QSpan{stage_q0[st], stage_qn[st]} : QSpan{pos.s, 1};
             if (seg_begin && !dead) {
                 // B fragments of Q^T: register 0 = Q[row][ks*16 + tig*2 + {0,1}], register 1 the
-                // same at + 8, row = nt*8 + gid; rows >= G are zero
+                // same at + 8, row = nt*8 + gid = token (row / G) x group member (row % G);
+                // rows past the segment's are zero
+                const int rows = qsp.n * G;
                 const uint32_t* qs = reinterpret_cast<const uint32_t*>(base_ptr + (size_t)st * Lay::kStageBytes +
                                                                        kKVBytes);
 #pragma unroll
@@ -860,8 +936,13 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const int wcol = (ks * 16 + tig * 2) >> 1;
-                        qb[ks][nt][0] = (row < G) ? qs[row * 64 + wcol] : 0u;
-                        qb[ks][nt][1] = (row < G) ? qs[row * 64 + wcol + 4] : 0u;
+                        qb[ks][nt][0] = (row < rows) ? qs[row * 64 + wcol] : 0u;
+                        qb[ks][nt][1] = (row < rows) ? qs[row * 64 + wcol + 4] : 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int r = nt * 8 + tig * 2 + j;   // a column of S^T this lane holds
+                        lim[nt][j] = (kMulti && r < rows) ? pos.L - qsp.n + r / G : -1;
                     }
                     m_run[nt][0] = m_run[nt][1] = -INFINITY;
                     l_run[nt][0] = l_run[nt][1] = 0.f;
@@ -918,16 +999,24 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 }
                 // online softmax per query row: lane holds rows tig*2 + j at tokens gid and gid + 8;
                 // the 8 lanes of a row (same tig) reduce with xor 4, 8, 16
-                const bool tok0_ok = t_warp + gid < nvalid, tok1_ok = t_warp + gid + 8 < nvalid;
+                // position of the lane's first token; one query token per sequence sees every valid
+                // token of the chunk, several see up to their own positions (lim)
+                const int tok0 = pos.k * kStageTokens + t_warp + gid;
+                const bool in0 = t_warp + gid < nvalid, in1 = t_warp + gid + 8 < nvalid;
                 float alpha[kNT][2];
-                uint32_t pb[kNT][2];
+                // bf16 keeps 8 significant bits: P goes in as a high and a low bf16 part (two PV
+                // products), so that rows attending to few tokens keep fp32-like weights
+                constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+                uint32_t pb[kNT][2], pl[kNT][2];
 #pragma unroll
                 for (int nt = 0; nt < kNT; ++nt) {
                     float pv[4];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const float x0 = tok0_ok ? (sc[nt][j] + sc2[nt][j]) * a.scale_log2 : -INFINITY;
-                        const float x1 = tok1_ok ? (sc[nt][2 + j] + sc2[nt][2 + j]) * a.scale_log2 : -INFINITY;
+                        const bool ok0 = kMulti ? tok0 <= lim[nt][j] : in0;
+                        const bool ok1 = kMulti ? tok0 + 8 <= lim[nt][j] : in1;
+                        const float x0 = ok0 ? (sc[nt][j] + sc2[nt][j]) * a.scale_log2 : -INFINITY;
+                        const float x1 = ok1 ? (sc[nt][2 + j] + sc2[nt][2 + j]) * a.scale_log2 : -INFINITY;
                         float mx = fmaxf(x0, x1);
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -941,8 +1030,14 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + (pv[j] + pv[2 + j]);
                     }
                     // P^T as the B operand: the C fragment (tokens x rows) transposed per 8x8 block
-                    pb[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0], pv[1]));
-                    pb[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2], pv[3]));
+                    const uint32_t h0 = Elem<T>::pack2(pv[0], pv[1]), h1 = Elem<T>::pack2(pv[2], pv[3]);
+                    pb[nt][0] = movmatrix_trans(h0);
+                    pb[nt][1] = movmatrix_trans(h1);
+                    if (kSplitP) {
+                        const float2 r0 = Elem<T>::to_float2(h0), r1 = Elem<T>::to_float2(h1);
+                        pl[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0] - r0.x, pv[1] - r0.y));
+                        pl[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2] - r1.x, pv[3] - r1.y));
+                    }
                 }
                 bool rescale = false;
 #pragma unroll
@@ -964,14 +1059,18 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(chunk_addr(vbase, tokV, 2 * mt + chV, R_log2), a0, a1, a2, a3);
 #pragma unroll
-                    for (int nt = 0; nt < kNT; ++nt) mma16816<T>(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                    for (int nt = 0; nt < kNT; ++nt) {
+                        mma16816<T>(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                        if (kSplitP) mma16816<T>(o[nt][mt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+                    }
                 }
             }
 
             if (seg_end) {
                 const unsigned long long tf = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
-                const bool merged = flush_segment<T, kNT>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
-                                                     C, c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone);
+                const bool merged = flush_segment<T, kNT, kMulti>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
+                                                     C, c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone,
+                                                     qsp);
                 if (a.timeline && tid == 0) {
                     flush_ns += global_timer_ns() - tf;
                     merges += merged ? 1 : 0;
@@ -1041,10 +1140,10 @@ bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtenso
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool kG16, int kStages>
+template <typename T, bool kG16, int kStages, bool kMulti>
 cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_persist_kernel<T, kG16, kStages>;
+    auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1070,6 +1169,21 @@ cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cu
     return e;
 }
 
+template <bool kMulti>
+cudaError_t dispatch(const DecodeArgs& a, const MmaMaps& maps, int R_log2, int dtype, bool g16, bool deep,
+                     cudaStream_t stream) {
+    if (dtype == PA_BF16) {
+        if (g16) return deep ? launch_impl<__nv_bfloat16, true, 6, kMulti>(a, maps, R_log2, stream)
+                             : launch_impl<__nv_bfloat16, true, 3, kMulti>(a, maps, R_log2, stream);
+        return deep ? launch_impl<__nv_bfloat16, false, 6, kMulti>(a, maps, R_log2, stream)
+                    : launch_impl<__nv_bfloat16, false, 3, kMulti>(a, maps, R_log2, stream);
+    }
+    if (g16) return deep ? launch_impl<__half, true, 6, kMulti>(a, maps, R_log2, stream)
+                         : launch_impl<__half, true, 3, kMulti>(a, maps, R_log2, stream);
+    return deep ? launch_impl<__half, false, 6, kMulti>(a, maps, R_log2, stream)
+                : launch_impl<__half, false, 3, kMulti>(a, maps, R_log2, stream);
+}
+
 }  // namespace
 
 int persist_ctas_per_sm(int group) { return group <= 8 ? 2 : 1; }
@@ -1083,19 +1197,11 @@ cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t s
     MmaMaps maps;
     if (!encode_map(a.k_cache, rows, R, &maps.k) || !encode_map(a.v_cache, rows, R, &maps.v))
         return cudaErrorInvalidValue;
-    const bool g16 = (a.num_q_heads / a.num_kv_heads) > 8;
+    const bool g16 = a.max_q * (a.num_q_heads / a.num_kv_heads) > 8;   // query rows per segment
     // as many CTAs as SMs (or fewer): one CTA per SM with the deep ring
     const bool deep = a.num_ctas <= sm_count_current();
-    if (dtype == PA_BF16) {
-        if (g16) return deep ? launch_impl<__nv_bfloat16, true, 6>(a, maps, R_log2, stream)
-                             : launch_impl<__nv_bfloat16, true, 3>(a, maps, R_log2, stream);
-        return deep ? launch_impl<__nv_bfloat16, false, 6>(a, maps, R_log2, stream)
-                    : launch_impl<__nv_bfloat16, false, 3>(a, maps, R_log2, stream);
-    }
-    if (g16) return deep ? launch_impl<__half, true, 6>(a, maps, R_log2, stream)
-                         : launch_impl<__half, true, 3>(a, maps, R_log2, stream);
-    return deep ? launch_impl<__half, false, 6>(a, maps, R_log2, stream)
-                : launch_impl<__half, false, 3>(a, maps, R_log2, stream);
+    if (a.q_start) return dispatch<true>(a, maps, R_log2, dtype, g16, deep, stream);
+    return dispatch<false>(a, maps, R_log2, dtype, g16, deep, stream);
 }
 
 }  // namespace pa

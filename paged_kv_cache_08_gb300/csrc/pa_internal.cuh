@@ -76,7 +76,31 @@ struct DecodeArgs {
     const void* pf_k;         // optional: pools whose blocks of this call's chunks are prefetched into L2
     const void* pf_v;
     int pf_own;               // early mode: prefetch this range's chunks beyond the ring into L2 before the wait
+    const int32_t* q_start;   // several query tokens per sequence: rows q_start[s] .. q_start[s+1]-1 of q and
+                              //   out (null: one query row per sequence, row s)
+    int max_q;                // query tokens per sequence at most (1 without q_start)
 };
+
+// New query tokens of sequence s (its newest ones, the last of its L cached tokens) and the
+// first q / out row they occupy.  Out-of-range counts are clamped to [0, min(L, max_q)] the
+// same way wherever they are read.
+struct QSpan {
+    int row0;
+    int n;
+};
+
+__device__ __forceinline__ QSpan q_span(const DecodeArgs& a, int s, int L) {
+    if (!a.q_start) return QSpan{s, 1};
+    const int r0 = a.q_start[s];
+    const int n = a.q_start[s + 1] - r0;
+    return QSpan{r0, max(0, min(n, min(L, a.max_q)))};
+}
+
+// Element offset in q / out of row r of the segment (sequence s, kv head h): query token r / G
+// of the span, group member r % G.
+__device__ __forceinline__ size_t q_offset(const DecodeArgs& a, const QSpan& q, int h, int G, int r) {
+    return ((size_t)(q.row0 + r / G) * a.num_q_heads + (size_t)h * G + r % G) * kHeadDim;
+}
 
 constexpr int kTimelineSlots = 16;
 

@@ -250,3 +250,19 @@ def to_device(wl: Workload, device) -> Workload:
     for key in ("q", "k_cache", "v_cache", "k_new", "v_new"):
         setattr(out, key, [t.to(device) for t in getattr(wl, key)])
     return out
+
+
+def multi_query_inputs(wl: Workload, new_tokens: Sequence[int], seed: int, device=None):
+    """Queries for several new tokens per sequence: ``new_tokens[s]`` rows for sequence s
+    (its newest tokens, already part of its context), drawn N(0, 1) in the workload's dtype.
+    Returns (q [T, num_q_heads, head_dim], query_start int32 [S + 1], max new tokens)."""
+    assert len(new_tokens) == wl.num_seqs
+    starts = [0]
+    for n in new_tokens:
+        starts.append(starts[-1] + int(n))
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn((starts[-1], wl.num_q_heads, wl.head_dim), generator=gen).to(wl.torch_dtype)
+    qs = torch.tensor(starts, dtype=torch.int32)
+    if device is not None:
+        q, qs = q.to(device), qs.to(device)
+    return q, qs, max([int(n) for n in new_tokens] + [1])
