@@ -101,9 +101,10 @@ typedef struct {
                                     pieces finished, 14 chunks streamed, 15 SM id.  Entries of CTAs
                                     that own no chunk stay as set. */
     /* Persistent kernel: another pool pair of the caches' shape that this call's block tables
-     * and lengths also address (the next layer's caches), or both NULL.  Once a CTA has issued
-     * its own copies it asks the L2 to prefetch the same blocks of these pools, so that a call
-     * on them that follows finds its rows there.  Read-only hints; 16-byte aligned. */
+     * and lengths also address (the next layer's caches), or both NULL.  Once the last chunk of
+     * a CTA's share has landed, the CTA asks the L2 to prefetch the same blocks of these pools,
+     * so that a call on them that follows finds its rows there.  Read-only hints; 16-byte
+     * aligned. */
     const void* prefetch_k_cache;
     const void* prefetch_v_cache;
 } pa_decode_options;
