@@ -56,6 +56,7 @@ constexpr int kKBytes = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (
 constexpr int kKVBytes = 2 * kKBytes;
 constexpr int kRedStride = kHeadDim + 4;                // padded rows of the merge scratch (bank spread)
 constexpr int kMergeBatch = 4;                          // pieces whose loads are in flight together
+constexpr float kLazyLog2 = 8.f;                        // exponent base lags the running max by < 2^8
 
 // Trace slots of one CTA: event times (global ns), then accumulated times and counters.
 enum : int {
@@ -1021,31 +1022,62 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 // token of the chunk, several see up to their own positions (lim)
                 const int tok0 = pos.k * kStageTokens + t_warp + gid;
                 const bool in0 = t_warp + gid < nvalid, in1 = t_warp + gid + 8 < nvalid;
-                float alpha[kNT][2];
                 // bf16 keeps 8 significant bits: P goes in as a high and a low bf16 part (two PV
                 // products), so that rows attending to few tokens keep fp32-like weights
                 constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+                // Exponent base per row: m_run, moved only when a score exceeds it by more than
+                // kLazyLog2 (then to the exact running max, rescaling O and l).  Weights stay below
+                // 2^kLazyLog2, and most chunks skip the cross-lane max and the rescale.
+                float xs[kNT][4];
+                bool move = false;
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const bool ok0 = kMulti ? tok0 <= lim[nt][j] : in0;
+                        const bool ok1 = kMulti ? tok0 + 8 <= lim[nt][j] : in1;
+                        xs[nt][j] = ok0 ? (sc[nt][j] + sc2[nt][j]) * a.scale_log2 : -INFINITY;
+                        xs[nt][2 + j] = ok1 ? (sc[nt][2 + j] + sc2[nt][2 + j]) * a.scale_log2 : -INFINITY;
+                        // (m_run = -inf: any visible token moves the base)
+                        move = move || xs[nt][j] > m_run[nt][j] + kLazyLog2 ||
+                               xs[nt][2 + j] > m_run[nt][j] + kLazyLog2;
+                    }
+                if (__any_sync(0xffffffffu, move)) {
+                    float alpha[kNT][2];
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            // the 8 lanes of a row (same tig) reduce with xor 4, 8, 16
+                            float mx = fmaxf(xs[nt][j], xs[nt][2 + j]);
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                            const float m_new = fmaxf(m_run[nt][j], mx);
+                            alpha[nt][j] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[nt][j] - m_new);
+                            m_run[nt][j] = m_new;
+                            l_run[nt][j] *= alpha[nt][j];
+                        }
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            o[nt][mt][0] *= alpha[nt][0];
+                            o[nt][mt][1] *= alpha[nt][1];
+                            o[nt][mt][2] *= alpha[nt][0];
+                            o[nt][mt][3] *= alpha[nt][1];
+                        }
+                }
                 uint32_t pb[kNT][2], pl[kNT][2];
 #pragma unroll
                 for (int nt = 0; nt < kNT; ++nt) {
                     float pv[4];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const bool ok0 = kMulti ? tok0 <= lim[nt][j] : in0;
-                        const bool ok1 = kMulti ? tok0 + 8 <= lim[nt][j] : in1;
-                        const float x0 = ok0 ? (sc[nt][j] + sc2[nt][j]) * a.scale_log2 : -INFINITY;
-                        const float x1 = ok1 ? (sc[nt][2 + j] + sc2[nt][2 + j]) * a.scale_log2 : -INFINITY;
-                        float mx = fmaxf(x0, x1);
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float m_new = fmaxf(m_run[nt][j], mx);
-                        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                        alpha[nt][j] = exp2f(m_run[nt][j] - m_use);
-                        m_run[nt][j] = m_new;
-                        pv[j] = exp2f(x0 - m_use);
-                        pv[2 + j] = exp2f(x1 - m_use);
-                        l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + (pv[j] + pv[2 + j]);
+                        const float m_use = (m_run[nt][j] == -INFINITY) ? 0.f : m_run[nt][j];
+                        pv[j] = exp2f(xs[nt][j] - m_use);
+                        pv[2 + j] = exp2f(xs[nt][2 + j] - m_use);
+                        l_run[nt][j] += pv[j] + pv[2 + j];
                     }
                     // P^T as the B operand: the C fragment (tokens x rows) transposed per 8x8 block
                     const uint32_t h0 = Elem<T>::pack2(pv[0], pv[1]), h1 = Elem<T>::pack2(pv[2], pv[3]);
@@ -1056,20 +1088,6 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         pl[nt][0] = movmatrix_trans(Elem<T>::pack2(pv[0] - r0.x, pv[1] - r0.y));
                         pl[nt][1] = movmatrix_trans(Elem<T>::pack2(pv[2] - r1.x, pv[3] - r1.y));
                     }
-                }
-                bool rescale = false;
-#pragma unroll
-                for (int nt = 0; nt < kNT; ++nt) rescale = rescale || alpha[nt][0] != 1.f || alpha[nt][1] != 1.f;
-                if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                    for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            o[nt][mt][0] *= alpha[nt][0];
-                            o[nt][mt][1] *= alpha[nt][1];
-                            o[nt][mt][2] *= alpha[nt][0];
-                            o[nt][mt][3] *= alpha[nt][1];
-                        }
                 }
                 // O^T += V^T P^T, one 16-dim tile of V^T at a time
 #pragma unroll
