@@ -394,6 +394,9 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& q
     const int G = a.num_q_heads / a.num_kv_heads;
     const int rows = qsp.n * G;
     const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + n - 1, N, C);
+    // piece slot: 0 = the piece holding its CTA's first chunk; only the first CTA's piece can
+    // start later than that
+    const int first_slot = (Pseg == range_begin(c_first, N, C)) ? 0 : 1;
     for (int e = t; e < rows * 16; e += nthreads) {
         const int row = e >> 4, d0 = (e & 15) * 8;
         // one online pass over the pieces, a few at a time, every load of a batch in flight
@@ -406,7 +409,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& q
             for (int k = 0; k < kMergeBatch; ++k) {
                 const int cc = cc0 + k;
                 if (cc <= c_last) {
-                    const size_t pc = (size_t)cc * 2 + ((Pseg <= range_begin(cc, N, C)) ? 0 : 1);
+                    const size_t pc = (size_t)cc * 2 + (cc == c_first ? first_slot : 0);
                     const size_t row_idx = pc * kPieceRows + row;
                     ml[k] = ld_cg2(&a.part_ml[row_idx]);
                     x0[k] = ld_cg4(a.part_o + row_idx * kHeadDim + d0);
