@@ -346,8 +346,8 @@ def run_ours(args):
                                          3: "split grid, tensor cores"}[kind],
                        "step": ("pa_decode_append per layer (cache write fused)" if fused
                                 else "pa_cache_write + pa_decode per layer"),
-                       "l2": "inputs larger than L2: 24 distinct layer caches (%.2f GB) read once per step"
-                             % (2 * sum(t.numel() * 2 for t in wl.k_cache) / 1e9),
+                       "l2": "inputs larger than L2: %d distinct layer caches (%.2f GB) read once per step"
+                             % (wl.layers, 2 * sum(t.numel() * 2 for t in wl.k_cache) / 1e9),
                        "parallelism": f"replicas x{world}", "cuda_graph": True},
             "pct_of_measured_peak": round(100 * value / world / peak, 2),
             "pct_of_8TBs_spec": round(100 * value / world / SPEC_PEAK_GBS, 2),
@@ -600,6 +600,119 @@ def run_swap(args):
     print(json.dumps(line), flush=True)
 
 
+def run_multi_query(args, new_tokens: int = 2):
+    """Several new tokens per sequence (speculative-decoding verification of one draft token per
+    sequence and its successor): the 1.1B edge shape of the decode bench, 24 layers, each layer
+    writing the 2 newest tokens' K/V (pa_cache_write) and attending with pa_multi_query (12 query
+    rows per sequence and kv head), in a CUDA graph.  Bytes: the decode ledger with 2 query and
+    output rows per sequence, plus the cache write of 2 rows per sequence."""
+    import paged_kv_cache_08_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workloads.config(2, device=dev, layers=args.layers)
+    S, Hq, D, Hkv = wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.num_kv_heads
+    new = [new_tokens] * S
+    q, qs, max_q = workloads.multi_query_inputs(wl, new, seed=777, device=dev)
+    g = torch.Generator().manual_seed(778)
+    k_new = [torch.randn((S * new_tokens, Hkv, D), generator=g).to(wl.torch_dtype).to(dev) for _ in range(wl.layers)]
+    v_new = [torch.randn((S * new_tokens, Hkv, D), generator=g).to(wl.torch_dtype).to(dev) for _ in range(wl.layers)]
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    # slots of each sequence's newest tokens: positions L - 2 and L - 1 (host bookkeeping)
+    tables = wl.block_tables.numpy()
+    slots = []
+    for s_ in range(S):
+        L = int(wl.context_lens[s_])
+        for t in range(L - new_tokens, L):
+            slots.append(int(tables[s_, t // wl.block_size]) * wl.block_size + t % wl.block_size)
+    slots = torch.tensor(slots, dtype=torch.int64, device=dev)
+    outs = [torch.empty_like(q) for _ in range(wl.layers)]
+    ws = pa.new_workspace(pa.decode_workspace_size(S, Hq, Hkv, D, wl.block_size, wl.max_blocks_per_seq), dev)
+
+    def step():
+        for i in range(wl.layers):
+            pa.cache_write(k_new[i], v_new[i], slots, wl.k_cache[i], wl.v_cache[i])
+            pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
+                           workspace=ws)
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        a.record()
+        for _ in range(args.steps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    lens64 = wl.context_lens.to(torch.int64)
+    kv = int(lens64.sum()) * Hkv * D * 2 * 2
+    qo = 2 * S * new_tokens * Hq * D * 2
+    table = 4 * int(((lens64 + wl.block_size - 1) // wl.block_size).sum())
+    mq_bytes = kv + qo + table + 4 * (2 * S + 1)
+    cw_bytes = 2 * (S * new_tokens * Hkv * D * 2 * 2) + 8 * S * new_tokens
+    step_bytes = wl.layers * (mq_bytes + cw_bytes)
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    per_layer_us = ms * 1e3 / wl.layers
+    line = {"metric": "several-token paged attention (2 new tokens per sequence): achieved HBM GB/s",
+            "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"edge1p1b_64seq_ctx16-2048_gqa12x2_f16_B16_{new_tokens}new_x{wl.layers}layers",
+                       "step": "pa_cache_write + pa_multi_query per layer", "cuda_graph": True,
+                       "l2": "inputs larger than L2: distinct layer caches read once per step"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "algorithmic_bytes_per_layer": mq_bytes + cw_bytes, "avg_layer_us": round(per_layer_us, 2),
+                         "kernel": "pa_multi_query (+ pa_cache_write)", "peak_source": f"{peak_kind} copy bandwidth"},
+            "gpu_launches": 2 * wl.layers * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512):
+    """Chunked prefill: the last 512 tokens of 16 sequences of 4096 (their K/V already in the
+    cache) attend causally over the paged cache, in the Llama-2-7B shape of the pages (32 query
+    and 32 kv heads, head dim 128, fp16, 32-token blocks, randomly permuted pool, 1 GiB of K/V).
+    Tensor-core bound: FLOPs = 4 * head_dim * (query row, visible token) pairs."""
+    import paged_kv_cache_08_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workloads.make_workload("prefill_llama7b", context_lens=[context] * seqs, num_q_heads=32, num_kv_heads=32,
+                                 block_size=32, dtype="f16", seed=4242, device=dev, values=True)
+    q, qs, max_q = workloads.multi_query_inputs(wl, [new_tokens] * seqs, seed=4243, device=dev)
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    out = torch.empty_like(q)
+
+    def call(_):
+        pa.multi_query(q, wl.k_cache[0], wl.v_cache[0], bt, lens, qs, wl.scale, wl.num_kv_heads, max_q, out=out)
+    with ClockSampler(0) as clk:
+        ms = _event_ms(call, args.steps, args.warmup)
+    pairs = seqs * wl.num_q_heads * sum(context - new_tokens + i + 1 for i in range(new_tokens))
+    flops = 4 * wl.head_dim * pairs
+    tflops = flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured cuBLAS bf16 burst (fp16 has the same dense rate)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    line = {"metric": "chunked prefill paged attention: achieved TFLOP/s", "value": round(tflops, 1),
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"prefill_{seqs}seq_ctx{context}_new{new_tokens}_mha32_f16_B32",
+                       "l2": "1 GiB of K/V, above L2"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4), "traffic": None, "flops_per_launch": flops,
+                         "kernel": "prefill_mma_kernel (mma.sync m16n8k16)", "peak_source": kind},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -615,8 +728,8 @@ def main():
                     help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
     ap.add_argument("--prefetch-own", action="store_true",
                     help="each layer prefetches its own chunks beyond the copy pipeline before its dependency wait")
-    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
-                    help="decode step (default), or the block-copy and swap benchmarks")
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap", "multi_query", "prefill"], default="decode",
+                    help="decode step (default), or the block-copy, swap, several-token and prefill benchmarks")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -625,6 +738,12 @@ def main():
         return
     if args.op == "swap" and args.impl == "ours":
         run_swap(args)
+        return
+    if args.op == "multi_query" and args.impl == "ours":
+        run_multi_query(args)
+        return
+    if args.op == "prefill" and args.impl == "ours":
+        run_prefill(args)
         return
     if args.impl == "reference":
         run_reference(args)

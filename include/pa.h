@@ -249,10 +249,13 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  * with row = query_start[s] + i and K/V of kv head h / (num_q_heads / num_kv_heads).
  * n_s = 1 everywhere is pa_decode.  query_start: int32 [num_seqs + 1], non-decreasing,
  * query_start[num_seqs] = num_q_tokens; max_q_per_seq bounds every n_s.  Counts outside
- * [0, min(L, max_q_per_seq)] are clamped and set PA_DEV_BAD_CONTEXT.
- * Runs the persistent kernel: supported while max_q_per_seq x (num_q_heads / num_kv_heads)
- * <= 16 and num_seqs <= 1024, else PA_ERR_UNSUPPORTED.  Workspace as for pa_decode (same size
- * query, persistent kind).  opts: num_ctas, timeline and the next-layer prefetch apply.
+ * [0, min(L, max_q_per_seq)], and spans outside [0, num_q_tokens), are clamped and set
+ * PA_DEV_BAD_CONTEXT.
+ * Kernels: while max_q_per_seq x (num_q_heads / num_kv_heads) <= 16 (and num_seqs <= 1024)
+ * the persistent kernel, with a workspace as for pa_decode (same size query, persistent kind;
+ * opts: num_ctas, timeline and the next-layer prefetch apply); beyond that, tensor-core tiles
+ * of 64 query rows per (sequence, kv head), one CTA each, no workspace (chunked prefill; at
+ * most 65535 sequences and kv heads).
  * Returns the codes of pa_decode.
  * ---------------------------------------------------------------------------------- */
 int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -347,7 +347,8 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
                        const void* v_cache, const int32_t* block_tables, const int32_t* context_lens, float scale,
                        int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
                        int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes, void* stream,
-                       const pa_decode_options* opts, const int32_t* q_start = nullptr, int max_q = 1) {
+                       const pa_decode_options* opts, const int32_t* q_start = nullptr, int max_q = 1,
+                       int q_rows = 0) {
     const bool append = k_new != nullptr;
     const bool multi = q_start != nullptr;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
@@ -370,10 +371,38 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     rc = choose_path(num_seqs, group, opts ? opts->math : PA_MATH_AUTO, &path);
     if (rc != PA_OK) return rc;
     if (multi) {
-        // several query tokens per sequence: the persistent kernel, at most 16 query rows per
-        // (sequence, kv head)
+        // several query tokens per sequence: the persistent kernel while a (sequence, kv head)
+        // has at most 16 query rows, else tiles of 64 rows (no workspace)
         if (append || max_q < 1 || !aligned4(q_start)) return PA_ERR_INVALID_ARG;
-        if (path != kPathPersist || (long long)max_q * group > kPieceRows) return PA_ERR_UNSUPPORTED;
+        if ((long long)max_q * group > kPieceRows) {
+            if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+            DecodeArgs a;
+            std::memset(&a, 0, sizeof(a));
+            a.out = out;
+            a.q = q;
+            a.k_cache = k_cache;
+            a.v_cache = v_cache;
+            a.block_tables = block_tables;
+            a.context_lens = context_lens;
+            a.scale_log2 = scale * 1.4426950408889634f;
+            a.num_seqs = num_seqs;
+            a.num_q_heads = num_q_heads;
+            a.num_kv_heads = num_kv_heads;
+            a.block_size = block_size;
+            a.num_blocks = num_blocks;
+            a.max_blocks_per_seq = max_blocks_per_seq;
+            a.status = device_status_ptr();
+            a.q_start = q_start;
+            a.max_q = max_q;
+            a.q_rows = q_rows;
+            const cudaError_t pe = launch_prefill_mma(a, dtype, static_cast<cudaStream_t>(stream));
+            if (pe != cudaSuccess) {
+                cudaGetLastError();
+                return PA_ERR_CUDA;
+            }
+            return PA_OK;
+        }
+        if (path != kPathPersist) return PA_ERR_UNSUPPORTED;
     }
     if (append) {
         if (path != kPathPersist) return PA_ERR_UNSUPPORTED;
@@ -418,6 +447,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.pf_own = (a.early && opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) ? 1 : 0;
         a.q_start = q_start;
         a.max_q = multi ? max_q : 1;
+        a.q_rows = q_rows;
         a.tokens_per_split = 0;
         a.max_splits = 1;
         a.status = device_status_ptr();
@@ -477,7 +507,7 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
     if (opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) return PA_ERR_INVALID_ARG;
     return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
-                       workspace_bytes, stream, opts, query_start, max_q_per_seq);
+                       workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);
 }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -651,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             Lc[s] = L;
             if constexpr (kMulti) {
                 const int n = a.q_start[s + 1] - a.q_start[s];
-                if (n < 0 || n > L || n > a.max_q) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+                const int r0 = a.q_start[s];
+                if (n < 0 || n > L || n > a.max_q || r0 < 0 || r0 + n > a.q_rows)
+                    flag_status(a.status, PA_DEV_BAD_CONTEXT);
             }
             local += seq_chunks<kMulti>(a, s, L);
         }

@@ -79,11 +79,12 @@ struct DecodeArgs {
     const int32_t* q_start;   // several query tokens per sequence: rows q_start[s] .. q_start[s+1]-1 of q and
                               //   out (null: one query row per sequence, row s)
     int max_q;                // query tokens per sequence at most (1 without q_start)
+    int q_rows;               // rows of q and out (several-token mode)
 };
 
 // New query tokens of sequence s (its newest ones, the last of its L cached tokens) and the
-// first q / out row they occupy.  Out-of-range counts are clamped to [0, min(L, max_q)] the
-// same way wherever they are read.
+// first q / out row they occupy.  Out-of-range counts are clamped to [0, min(L, max_q)] (and to
+// the rows of q) the same way wherever they are read.
 struct QSpan {
     int row0;
     int n;
@@ -91,9 +92,9 @@ struct QSpan {
 
 __device__ __forceinline__ QSpan q_span(const DecodeArgs& a, int s, int L) {
     if (!a.q_start) return QSpan{s, 1};
-    const int r0 = a.q_start[s];
-    const int n = a.q_start[s + 1] - r0;
-    return QSpan{r0, max(0, min(n, min(L, a.max_q)))};
+    const int r0 = max(0, min(a.q_start[s], a.q_rows));   // rows stay inside q and out
+    const int n = a.q_start[s + 1] - a.q_start[s];
+    return QSpan{r0, max(0, min(min(n, a.q_rows - r0), min(L, a.max_q)))};
 }
 
 // Element offset in q / out of row r of the segment (sequence s, kv head h): query token r / G
@@ -260,6 +261,9 @@ bool fma_supports_group(int group);
 // Persistent load-balanced tensor-core kernel (G <= 16, num_seqs <= kPersistMaxSeqs); one launch.
 cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t stream);
 int persist_ctas_per_sm(int group);
+
+// Several query tokens per sequence, any number: tiles of 64 query rows (prefill_mma.cu).
+cudaError_t launch_prefill_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
 // Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.
 cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);

@@ -1,7 +1,7 @@
 """GPU parity of pa_multi_query: several new query tokens per sequence attending causally over
 the paged cache, against the oracle; one token per sequence equal to pa_decode; sequences cut
 between CTAs (the causal limit can leave a piece without a visible token for some rows);
-clamped counts flagged; shapes beyond the kernel refused."""
+clamped counts flagged; more than 16 rows per (sequence, kv head) through the 64-row tiles."""
 import numpy as np
 import pytest
 import torch
@@ -87,13 +87,36 @@ def test_counts_beyond_the_context_are_clamped_and_flagged(oracle):
         assert max_abs_err(out[4 * s:4 * s + 2], ref) <= TOL
 
 
-def test_rows_beyond_the_kernel_are_refused():
-    wl = workloads.make_workload("mq_big", context_lens=[40], num_q_heads=8, num_kv_heads=2, block_size=16, seed=2)
+@pytest.mark.parametrize("G,lens,new,B,dtype", [
+    (4, [40, 300, 5], [5, 5, 5], 16, "f16"),                       # 20 rows: one 64-row tile
+    (6, [129, 1000, 64], [16, 16, 16], 16, "bf16"),                # 96 rows: two tiles
+    (1, [100, 700, 2049], [100, 64, 100], 32, "bf16"),             # full prefill of the first
+    (2, [300, 31, 500], [300, 31, 1], 16, "f16"),                  # full prefills, 600 rows
+    (3, [77, 0, 513, 900, 2], [37, 0, 1, 20, 2], 64, "f16"),       # ragged, an empty sequence
+    (2, [260, 1024], [70, 130], 128, "bf16"),                      # 128-token blocks
+])
+def test_prefill_tiles_parity(oracle, G, lens, new, B, dtype):
+    """More than 16 query rows per (sequence, kv head): tensor-core tiles of 64 rows."""
+    wl = workloads.make_workload(f"pf_G{G}_B{B}", context_lens=lens, num_q_heads=2 * G, num_kv_heads=2,
+                                 block_size=B, dtype=dtype, seed=G * 13 + B, max_context=max(lens) + B)
+    assert max(new) * G > 16
+    _run(oracle, wl, new, seed=G + B)
+
+
+def test_prefill_counts_beyond_the_context_are_flagged(oracle):
+    lens = [10, 40]
+    wl = workloads.make_workload("pf_bad", context_lens=lens, num_q_heads=8, num_kv_heads=1, block_size=16, seed=19)
     dev = torch.device("cuda")
-    q, qs, _ = workloads.multi_query_inputs(wl, [5], seed=1)
-    before = pa.kernel_launch_count()
-    with pytest.raises(pa.PAError) as e:
-        pa.multi_query(q.to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), wl.block_tables.to(dev),
-                       wl.context_lens.to(dev), qs.to(dev), wl.scale, 2, 5)     # 5 tokens x G 4 = 20 rows
-    assert e.value.code == -2
-    assert pa.kernel_launch_count() == before
+    q, _, _ = workloads.multi_query_inputs(wl, [12, 12], seed=4)
+    qs = torch.tensor([0, 12, 24], dtype=torch.int32)
+    # 12 new tokens claimed for a 10-token context: clamped to 10 and flagged
+    out = pa.multi_query(q.to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), wl.block_tables.to(dev),
+                         wl.context_lens.to(dev), qs.to(dev), wl.scale, 1, 12)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) & pa._native.DEV_BAD_CONTEXT
+    ref = oracle.multi_query(q[12:24], wl.k_cache[0], wl.v_cache[0], wl.block_tables[1:2], wl.context_lens[1:2],
+                             torch.tensor([0, 12], dtype=torch.int32), wl.scale, 1, False)
+    assert max_abs_err(out[12:24], ref) <= TOL
+    ref0 = oracle.multi_query(q[0:10], wl.k_cache[0], wl.v_cache[0], wl.block_tables[0:1], wl.context_lens[0:1],
+                              torch.tensor([0, 10], dtype=torch.int32), wl.scale, 1, False)
+    assert max_abs_err(out[0:10], ref0) <= TOL
