@@ -22,6 +22,9 @@ it follows:
   causally up to its own position (the chunked prefill the second page's closing section
   points to).
 * ``copy_blocks`` -- whole-block deep copy (§四 copy-on-write of the second page).
+* ``decode_runs`` / ``gather_runs`` -- contexts given as runs (block_id, slot_offset, length)
+  and row-run moves: the slotted blocks and online defragmentation of the radix-tree
+  fragmentation page.
 
 Pins (tests/test_oracle.py): exhaustive element decoding against numpy, the
 pages' worked address example and byte counts, torch's fp64
@@ -97,6 +100,11 @@ class Oracle:
         L.pao_multi_query.restype = _c_int
         L.pao_multi_query.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _c_int, _ptr, _ptr, ctypes.c_double,
                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]
+        L.pao_decode_runs.restype = _c_int
+        L.pao_decode_runs.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, ctypes.c_double, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_int, _c_int, _c_int]
+        L.pao_gather_runs.restype = _c_int
+        L.pao_gather_runs.argtypes = [_ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _ptr, _c_int, _c_int, _c_int, _c_int]
         L.pao_num_threads.restype = _c_int
         L.pao_num_threads.argtypes = []
 
@@ -192,6 +200,35 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle: arguments do not describe a valid multi-query problem")
         return out
+
+    def decode_runs(self, q, k_cache, v_cache, runs, seq_runs, scale: float, num_kv_heads: int, is_bf16: bool,
+                    num_threads: int = 0) -> np.ndarray:
+        """One query token per sequence over a context given by runs (block, slot_offset, length):
+        runs int32 [R, 3], sequence s owning runs seq_runs[s] .. seq_runs[s+1]-1."""
+        qq = as_u16(q)
+        kc, vc = as_u16(k_cache), as_u16(v_cache)
+        rr = np.ascontiguousarray(np.asarray(runs, dtype=np.int32).reshape(-1, 3))
+        sr = as_i32(seq_runs)
+        S, Hq, D = qq.shape
+        assert sr.size == S + 1
+        NB, _, B, _ = kc.shape
+        out = np.empty((S, Hq, D), dtype=np.float64)
+        rc = self._L.pao_decode_runs(out.ctypes.data, qq.ctypes.data, kc.ctypes.data, vc.ctypes.data, rr.ctypes.data,
+                                     sr.ctypes.data, float(scale), S, Hq, int(num_kv_heads), D, B, NB, int(is_bf16),
+                                     int(num_threads))
+        if rc != 0:
+            raise ValueError("oracle: a run leaves its block or the pool")
+        return out
+
+    def gather_runs(self, src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray, moves) -> int:
+        """In place on the uint16 pools dst_k/dst_v; moves int32 [M, 5] = (src_block, src_off, length,
+        dst_block, dst_off).  Returns how many moves were left out."""
+        for a in (src_k, src_v, dst_k, dst_v):
+            assert a.dtype == np.uint16 and a.flags.c_contiguous
+        mv = np.ascontiguousarray(np.asarray(moves, dtype=np.int32).reshape(-1, 5))
+        NBs, H, B, D = src_k.shape
+        return int(self._L.pao_gather_runs(src_k.ctypes.data, src_v.ctypes.data, NBs, dst_k.ctypes.data,
+                                           dst_v.ctypes.data, dst_k.shape[0], mv.ctypes.data, mv.shape[0], H, B, D))
 
     def num_threads(self) -> int:
         return int(self._L.pao_num_threads())

@@ -339,6 +339,112 @@ int pao_multi_query(double* out, const uint16_t* q, const uint16_t* k_cache, con
     return bad ? -1 : 0;
 }
 
+/* ---- slotted blocks (the radix-tree fragmentation page, "Slotted Block 分槽与微块共享架构"):
+ * a sequence's context is a list of runs (block_id, slot_offset, length), read in order;
+ * token t of the sequence is row slot_offset + (t - run start) of block block_id. ---- */
+
+/* Gather the cached rows of (sequence, kv head hk) given by runs[r0 .. r1) into contiguous fp64
+ * rows; returns the number of rows, or -1 if a run leaves its block or the pool. */
+static int gather_runs(const uint16_t* cache, const int32_t* runs, int r0, int r1, int hk, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, int is_bf16, double* dst) {
+    int t = 0;
+    for (int r = r0; r < r1; ++r) {
+        const int32_t blk = runs[3 * r], off = runs[3 * r + 1], len = runs[3 * r + 2];
+        if (blk < 0 || blk >= num_blocks || off < 0 || len < 0 || off + len > block_size) return -1;
+        for (int k = 0; k < len; ++k, ++t) {
+#if PAO_MUTANT == 10
+            const int64_t row = ((int64_t)blk * num_kv_heads + hk) * block_size + k;          /* planted: offset dropped */
+#else
+            const int64_t row = ((int64_t)blk * num_kv_heads + hk) * block_size + off + k;
+#endif
+            if (dst)
+                for (int d = 0; d < head_dim; ++d) dst[(int64_t)t * head_dim + d] = elem(cache + row * head_dim + d, is_bf16);
+        }
+    }
+    return t;
+}
+
+/* One query token per sequence over a context given by runs: sequence s owns runs
+ * seq_runs[s] .. seq_runs[s+1]-1; its length is the sum of their lengths.  out as pao_decode. */
+int pao_decode_runs(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                    const int32_t* runs, const int32_t* seq_runs, double scale, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks, int is_bf16, int num_threads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0) return -1;
+    const int G = num_q_heads / num_kv_heads;
+    const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : bad)
+#endif
+    for (int64_t pr = 0; pr < pairs; ++pr) {
+        const int s = (int)(pr / num_kv_heads);
+        const int hk = (int)(pr % num_kv_heads);
+        const int L = gather_runs(k_cache, runs, seq_runs[s], seq_runs[s + 1], hk, num_kv_heads, head_dim,
+                                  block_size, num_blocks, is_bf16, NULL);
+        if (L < 0) { bad = 1; continue; }
+        double* K = (double*)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double* V = (double*)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double* z = (double*)malloc(sizeof(double) * ((size_t)L + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        gather_runs(k_cache, runs, seq_runs[s], seq_runs[s + 1], hk, num_kv_heads, head_dim, block_size, num_blocks,
+                    is_bf16, K);
+        gather_runs(v_cache, runs, seq_runs[s], seq_runs[s + 1], hk, num_kv_heads, head_dim, block_size, num_blocks,
+                    is_bf16, V);
+        for (int g = 0; g < G; ++g) {
+            const int h = hk * G + g;
+            double* o = out + ((int64_t)s * num_q_heads + h) * head_dim;
+            const uint16_t* qr = q + ((int64_t)s * num_q_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) qv[d] = elem(qr + d, is_bf16);
+            double zmax = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int d = 0; d < head_dim; ++d) acc += qv[d] * K[(int64_t)t * head_dim + d];
+                z[t] = scale * acc;
+                if (z[t] > zmax) zmax = z[t];
+            }
+            double denom = 0.0;
+            for (int t = 0; t < L; ++t) {
+                z[t] = exp(z[t] - zmax);
+                denom += z[t];
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int t = 0; t < L; ++t) acc += z[t] * V[(int64_t)t * head_dim + d];
+                o[d] = (L > 0) ? acc / denom : 0.0;
+            }
+        }
+        free(K); free(V); free(z); free(qv);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Online defragmentation (same page): move runs of rows.  moves[m] = (src_block, src_off,
+ * length, dst_block, dst_off); every kv head's rows src_off .. src_off+length-1 of src_block
+ * are copied to dst_off .. of dst_block, moves applied in order.  A move leaving a block or a
+ * pool is left out; returns how many were. */
+int pao_gather_runs(const uint16_t* src_k, const uint16_t* src_v, int src_blocks, uint16_t* dst_k, uint16_t* dst_v,
+                    int dst_blocks, const int32_t* moves, int num_moves, int num_kv_heads, int block_size,
+                    int head_dim) {
+    int left_out = 0;
+    for (int m = 0; m < num_moves; ++m) {
+        const int32_t sb = moves[5 * m], so = moves[5 * m + 1], len = moves[5 * m + 2];
+        const int32_t db = moves[5 * m + 3], dof = moves[5 * m + 4];
+        if (sb < 0 || sb >= src_blocks || db < 0 || db >= dst_blocks || len < 0 || so < 0 || dof < 0 ||
+            so + len > block_size || dof + len > block_size) {
+            ++left_out;
+            continue;
+        }
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const int64_t s_row = ((int64_t)sb * num_kv_heads + h) * block_size + so;
+            const int64_t d_row = ((int64_t)db * num_kv_heads + h) * block_size + dof;
+            memmove(dst_k + d_row * head_dim, src_k + s_row * head_dim, sizeof(uint16_t) * (size_t)len * head_dim);
+            memmove(dst_v + d_row * head_dim, src_v + s_row * head_dim, sizeof(uint16_t) * (size_t)len * head_dim);
+        }
+    }
+    return left_out;
+}
+
 int pao_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -13,6 +13,9 @@
 * several query tokens per sequence: torch's fp64 attention with an explicit causal mask on
   the unpaged data (full causal prefill, one token, none), and bit-for-bit the decode at one
   token per sequence;
+* slotted blocks: the radix-tree page's slotted block (tests/golden/slotted_worked_example.txt)
+  read through runs against torch's fp64 attention on the concatenated rows, whole-block runs
+  against the block-table decode, and compaction into fresh blocks (bit for bit);
 * block copy: the copy-on-write fork of the PagedAttention explainer page
   (tests/golden/cow_worked_example.txt) checked against torch's fp64 attention on
   each branch's contiguous context, and a move to another pool and back that must
@@ -377,9 +380,93 @@ def pin_multi_query_vs_sdpa(o):
     assert np.array_equal(dec, one)
 
 
+def _slotted_golden():
+    kv = {}
+    for r in _read_golden("slotted_worked_example.txt"):
+        if r[0] == "slot":
+            kv["slot_" + r[1]] = (int(r[2]), int(r[3]))
+        else:
+            kv[r[0]] = float(r[1]) if "." in r[1] else int(r[1])
+    return kv
+
+
+def pin_slotted_runs(o):
+    """Contexts given as runs (block_id, slot_offset, length): the page's slotted block (Node A in
+    slots 0..4, Node B in 5..12 of one 16-slot block, tests/golden/slotted_worked_example.txt),
+    sequences reading a node's slot and then blocks of their own.  Attention must equal torch's
+    fp64 attention on the concatenated rows; runs of whole blocks must give the block-table decode
+    bit for bit; compacting the runs into fresh blocks (the page's online defragmentation) must
+    give the same decode bit for bit through a plain block table."""
+    kv = _slotted_golden()
+    B = kv["block_size"]
+    (a_off, a_len), (b_off, b_len) = kv["slot_A"], kv["slot_B"]
+    assert a_off + a_len == b_off and B - (b_off + b_len) == kv["free_tail"]
+    assert B - kv["lone_node_tokens"] == kv["lone_node_idle_slots"]
+    # 11 / 16 = 68.75 %, which the page prints cut to one decimal
+    assert math.floor(1000 * kv["lone_node_idle_slots"] / B) / 10 == kv["lone_node_idle_pct"]
+    gen = torch.Generator().manual_seed(55)
+    Hkv, G, D = 2, 3, 128
+    Hq = Hkv * G
+    NB = 24
+    kc = _rand16((NB, Hkv, B, D), gen)
+    vc = _rand16((NB, Hkv, B, D), gen)
+    shared = 7                                   # the slotted block
+    # seq 0: node A's slot, then blocks 3 and 11 (whole) and 4 tokens of block 2
+    # seq 1: node B's slot, then 9 tokens of block 20; seq 2: node A only; seq 3: empty
+    runs = [(shared, a_off, a_len), (3, 0, B), (11, 0, B), (2, 0, 4),
+            (shared, b_off, b_len), (20, 0, 9),
+            (shared, a_off, a_len)]
+    seq_runs = [0, 4, 6, 7, 7]
+    S = len(seq_runs) - 1
+    q = _rand16((S, Hq, D), gen)
+    scale = 1.0 / math.sqrt(D)
+    got = o.decode_runs(q, kc, vc, runs, seq_runs, scale, Hkv, False)
+    Kc, Vc = [], []
+    for s in range(S):
+        ks = [kc[blk, :, off:off + ln, :] for blk, off, ln in runs[seq_runs[s]:seq_runs[s + 1]]]
+        vs = [vc[blk, :, off:off + ln, :] for blk, off, ln in runs[seq_runs[s]:seq_runs[s + 1]]]
+        Kc.append(torch.cat(ks, dim=1) if ks else torch.zeros((Hkv, 0, D), dtype=kc.dtype))
+        Vc.append(torch.cat(vs, dim=1) if vs else torch.zeros((Hkv, 0, D), dtype=vc.dtype))
+    want = _sdpa_fp64(q, Kc, Vc, Hkv, scale)
+    assert np.max(np.abs(got - want)) < 1e-12
+    # whole-block runs are a block table
+    lens = [37, 16, 64]
+    q2, _, _, kc2, vc2, tables = _paged_problem(lens, Hq, Hkv, D, B, seed=56)
+    r2, sr2 = [], [0]
+    for s, L in enumerate(lens):
+        for t0 in range(0, L, B):
+            r2.append((int(tables[s, t0 // B]), 0, min(B, L - t0)))
+        sr2.append(len(r2))
+    dec = o.decode(q2, kc2, vc2, tables, np.array(lens, np.int32), scale, Hkv, False)
+    assert np.array_equal(dec, o.decode_runs(q2, kc2, vc2, r2, sr2, scale, Hkv, False))
+    # compaction: each sequence's runs moved into fresh whole blocks, then a plain table
+    ku, vu = oracle_pkg.as_u16(kc).copy(), oracle_pkg.as_u16(vc).copy()
+    moves, table, nxt = [], np.full((S, 8), -1, np.int32), 12
+    lens3 = []
+    for s in range(S):
+        t = 0
+        for blk, off, ln in runs[seq_runs[s]:seq_runs[s + 1]]:
+            k = 0
+            while k < ln:
+                if t % B == 0:
+                    table[s, t // B] = nxt
+                    nxt += 1
+                take = min(ln - k, B - t % B)
+                moves.append((blk, off + k, take, int(table[s, t // B]), t % B))
+                t += take
+                k += take
+        lens3.append(t)
+    assert nxt <= NB and not set(range(12, nxt)) & {b for b, _, _ in runs}
+    assert o.gather_runs(ku, vu, ku, vu, moves) == 0
+    comp = o.decode(q, ku, vu, table, np.array(lens3, np.int32), scale, Hkv, False)
+    assert np.array_equal(comp, got)
+    # a move that leaves its block is left out
+    assert o.gather_runs(ku, vu, ku.copy(), vu.copy(), [(0, 10, 8, 1, 0)]) == 1
+
+
 PINS = [pin_f16_exhaustive, pin_bf16_exhaustive, pin_address_worked_example, pin_byte_ledger,
         pin_decode_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write,
-        pin_copy_on_write_fork, pin_block_moves, pin_multi_query_vs_sdpa]
+        pin_copy_on_write_fork, pin_block_moves, pin_multi_query_vs_sdpa, pin_slotted_runs]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -398,6 +485,7 @@ MUTANTS = {
     7: "cache rows written with a [NB][B][H][D] layout",
     8: "block copy moves kv head 0 only",
     9: "a query token does not attend to its own position",
+    10: "a run's slot offset is ignored",
 }
 
 
