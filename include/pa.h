@@ -4,6 +4,9 @@
  * block tables and slot mappings those two calls consume.
  *
  * Sources for what each call computes (page title, then section):
+ *   [P2] the radix-tree prefix-cache fragmentation page (mhpq.cn) -- "Slotted Block 分槽与微块
+ *        共享架构" (nodes packed as slots into shared blocks, (block_id, slot_offset, length)
+ *        addressing, copy-on-write split-off on append, online defragmentation).
  *   [P1] "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块"
  *        -- "注意力寻址：非连续物理块的间接寻址内核" (token t lives in logical block
  *        t / B at offset t % B; physical block = block_table[t / B]);
@@ -266,6 +269,45 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
                    void* workspace, size_t workspace_bytes, void* stream,
                    const pa_decode_options* opts);
 
+/* ------------------------------------------------------------------------------------
+ * pa_decode_runs  [P2 "Slotted Block 分槽与微块共享架构": nodes addressed by
+ *                  (block_id, slot_offset, length) triples; P4 §五.1 attention]
+ * One query token per sequence over a context given as runs instead of a block table:
+ * sequence s reads runs seq_runs[s] .. seq_runs[s+1]-1 of `runs` (int32 [R][3]: block id,
+ * slot offset, length) in order, so its token t is row slot_offset + (t - run start) of the
+ * run's block, and its length L is the sum of its runs' lengths.  Otherwise as pa_decode:
+ *   out[s][h][:] = sum_t softmax_t(scale * q[s][h] . K[t]) * V[t][:]   (L == 0: zero row).
+ * max_context bounds every L (longer contexts are cut there and set PA_DEV_BAD_CONTEXT).  A run
+ * that leaves its block or the pool counts as empty and sets PA_DEV_BAD_BLOCK_ID.
+ * Runs on the split CUDA-core kernel (each run piece one bulk copy of contiguous rows):
+ * num_q_heads / num_kv_heads in {1, 2, 3, 4, 6, 8}, block_size 16/32/64/128, head_dim 128.
+ * workspace: pa_decode_runs_workspace_size(...) bytes (0: none needed).
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------------------- */
+int pa_decode_runs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* runs, const int32_t* seq_runs, float scale, int num_kv_heads,
+                   int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                   int max_context, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+size_t pa_decode_runs_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_context);
+
+/* ------------------------------------------------------------------------------------
+ * pa_gather_runs  [P2 online defragmentation: scattered read-only slots moved into
+ *                  contiguous blocks; copy-on-write split-off of a shared slot]
+ * For m = 0..num_moves-1, moves[m] = (src_block, src_off, length, dst_block, dst_off): every
+ * kv head's rows src_off .. src_off+length-1 of src_block in (src_k, src_v) are copied bit
+ * for bit to rows dst_off .. of dst_block in (dst_k, dst_v).  Pools [blocks][Hkv][B][D] on the
+ * device (they may be the same pool).  A move that leaves a block or a pool is skipped and
+ * sets PA_DEV_BAD_BLOCK_ID.  Destination rows of different moves must not overlap, nor any
+ * move's source rows (else which bytes land is unspecified).  moves: int32 [num_moves][5],
+ * device memory.  head_dim a positive multiple of 8; pools 16-byte aligned.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------------------- */
+int pa_gather_runs(const void* src_k, const void* src_v, int src_blocks,
+                   void* dst_k, void* dst_v, int dst_blocks,
+                   const int32_t* moves, int num_moves,
+                   int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
+
 /* Bytes of workspace pa_decode needs for this shape on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq);
@@ -361,6 +403,22 @@ int pa_pool_release(pa_pool* pool, int32_t* table_row, int max_blocks, int conte
  * PA_ERR_BOUNDS (a table entry not allocated in `from`) or PA_ERR_POOL_EXHAUSTED. */
 int pa_pool_move_blocks(pa_pool* from, pa_pool* to, int32_t* table_row, int n,
                         int32_t* src_ids, int32_t* dst_ids);
+
+/* ---- Slotted blocks (host)  [P2 "Slotted Block 分槽与微块共享架构"] ----
+ * Nodes of n <= block_size tokens packed into shared blocks.  A node goes to the
+ * earliest-opened block whose free tail still holds n (offset = tokens already placed there),
+ * else to a fresh block, the lowest free id.  A released slot's space is reused only once its
+ * block has no live slot left and returns to the free set. */
+typedef struct pa_slots pa_slots;
+pa_slots* pa_slots_create(int num_blocks, int block_size);
+void pa_slots_destroy(pa_slots* pool);
+/* PA_OK with (*block, *offset), PA_ERR_POOL_EXHAUSTED or PA_ERR_INVALID_ARG. */
+int pa_slots_alloc(pa_slots* pool, int n, int32_t* block, int32_t* offset);
+/* Live slots left in the block, or PA_ERR_BOUNDS for a slot that is not placed there. */
+int pa_slots_release(pa_slots* pool, int32_t block, int32_t offset, int n);
+int pa_slots_tail(const pa_slots* pool, int32_t block);   /* tokens placed (next offset) */
+int pa_slots_live(const pa_slots* pool, int32_t block);   /* live slots */
+int pa_slots_num_free(const pa_slots* pool);
 
 /* slots[s] = slot of token context_lens[s] - 1 (the newest one), or -1 when the
  * context is empty; host arrays.  Returns PA_OK or PA_ERR_BOUNDS if a length

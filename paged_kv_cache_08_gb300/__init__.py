@@ -23,7 +23,8 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "multi_query", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "multi_query", "decode_runs", "gather_runs",
+           "SlotPool", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
 
@@ -288,6 +289,100 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                               ws_bytes, _stream_ptr(stream), ctypes.byref(o))
     _native.check("pa_multi_query", rc)
     return out
+
+
+def decode_runs(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, runs: torch.Tensor,
+                seq_runs: torch.Tensor, scale: float, num_kv_heads: int, max_context: int,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode over contexts given as runs (block_id, slot_offset, length): runs int32 [R, 3],
+    sequence s reading runs seq_runs[s] .. seq_runs[s+1]-1 (int32 [S + 1]).  See pa_decode_runs."""
+    _need_cuda("q", q)
+    if q.dtype not in _DTYPE:
+        raise TypeError("q must be float16 or bfloat16")
+    _need_cuda("k_cache", k_cache, q.dtype)
+    _need_cuda("v_cache", v_cache, q.dtype)
+    _need_cuda("runs", runs, torch.int32)
+    _need_cuda("seq_runs", seq_runs, torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if Hkv != num_kv_heads or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape does not match q / num_kv_heads")
+    if seq_runs.numel() != S + 1 or (runs.numel() and runs.shape[-1] != 3):
+        raise ValueError("seq_runs must have S + 1 entries and runs 3 columns")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+    need = int(lib().pa_decode_runs_workspace_size(S, Hq, Hkv, D, B, int(max_context)))
+    if workspace is None and need:
+        workspace = _workspace(q.device, need, -1, 0)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_decode_runs(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              runs.data_ptr() if runs.numel() else seq_runs.data_ptr(), seq_runs.data_ptr(),
+                              float(scale), int(num_kv_heads), S, Hq, D, B, NB, int(max_context), _DTYPE[q.dtype],
+                              ws_ptr, ws_bytes, _stream_ptr(stream))
+    _native.check("pa_decode_runs", rc)
+    return out
+
+
+def gather_runs(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                moves: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Row-run moves: moves int32 [M, 5] = (src_block, src_off, length, dst_block, dst_off)."""
+    if src_k.dtype not in _DTYPE:
+        raise TypeError("pools must be float16 or bfloat16")
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        _need_cuda(n, t, src_k.dtype)
+    _need_cuda("moves", moves, torch.int32)
+    NBs, H, B, D = src_k.shape
+    if src_v.shape != src_k.shape or dst_k.shape[1:] != src_k.shape[1:] or dst_v.shape != dst_k.shape:
+        raise ValueError("shape mismatch")
+    M = moves.numel() // 5
+    rc = lib().pa_gather_runs(src_k.data_ptr(), src_v.data_ptr(), NBs, dst_k.data_ptr(), dst_v.data_ptr(),
+                              dst_k.shape[0], moves.data_ptr(), M, H, D, B, _DTYPE[src_k.dtype], _stream_ptr(stream))
+    _native.check("pa_gather_runs", rc)
+
+
+class SlotPool:
+    """Slotted blocks (host): nodes of up to block_size tokens packed into shared blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = lib()
+        self._h = self._lib.pa_slots_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError("pa_slots_create failed")
+
+    def close(self):
+        if self._h:
+            self._lib.pa_slots_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int):
+        """(block, offset) of a new slot of n tokens."""
+        b = ctypes.c_int32(-1)
+        o = ctypes.c_int32(-1)
+        _native.check("pa_slots_alloc", self._lib.pa_slots_alloc(self._h, int(n), ctypes.byref(b), ctypes.byref(o)))
+        return int(b.value), int(o.value)
+
+    def release(self, block: int, offset: int, n: int) -> int:
+        return _native.check("pa_slots_release", self._lib.pa_slots_release(self._h, int(block), int(offset), int(n)))
+
+    def tail(self, block: int) -> int:
+        return _native.check("pa_slots_tail", self._lib.pa_slots_tail(self._h, int(block)))
+
+    def live(self, block: int) -> int:
+        return _native.check("pa_slots_live", self._lib.pa_slots_live(self._h, int(block)))
+
+    @property
+    def num_free(self) -> int:
+        return self._lib.pa_slots_num_free(self._h)
 
 
 def read_device_status(clear: bool = True, stream: Optional[torch.cuda.Stream] = None) -> int:

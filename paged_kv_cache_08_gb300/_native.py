@@ -47,6 +47,17 @@ _SIGNATURES = {
                                  c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
     "pa_multi_query": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_runs": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int, c_int,
+                               c_int, c_int, c_vp, c_size, c_vp]),
+    "pa_decode_runs_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),
+    "pa_gather_runs": (c_int, [c_vp, c_vp, c_int, c_vp, c_vp, c_int, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp]),
+    "pa_slots_create": (c_vp, [c_int, c_int]),
+    "pa_slots_destroy": (None, [c_vp]),
+    "pa_slots_alloc": (c_int, [c_vp, c_int, c_i32p, c_i32p]),
+    "pa_slots_release": (c_int, [c_vp, c_int, c_int, c_int]),
+    "pa_slots_tail": (c_int, [c_vp, c_int]),
+    "pa_slots_live": (c_int, [c_vp, c_int]),
+    "pa_slots_num_free": (c_int, [c_vp]),
     "pa_decode_static": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int,
                                  c_int, c_int, c_int, c_vp]),
     "pa_decode_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),

@@ -263,6 +263,110 @@ static const void* device_view(const void* p) {
     }
 }
 
+int pa_gather_runs(const void* src_k, const void* src_v, int src_blocks, void* dst_k, void* dst_v, int dst_blocks,
+                   const int32_t* moves, int num_moves, int num_kv_heads, int head_dim, int block_size, int dtype,
+                   void* stream) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (num_moves < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 || block_size <= 0 || src_blocks < 0 ||
+        dst_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_moves == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !moves) return PA_ERR_INVALID_ARG;
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) || !aligned4(moves))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)num_kv_heads * block_size * (head_dim / 8) > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    RowMoveArgs a;
+    a.src_k = static_cast<const uint4*>(src_k);
+    a.src_v = static_cast<const uint4*>(src_v);
+    a.dst_k = static_cast<uint4*>(dst_k);
+    a.dst_v = static_cast<uint4*>(dst_v);
+    a.moves = moves;
+    a.status = device_status_ptr();
+    a.num_moves = num_moves;
+    a.src_blocks = src_blocks;
+    a.dst_blocks = dst_blocks;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.vecs_per_row = head_dim / 8;
+    cudaError_t e = launch_gather_runs(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+// Slotted decode: the split CUDA-core kernel with its copies driven by runs.
+static int runs_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_context,
+                     int* tps, int* maxb, int* max_splits) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || max_context < 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim || !supported_block_size(block_size)) return PA_ERR_UNSUPPORTED;
+    if (!fma_supports_group(num_q_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
+    *maxb = (max_context + block_size - 1) / block_size;
+    if ((long long)*maxb * block_size > (1LL << 30)) return PA_ERR_UNSUPPORTED;
+    *tps = plan_tps(num_seqs, num_kv_heads, block_size, *maxb, nullptr);
+    if (*tps <= 0) return PA_ERR_INVALID_ARG;
+    *max_splits = max_splits_for(block_size, *maxb, *tps);
+    return PA_OK;
+}
+
+size_t pa_decode_runs_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                     int max_context) {
+    int tps, maxb, ms;
+    if (runs_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context, &tps, &maxb, &ms) != PA_OK)
+        return 0;
+    return ms > 1 ? workspace_bytes_for(num_seqs, num_q_heads, ms) : 0;
+}
+
+int pa_decode_runs(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* runs,
+                   const int32_t* seq_runs, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                   int head_dim, int block_size, int num_blocks, int max_context, int dtype, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    int tps, maxb, ms;
+    int rc = runs_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context, &tps, &maxb, &ms);
+    if (rc != PA_OK) return rc;
+    if (num_seqs == 0) return PA_OK;
+    if (num_blocks <= 0 || !out || !q || !k_cache || !v_cache || !runs || !seq_runs) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(runs) ||
+        !aligned4(seq_runs))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const size_t need = ms > 1 ? workspace_bytes_for(num_seqs, num_q_heads, ms) : 0;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.runs = runs;
+    a.seq_runs = seq_runs;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = maxb;
+    a.tokens_per_split = tps;
+    a.max_splits = ms;
+    const size_t n_part = (size_t)num_seqs * num_q_heads * ms;
+    a.part_o = need ? static_cast<float*>(workspace) : nullptr;
+    a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + n_part * kHeadDim * sizeof(float))
+                     : nullptr;
+    a.status = device_status_ptr();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode_split_fma(a, dtype, num_q_heads / num_kv_heads, st);
+    if (e == cudaSuccess && ms > 1) e = launch_decode_combine(a, dtype, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 int pa_copy_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k, void* dst_v, int dst_blocks,
                    const int32_t* src_ids, const int32_t* dst_ids, int num_pairs, int num_kv_heads, int head_dim,
                    int block_size, int dtype, void* stream) {

@@ -110,6 +110,56 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const int32_t* 
     }
 }
 
+// Slotted mode: position in a sequence's run list (run r, rows already taken from it).
+struct RunCursor {
+    int r;
+    int in_run;
+};
+
+// Issue the bulk copies of tokens [base, min(base + 64, tok_end)) read through runs: each piece
+// of a run is one contiguous group of rows of its (block, kv head) tile, copied to shared rows
+// t - base.  The cursor stands at token base and is left at the stage's end.
+template <typename T>
+__device__ __forceinline__ void issue_stage_runs(const DecodeArgs& a, RunCursor& cur, int r_end, int hk, int base,
+                                                 int tok_end, T* kdst, T* vdst, uint64_t* bar) {
+    const T* kc = static_cast<const T*>(a.k_cache);
+    const T* vc = static_cast<const T*>(a.v_cache);
+    const int end = min(base + kStageTokens, tok_end);
+    const uint32_t row_bytes = kHeadDim * sizeof(T);
+    // pass 1: bytes of the stage's pieces; pass 2: the copies
+    uint32_t total = 0;
+    {
+        RunCursor c = cur;
+        for (int t = base; t < end && c.r < r_end;) {
+            const int take = min(run_len(a, c.r) - c.in_run, end - t);
+            total += 2u * (uint32_t)max(take, 0) * row_bytes;
+            t += max(take, 0);
+            c.in_run += max(take, 0);
+            if (c.in_run >= run_len(a, c.r)) {
+                ++c.r;
+                c.in_run = 0;
+            }
+        }
+    }
+    mbar_arrive_expect_tx(bar, total);
+    for (int t = base; t < end && cur.r < r_end;) {
+        const int len = run_len(a, cur.r);
+        const int take = min(len - cur.in_run, end - t);
+        if (take > 0) {
+            const int blk = a.runs[3 * cur.r], off = a.runs[3 * cur.r + 1];
+            const size_t src = (((size_t)blk * a.num_kv_heads + hk) * a.block_size + off + cur.in_run) * kHeadDim;
+            bulk_copy_g2s(kdst + (size_t)(t - base) * kHeadDim, kc + src, (uint32_t)take * row_bytes, bar);
+            bulk_copy_g2s(vdst + (size_t)(t - base) * kHeadDim, vc + src, (uint32_t)take * row_bytes, bar);
+            t += take;
+            cur.in_run += take;
+        }
+        if (cur.in_run >= len) {
+            ++cur.r;
+            cur.in_run = 0;
+        }
+    }
+}
+
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 2) decode_split_fma_kernel(const DecodeArgs a) {
     using L = FmaSmem<G>;
@@ -132,11 +182,41 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_fma_kernel(const Dec
     }
     grid_dependency_wait();  // the cache and q may come from the preceding kernel
 
-    int Lctx = a.context_lens[s];
     const int cap = a.max_blocks_per_seq * a.block_size;
-    if (Lctx < 0 || Lctx > cap) {
-        if (tid == 0 && split == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
-        Lctx = Lctx < 0 ? 0 : cap;
+    int Lctx;
+    RunCursor cur{0, 0};
+    int r_end = 0;
+    if (a.runs) {
+        // slotted mode: the context is the runs' total length; a run that leaves its block or
+        // the pool counts as empty and is flagged; the total is capped at the planned capacity
+        const int r0 = a.seq_runs[s];
+        r_end = a.seq_runs[s + 1];
+        int* total_s = reinterpret_cast<int*>(alpha_s);   // scratch before the first stage
+        if (tid == 0) *total_s = 0;
+        __syncthreads();
+        int part = 0;
+        for (int r = r0 + tid; r < r_end; r += kThreads) {
+            const int len = run_len(a, r);
+            if (len != a.runs[3 * r + 2] && split == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            part += len;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) atomicAdd(total_s, part);
+        __syncthreads();
+        Lctx = *total_s;
+        __syncthreads();
+        if (Lctx > cap) {
+            if (tid == 0 && split == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+            Lctx = cap;
+        }
+        cur.r = r0;
+    } else {
+        Lctx = a.context_lens[s];
+        if (Lctx < 0 || Lctx > cap) {
+            if (tid == 0 && split == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+            Lctx = Lctx < 0 ? 0 : cap;
+        }
     }
     const int tps = a.tokens_per_split;
     const int tok0 = split * tps;
@@ -152,14 +232,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_fma_kernel(const Dec
     const int tok1 = min(Lctx, tok0 + tps);
     const int nsplit_s = (Lctx + tps - 1) / tps;
     const int nst = (tok1 - tok0 + kStageTokens - 1) / kStageTokens;
-    const int32_t* table = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+    const int32_t* table = a.block_tables ? a.block_tables + (size_t)s * a.max_blocks_per_seq : nullptr;
 
     __syncthreads();  // barriers initialised
     if (tid == 0) {
+        if (a.runs) {
+            // move the cursor to the split's first token
+            for (int t = 0; t < tok0 && cur.r < r_end;) {
+                const int take = min(run_len(a, cur.r) - cur.in_run, tok0 - t);
+                t += take;
+                cur.in_run += take;
+                if (cur.in_run >= run_len(a, cur.r)) {
+                    ++cur.r;
+                    cur.in_run = 0;
+                }
+            }
+        }
         const int pre = min(kStages, nst);
-        for (int i = 0; i < pre; ++i)
-            issue_stage<T>(a, table, hk, tok0 + i * kStageTokens, tok1, ring + (size_t)i * 2 * kTileElems,
-                           ring + (size_t)i * 2 * kTileElems + kTileElems, &bars[i]);
+        for (int i = 0; i < pre; ++i) {
+            T* kd = ring + (size_t)i * 2 * kTileElems;
+            if (a.runs)
+                issue_stage_runs<T>(a, cur, r_end, hk, tok0 + i * kStageTokens, tok1, kd, kd + kTileElems, &bars[i]);
+            else
+                issue_stage<T>(a, table, hk, tok0 + i * kStageTokens, tok1, kd, kd + kTileElems, &bars[i]);
+        }
     }
     grid_launch_dependents();
 
@@ -269,9 +365,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_fma_kernel(const Dec
         __syncthreads();  // stage buffer and scores free again
         if (tid == 0 && i + kStages < nst) {
             fence_proxy_async_smem();
-            issue_stage<T>(a, table, hk, tok0 + (i + kStages) * kStageTokens, tok1,
-                           ring + (size_t)st * 2 * kTileElems, ring + (size_t)st * 2 * kTileElems + kTileElems,
-                           &bars[st]);
+            T* kd = ring + (size_t)st * 2 * kTileElems;
+            if (a.runs)
+                issue_stage_runs<T>(a, cur, r_end, hk, tok0 + (i + kStages) * kStageTokens, tok1, kd, kd + kTileElems,
+                                    &bars[st]);
+            else
+                issue_stage<T>(a, table, hk, tok0 + (i + kStages) * kStageTokens, tok1, kd, kd + kTileElems,
+                               &bars[st]);
         }
     }
 
@@ -315,8 +415,13 @@ template <typename T>
 __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodeArgs a) {
     grid_dependency_wait();  // partials come from the split pass
     const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
-    int Lctx = a.context_lens[s];
     const int cap = a.max_blocks_per_seq * a.block_size;
+    int Lctx = 0;
+    if (a.runs) {
+        for (int r = a.seq_runs[s]; r < a.seq_runs[s + 1]; ++r) Lctx += run_len(a, r);   // as the split pass
+    } else {
+        Lctx = a.context_lens[s];
+    }
     Lctx = Lctx < 0 ? 0 : (Lctx > cap ? cap : Lctx);
     const int n = (Lctx + a.tokens_per_split - 1) / a.tokens_per_split;
     if (n <= 1) return;

@@ -80,6 +80,30 @@ struct DecodeArgs {
                               //   out (null: one query row per sequence, row s)
     int max_q;                // query tokens per sequence at most (1 without q_start)
     int q_rows;               // rows of q and out (several-token mode)
+    const int32_t* runs;      // slotted mode (split CUDA-core kernel): [R][3] (block, slot_offset, length);
+    const int32_t* seq_runs;  //   sequence s reads runs seq_runs[s] .. seq_runs[s+1]-1 in order; null = off
+};
+
+// Length of run r in slotted mode: 0 for a run that leaves its block or the pool.
+__device__ __forceinline__ int run_len(const DecodeArgs& a, int r) {
+    const int blk = a.runs[3 * r], off = a.runs[3 * r + 1], len = a.runs[3 * r + 2];
+    const bool ok = blk >= 0 && blk < a.num_blocks && off >= 0 && len >= 0 && off + len <= a.block_size;
+    return ok ? len : 0;
+}
+
+struct RowMoveArgs {
+    const uint4* src_k;       // [src_blocks][Hkv][B][D] as 16-byte vectors
+    const uint4* src_v;
+    uint4* dst_k;             // [dst_blocks][Hkv][B][D]
+    uint4* dst_v;
+    const int32_t* moves;     // [M][5]: src_block, src_off, length, dst_block, dst_off
+    unsigned int* status;
+    int num_moves;
+    int src_blocks;
+    int dst_blocks;
+    int num_kv_heads;
+    int block_size;
+    int vecs_per_row;         // D / 8
 };
 
 // New query tokens of sequence s (its newest ones, the last of its L cached tokens) and the
@@ -251,6 +275,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ---------------------------------------------------------------------------------------
 cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_runs(const RowMoveArgs& a, cudaStream_t stream);
 
 // FMA (CUDA-core) split pass for group size G and element type; returns cudaErrorInvalidValue
 // when G has no instantiation.

@@ -6,9 +6,13 @@
 // Reference counts: shared prefix blocks ("共享前缀块（Prefix Caching）" on the same page)
 // and copy-on-write on append ("显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §四).
 // Token append and release follow the lifecycle diagram of that page's §三.
+// Slotted blocks (pa_slots_*): short nodes packed into shared blocks and addressed by
+// (block_id, slot_offset, length), the radix-tree fragmentation page's "Slotted Block 分槽与
+// 微块共享架构".
 #include <cstdint>
 #include <cstdlib>
 #include <new>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/pa.h"
@@ -173,6 +177,89 @@ int pa_pool_move_blocks(pa_pool* from, pa_pool* to, int32_t* table_row, int n, i
     }
     return n;
 }
+
+// ---- slotted blocks ----
+// A node of n <= B tokens goes to the earliest-opened block whose free tail still holds n
+// (slots are appended at the tail: offset = tokens already placed), else to a fresh block, the
+// lowest free id.  A block counts its live slots; a released slot's space is reused only once
+// the block has emptied and gone back to the free set, so live slots never overlap.
+struct pa_slots {
+    int num_blocks, block_size;
+    std::vector<int> tail;     // tokens placed in the block (next slot offset)
+    std::vector<int> live;     // live slots in the block
+    std::vector<int> open;     // blocks with room left, in the order they were opened
+    int num_free;
+};
+
+pa_slots* pa_slots_create(int num_blocks, int block_size) {
+    if (num_blocks <= 0 || block_size <= 0) return nullptr;
+    pa_slots* p = new (std::nothrow) pa_slots;
+    if (!p) return nullptr;
+    try {
+        p->num_blocks = num_blocks;
+        p->block_size = block_size;
+        p->tail.assign((size_t)num_blocks, 0);
+        p->live.assign((size_t)num_blocks, 0);
+        p->num_free = num_blocks;
+    } catch (...) {
+        delete p;
+        return nullptr;
+    }
+    return p;
+}
+
+void pa_slots_destroy(pa_slots* p) { delete p; }
+
+int pa_slots_alloc(pa_slots* p, int n, int32_t* block, int32_t* offset) {
+    if (!p || !block || !offset || n <= 0 || n > p->block_size) return PA_ERR_INVALID_ARG;
+    for (size_t i = 0; i < p->open.size(); ++i) {
+        const int b = p->open[i];
+        if (p->block_size - p->tail[b] >= n) {
+            *block = b;
+            *offset = p->tail[b];
+            p->tail[b] += n;
+            ++p->live[b];
+            if (p->tail[b] == p->block_size) p->open.erase(p->open.begin() + (long)i);
+            return PA_OK;
+        }
+    }
+    for (int b = 0; b < p->num_blocks; ++b) {
+        if (p->live[b] == 0 && p->tail[b] == 0) {   // free
+            *block = b;
+            *offset = 0;
+            p->tail[b] = n;
+            p->live[b] = 1;
+            --p->num_free;
+            if (n < p->block_size) p->open.push_back(b);
+            return PA_OK;
+        }
+    }
+    return PA_ERR_POOL_EXHAUSTED;
+}
+
+int pa_slots_release(pa_slots* p, int32_t block, int32_t offset, int n) {
+    if (!p || block < 0 || block >= p->num_blocks || p->live[block] <= 0 || offset < 0 || n <= 0 ||
+        offset + n > p->tail[block])
+        return PA_ERR_BOUNDS;
+    if (--p->live[block] == 0) {
+        p->tail[block] = 0;
+        ++p->num_free;
+        p->open.erase(std::remove(p->open.begin(), p->open.end(), (int)block), p->open.end());
+    }
+    return p->live[block];
+}
+
+int pa_slots_tail(const pa_slots* p, int32_t block) {
+    if (!p || block < 0 || block >= p->num_blocks) return PA_ERR_BOUNDS;
+    return p->tail[block];
+}
+
+int pa_slots_live(const pa_slots* p, int32_t block) {
+    if (!p || block < 0 || block >= p->num_blocks) return PA_ERR_BOUNDS;
+    return p->live[block];
+}
+
+int pa_slots_num_free(const pa_slots* p) { return p ? p->num_free : PA_ERR_INVALID_ARG; }
 
 int pa_build_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                           int num_seqs, int block_size, int64_t* slots) {

@@ -223,3 +223,45 @@ def test_pool_builds_config5_shared_prefix_tables():
     assert len(set(used.tolist())) == used.size     # tail blocks are private
     slots = pa.build_slot_mapping(rows, wl.context_lens, B)
     assert not np.isin(slots // B, prefix[:n_prefix]).any()   # no write lands in the shared prefix
+
+
+def _slotted_golden():
+    kv = {}
+    for line in (GOLDEN / "slotted_worked_example.txt").read_text(encoding="utf-8").splitlines():
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, *rest = line.split()
+            kv[k if k != "slot" else "slot_" + rest[0]] = rest if k != "slot" else [int(x) for x in rest[1:]]
+    return kv
+
+
+def test_slotted_blocks_worked_example():
+    """The radix-tree page's slotted block (tests/golden/slotted_worked_example.txt): Node A (5
+    tokens) at offset 0 and Node B (8) at offset 5 of one 16-slot block, 3 slots left; a node
+    that does not fit the tail opens a fresh block; one that fits takes the tail."""
+    g = _slotted_golden()
+    B = int(g["block_size"][0])
+    p = pa.SlotPool(8, B)
+    a_off, a_len = g["slot_A"]
+    b_off, b_len = g["slot_B"]
+    assert p.alloc(a_len) == (0, a_off)
+    assert p.alloc(b_len) == (0, b_off)
+    assert B - p.tail(0) == int(g["free_tail"][0])
+    assert p.alloc(4) == (1, 0)            # 4 > 3 free slots: a fresh block
+    assert p.alloc(3) == (0, 13)           # fills block 0
+    assert p.live(0) == 3 and p.num_free == 6
+    # releasing a middle slot does not make its space reusable while the block has live slots
+    assert p.release(0, b_off, b_len) == 2
+    assert p.alloc(2) == (1, 4)
+    assert p.release(0, a_off, a_len) == 1 and p.release(0, 13, 3) == 0
+    assert p.num_free == 7 and p.tail(0) == 0
+    assert p.alloc(16) == (0, 0)           # the emptied block is whole again
+    with pytest.raises(pa.PAError):
+        p.release(0, 0, 17)
+    with pytest.raises(pa.PAError):
+        p.alloc(17)
+    small = pa.SlotPool(1, B)
+    small.alloc(16)
+    with pytest.raises(pa.PAError) as e:
+        small.alloc(1)
+    assert e.value.code == -4
