@@ -713,6 +713,87 @@ def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512
     print(json.dumps(line), flush=True)
 
 
+def run_runs(args):
+    """Slotted contexts: the decode bench's 24-layer 1.1B shape with every 16-token block of every
+    context read as two runs cut at a seeded random offset (about 2 x 4300 runs per layer), on
+    pa_decode_runs; then the compaction of one layer's runs into fresh whole blocks
+    (pa_gather_runs).  Bytes: the decode ledger with 12 bytes per run in place of 4 per table
+    entry; the compaction moves every context row of K and V once (read + written)."""
+    import paged_kv_cache_08_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workloads.config(2, device=dev, layers=args.layers)
+    B = wl.block_size
+    tables = wl.block_tables.numpy()
+    g = torch.Generator().manual_seed(99)
+    runs, seq_runs = [], [0]
+    for s_, L in enumerate(wl.context_lens.tolist()):
+        for t0 in range(0, L, B):
+            n = min(B, L - t0)
+            blk = int(tables[s_, t0 // B])
+            cut = int(torch.randint(1, B, (1,), generator=g)) if n > 1 else n
+            cut = min(cut, n)
+            runs.append((blk, 0, cut))
+            if n > cut:
+                runs.append((blk, cut, n - cut))
+        seq_runs.append(len(runs))
+    runs_t = torch.tensor(runs, dtype=torch.int32, device=dev)
+    seq_t = torch.tensor(seq_runs, dtype=torch.int32, device=dev)
+    max_ctx = int(wl.context_lens.max())
+    outs = [torch.empty_like(wl.q[i]) for i in range(wl.layers)]
+    S, Hq, D, Hkv = wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.num_kv_heads
+    ws = pa.new_workspace(pa.lib().pa_decode_runs_workspace_size(S, Hq, Hkv, D, B, max_ctx), dev)
+
+    def step():
+        for i in range(wl.layers):
+            pa.decode_runs(wl.q[i], wl.k_cache[i], wl.v_cache[i], runs_t, seq_t, wl.scale, Hkv, max_ctx, out=outs[i],
+                           workspace=ws)
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    with ClockSampler(0) as clk:
+        ms = _event_ms(lambda _: graph.replay(), args.steps, args.warmup)
+    lens64 = wl.context_lens.to(torch.int64)
+    per_layer = int(lens64.sum()) * Hkv * D * 2 * 2 + 2 * S * Hq * D * 2 + 12 * len(runs) + 4 * (S + 1)
+    gbs = wl.layers * per_layer / (ms * 1e-3) / 1e9
+    # compaction of layer 0's runs into fresh whole blocks of a second pool
+    moves, nxt = [], 0
+    for s_ in range(S):
+        t = 0
+        for blk, off, ln in runs[seq_runs[s_]:seq_runs[s_ + 1]]:
+            k = 0
+            while k < ln:
+                if t % B == 0:
+                    nxt += 1
+                take = min(ln - k, B - t % B)
+                moves.append((blk, off + k, take, nxt - 1, t % B))
+                t += take
+                k += take
+    moves_t = torch.tensor(moves, dtype=torch.int32, device=dev)
+    dk = torch.empty((nxt,) + tuple(wl.k_cache[0].shape[1:]), dtype=wl.torch_dtype, device=dev)
+    dv = torch.empty_like(dk)
+    cms = _event_ms(lambda i: pa.gather_runs(wl.k_cache[i % wl.layers], wl.v_cache[i % wl.layers], dk, dv, moves_t),
+                    args.steps, args.warmup)
+    moved = 2 * 2 * int(lens64.sum()) * Hkv * D * 2
+    peak, peak_kind = measured_peak_gbs()
+    line = {"metric": "slotted-context paged decode (runs): achieved HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"edge1p1b_64seq_ctx16-2048_gqa12x2_f16_B16_2runs_per_block_x{wl.layers}layers",
+                       "runs_per_layer": len(runs), "cuda_graph": True,
+                       "l2": "inputs larger than L2: distinct layer caches read once per step"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None, "algorithmic_bytes_per_layer": per_layer,
+                         "avg_layer_us": round(ms * 1e3 / wl.layers, 2),
+                         "kernel": "decode_split_fma_kernel (runs) + combine", "peak_source": f"{peak_kind} copy bandwidth"},
+            "compaction": {"moves": len(moves), "us": round(cms * 1e3, 2),
+                           "gbs": round(moved / (cms * 1e-3) / 1e9, 1), "frac": round(moved / (cms * 1e-3) / 1e9 / peak, 4)},
+            "gpu_launches": wl.layers * 2 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -728,8 +809,8 @@ def main():
                     help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
     ap.add_argument("--prefetch-own", action="store_true",
                     help="each layer prefetches its own chunks beyond the copy pipeline before its dependency wait")
-    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap", "multi_query", "prefill"], default="decode",
-                    help="decode step (default), or the block-copy, swap, several-token and prefill benchmarks")
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap", "multi_query", "prefill", "runs"], default="decode",
+                    help="decode step (default), or the block-copy, swap, several-token, prefill and slotted benchmarks")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -744,6 +825,9 @@ def main():
         return
     if args.op == "prefill" and args.impl == "ours":
         run_prefill(args)
+        return
+    if args.op == "runs" and args.impl == "ours":
+        run_runs(args)
         return
     if args.impl == "reference":
         run_reference(args)
