@@ -603,9 +603,10 @@ def run_swap(args):
 def run_multi_query(args, new_tokens: int = 2):
     """Several new tokens per sequence (speculative-decoding verification of one draft token per
     sequence and its successor): the 1.1B edge shape of the decode bench, 24 layers, each layer
-    writing the 2 newest tokens' K/V (pa_cache_write) and attending with pa_multi_query (12 query
-    rows per sequence and kv head), in a CUDA graph.  Bytes: the decode ledger with 2 query and
-    output rows per sequence, plus the cache write of 2 rows per sequence."""
+    writing the 2 newest tokens' K/V and attending over the cache (12 query rows per sequence
+    and kv head) in one pa_multi_query_append launch with early reads (``--path separate``:
+    pa_cache_write, then pa_multi_query), in a CUDA graph.  Bytes: the decode ledger with 2 query
+    and output rows per sequence, plus the cache write of 2 rows per sequence."""
     import paged_kv_cache_08_gb300 as pa
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -628,8 +629,14 @@ def run_multi_query(args, new_tokens: int = 2):
     outs = [torch.empty_like(q) for _ in range(wl.layers)]
     ws = pa.new_workspace(pa.decode_workspace_size(S, Hq, Hkv, D, wl.block_size, wl.max_blocks_per_seq), dev)
 
+    fused = args.path == "fused"
+
     def step():
         for i in range(wl.layers):
+            if fused:
+                pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
+                               workspace=ws, k_new=k_new[i], v_new=v_new[i])
+                continue
             pa.cache_write(k_new[i], v_new[i], slots, wl.k_cache[i], wl.v_cache[i])
             pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
                            workspace=ws)
@@ -665,13 +672,15 @@ def run_multi_query(args, new_tokens: int = 2):
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": {"workload": f"edge1p1b_64seq_ctx16-2048_gqa12x2_f16_B16_{new_tokens}new_x{wl.layers}layers",
-                       "step": "pa_cache_write + pa_multi_query per layer", "cuda_graph": True,
+                       "step": ("pa_multi_query_append (cache write + attention, early reads)" if fused
+                                else "pa_cache_write + pa_multi_query") + " per layer", "cuda_graph": True,
                        "l2": "inputs larger than L2: distinct layer caches read once per step"},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "traffic": None,
                          "algorithmic_bytes_per_layer": mq_bytes + cw_bytes, "avg_layer_us": round(per_layer_us, 2),
-                         "kernel": "pa_multi_query (+ pa_cache_write)", "peak_source": f"{peak_kind} copy bandwidth"},
-            "gpu_launches": 2 * wl.layers * args.steps, "clocks": clk.summary()}
+                         "kernel": "pa_multi_query_append" if fused else "pa_multi_query (+ pa_cache_write)",
+                         "peak_source": f"{peak_kind} copy bandwidth"},
+            "gpu_launches": (1 if fused else 2) * wl.layers * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 

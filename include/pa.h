@@ -270,6 +270,33 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
                    const pa_decode_options* opts);
 
 /* ------------------------------------------------------------------------------------
+ * pa_multi_query_append  [P4 §三 sequence diagram + §五.1; P4's closing section on chunked
+ *                         prefill; P1 address formula]
+ * The cache write of every sequence's n_s new tokens followed by pa_multi_query, in one
+ * launch: the effect of
+ *   pa_cache_write(k_new, v_new, slot(row) = block_tables[s][p / B] * B + p % B, ...)
+ *   pa_multi_query(out, q, k_cache, v_cache, ...)
+ * where row = query_start[s] + i holds the token at position p = L - n_s + i (after the
+ * clamping of n_s that pa_multi_query describes; rows it drops write nothing).  k_new, v_new: [num_q_tokens][num_kv_heads][head_dim],
+ * rows as q's.  A slot whose block id lies outside [0, num_blocks) is not written.
+ * Supported: the persistent kernel's shapes (max_q_per_seq x (num_q_heads / num_kv_heads)
+ * <= 16); beyond that PA_ERR_UNSUPPORTED (write the rows with pa_cache_write, then call
+ * pa_multi_query).  Early reads as for pa_decode_append: unless opts->flags has
+ * PA_DECODE_NO_EARLY_READS, context_lens, block_tables, query_start and the cached rows of
+ * earlier tokens may be read before the preceding kernel in the stream has finished; q,
+ * k_new and v_new are read, and out, the new slots and the workspace written, only after it.
+ * Returns the codes of pa_decode.
+ * ---------------------------------------------------------------------------------- */
+int pa_multi_query_append(void* out, const void* q, const void* k_new, const void* v_new,
+                          void* k_cache, void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          const int32_t* query_start, float scale, int num_kv_heads,
+                          int num_seqs, int num_q_tokens, int max_q_per_seq, int num_q_heads,
+                          int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                          int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                          const pa_decode_options* opts);
+
+/* ------------------------------------------------------------------------------------
  * pa_decode_runs  [P2 "Slotted Block 分槽与微块共享架构": nodes addressed by
  *                  (block_id, slot_offset, length) triples; P4 §五.1 attention]
  * One query token per sequence over a context given as runs instead of a block table:

@@ -7,7 +7,8 @@ as the device-memory and stream provider.
 
     cache_write(k, v, slot_mapping, k_cache, v_cache)
     decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads) -> out
-    multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, num_kv_heads, max_q)
+    multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, num_kv_heads, max_q,
+                k_new=None, v_new=None)      # with k_new / v_new: their cache write in the same launch
     copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids)   # copy-on-write, swap out / in
     BlockPool(num_blocks)                       # host block pool (untimed)
     build_slot_mapping(block_tables, context_lens, block_size)
@@ -251,10 +252,15 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                 context_lens: torch.Tensor, query_start: torch.Tensor, scale: float, num_kv_heads: int,
                 max_q: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
+                k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                early_reads: bool = True, prefetch=None, prefetch_own: bool = False,
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Several new query tokens per sequence attending causally over the paged cache.
     q: [T, Hq, D]; sequence s owns rows query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its
-    newest tokens; at most ``max_q`` per sequence.  See pa_multi_query in include/pa.h."""
+    newest tokens; at most ``max_q`` per sequence.  See pa_multi_query in include/pa.h.
+    With k_new / v_new ([T, Hkv, D], rows as q's) the same launch first writes them into the
+    slots of their positions (pa_multi_query_append; early reads, prefetch and prefetch_own as
+    for decode_append)."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -277,12 +283,29 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(0, "mma", num_ctas, timeline)
+    append = k_new is not None or v_new is not None
+    if append:
+        for n, t in (("k_new", k_new), ("v_new", v_new)):
+            _need_cuda(n, t, q.dtype)
+        if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape:
+            raise ValueError("k_new / v_new must be [T, Hkv, D]")
+        flags = (0 if early_reads else _native.NO_EARLY_READS) | (_native.PREFETCH_OWN if prefetch_own else 0)
+        o = _opts(0, "mma", num_ctas, timeline, flags, prefetch=prefetch, like=k_cache)
+    else:
+        o = _opts(0, "mma", num_ctas, timeline, prefetch=prefetch, like=k_cache)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         workspace = _workspace(q.device, need, 2, int(num_ctas))
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if append:
+        rc = lib().pa_multi_query_append(
+            out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+            v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(),
+            float(scale), int(num_kv_heads), S, T, int(max_q), Hq, D, B, NB, max_blocks, _DTYPE[q.dtype], ws_ptr,
+            ws_bytes, _stream_ptr(stream), ctypes.byref(o))
+        _native.check("pa_multi_query_append", rc)
+        return out
     rc = lib().pa_multi_query(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                               block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), float(scale),
                               int(num_kv_heads), S, T, int(max_q), Hq, D, B, NB, max_blocks, _DTYPE[q.dtype], ws_ptr,

@@ -47,6 +47,9 @@ _SIGNATURES = {
                                  c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
     "pa_multi_query": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
+    "pa_multi_query_append": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int,
+                                      c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_vp, c_size, c_vp,
+                                      ctypes.POINTER(DecodeOptions)]),
     "pa_decode_runs": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_vp, c_size, c_vp]),
     "pa_decode_runs_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),

@@ -477,8 +477,9 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     if (multi) {
         // several query tokens per sequence: the persistent kernel while a (sequence, kv head)
         // has at most 16 query rows, else tiles of 64 rows (no workspace)
-        if (append || max_q < 1 || !aligned4(q_start)) return PA_ERR_INVALID_ARG;
+        if (max_q < 1 || !aligned4(q_start)) return PA_ERR_INVALID_ARG;
         if ((long long)max_q * group > kPieceRows) {
+            if (append) return PA_ERR_UNSUPPORTED;   // the tiles kernel writes no cache rows
             if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
             DecodeArgs a;
             std::memset(&a, 0, sizeof(a));
@@ -610,6 +611,19 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
     if (num_q_tokens == 0) return num_seqs >= 0 ? PA_OK : PA_ERR_INVALID_ARG;
     if (opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) return PA_ERR_INVALID_ARG;
     return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
+                       workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);
+}
+
+int pa_multi_query_append(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                          const int32_t* query_start, float scale, int num_kv_heads, int num_seqs, int num_q_tokens,
+                          int max_q_per_seq, int num_q_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                          const pa_decode_options* opts) {
+    if (num_q_tokens < 0 || !query_start || !k_new || !v_new) return PA_ERR_INVALID_ARG;
+    if (num_q_tokens == 0) return num_seqs >= 0 ? PA_OK : PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
                        workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);
 }

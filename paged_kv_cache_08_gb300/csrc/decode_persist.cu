@@ -987,8 +987,33 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
+                if (kMulti && append) {
+                    // the segment's new tokens (positions L - n .. L - 1) in this warp's 16 rows:
+                    // their K/V rows go into the staged tile and into their cache slots
+                    const int c0 = pos.k * kStageTokens + t_warp;
+                    const int p_lo = max(pos.L - qsp.n, c0), p_hi = min(pos.L, c0 + 16);
+                    const int cc = lane & 15;
+                    const bool isv = lane >= 16;
+                    for (int p = p_lo; p < p_hi; ++p) {
+                        const int i_new = p - (pos.L - qsp.n);
+                        const size_t src_off = ((size_t)(qsp.row0 + i_new) * Hkv + pos.h) * kHeadDim + cc * 8;
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            static_cast<const T*>(isv ? a.v_new : a.k_new) + src_off);
+                        st_shared_v4(chunk_addr(isv ? vbase : kbase, p - pos.k * kStageTokens, cc, R_log2), val);
+                        const int phys = a.block_tables[(size_t)pos.s * a.max_blocks_per_seq + p / B];
+                        if (phys >= 0 && phys < a.num_blocks) {
+                            const size_t row = ((size_t)phys * Hkv + pos.h) * B + (size_t)(p % B);
+                            T* cache = const_cast<T*>(static_cast<const T*>(isv ? a.v_cache : a.k_cache));
+                            *reinterpret_cast<uint4*>(cache + row * kHeadDim + cc * 8) = val;
+                        }
+                    }
+                    if (p_lo < p_hi) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
                 const int tn = nvalid - 1;   // the newest token, when this is the segment's last chunk
-                if (append && pos.k == pos.n - 1 && (tn >> 4) == warp) {
+                if (!kMulti && append && pos.k == pos.n - 1 && (tn >> 4) == warp) {
                     // append: the new K/V row goes into the staged tile and into its cache slot
                     const int cc = lane & 15;
                     const bool isv = lane >= 16;

@@ -266,3 +266,15 @@ def multi_query_inputs(wl: Workload, new_tokens: Sequence[int], seed: int, devic
     if device is not None:
         q, qs = q.to(device), qs.to(device)
     return q, qs, max([int(n) for n in new_tokens] + [1])
+
+
+def new_token_rows(wl: Workload, num_rows: int, seed: int, device=None):
+    """K and V rows of ``num_rows`` new tokens ([num_rows, num_kv_heads, head_dim] each), drawn
+    N(0, 1) in the workload's dtype from their own seeded generator."""
+    gen = torch.Generator().manual_seed(seed)
+    shape = (num_rows, wl.num_kv_heads, wl.head_dim)
+    k = torch.randn(shape, generator=gen).to(wl.torch_dtype)
+    v = torch.randn(shape, generator=gen).to(wl.torch_dtype)
+    if device is not None:
+        k, v = k.to(device), v.to(device)
+    return k, v
