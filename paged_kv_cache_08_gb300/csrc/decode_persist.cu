@@ -92,9 +92,10 @@ struct PLayout {
                                                        // int [kStages] x 2 first q row / query tokens of
                                                        // the segment a stage starts
     static constexpr size_t kPrefix = kNewPhys + ((4 * kStages * sizeof(int32_t) + 15) & ~size_t(15));
-    // then int P[S + 1], int L[S]
-    static constexpr size_t total(int num_seqs) {
-        return 1024 /*alignment slack*/ + kPrefix + (size_t)(2 * num_seqs + 1) * sizeof(int32_t);
+    // then int P[S + 1], int L[S] and, for the weighted cut, int E[S + 1]
+    static constexpr size_t total(int num_seqs, bool weighted = false) {
+        return 1024 /*alignment slack*/ + kPrefix +
+               (size_t)(2 * num_seqs + 1 + (weighted ? num_seqs + 1 : 0)) * sizeof(int32_t);
     }
     static_assert(1024 + kPrefix + (2 * kPersistMaxSeqs + 1) * sizeof(int32_t) <= 227 * 1024,
                   "one CTA's shared memory must fit in 227 KB");
@@ -221,12 +222,98 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int t, int c, int 
     return base + line_of(t, c >> 3, R_log2) * 128u + ((uint32_t)((c & 7) ^ (t & 7)) << 4);
 }
 
-// CTA whose chunk range holds global chunk g: the largest c with floor(N c / C) <= g.
-__device__ __forceinline__ int cta_of(long long g, long long N, int C) {
-    return (int)(((g + 1) * (long long)C - 1) / N);
+// The cut of the chunk list into the ranges of the C CTAs that take part.
+//   Plain (W == 0): equal chunk counts, range c = [floor(N c / C), floor(N (c + 1) / C)).
+//   Weighted: chunk g of segment (s, h) sits at weight u g + e (E[s] + h), E[s] being the
+//   non-empty segments before sequence s, so that every segment end weighs e on top of its
+//   chunk's u; range c holds the chunks whose weight w has floor(w C / W) == c, W the total.
+//   Used when a CTA finishes many segments (the cost of a segment's end then rivals that of
+//   its chunks) and only while W >= (u + e) C, which leaves no range empty.
+// Quotient of non-negative 64-bit integers, through the 32-bit divide when both fit (the
+// partition's numbers nearly always do, and the 64-bit divide is a long software sequence).
+__device__ __forceinline__ long long div_nn(long long x, long long y) {
+    if (((unsigned long long)x | (unsigned long long)y) >> 32 == 0) return (long long)((uint32_t)x / (uint32_t)y);
+    return x / y;
 }
 
-__device__ __forceinline__ long long range_begin(int c, long long N, int C) { return (N * c) / C; }
+struct Cut {
+    long long N;        // chunks
+    int C;              // CTAs that take part
+    long long W;        // total weight, 0 for the plain cut
+    int u, e;
+    const int32_t* P;   // [S + 1] first chunk of each sequence
+    const int32_t* E;   // [S + 1] non-empty segments before each sequence (weighted cut)
+};
+
+// The cut as the prefix sums in shared memory define it (P[S] chunks; E follows Lc, i.e. starts
+// at P + 2 S + 1).  Rebuilt where it is needed rather than kept live through the chunk loop.
+// Kernels built without kCut always cut plainly (their code carries none of the weighted cut).
+template <bool kCut>
+__device__ __forceinline__ Cut make_cut(const DecodeArgs& a, const int32_t* P, int S) {
+    Cut k;
+    k.P = P;
+    k.E = P + 2 * S + 1;
+    k.N = P[S];
+    k.C = k.N > 0 ? (int)min((long long)gridDim.x, k.N) : 0;
+    k.u = a.cut_unit;
+    k.e = a.cut_seg;
+    k.W = 0;
+    if (kCut && a.cut_seg > 0 && k.C > 0) {
+        const long long W = (long long)k.u * k.N + (long long)k.e * k.E[S];
+        if (W >= (long long)(k.u + k.e) * k.C) k.W = W;
+    }
+    return k;
+}
+
+__device__ __forceinline__ long long cut_weight(const Cut& k, long long g, int s, int h) {
+    return (long long)k.u * g + (long long)k.e * (k.E[s] + h);
+}
+
+// CTA of the weighted cut whose range holds the chunk of weight w (out of line: once per cut
+// segment).
+__device__ __noinline__ int cta_of_weight(const Cut& k, long long w) { return (int)div_nn(w * k.C, k.W); }
+
+// CTA whose range holds chunk g of segment (s, h).
+__device__ __forceinline__ int cta_of(const Cut& k, long long g, int s, int h) {
+    if (!k.W) return (int)(((g + 1) * (long long)k.C - 1) / k.N);
+    return cta_of_weight(k, cut_weight(k, g, s, h));
+}
+
+// Whether the segment (s, h), whose first chunk Pseg belongs to CTA c_first, starts that
+// CTA's range (weighted: the chunk before it, a segment end, weighs u + e less).
+__device__ __forceinline__ bool starts_range(const Cut& k, long long Pseg, int s, int h, int c_first) {
+    if (!k.W) return Pseg == (k.N * c_first) / k.C;
+    if (Pseg == 0) return true;
+    return cta_of_weight(k, cut_weight(k, Pseg, s, h) - k.u - k.e) < c_first;
+}
+
+// First chunk of range c < C of the weighted cut (kept out of line: it runs once per CTA).
+__device__ __noinline__ long long range_begin_weighted(const Cut& k, int c, int S, int Hkv) {
+    const long long T = div_nn((long long)c * k.W + k.C - 1, k.C);   // the range's least weight
+    // the last sequence whose first chunk weighs at most T
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)k.u * k.P[mid] + (long long)k.e * k.E[mid] <= T) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = (k.P[lo + 1] - k.P[lo]) / Hkv;
+    if (n == 0) return k.P[lo];
+    const long long span = (long long)k.u * n + k.e;   // one segment of the sequence
+    const long long off = T - ((long long)k.u * k.P[lo] + (long long)k.e * k.E[lo]);
+    const long long h = div_nn(off, span);
+    if (h >= Hkv) return k.P[lo + 1];
+    const long long kk = div_nn(off - h * span + k.u - 1, k.u);
+    if (kk >= n) return k.P[lo] + (h + 1) * n;
+    return k.P[lo] + h * n + kk;
+}
+
+// First chunk of range c (N for c == C).
+__device__ __forceinline__ long long range_begin(const Cut& k, int c, int S, int Hkv) {
+    if (!k.W) return (k.N * c) / k.C;
+    if (c >= k.C) return k.N;
+    return range_begin_weighted(k, c, S, Hkv);
+}
 
 // Largest s in [0, S) with P[s] <= g (skips empty sequences because P repeats for them).
 __device__ __forceinline__ int seq_of(const int32_t* P, int S, long long g) {
@@ -389,14 +476,14 @@ __device__ __forceinline__ void zero_empty_rows(const DecodeArgs& a, const int32
 // cut by the CTA ranges -- into its normalised output rows.  Threads t = 0..nthreads-1 share the
 // G x 16 (row, 8-column) items; one online pass over the pieces, a batch of loads in flight.
 template <typename T, bool kMulti>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& qsp, int h, long long Pseg, int n,
-                                             long long N, int C, int t, int nthreads) {
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& qsp, int s, int h, long long Pseg,
+                                             int n, const Cut& cut, int t, int nthreads) {
     const int G = a.num_q_heads / a.num_kv_heads;
     const int rows = qsp.n * G;
-    const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + n - 1, N, C);
+    const int c_first = cta_of(cut, Pseg, s, h), c_last = cta_of(cut, Pseg + n - 1, s, h);
     // piece slot: 0 = the piece holding its CTA's first chunk; only the first CTA's piece can
     // start later than that
-    const int first_slot = (Pseg == range_begin(c_first, N, C)) ? 0 : 1;
+    const int first_slot = starts_range(cut, Pseg, s, h, c_first) ? 0 : 1;
     for (int e = t; e < rows * 16; e += nthreads) {
         const int row = e >> 4, d0 = (e & 15) * 8;
         // one online pass over the pieces, a few at a time, every load of a batch in flight
@@ -459,9 +546,9 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& q
 // the epilogue warp (`handoff`: every consumer thread arrives on `pdone` after its stores) or
 // finished here: count the arrival and, as the last CTA of the segment to arrive, merge all
 // pieces.  Returns true if this call merged a cut segment.
-template <typename T, int kNT, bool kMulti>
+template <typename T, int kNT, bool kMulti, bool kCut>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
-                                              const int32_t* P, long long b_c, long long b_e, long long N, int C,
+                                              const int32_t* P, long long b_c, long long b_e,
                                               int c, const float (&o)[kNT][8][4], const float (&m_run)[kNT][2],
                                               const float (&l_run)[kNT][2], bool dead, volatile int* last_flag,
                                               bool handoff, uint64_t* pdone, const QSpan& qsp) {
@@ -550,7 +637,10 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
                 if ((tid & 15) == 0) a.part_ml[piece * kPieceRows + row] = make_float2(M, den);
             }
         }
-        consumers_sync();   // the scratch is rewritten next
+        // The scratch is rewritten by the next column tile; a cut piece finished here also needs
+        // every thread's partial stores ahead of thread 0's release.  Otherwise the stage goes
+        // back to the producer only once every thread has arrived on its empty barrier.
+        if (nt + 1 < kNT || (!whole && !handoff)) consumers_sync();
     }
     if (!whole && handoff) {
         mbar_arrive(pdone);   // release: this thread's partial stores precede the epilogue's arrival
@@ -562,7 +652,8 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         // (the barrier that closed the loop above orders every thread's partial stores before
         // thread 0's release)
         const int sigma = pos.s * Hkv + pos.h;
-        const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + pos.n - 1, N, C);
+        const Cut cut = make_cut<kCut>(a, P, a.num_seqs);
+        const int c_first = cta_of(cut, Pseg, pos.s, pos.h), c_last = cta_of(cut, Pseg + pos.n - 1, pos.s, pos.h);
         if (tid == 0) {
             *last_flag = 0;
             if (!dead) {
@@ -573,7 +664,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         consumers_sync();
         const bool last = *last_flag != 0 && !dead;
         if (last) {
-            merge_pieces<T, kMulti>(a, qsp, pos.h, Pseg, pos.n, N, C, tid, kConsumerThreads);
+            merge_pieces<T, kMulti>(a, qsp, pos.s, pos.h, Pseg, pos.n, cut, tid, kConsumerThreads);
             if (tid == 0) a.seg_counters[sigma] = 0;   // ready for the next call
         }
         fence_proxy_async_smem();   // generic writes to the stage precede its next TMA fill
@@ -583,7 +674,77 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
     return false;
 }
 
-template <typename T, bool kG16, int kStages, bool kMulti>
+// Exclusive prefix sums over the sequences, by the whole CTA: Lc[s] = the clamped length,
+// P[s] = Hkv * (chunks of the sequences before s) and, with kSeqs, E[s] = Hkv * (sequences
+// with chunks before s), both counted in one pass (chunks in the low 40 bits of a 64-bit
+// count, sequences above).  P[S] (and E[S]) hold the totals.
+template <bool kMulti, bool kSeqs>
+__device__ __forceinline__ void chunk_prefix(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
+                                             int32_t* E) {
+    using Acc = typename std::conditional<kSeqs, long long, int>::type;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Hkv = a.num_kv_heads;
+    auto count = [](int n) -> Acc {
+        if constexpr (kSeqs) return (Acc)n + (n > 0 ? (1ll << 40) : 0ll);
+        else return n;
+    };
+    const int per = (S + kThreads - 1) / kThreads;
+    const int lo = min(S, tid * per), hi = min(S, lo + per);
+    Acc local = 0;
+    for (int s = lo; s < hi; ++s) {
+        int L = a.context_lens[s];
+        if (L < 0 || L > cap) {
+            flag_status(a.status, PA_DEV_BAD_CONTEXT);
+            L = L < 0 ? 0 : cap;
+        }
+        Lc[s] = L;
+        if constexpr (kMulti) {
+            const int n = a.q_start[s + 1] - a.q_start[s];
+            const int r0 = a.q_start[s];
+            if (n < 0 || n > L || n > a.max_q || r0 < 0 || r0 + n > a.q_rows) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+        }
+        local += count(seq_chunks<kMulti>(a, s, L));
+    }
+    // exclusive scan of `local` over the CTA
+    Acc incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Acc v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    __shared__ Acc warp_tot[kThreads / 32];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    Acc before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    Acc run = before + incl - local;
+    auto put = [&](int s, Acc v) {
+        if constexpr (kSeqs) {
+            P[s] = (int32_t)(v & ((1ll << 40) - 1)) * Hkv;
+            E[s] = (int32_t)(v >> 40) * Hkv;
+        } else {
+            P[s] = v * Hkv;
+        }
+    };
+    for (int s = lo; s < hi; ++s) {
+        put(s, run);
+        run += count(seq_chunks<kMulti>(a, s, Lc[s]));
+    }
+    if (tid == kThreads - 1) {
+        Acc tot = 0;
+        for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
+        put(S, tot);
+    }
+}
+
+// The weighted cut's prefix sums, out of line (the plain ones stay inline).
+template <bool kMulti>
+__device__ __noinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
+                                                   int32_t* E) {
+    chunk_prefix<kMulti, true>(a, S, cap, P, Lc, E);
+}
+
+template <typename T, bool kG16, int kStages, bool kMulti, bool kCut>
 __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
     using Lay = PLayout<kG16, kStages>;
@@ -606,6 +767,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
     const int S = a.num_seqs;
     int32_t* Lc = P + S + 1;                                              // [S], clamped lengths
+    int32_t* E = Lc + S;   // [S + 1] non-empty segments before each sequence (weighted cut only)
+    const bool weighted_layout = kCut && a.cut_seg > 0;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -637,49 +800,9 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         if (tid == 0) trace(a.timeline, c, kTrDeps);
     }
 
-    // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) ----
-    {
-        const int per = (S + kThreads - 1) / kThreads;
-        const int lo = min(S, tid * per), hi = min(S, lo + per);
-        int local = 0;
-        for (int s = lo; s < hi; ++s) {
-            int L = a.context_lens[s];
-            if (L < 0 || L > cap) {
-                flag_status(a.status, PA_DEV_BAD_CONTEXT);
-                L = L < 0 ? 0 : cap;
-            }
-            Lc[s] = L;
-            if constexpr (kMulti) {
-                const int n = a.q_start[s + 1] - a.q_start[s];
-                const int r0 = a.q_start[s];
-                if (n < 0 || n > L || n > a.max_q || r0 < 0 || r0 + n > a.q_rows)
-                    flag_status(a.status, PA_DEV_BAD_CONTEXT);
-            }
-            local += seq_chunks<kMulti>(a, s, L);
-        }
-        // exclusive scan of `local` over the CTA
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        __shared__ int warp_tot[kThreads / 32];
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += warp_tot[w];
-        int run = before + incl - local;
-        for (int s = lo; s < hi; ++s) {
-            P[s] = run * Hkv;
-            run += seq_chunks<kMulti>(a, s, Lc[s]);
-        }
-        if (tid == kThreads - 1) {
-            int tot = 0;
-            for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
-            P[S] = tot * Hkv;
-        }
-    }
+    // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) (and E) ----
+    if (weighted_layout) chunk_prefix_weighted<kMulti>(a, S, cap, P, Lc, E);
+    else chunk_prefix<kMulti, false>(a, S, cap, P, Lc, E);
     __syncthreads();
     if (tid == 0) trace(a.timeline, c, kTrScan);
 
@@ -692,7 +815,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         zero_empty_rows<kMulti>(a, P, c, tid, kThreads);
         return;
     }
-    const long long b_c = range_begin(c, N, C), b_e = range_begin(c + 1, N, C);
+    long long b_c, b_e;
+    {
+        const Cut cut = make_cut<kCut>(a, P, S);
+        b_c = range_begin(cut, c, S, Hkv);
+        b_e = range_begin(cut, c + 1, S, Hkv);
+    }
     if (!a.early) grid_launch_dependents();
 
     if (warp == kProducerWarp) {
@@ -855,13 +983,15 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             } else if (*abort_flag == 0) {
                 // acquired through pdone: the consumers' partial stores; the release publishes them
                 const int sigma = p0.s * Hkv + p0.h;
-                const int c_first = cta_of(Pseg, N, C), c_last = cta_of(Pseg + p0.n - 1, N, C);
+                const Cut cut = make_cut<kCut>(a, P, S);
+                const int c_first = cta_of(cut, Pseg, p0.s, p0.h), c_last = cta_of(cut, Pseg + p0.n - 1, p0.s, p0.h);
                 int last = 0;
                 if (lane == 0) last = atom_add_acq_rel_gpu(&a.seg_counters[sigma], 1) == c_last - c_first;
                 last = __shfl_sync(0xffffffffu, last, 0);
                 __syncwarp();   // the lanes' merge reads come after lane 0's acquire
                 if (last) {
-                    merge_pieces<T, kMulti>(a, span_of<kMulti>(a, p0.s, p0.L), p0.h, Pseg, p0.n, N, C, lane, 32);
+                    merge_pieces<T, kMulti>(a, span_of<kMulti>(a, p0.s, p0.L), p0.s, p0.h, Pseg, p0.n, cut, lane,
+                                            32);
                     if (lane == 0) {
                         a.seg_counters[sigma] = 0;   // ready for the next call
                         *epi_merges = 1;
@@ -1134,8 +1264,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
 
             if (seg_end) {
                 const unsigned long long tf = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
-                const bool merged = flush_segment<T, kNT, kMulti>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e, N,
-                                                     C, c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone,
+                const bool merged = flush_segment<T, kNT, kMulti, kCut>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
+                                                     c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone,
                                                      qsp);
                 if (a.timeline && tid == 0) {
                     flush_ns += global_timer_ns() - tf;
@@ -1206,10 +1336,10 @@ bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtenso
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool kG16, int kStages, bool kMulti>
+template <typename T, bool kG16, int kStages, bool kMulti, bool kCut = false>
 cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti>;
+    auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti, kCut>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1223,7 +1353,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cu
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = PLayout<kG16, kStages>::total(a.num_seqs);
+    cfg.dynamicSmemBytes = PLayout<kG16, kStages>::total(a.num_seqs, a.cut_seg > 0);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1241,11 +1371,15 @@ cudaError_t dispatch(const DecodeArgs& a, const MmaMaps& maps, int R_log2, int d
     if (dtype == PA_BF16) {
         if (g16) return deep ? launch_impl<__nv_bfloat16, true, 6, kMulti>(a, maps, R_log2, stream)
                              : launch_impl<__nv_bfloat16, true, 3, kMulti>(a, maps, R_log2, stream);
+        if constexpr (!kMulti)
+            if (!deep && a.cut_seg > 0) return launch_impl<__nv_bfloat16, false, 3, false, true>(a, maps, R_log2, stream);
         return deep ? launch_impl<__nv_bfloat16, false, 6, kMulti>(a, maps, R_log2, stream)
                     : launch_impl<__nv_bfloat16, false, 3, kMulti>(a, maps, R_log2, stream);
     }
     if (g16) return deep ? launch_impl<__half, true, 6, kMulti>(a, maps, R_log2, stream)
                          : launch_impl<__half, true, 3, kMulti>(a, maps, R_log2, stream);
+    if constexpr (!kMulti)
+        if (!deep && a.cut_seg > 0) return launch_impl<__half, false, 3, false, true>(a, maps, R_log2, stream);
     return deep ? launch_impl<__half, false, 6, kMulti>(a, maps, R_log2, stream)
                 : launch_impl<__half, false, 3, kMulti>(a, maps, R_log2, stream);
 }
@@ -1266,8 +1400,17 @@ cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t s
     const bool g16 = a.max_q * (a.num_q_heads / a.num_kv_heads) > 8;   // query rows per segment
     // as many CTAs as SMs (or fewer): one CTA per SM with the deep ring
     const bool deep = a.num_ctas <= sm_count_current();
-    if (a.q_start) return dispatch<true>(a, maps, R_log2, dtype, g16, deep, stream);
-    return dispatch<false>(a, maps, R_log2, dtype, g16, deep, stream);
+    DecodeArgs b = a;
+    // Many segments per CTA (short contexts, many kv heads): a segment's end then costs about
+    // half a chunk's share of the stream, and the cut weighs it so (measured best of 1:1, 2:1,
+    // 3:2, 3:4, 1:2, 1:3 on 256 sequences x 32 kv heads; the third prefix array fits beside two
+    // CTAs per SM up to 512 sequences).
+    // Only the one-token kernel with two CTAs per SM and at most 8 query rows is built with it.
+    const bool many_ends = a.num_seqs <= 512 && (long long)a.num_seqs * a.num_kv_heads >= 4ll * a.num_ctas;
+    b.cut_unit = 2;
+    b.cut_seg = (many_ends && !g16 && !deep && !a.q_start) ? 1 : 0;
+    if (a.q_start) return dispatch<true>(b, maps, R_log2, dtype, g16, deep, stream);
+    return dispatch<false>(b, maps, R_log2, dtype, g16, deep, stream);
 }
 
 }  // namespace pa

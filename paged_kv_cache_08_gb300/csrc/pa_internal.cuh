@@ -76,6 +76,8 @@ struct DecodeArgs {
     const void* pf_k;         // optional: pools whose blocks of this call's chunks are prefetched into L2
     const void* pf_v;
     int pf_own;               // early mode: prefetch this range's chunks beyond the ring into L2 before the wait
+    int cut_unit, cut_seg;    // persistent path: weights of a chunk and of a segment end in the cut of the
+                              // chunk list into CTA ranges (cut_seg == 0: equal chunk counts)
     const int32_t* q_start;   // several query tokens per sequence: rows q_start[s] .. q_start[s+1]-1 of q and
                               //   out (null: one query row per sequence, row s)
     int max_q;                // query tokens per sequence at most (1 without q_start)

@@ -92,6 +92,25 @@ def test_persistent_cut_segments(oracle, B, G):
         _check(oracle, wl, math="mma", num_ctas=ctas)
 
 
+@pytest.mark.parametrize("num_ctas", [153, 170, 199, 0])
+@pytest.mark.parametrize("G,B", [(1, 32), (2, 16), (4, 64)])
+def test_weighted_cut_many_short_segments(oracle, num_ctas, G, B):
+    """Many short segments per CTA: 100 sequences x 8 kv heads (empty ones among them) on grids
+    of more CTAs than SMs, so that two CTAs share an SM and at least 4 segments fall to each
+    CTA: the cut then weighs segment ends and ranges start inside segments at other places than
+    the plain cut's (the default grid of 2 CTAs per SM keeps the plain cut here).  Two calls in
+    a row check that the arrival counters reset."""
+    gen = torch.Generator().manual_seed(1000 + G * B)
+    lens = torch.randint(0, 300, (100,), generator=gen).tolist()
+    lens[3] = lens[17] = lens[99] = 0
+    lens[9] = 1000
+    lens[25] = 64
+    wl = workloads.make_workload(f"wcut_G{G}_B{B}", context_lens=lens, num_q_heads=8 * G, num_kv_heads=8,
+                                 block_size=B, seed=G + B, max_context=1024)
+    for _ in range(2):
+        _check(oracle, wl, math="mma", num_ctas=num_ctas)
+
+
 def test_unsupported_group_is_rejected():
     wl = workloads.make_workload("g5", context_lens=[5], num_q_heads=10, num_kv_heads=2, block_size=16, seed=1)
     with pytest.raises(pa.PAError):
