@@ -684,6 +684,62 @@ def run_multi_query(args, new_tokens: int = 2):
     print(json.dumps(line), flush=True)
 
 
+def run_config(args):
+    """One decode layer of another seeded configuration, timed alone: the cache write of each
+    sequence's new token plus decode attention (pa_decode_append), the L2 flushed (a 512 MB
+    write) before every timed launch, median of ``--steps`` launches by CUDA events.  Config 2
+    rotates over 4 layer caches; config 5 is served from L2 by design (its shared prefix is
+    read by all 128 sequences), so its bytes are logical ones."""
+    import paged_kv_cache_08_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfg = args.config
+    layers = 4 if cfg == 2 else 1
+    wl = workloads.config(cfg, device=dev, layers=layers, block_size=args.block_size)
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    kcs = [wl.k_cache[i].clone() for i in range(layers)]
+    vcs = [wl.v_cache[i].clone() for i in range(layers)]
+    outs = [torch.empty_like(wl.q[i]) for i in range(layers)]
+    ws = pa.new_workspace(pa.decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                   wl.block_size, wl.max_blocks_per_seq), dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def launch(i):
+        pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], kcs[i], vcs[i], bt, lens, wl.scale, wl.num_kv_heads,
+                         out=outs[i], workspace=ws)
+    for i in range(max(args.warmup, layers)):
+        launch(i % layers)
+    torch.cuda.synchronize()
+    times = []
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        for r in range(args.steps):
+            flush.zero_()
+            a.record()
+            launch(r % layers)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nbytes = decode_bytes(wl) + cache_write_bytes(wl)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    B = wl.block_size
+    line = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": f"config{cfg}_{wl.num_seqs}seq_gqa{wl.num_q_heads}x{wl.num_kv_heads}_{wl.dtype}_B{B}",
+                       "step": "one pa_decode_append launch, timed alone", "layers_rotated": layers,
+                       "l2": "flushed (512 MB write) before every timed launch",
+                       "kv_tokens_per_s": round(float(wl.context_lens.sum()) / (ms * 1e-3), 1)},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": nbytes,
+                         "kernel": "pa_decode_append", "peak_source": f"{peak_kind} copy bandwidth"},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512):
     """Chunked prefill: the last 512 tokens of 16 sequences of 4096 (their K/V already in the
     cache) attend causally over the paged cache, in the Llama-2-7B shape of the pages (32 query
@@ -818,8 +874,12 @@ def main():
                     help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
     ap.add_argument("--prefetch-own", action="store_true",
                     help="each layer prefetches its own chunks beyond the copy pipeline before its dependency wait")
-    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap", "multi_query", "prefill", "runs"], default="decode",
-                    help="decode step (default), or the block-copy, swap, several-token, prefill and slotted benchmarks")
+    ap.add_argument("--op", choices=["decode", "config", "copy_blocks", "swap", "multi_query", "prefill", "runs"],
+                    default="decode",
+                    help="decode step (default), one layer of another config (--config), or the block-copy, swap, "
+                         "several-token, prefill and slotted benchmarks")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5], help="--op config: which configuration")
+    ap.add_argument("--block-size", type=int, default=None, help="--op config: block size (config 5 sweeps it)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -831,6 +891,9 @@ def main():
         return
     if args.op == "multi_query" and args.impl == "ours":
         run_multi_query(args)
+        return
+    if args.op == "config" and args.impl == "ours":
+        run_config(args)
         return
     if args.op == "prefill" and args.impl == "ours":
         run_prefill(args)

@@ -247,8 +247,8 @@ struct Cut {
 
 // The cut as the prefix sums in shared memory define it (P[S] chunks; E follows Lc, i.e. starts
 // at P + 2 S + 1).  Rebuilt where it is needed rather than kept live through the chunk loop.
-// Kernels built without kCut always cut plainly (their code carries none of the weighted cut).
-template <bool kCut>
+// Kernels built without kManyEnds always cut plainly (their code carries none of the weighted cut).
+template <bool kManyEnds>
 __device__ __forceinline__ Cut make_cut(const DecodeArgs& a, const int32_t* P, int S) {
     Cut k;
     k.P = P;
@@ -258,7 +258,7 @@ __device__ __forceinline__ Cut make_cut(const DecodeArgs& a, const int32_t* P, i
     k.u = a.cut_unit;
     k.e = a.cut_seg;
     k.W = 0;
-    if (kCut && a.cut_seg > 0 && k.C > 0) {
+    if (kManyEnds && a.cut_seg > 0 && k.C > 0) {
         const long long W = (long long)k.u * k.N + (long long)k.e * k.E[S];
         if (W >= (long long)(k.u + k.e) * k.C) k.W = W;
     }
@@ -376,7 +376,7 @@ struct ChunkDesc {
     int s, h, t0, nblk, load_q;
     int q0, qn;   // the segment's query rows (first row, tokens), read when load_q
     int ids[4];   // physical blocks of the chunk (-1: none or outside the pool)
-    int newblk;   // physical block of token L - 1 when this chunk holds it, else -1
+    int newblk;   // physical block of token L - 1 when this chunk holds it (-2: a bad id), else -1
 };
 
 template <bool kMulti>
@@ -422,7 +422,7 @@ __device__ __forceinline__ ChunkDesc describe(const DecodeArgs& a, const int32_t
     if (t1 == p.L) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            if (e == d.nblk - 1) d.newblk = d.ids[e];
+            if (e == d.nblk - 1) d.newblk = d.ids[e] >= 0 ? d.ids[e] : -2;
     }
     return d;
 }
@@ -546,7 +546,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, const QSpan& q
 // the epilogue warp (`handoff`: every consumer thread arrives on `pdone` after its stores) or
 // finished here: count the arrival and, as the last CTA of the segment to arrive, merge all
 // pieces.  Returns true if this call merged a cut segment.
-template <typename T, int kNT, bool kMulti, bool kCut>
+template <typename T, int kNT, bool kMulti, bool kManyEnds>
 __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char* scratch, const SegPos& pos,
                                               const int32_t* P, long long b_c, long long b_e,
                                               int c, const float (&o)[kNT][8][4], const float (&m_run)[kNT][2],
@@ -652,7 +652,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
         // (the barrier that closed the loop above orders every thread's partial stores before
         // thread 0's release)
         const int sigma = pos.s * Hkv + pos.h;
-        const Cut cut = make_cut<kCut>(a, P, a.num_seqs);
+        const Cut cut = make_cut<kManyEnds>(a, P, a.num_seqs);
         const int c_first = cta_of(cut, Pseg, pos.s, pos.h), c_last = cta_of(cut, Pseg + pos.n - 1, pos.s, pos.h);
         if (tid == 0) {
             *last_flag = 0;
@@ -744,7 +744,7 @@ __device__ __noinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, i
     chunk_prefix<kMulti, true>(a, S, cap, P, Lc, E);
 }
 
-template <typename T, bool kG16, int kStages, bool kMulti, bool kCut>
+template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds>
 __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
     using Lay = PLayout<kG16, kStages>;
@@ -764,16 +764,26 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     volatile int* new_phys = reinterpret_cast<volatile int*>(base_ptr + Lay::kNewPhys);
     volatile int* stage_q0 = new_phys + 2 * kStages;   // first q row of the segment a stage starts
     volatile int* stage_qn = new_phys + 3 * kStages;   // and its query tokens
+    // One query token: s * Hkv + h of the new K/V row a deferred stage holds, or -1 (the slots of
+    // stage_q0, which only the several-token mode uses).
+    volatile int* stage_new = stage_q0;
     int32_t* P = reinterpret_cast<int32_t*>(base_ptr + Lay::kPrefix);   // [S + 1]
     const int S = a.num_seqs;
     int32_t* Lc = P + S + 1;                                              // [S], clamped lengths
     int32_t* E = Lc + S;   // [S + 1] non-empty segments before each sequence (weighted cut only)
-    const bool weighted_layout = kCut && a.cut_seg > 0;
+    const bool weighted_layout = kManyEnds && a.cut_seg > 0;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv, B = a.block_size;
     const int cap = a.max_blocks_per_seq * B;
+    // Many segment ends per CTA, one query token per sequence and a group of at most kQRows - 2
+    // heads: the producer copies a segment's new K and V rows into the last two q rows of the
+    // stage holding its last chunk, so that the consumer finds them in shared memory rather than
+    // waiting on a global load at every segment end.  (Kernels for few segment ends per CTA keep
+    // the global load: there the extra producer work measured slower on a chain of launches.)
+    const bool new_in_q = kManyEnds && !kMulti && a.k_new != nullptr && G <= Lay::kQRows - 2;
+    constexpr uint32_t kNewRowK = (uint32_t)(Lay::kQRows - 2) * kHeadDim * 2u;   // offset in the q rows
 
     if (tid == 0) {
         trace(a.timeline, c, kTrEntry);
@@ -817,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     }
     long long b_c, b_e;
     {
-        const Cut cut = make_cut<kCut>(a, P, S);
+        const Cut cut = make_cut<kManyEnds>(a, P, S);
         b_c = range_begin(cut, c, S, Hkv);
         b_e = range_begin(cut, c + 1, S, Hkv);
     }
@@ -850,9 +860,20 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                 const int n = min(issued, kStages);
                 const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
                 uint32_t bytes = 0;
-                for (int e = 0; e < n; ++e)
+                for (int e = 0; e < n; ++e) {
                     if (qdef[e] >= 0) bytes += (uint32_t)(kMulti ? stage_qn[e] : 1) * group_bytes;
+                    if (new_in_q && stage_new[e] >= 0) bytes += 4u * kHeadDim;
+                }
                 mbar_arrive_expect_tx(qbar, bytes);
+                for (int e = 0; e < n; ++e) {
+                    const int sh = new_in_q ? stage_new[e] : -1;
+                    if (sh >= 0) {
+                        const uint32_t nd = ring + (uint32_t)e * Lay::kStageBytes + kKVBytes + kNewRowK;
+                        bulk_g2s(nd, static_cast<const T*>(a.k_new) + (size_t)sh * kHeadDim, 2u * kHeadDim, qbar);
+                        bulk_g2s(nd + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)sh * kHeadDim,
+                                 2u * kHeadDim, qbar);
+                    }
+                }
                 for (int e = 0; e < n; ++e) {
                     const int sh = qdef[e];
                     if (sh >= 0) {
@@ -922,12 +943,15 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
                         if (defer_q) qdef[i] = loadq_j ? s_j * Hkv + h_j : -1;
                         new_phys[st] = append ? newblk_j : -1;
+                        const bool new_row = new_in_q && newblk_j != -1;   // this chunk holds token L - 1
+                        if (new_in_q && defer_q) stage_new[i] = new_row ? s_j * Hkv + h_j : -1;
                         if (kMulti) {
                             stage_q0[st] = q0_j;
                             stage_qn[st] = qn_j;
                         }
                         const int nq = kMulti ? qn_j : 1;
                         uint32_t bytes = (loadq_j && !defer_q) ? (uint32_t)nq * group_bytes : 0u;
+                        if (new_row && !defer_q) bytes += 4u * kHeadDim;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
@@ -951,6 +975,13 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                                     static_cast<const T*>(a.q) + ((size_t)(q0_j + r) * Hq + h_j * G) * kHeadDim;
                                 bulk_g2s(dst + kKVBytes + (uint32_t)r * group_bytes, qsrc, group_bytes, &full[st]);
                             }
+                        }
+                        if (new_row && !defer_q) {
+                            const size_t sh = (size_t)s_j * Hkv + h_j;
+                            bulk_g2s(dst + kKVBytes + kNewRowK, static_cast<const T*>(a.k_new) + sh * kHeadDim,
+                                     2u * kHeadDim, &full[st]);
+                            bulk_g2s(dst + kKVBytes + kNewRowK + 2u * kHeadDim,
+                                     static_cast<const T*>(a.v_new) + sh * kHeadDim, 2u * kHeadDim, &full[st]);
                         }
                     }
                 }
@@ -983,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
             } else if (*abort_flag == 0) {
                 // acquired through pdone: the consumers' partial stores; the release publishes them
                 const int sigma = p0.s * Hkv + p0.h;
-                const Cut cut = make_cut<kCut>(a, P, S);
+                const Cut cut = make_cut<kManyEnds>(a, P, S);
                 const int c_first = cta_of(cut, Pseg, p0.s, p0.h), c_last = cta_of(cut, Pseg + p0.n - 1, p0.s, p0.h);
                 int last = 0;
                 if (lane == 0) last = atom_add_acq_rel_gpu(&a.seg_counters[sigma], 1) == c_last - c_first;
@@ -1147,9 +1178,15 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                     // append: the new K/V row goes into the staged tile and into its cache slot
                     const int cc = lane & 15;
                     const bool isv = lane >= 16;
-                    const size_t src_off = ((size_t)pos.s * Hkv + pos.h) * kHeadDim + cc * 8;
-                    const uint4 val = *reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) +
-                                                                      src_off);
+                    uint4 val;
+                    if (new_in_q) {
+                        // staged by the producer with the chunk (or, in the first stages, with q)
+                        val = *reinterpret_cast<const uint4*>(base_ptr + (size_t)st * Lay::kStageBytes + kKVBytes +
+                                                              kNewRowK + (isv ? 2u * kHeadDim : 0u) + cc * 16);
+                    } else {
+                        const size_t src_off = ((size_t)pos.s * Hkv + pos.h) * kHeadDim + cc * 8;
+                        val = *reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) + src_off);
+                    }
                     st_shared_v4(chunk_addr(isv ? vbase : kbase, tn, cc, R_log2), val);
                     const int phys = new_phys[st];
                     if (phys >= 0) {
@@ -1264,7 +1301,7 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
 
             if (seg_end) {
                 const unsigned long long tf = (a.timeline && tid == 0) ? global_timer_ns() : 0ull;
-                const bool merged = flush_segment<T, kNT, kMulti, kCut>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
+                const bool merged = flush_segment<T, kNT, kMulti, kManyEnds>(a, base_ptr + (size_t)st * Lay::kStageBytes, pos, P, b_c, b_e,
                                                      c, o, m_run, l_run, dead, last_flag, g != b_e - 1, pdone,
                                                      qsp);
                 if (a.timeline && tid == 0) {
@@ -1336,10 +1373,10 @@ bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtenso
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool kG16, int kStages, bool kMulti, bool kCut = false>
+template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds = false>
 cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti, kCut>;
+    auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti, kManyEnds>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -66,13 +66,33 @@ def test_append_cut_segments(oracle, num_ctas, early):
 
 
 @pytest.mark.parametrize("B", [16, 32, 64, 128])
-@pytest.mark.parametrize("G,dtype", [(1, "f16"), (6, "bf16"), (8, "f16"), (16, "bf16")])
+@pytest.mark.parametrize("G,dtype", [(1, "f16"), (6, "bf16"), (8, "f16"), (12, "f16"), (16, "bf16")])
 def test_append_ragged(oracle, B, G, dtype):
     lens = [1, B - 1, B, B + 1, 63, 64, 65, 129, 300, 2 * B + 3]
     wl = workloads.make_workload(f"append_B{B}_G{G}", context_lens=lens, num_q_heads=2 * G, num_kv_heads=2,
                                  block_size=B, dtype=dtype, seed=3 * B + G, max_context=512)
     _check(oracle, wl)
     _check(oracle, wl, num_ctas=5)
+
+
+@pytest.mark.parametrize("early", [True, False])
+@pytest.mark.parametrize("num_ctas", [153, 199])
+@pytest.mark.parametrize("G,B", [(1, 32), (2, 16), (6, 64)])
+def test_append_many_segment_ends(oracle, num_ctas, early, G, B):
+    """100 sequences x 8 kv heads on grids of more CTAs than SMs: at least 4 segments per CTA,
+    so the launch takes the kernel built for many segment ends (weighted cut; each segment's
+    new K/V rows staged in shared memory with its last chunk, or with q in the first stages).
+    Two rounds check that the arrival counters reset."""
+    gen = torch.Generator().manual_seed(2000 + G * B)
+    lens = torch.randint(1, 300, (100,), generator=gen).tolist()
+    lens[3] = lens[17] = 0
+    lens[9] = 1000
+    lens[25] = 64
+    lens[26] = 65
+    wl = workloads.make_workload(f"append_ends_G{G}_B{B}", context_lens=lens, num_q_heads=8 * G, num_kv_heads=8,
+                                 block_size=B, seed=3 * G + B, max_context=1024)
+    for _ in range(2):
+        _check(oracle, wl, num_ctas=num_ctas, early_reads=early)
 
 
 def test_append_layer_chain_reads_q_after_previous_layer(oracle):
