@@ -103,10 +103,24 @@ struct PLayout {
 };
 static_assert(kConsumerWarps * 8 * kRedStride * 4 + kConsumerWarps * 8 * 8 <= kKVBytes, "merge scratch");
 
+// Tensor maps of the two pools, boxes of R = min(block_size, 64) rows.
 struct MmaMaps {
     CUtensorMap k;
     CUtensorMap v;
 };
+
+// The kernel for many segment ends per CTA also has boxes of R / 2 and R / 4 rows: a chunk's last
+// block is fetched with the lowest box that covers its valid rows.  (Other kernels keep the two
+// maps: a rarely used descriptor is a cold fetch on a CTA's critical path.)
+struct MmaMapsTails {
+    CUtensorMap k;
+    CUtensorMap v;
+    CUtensorMap k2, v2;
+    CUtensorMap k4, v4;
+};
+
+template <bool kManyEnds>
+using MapsOf = typename std::conditional<kManyEnds, MmaMapsTails, MmaMaps>::type;
 
 template <typename T>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -746,7 +760,7 @@ __device__ __noinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, i
 
 template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds>
 __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
-    decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MmaMaps maps, const int R_log2) {
+    decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MapsOf<kManyEnds> maps, const int R_log2) {
     using Lay = PLayout<kG16, kStages>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -789,6 +803,12 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
         trace(a.timeline, c, kTrEntry);
         prefetch_map(&maps.k);
         prefetch_map(&maps.v);
+        if constexpr (kManyEnds) {
+            prefetch_map(&maps.k2);
+            prefetch_map(&maps.v2);
+            prefetch_map(&maps.k4);
+            prefetch_map(&maps.v4);
+        }
 #pragma unroll
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
@@ -952,9 +972,16 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                         const int nq = kMulti ? qn_j : 1;
                         uint32_t bytes = (loadq_j && !defer_q) ? (uint32_t)nq * group_bytes : 0u;
                         if (new_row && !defer_q) bytes += 4u * kHeadDim;
+                        // box height of block e: the lowest of R, R / 2, R / 4 rows that covers its
+                        // valid rows (shift 0, 1 or 2); rows past them are never read
+                        auto box_shift = [&](int e) {
+                            if constexpr (!kManyEnds) return 0;
+                            const int rows = min(kStageTokens, Lc[s_j] - t0_j) - e * R;   // valid rows
+                            return rows <= (R >> 2) ? 2 : (rows <= (R >> 1) ? 1 : 0);
+                        };
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
+                            if (e < nblk_j && ids[e] >= 0) bytes += 4u * (uint32_t)(R >> box_shift(e)) * 128u;
                         if (i >= kStages) fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&full[st], bytes);
 #pragma unroll
@@ -962,10 +989,19 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
                             if (e < nblk_j && ids[e] >= 0) {
                                 const int row = (ids[e] * Hkv + h_j) * B + within;
                                 const uint32_t box = dst + (uint32_t)(e * 2 * R) * 128u;
-                                tma_load_2d(box, &maps.k, 0, row, &full[st]);
-                                tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &full[st]);
-                                tma_load_2d(box + kKBytes, &maps.v, 0, row, &full[st]);
-                                tma_load_2d(box + kKBytes + (uint32_t)R * 128u, &maps.v, 64, row, &full[st]);
+                                const CUtensorMap* mk = &maps.k;
+                                const CUtensorMap* mv = &maps.v;
+                                if constexpr (kManyEnds) {
+                                    const int sh = box_shift(e);
+                                    if (sh) {
+                                        mk = sh == 1 ? &maps.k2 : &maps.k4;
+                                        mv = sh == 1 ? &maps.v2 : &maps.v4;
+                                    }
+                                }
+                                tma_load_2d(box, mk, 0, row, &full[st]);
+                                tma_load_2d(box + (uint32_t)R * 128u, mk, 64, row, &full[st]);
+                                tma_load_2d(box + kKBytes, mv, 0, row, &full[st]);
+                                tma_load_2d(box + kKBytes + (uint32_t)R * 128u, mv, 64, row, &full[st]);
                             }
                         }
                         if (i == 0) trace(a.timeline, c, kTrIssue);
@@ -1374,7 +1410,10 @@ bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtenso
 }
 
 template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds = false>
-cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cudaStream_t stream) {
+cudaError_t launch_impl(const DecodeArgs& a, const MmaMapsTails& all, int R_log2, cudaStream_t stream) {
+    MapsOf<kManyEnds> maps;
+    if constexpr (kManyEnds) maps = all;
+    else maps = MmaMaps{all.k, all.v};
     static std::atomic<unsigned long long> configured{0};
     auto kernel = decode_persist_kernel<T, kG16, kStages, kMulti, kManyEnds>;
     int dev = 0;
@@ -1403,7 +1442,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const MmaMaps& maps, int R_log2, cu
 }
 
 template <bool kMulti>
-cudaError_t dispatch(const DecodeArgs& a, const MmaMaps& maps, int R_log2, int dtype, bool g16, bool deep,
+cudaError_t dispatch(const DecodeArgs& a, const MmaMapsTails& maps, int R_log2, int dtype, bool g16, bool deep,
                      cudaStream_t stream) {
     if (dtype == PA_BF16) {
         if (g16) return deep ? launch_impl<__nv_bfloat16, true, 6, kMulti>(a, maps, R_log2, stream)
@@ -1431,7 +1470,7 @@ cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t s
     while ((1 << R_log2) < R) ++R_log2;
     const unsigned long long rows = (unsigned long long)a.num_blocks * a.num_kv_heads * a.block_size;
     if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
-    MmaMaps maps;
+    MmaMapsTails maps;
     if (!encode_map(a.k_cache, rows, R, &maps.k) || !encode_map(a.v_cache, rows, R, &maps.v))
         return cudaErrorInvalidValue;
     const bool g16 = a.max_q * (a.num_q_heads / a.num_kv_heads) > 8;   // query rows per segment
@@ -1446,6 +1485,10 @@ cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t s
     const bool many_ends = a.num_seqs <= 512 && (long long)a.num_seqs * a.num_kv_heads >= 4ll * a.num_ctas;
     b.cut_unit = 2;
     b.cut_seg = (many_ends && !g16 && !deep && !a.q_start) ? 1 : 0;
+    if (b.cut_seg > 0 &&
+        (!encode_map(a.k_cache, rows, R / 2, &maps.k2) || !encode_map(a.v_cache, rows, R / 2, &maps.v2) ||
+         !encode_map(a.k_cache, rows, R / 4, &maps.k4) || !encode_map(a.v_cache, rows, R / 4, &maps.v4)))
+        return cudaErrorInvalidValue;
     if (a.q_start) return dispatch<true>(b, maps, R_log2, dtype, g16, deep, stream);
     return dispatch<false>(b, maps, R_log2, dtype, g16, deep, stream);
 }
