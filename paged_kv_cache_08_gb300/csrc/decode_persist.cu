@@ -283,9 +283,8 @@ __device__ __forceinline__ long long cut_weight(const Cut& k, long long g, int s
     return (long long)k.u * g + (long long)k.e * (k.E[s] + h);
 }
 
-// CTA of the weighted cut whose range holds the chunk of weight w (out of line: once per cut
-// segment).
-__device__ __noinline__ int cta_of_weight(const Cut& k, long long w) { return (int)div_nn(w * k.C, k.W); }
+// CTA of the weighted cut whose range holds the chunk of weight w.
+__device__ __forceinline__ int cta_of_weight(const Cut& k, long long w) { return (int)div_nn(w * k.C, k.W); }
 
 // CTA whose range holds chunk g of segment (s, h).
 __device__ __forceinline__ int cta_of(const Cut& k, long long g, int s, int h) {
@@ -301,8 +300,8 @@ __device__ __forceinline__ bool starts_range(const Cut& k, long long Pseg, int s
     return cta_of_weight(k, cut_weight(k, Pseg, s, h) - k.u - k.e) < c_first;
 }
 
-// First chunk of range c < C of the weighted cut (kept out of line: it runs once per CTA).
-__device__ __noinline__ long long range_begin_weighted(const Cut& k, int c, int S, int Hkv) {
+// First chunk of range c < C of the weighted cut.
+__device__ __forceinline__ long long range_begin_weighted(const Cut& k, int c, int S, int Hkv) {
     const long long T = div_nn((long long)c * k.W + k.C - 1, k.C);   // the range's least weight
     // the last sequence whose first chunk weighs at most T
     int lo = 0, hi = S - 1;
@@ -751,9 +750,9 @@ __device__ __forceinline__ void chunk_prefix(const DecodeArgs& a, int S, int cap
     }
 }
 
-// The weighted cut's prefix sums, out of line (the plain ones stay inline).
+// The weighted cut's prefix sums (only the kernel for many segment ends has them).
 template <bool kMulti>
-__device__ __noinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
+__device__ __forceinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
                                                    int32_t* E) {
     chunk_prefix<kMulti, true>(a, S, cap, P, Lc, E);
 }
