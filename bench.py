@@ -113,9 +113,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def profiled_traffic(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary of the kernel, if the kernel
-    source still hashes to what was profiled (else None: the counters are stale)."""
+def profiled_traffic(kernel_file: str, bench_op: str = "decode"):
+    """DRAM bytes per launch from the committed ncu summary of the kernel on this bench line's
+    workload (``bench_op``), if the kernel source still hashes to what was profiled (else None:
+    the counters are stale)."""
     import glob
     import hashlib
     src = os.path.join(ROOT, kernel_file)
@@ -129,7 +130,8 @@ def profiled_traffic(kernel_file: str):
             if ":" in line and not line.startswith((" ", "|", "#")):
                 k, _, v = line.partition(":")
                 fields[k.strip()] = v.strip()
-        if fields.get("kernel_source") == kernel_file and fields.get("source_sha256_16") == sha:
+        if (fields.get("kernel_source") == kernel_file and fields.get("source_sha256_16") == sha and
+                fields.get("bench_op", "decode") == bench_op):
             try:
                 return int(fields["traffic_bytes_per_launch"])
             except (KeyError, ValueError):
@@ -734,7 +736,10 @@ def run_config(args):
                        "l2": "flushed (512 MB write) before every timed launch",
                        "kv_tokens_per_s": round(float(wl.context_lens.sum()) / (ms * 1e-3), 1)},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": nbytes,
+                         "frac": round(gbs / peak, 4),
+                         "traffic": profiled_traffic("paged_kv_cache_08_gb300/csrc/decode_persist.cu",
+                                                     f"config{cfg}" + (f"_B{B}" if cfg == 5 else "")),
+                         "algorithmic_bytes_per_launch": nbytes,
                          "kernel": "pa_decode_append", "peak_source": f"{peak_kind} copy bandwidth"},
             "gpu_launches": args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
