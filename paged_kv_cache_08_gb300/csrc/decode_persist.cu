@@ -693,7 +693,7 @@ __device__ __forceinline__ bool flush_segment(const DecodeArgs& a, unsigned char
 // count, sequences above).  P[S] (and E[S]) hold the totals.
 template <bool kMulti, bool kSeqs>
 __device__ __forceinline__ void chunk_prefix(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
-                                             int32_t* E) {
+                                             int32_t* E, long long* bounds = nullptr) {
     using Acc = typename std::conditional<kSeqs, long long, int>::type;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hkv = a.num_kv_heads;
@@ -739,22 +739,51 @@ __device__ __forceinline__ void chunk_prefix(const DecodeArgs& a, int S, int cap
             P[s] = v * Hkv;
         }
     };
+    Acc tot = 0;
+    for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
+    // Weighted cut: the first chunks of this CTA's range and of the next (bounds[0], bounds[1];
+    // the latter only when the next range exists), each written by the one thread whose
+    // sequence holds the boundary weight (see Cut).  Nothing is written when the cut falls back
+    // to the plain one (make_cut then gives W == 0 as well).
+    long long W = 0, T[2] = {-1, -1};
+    int C = 0;
+    const int c = blockIdx.x;
+    if constexpr (kSeqs) {
+        const long long N = (tot & ((1ll << 40) - 1)) * Hkv, nseg = (tot >> 40) * Hkv;
+        C = N > 0 ? (int)min((long long)gridDim.x, N) : 0;
+        W = (long long)a.cut_unit * N + (long long)a.cut_seg * nseg;
+        if (C == 0 || c >= C || W < (long long)(a.cut_unit + a.cut_seg) * C) W = 0;
+        if (W)
+            for (int j = 0; j < 2; ++j)
+                if (c + j < C) T[j] = div_nn((long long)(c + j) * W + C - 1, C);   // the range's least weight
+    }
     for (int s = lo; s < hi; ++s) {
         put(s, run);
-        run += count(seq_chunks<kMulti>(a, s, Lc[s]));
+        const int n = seq_chunks<kMulti>(a, s, Lc[s]);
+        if constexpr (kSeqs) {
+            if (W && n > 0) {
+                const long long p0 = (run & ((1ll << 40) - 1)) * Hkv, e0 = (run >> 40) * Hkv;
+                const long long w0 = (long long)a.cut_unit * p0 + (long long)a.cut_seg * e0;
+                const long long span = (long long)a.cut_unit * n + a.cut_seg;   // one segment
+                for (int j = 0; j < 2; ++j) {
+                    const long long off = T[j] - w0;
+                    if (T[j] < 0 || off < 0 || off >= span * Hkv) continue;
+                    const long long h = div_nn(off, span);
+                    const long long kk = div_nn(off - h * span + a.cut_unit - 1, a.cut_unit);
+                    bounds[j] = kk >= n ? p0 + (h + 1) * n : p0 + h * n + kk;
+                }
+            }
+        }
+        run += count(n);
     }
-    if (tid == kThreads - 1) {
-        Acc tot = 0;
-        for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
-        put(S, tot);
-    }
+    if (tid == kThreads - 1) put(S, tot);
 }
 
 // The weighted cut's prefix sums (only the kernel for many segment ends has them).
 template <bool kMulti>
 __device__ __forceinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S, int cap, int32_t* P, int32_t* Lc,
-                                                   int32_t* E) {
-    chunk_prefix<kMulti, true>(a, S, cap, P, Lc, E);
+                                                   int32_t* E, long long* bounds) {
+    chunk_prefix<kMulti, true>(a, S, cap, P, Lc, E, bounds);
 }
 
 template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds>
@@ -830,7 +859,8 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     }
 
     // ---- prefix sums of chunk counts: P[s] = Hkv * sum_{s' < s} ceil(L_s' / 64) (and E) ----
-    if (weighted_layout) chunk_prefix_weighted<kMulti>(a, S, cap, P, Lc, E);
+    __shared__ long long cut_bounds[2];   // weighted cut: this range's first chunk and the next's
+    if (weighted_layout) chunk_prefix_weighted<kMulti>(a, S, cap, P, Lc, E, cut_bounds);
     else chunk_prefix<kMulti, false>(a, S, cap, P, Lc, E);
     __syncthreads();
     if (tid == 0) trace(a.timeline, c, kTrScan);
@@ -847,8 +877,14 @@ __global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
     long long b_c, b_e;
     {
         const Cut cut = make_cut<kManyEnds>(a, P, S);
-        b_c = range_begin(cut, c, S, Hkv);
-        b_e = range_begin(cut, c + 1, S, Hkv);
+        if (weighted_layout && cut.W) {
+            // found with the prefix sums (the cut range_begin would search for)
+            b_c = cut_bounds[0];
+            b_e = c + 1 < C ? cut_bounds[1] : N;
+        } else {
+            b_c = range_begin(cut, c, S, Hkv);
+            b_e = range_begin(cut, c + 1, S, Hkv);
+        }
     }
     if (!a.early) grid_launch_dependents();
 
