@@ -689,7 +689,8 @@ def run_multi_query(args, new_tokens: int = 2):
 def run_config(args):
     """One decode layer of another seeded configuration, timed alone: the cache write of each
     sequence's new token plus decode attention (pa_decode_append), the L2 flushed (a 512 MB
-    write) before every timed launch, median of ``--steps`` launches by CUDA events.  Config 2
+    write) before every timed launch, mean of ``--steps`` launches by CUDA events (each event
+    pair resolves about 2 us; the mean of many resolves finer).  Config 2
     rotates over 4 layer caches; config 5 is served from L2 by design (its shared prefix is
     read by all 128 sequences), so its bytes are logical ones."""
     import paged_kv_cache_08_gb300 as pa
@@ -723,7 +724,7 @@ def run_config(args):
             b.record()
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
+    ms = statistics.fmean(times)
     nbytes = decode_bytes(wl) + cache_write_bytes(wl)
     gbs = nbytes / (ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak_gbs()
@@ -732,7 +733,8 @@ def run_config(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": f"config{cfg}_{wl.num_seqs}seq_gqa{wl.num_q_heads}x{wl.num_kv_heads}_{wl.dtype}_B{B}",
-                       "step": "one pa_decode_append launch, timed alone", "layers_rotated": layers,
+                       "step": "one pa_decode_append launch, timed alone (mean)", "layers_rotated": layers,
+                       "median_ms": round(statistics.median(times), 5),
                        "l2": "flushed (512 MB write) before every timed launch",
                        "kv_tokens_per_s": round(float(wl.context_lens.sum()) / (ms * 1e-3), 1)},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
