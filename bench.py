@@ -152,6 +152,24 @@ def measured_peak_gbs():
 # our arm
 # ------------------------------------------------------------------------------------------
 
+def _pack(tensors, device):
+    """One contiguous device buffer holding copies of ``tensors`` (each at a 256-byte aligned
+    offset) and views of it with their shapes and dtypes, so that a step's inputs (or outputs)
+    cross the host link as one copy."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(n, dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(tensors, offs):
+        nb = t.numel() * t.element_size()
+        v = buf[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class Step:
     """All device buffers of one bench step plus the captured CUDA graph.
 
@@ -169,11 +187,16 @@ class Step:
         self.wl = wl
         self.dev = device
         L = wl.layers
-        self.bt = wl.block_tables.to(device)
-        self.lens = wl.context_lens.to(device)
-        slots = pa.build_slot_mapping(wl.block_tables, wl.context_lens, wl.block_size)
-        self.slots = torch.from_numpy(slots).to(device)
-        self.out = [torch.empty_like(wl.q[i]) for i in range(L)]
+        slots = torch.from_numpy(pa.build_slot_mapping(wl.block_tables, wl.context_lens, wl.block_size))
+        # every per-step input (queries, new K/V rows, tables, lengths, slots) in one buffer and
+        # the outputs in another: the end-to-end pass moves each across the host link in one copy
+        self.inbuf, views = _pack(list(wl.q) + list(wl.k_new) + list(wl.v_new) +
+                                  [wl.block_tables, wl.context_lens, slots], device)
+        wl.q = views[:L]
+        wl.k_new = views[L:2 * L]
+        wl.v_new = views[2 * L:3 * L]
+        self.bt, self.lens, self.slots = views[3 * L:]
+        self.outbuf, self.out = _pack([torch.zeros_like(wl.q[i]) for i in range(L)], device)
         S, Hq, D = wl.q[0].shape
         ws = pa.decode_workspace_size(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq,
                                       num_ctas=num_ctas)
@@ -368,32 +391,17 @@ def run_ours(args):
 
 def run_e2e(st, wl, args, step_bytes):
     """Same step through the public API with inputs in pinned host memory: every step
-    copies q, the new K/V rows, the tables, lengths and slots to the device, runs the
-    24 layers and copies the outputs back."""
-    dev = st.dev
-    host_in = {
-        "q": [t.cpu().pin_memory() for t in wl.q],
-        "k": [t.cpu().pin_memory() for t in wl.k_new],
-        "v": [t.cpu().pin_memory() for t in wl.v_new],
-        "bt": wl.block_tables.pin_memory(), "lens": wl.context_lens.pin_memory(),
-        "slots": st.slots.cpu().pin_memory(),
-    }
-    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in st.out]
-    h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host_in[k])
-    h2d += sum(host_in[k].numel() * host_in[k].element_size() for k in ("bt", "lens", "slots"))
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    copies q, the new K/V rows, the tables, lengths and slots to the device (one copy of the
+    packed input buffer), runs the 24 layers and copies the outputs back (one copy)."""
+    host_in = st.inbuf.cpu().pin_memory()
+    host_out = torch.empty(st.outbuf.shape, dtype=st.outbuf.dtype).pin_memory()
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
 
     def one():
-        for i in range(wl.layers):
-            wl.q[i].copy_(host_in["q"][i], non_blocking=True)
-            wl.k_new[i].copy_(host_in["k"][i], non_blocking=True)
-            wl.v_new[i].copy_(host_in["v"][i], non_blocking=True)
-        st.bt.copy_(host_in["bt"], non_blocking=True)
-        st.lens.copy_(host_in["lens"], non_blocking=True)
-        st.slots.copy_(host_in["slots"], non_blocking=True)
+        st.inbuf.copy_(host_in, non_blocking=True)
         st.replay()
-        for i in range(wl.layers):
-            host_out[i].copy_(st.out[i], non_blocking=True)
+        host_out.copy_(st.outbuf, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         one()
