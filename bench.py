@@ -811,8 +811,11 @@ def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512
     bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
     out = torch.empty_like(q)
 
+    tiles = args.prefill_tiles
+
     def call(_):
-        pa.multi_query(q, wl.k_cache[0], wl.v_cache[0], bt, lens, qs, wl.scale, wl.num_kv_heads, max_q, out=out)
+        pa.multi_query(q, wl.k_cache[0], wl.v_cache[0], bt, lens, qs, wl.scale, wl.num_kv_heads, max_q, out=out,
+                       tiles=tiles)
     with ClockSampler(0) as clk:
         ms = _event_ms(call, args.steps, args.warmup)
     pairs = seqs * wl.num_q_heads * sum(context - new_tokens + i + 1 for i in range(new_tokens))
@@ -827,10 +830,11 @@ def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512
             "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": f"prefill_{seqs}seq_ctx{context}_new{new_tokens}_mha32_f16_B32",
-                       "l2": "1 GiB of K/V, above L2"},
+                       "l2": "1 GiB of K/V, above L2", "tiles": tiles},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tflops / peak, 4), "traffic": None, "flops_per_launch": flops,
-                         "kernel": "prefill_mma_kernel (mma.sync m16n8k16)", "peak_source": kind},
+                         "kernel": ("prefill_tc_kernel (tcgen05.mma, accumulators in tensor memory)" if tiles == "tc"
+                                    else "prefill_mma_kernel (mma.sync m16n8k16)"), "peak_source": kind},
             "gpu_launches": args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
@@ -935,6 +939,8 @@ def main():
                     default="decode",
                     help="decode step (default), one layer of another config (--config), or the block-copy, swap, "
                          "several-token, prefill and slotted benchmarks")
+    ap.add_argument("--prefill-tiles", choices=["tc", "mma"], default="tc",
+                    help="--op prefill: tcgen05 tiles of 128 rows or mma.sync tiles of 64 rows")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5], help="--op config: which configuration")
     ap.add_argument("--block-size", type=int, default=None, help="--op config: block size (config 5 sweeps it)")
     args = ap.parse_args()

@@ -214,6 +214,9 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
 /* pa_decode_append with early reads: before waiting for the preceding kernel, each CTA also
  * asks the L2 to prefetch the blocks of its chunks that do not fit its copy pipeline. */
 #define PA_DECODE_PREFETCH_OWN 2
+/* pa_multi_query beyond 16 query rows per (sequence, kv head): the mma.sync tiles of 64 rows
+ * instead of the default tcgen05 tiles of 128 rows (same results within the parity tolerance). */
+#define PA_PREFILL_MMA_SYNC 4
 
 /* ------------------------------------------------------------------------------------
  * pa_decode_append  [P4 §三 sequence diagram + §五.1; P1 address formula]
@@ -256,9 +259,10 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  * PA_DEV_BAD_CONTEXT.
  * Kernels: while max_q_per_seq x (num_q_heads / num_kv_heads) <= 16 (and num_seqs <= 1024)
  * the persistent kernel, with a workspace as for pa_decode (same size query, persistent kind;
- * opts: num_ctas, timeline and the next-layer prefetch apply); beyond that, tensor-core tiles
- * of 64 query rows per (sequence, kv head), one CTA each, no workspace (chunked prefill; at
- * most 65535 sequences and kv heads).
+ * opts: num_ctas, timeline and the next-layer prefetch apply); beyond that, tcgen05 tiles of
+ * 128 query rows per (sequence, kv head) with accumulators in tensor memory, one CTA each, no
+ * workspace (chunked prefill; at most 65535 sequences and kv heads); opts->flags with
+ * PA_PREFILL_MMA_SYNC selects mma.sync tiles of 64 rows instead.
  * Returns the codes of pa_decode.
  * ---------------------------------------------------------------------------------- */
 int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_cache,

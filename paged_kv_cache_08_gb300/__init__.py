@@ -253,14 +253,15 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                 max_q: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
                 k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
-                early_reads: bool = True, prefetch=None, prefetch_own: bool = False,
+                early_reads: bool = True, prefetch=None, prefetch_own: bool = False, tiles: str = "tc",
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Several new query tokens per sequence attending causally over the paged cache.
     q: [T, Hq, D]; sequence s owns rows query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its
     newest tokens; at most ``max_q`` per sequence.  See pa_multi_query in include/pa.h.
     With k_new / v_new ([T, Hkv, D], rows as q's) the same launch first writes them into the
     slots of their positions (pa_multi_query_append; early reads, prefetch and prefetch_own as
-    for decode_append)."""
+    for decode_append).  ``tiles``: beyond 16 query rows per (sequence, kv head), "tc" runs the
+    tcgen05 tiles of 128 rows, "mma" the mma.sync tiles of 64 rows."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -292,7 +293,10 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
         flags = (0 if early_reads else _native.NO_EARLY_READS) | (_native.PREFETCH_OWN if prefetch_own else 0)
         o = _opts(0, "mma", num_ctas, timeline, flags, prefetch=prefetch, like=k_cache)
     else:
-        o = _opts(0, "mma", num_ctas, timeline, prefetch=prefetch, like=k_cache)
+        if tiles not in ("tc", "mma"):
+            raise ValueError('tiles must be "tc" or "mma"')
+        o = _opts(0, "mma", num_ctas, timeline, _native.PREFILL_MMA_SYNC if tiles == "mma" else 0,
+                  prefetch=prefetch, like=k_cache)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         workspace = _workspace(q.device, need, 2, int(num_ctas))

@@ -34,6 +34,7 @@ DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x
 MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 NO_EARLY_READS = 1
 PREFETCH_OWN = 2
+PREFILL_MMA_SYNC = 4
 
 _SIGNATURES = {
     "pa_cache_write": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp]),

@@ -21,7 +21,7 @@ BUILD = PKG / "_build"
 LIB = BUILD / "libpa.so"
 
 CUDA_SOURCES = ["api.cu", "cache_write.cu", "copy_blocks.cu", "decode_fma.cu", "decode_mma.cu", "decode_persist.cu", "decode_static.cu",
-                "prefill_mma.cu"]
+                "prefill_mma.cu", "prefill_tc.cu"]
 CXX_SOURCES = ["pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -476,7 +476,8 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     if (rc != PA_OK) return rc;
     if (multi) {
         // several query tokens per sequence: the persistent kernel while a (sequence, kv head)
-        // has at most 16 query rows, else tiles of 64 rows (no workspace)
+        // has at most 16 query rows, else tcgen05 tiles of 128 rows (or mma.sync tiles of 64 rows
+        // on request), no workspace
         if (max_q < 1 || !aligned4(q_start)) return PA_ERR_INVALID_ARG;
         if ((long long)max_q * group > kPieceRows) {
             if (append) return PA_ERR_UNSUPPORTED;   // the tiles kernel writes no cache rows
@@ -500,7 +501,9 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
             a.q_start = q_start;
             a.max_q = max_q;
             a.q_rows = q_rows;
-            const cudaError_t pe = launch_prefill_mma(a, dtype, static_cast<cudaStream_t>(stream));
+            const bool mma_sync_tiles = opts && (opts->flags & PA_PREFILL_MMA_SYNC);
+            const cudaError_t pe = mma_sync_tiles ? launch_prefill_mma(a, dtype, static_cast<cudaStream_t>(stream))
+                                                  : launch_prefill_tc(a, dtype, static_cast<cudaStream_t>(stream));
             if (pe != cudaSuccess) {
                 cudaGetLastError();
                 return PA_ERR_CUDA;

@@ -291,6 +291,8 @@ int persist_ctas_per_sm(int group);
 
 // Several query tokens per sequence, any number: tiles of 64 query rows (prefill_mma.cu).
 cudaError_t launch_prefill_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
+// Several query tokens per sequence beyond 16 rows on tcgen05 tiles of 128 rows.
+cudaError_t launch_prefill_tc(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
 // Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.
 cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);

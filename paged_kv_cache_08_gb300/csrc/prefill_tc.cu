@@ -1,0 +1,587 @@
+// Several new query tokens per sequence on the fifth-generation tensor cores: tcgen05.mma with
+// operands in shared memory and accumulators in tensor memory, tiles of 128 query rows.
+//
+// What it computes (the same as the persistent kernel's several-token mode and the mma.sync
+// tiles): sequence s owns query rows q_start[s] .. q_start[s+1]-1, its n newest tokens, the last
+// n of its L cached ones; token i sits at position L - n + i and attends causally over positions
+// 0 .. L - n + i ("显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §五.1: walk the
+// logical blocks through block_tables, q.k, running-max softmax, weight V, normalise; the
+// chunked prefill of its closing section).
+//
+// One CTA per (128-row tile, kv head, sequence); rows r = i * G + g (new token i, group member g).
+//   warps 0-3  softmax: thread t owns row t of the tile (tensor-memory lane t)
+//   warp 4     producer: TMA copies of 64-token K and V stages into a 3-deep ring
+//   warp 5     MMA: allocates tensor memory; one thread issues
+//                S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
+//                O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major, V N-major)
+//              with S double-buffered in tensor memory, so S_{j+1} runs under the softmax of S_j.
+// The softmax keeps a lazy exponent base per row (moved to the running max only when a score
+// exceeds it by more than 2^8, then O is rescaled in tensor memory), writes P = exp2(s - base)
+// to shared memory in the operand layout (bf16: a high and a low part, two MMAs), and at the end
+// normalises its O row.  Every wait is bounded; tensor memory is freed on every path.
+#include "pa_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <type_traits>
+
+namespace pa {
+
+namespace {
+
+constexpr int kTRows = 128;                                  // query rows per tile: the MMA's M
+constexpr int kSoftWarps = 4;                                // one row per thread
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kTThreads = 6 * 32;
+constexpr int kTStages = 3;
+constexpr uint32_t kQHalf = kTRows * 128;                    // 16 KB: 128 rows x 64 dims
+constexpr uint32_t kKVHalf = kStageTokens * 128;             // 8 KB: 64 tokens x 64 dims
+constexpr uint32_t kKBytes = 2 * kKVHalf;                    // 16 KB of K per stage (V the same)
+constexpr uint32_t kStage = 2 * kKBytes;
+constexpr uint32_t kPBytes = kTRows * kStageTokens * 2;      // 16 KB: 128 rows x 64 tokens
+constexpr uint32_t kOffQ = 0;                                // [2 halves][128 rows][128 B]
+constexpr uint32_t kOffRing = 2 * kQHalf;                    // [stage][K, V][2 halves][64 tokens][128 B]
+constexpr uint32_t kOffP = kOffRing + kTStages * kStage;     // [2 buffers][high, low][128 rows][128 B]
+constexpr uint32_t kOffBar = kOffP + 4 * kPBytes;
+constexpr int kNumBars = 16;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // tensor-memory address, abort flag, issued count
+constexpr size_t kSmemTc = 1024 /*alignment slack*/ + kOffMisc + 16;
+constexpr uint32_t kTmemCols = 256;                          // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kColO = 128;
+constexpr float kLazyLog2 = 8.f;                             // exponent-base slack (weights below 2^8)
+
+struct TcMaps {
+    CUtensorMap k;
+    CUtensorMap v;
+};
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, swizzle mode 2 (128 bytes).
+// K-major tiles (rows of 64 16-bit elements): stride 1024 between groups of 8 rows, leading
+// offset unused.  N-major tiles (V: rows of 64 dims per token): leading offset = the distance
+// between the two 64-dim halves, stride 1024 between groups of 8 tokens.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both f16 or both bf16, A
+// K-major, B K-major or N-major, M = 128, N = n.
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc(int n, bool b_n_major) {
+    return (1u << 4) | ((std::is_same<T, __nv_bfloat16>::value ? 1u : 0u) << 7) |
+           ((std::is_same<T, __nv_bfloat16>::value ? 1u : 0u) << 10) | ((b_n_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t id,
+                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread has issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Copies of one stage: the blocks holding tokens [base, min(base + 64, tok_end)), K and V,
+// each 64-dim half of a block to [half][token] of the stage (tokens contiguous per half).
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const TcMaps& maps, const int32_t* table_row,
+                                            int hk, int base, int tok_end, uint32_t kdst, uint64_t* bar,
+                                            int R_log2) {
+    const int B = a.block_size;
+    const int R = 1 << R_log2;
+    const int first = base / B;
+    const int last = (min(base + kStageTokens, tok_end) - 1) / B;
+    const int within = (B > kStageTokens) ? (base % B) : 0;
+    int phys[4];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        phys[j] = -1;
+        if (first + j <= last) {
+            const int p = table_row[first + j];
+            if (p >= 0 && p < a.num_blocks) {
+                phys[j] = p;
+                bytes += 4u * (uint32_t)R * 128u;   // K and V, two 64-dim halves
+            } else {
+                flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            }
+        }
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (phys[j] >= 0) {
+            const int row = (phys[j] * a.num_kv_heads + hk) * B + within;
+            const uint32_t off = (uint32_t)(j * R) * 128u;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tma_load_2d(kdst + h * kKVHalf + off, &maps.k, 64 * h, row, bar);
+                tma_load_2d(kdst + kKBytes + h * kKVHalf + off, &maps.v, 64 * h, row, bar);
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTThreads, 1)
+    prefill_tc_kernel(const DecodeArgs a, const __grid_constant__ TcMaps maps, const int R_log2) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 1024-aligned for the swizzle
+    unsigned char* bp = smem_raw + (base - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kOffBar);
+    uint64_t* kv_full = bars;           // [3] a stage's K and V landed
+    uint64_t* kv_empty = bars + 3;      // [3] the MMAs reading a stage are done
+    uint64_t* s_full = bars + 6;        // [2] S_j is in tensor memory
+    uint64_t* p_full = bars + 8;        // [2] P_j is in shared memory (128 arrivals)
+    uint64_t* pv_done = bars + 10;      // [2] O += P_j V_j is complete
+    uint64_t* q_ready = bars + 12;      // the Q tile is in shared memory (128 arrivals)
+    uint64_t* drain = bars + 13;        // every MMA issued is complete
+    volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + kOffMisc + 4);
+    volatile int* issued_count = abort_flag + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int cap = a.max_blocks_per_seq * a.block_size;
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+
+    grid_dependency_wait();
+    int L = a.context_lens[s];
+    if (L < 0 || L > cap) {
+        if (tid == 0 && tile == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+        L = L < 0 ? 0 : cap;
+    }
+    if (tid == 0 && tile == 0 && hk == 0) {
+        const int n_raw = a.q_start[s + 1] - a.q_start[s];
+        const int r0_raw = a.q_start[s];
+        if (n_raw < 0 || n_raw > L || n_raw > a.max_q || r0_raw < 0 || r0_raw + n_raw > a.q_rows)
+            flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    }
+    const QSpan qs = q_span(a, s, L);
+    const int rows = qs.n * G;
+    const int r0 = tile * kTRows;
+    if (r0 >= rows) return;   // uniform for the CTA, before any tensor memory is held
+    const int r_last = min(r0 + kTRows, rows) - 1;
+    const int t_end = L - qs.n + r_last / G + 1;   // tokens the tile needs: up to its last row's position
+    const int nst = (t_end + kStageTokens - 1) / kStageTokens;
+
+    if (tid == 0) {
+        prefetch_map(&maps.k);
+        prefetch_map(&maps.v);
+        for (int i = 0; i < kTStages; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], kSoftWarps * 32);
+            mbar_init(&pv_done[b], 1);
+        }
+        mbar_init(q_ready, kSoftWarps * 32);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *issued_count = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(
+                         const_cast<uint32_t*>(tslot))),
+                     "n"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    grid_launch_dependents();
+
+    auto give_up = [&]() {
+        flag_status(a.status, PA_DEV_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == kProdWarp) {
+        // ---------------- producer: one lane keeps the ring full ----------------
+        if (lane == 0) {
+            const int32_t* table_row = a.block_tables + (size_t)s * a.max_blocks_per_seq;
+            int i = 0;
+            for (; i < nst; ++i) {
+                const int st = i % kTStages;
+                if (i >= kTStages && !mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kTStages) - 1) & 1u)) {
+                    give_up();
+                    break;
+                }
+                if (*abort_flag) break;
+                issue_stage(a, maps, table_row, hk, i * kStageTokens, t_end, base + kOffRing + (uint32_t)st * kStage,
+                            &kv_full[st], R_log2);
+            }
+            *issued_count = i;
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue: one thread ----------------
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc<T>(kStageTokens, false);
+            constexpr uint32_t kIdPV = idesc<T>(kHeadDim, true);
+            bool ok = mbar_wait_bounded(q_ready, 0u);
+            if (!ok) give_up();
+            tc_fence_after();
+            // S_j = Q K_j^T into S buffer j % 2: two 64-dim halves x four 16-dim steps
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kTStages;
+                if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(j & 1) * kStageTokens;
+                const uint32_t kst = base + kOffRing + (uint32_t)st * kStage;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(d, sdesc(base + kOffQ + h * kQHalf + kk * 32, 16, 1024),
+                             sdesc(kst + h * kKVHalf + kk * 32, 16, 1024), kIdS, (h | kk) != 0 ? 1u : 0u);
+                umma_commit(&s_full[j & 1]);
+                return true;
+            };
+            if (ok && !*abort_flag) ok = issue_s(0);
+            for (int j = 0; j < nst && ok; ++j) {
+                if (*abort_flag) break;
+                if (j + 1 < nst && !issue_s(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait_bounded(&p_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // O += P_j V_j: four 16-token steps (and the low part of P for bf16)
+                const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
+                const uint32_t pb = base + kOffP + (uint32_t)(j & 1) * 2u * kPBytes;
+#pragma unroll
+                for (int kt = 0; kt < 4; ++kt) {
+                    const uint64_t vd = sdesc(vst + kt * 2048, kKVHalf, 1024);
+                    umma(tmem + kColO, sdesc(pb + kt * 32, 16, 1024), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
+                    if (kSplitP) umma(tmem + kColO, sdesc(pb + kPBytes + kt * 32, 16, 1024), vd, kIdPV, 1u);
+                }
+                umma_commit(&pv_done[j & 1]);
+                umma_commit(&kv_empty[j % kTStages]);
+            }
+            if (!ok) give_up();
+            // nothing of this CTA's may still run on the tensor cores when it frees its memory
+            umma_commit(drain);
+            (void)mbar_wait_bounded(drain, 0u);
+        }
+    } else {
+        // ---------------- softmax: thread tid owns row r0 + tid (tensor-memory lane tid) ----------------
+        const int r = r0 + tid;
+        const bool row_ok = r < rows;
+        const int lim = row_ok ? L - qs.n + r / G : -1;   // newest position the row attends to
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t sw = (uint32_t)(tid & 7);          // 128-byte swizzle phase of this row
+        // Q row into the K-major operand tile (two 64-dim halves); rows past the segment are zero
+        {
+            const uint4* src = row_ok ? reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
+                                                                      q_offset(a, qs, hk, G, r))
+                                      : nullptr;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(base + kOffQ + h * kQHalf + tid * 128 + ((c ^ sw) << 4),
+                                 row_ok ? src[h * 8 + c] : make_uint4(0, 0, 0, 0));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+
+        // waits and give-ups are decided per warp: the tensor-memory accesses are warp-wide
+        auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+        };
+        float m_run = -INFINITY, l_run = 0.f;
+        bool dead = false;
+        for (int j = 0; j < nst && !dead; ++j) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&s_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
+                dead = true;
+                break;
+            }
+            tc_fence_after();
+            float x[64];
+            {
+                float v[32];
+                tmem_ld32(lane_addr + (uint32_t)(j & 1) * kStageTokens, v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = v[c];
+                tmem_ld32(lane_addr + (uint32_t)(j & 1) * kStageTokens + 32, v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
+            }
+            const int t0 = j * kStageTokens;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                x[c] = (t0 + c <= lim) ? x[c] * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            if (j == nst - 1) {
+                // the last stage: V rows from t_end on are masked, but they can hold pool slots past
+                // the context or stale data; zero them so that P = 0 never meets a non-finite V
+                const int nvalid = t_end - t0;
+                const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
+                for (int idx = tid; idx < (kStageTokens - nvalid) * 16; idx += kSoftWarps * 32) {
+                    const int t = nvalid + (idx >> 4);
+                    st_shared_v4(vst + ((idx >> 3) & 1) * kKVHalf + t * 128 + (idx & 7) * 16, make_uint4(0, 0, 0, 0));
+                }
+            }
+            // Exponent base: moved to the running max only when a score passes it by more than
+            // kLazyLog2; O (which then holds stages 0 .. j-1) is rescaled in tensor memory.
+            const bool move = mx > m_run + kLazyLog2;
+            if (__any_sync(0xffffffffu, move && j > 0 && m_run != -INFINITY)) {
+                // some row of the warp rescales O, which holds stages 0 .. j-1: wait (warp-wide) for
+                // O += P_{j-1} V_{j-1}; tensor-memory accesses are warp-wide, so every lane scales
+                // its O row (by 1 where the base stays)
+                if (!warp_wait(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
+                    dead = true;
+                    break;
+                }
+                tc_fence_after();
+                const float alpha = (move && j > 0 && m_run != -INFINITY) ? exp2f(m_run - mx) : 1.f;
+#pragma unroll
+                for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(lane_addr + kColO + c0, o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                    tmem_st32(lane_addr + kColO + c0, o);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                l_run *= alpha;
+            }
+            if (move) m_run = mx;
+            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+            // P buffer j % 2 was last read by O += P_{j-2} V_{j-2}
+            if (j >= 2 && !warp_wait(&pv_done[j & 1], (uint32_t)((j - 2) >> 1) & 1u)) {
+                dead = true;
+                break;
+            }
+            const uint32_t pb = base + kOffP + (uint32_t)(j & 1) * 2u * kPBytes + (uint32_t)tid * 128u;
+            float rs = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    p[e] = exp2f(x[c8 * 8 + e] - m_use);
+                    rs += p[e];
+                }
+                uint4 hi;
+                hi.x = Elem<T>::pack2(p[0], p[1]);
+                hi.y = Elem<T>::pack2(p[2], p[3]);
+                hi.z = Elem<T>::pack2(p[4], p[5]);
+                hi.w = Elem<T>::pack2(p[6], p[7]);
+                st_shared_v4(pb + (((uint32_t)c8 ^ sw) << 4), hi);
+                if (kSplitP) {
+                    const float2 h0 = Elem<T>::to_float2(hi.x), h1 = Elem<T>::to_float2(hi.y);
+                    const float2 h2 = Elem<T>::to_float2(hi.z), h3 = Elem<T>::to_float2(hi.w);
+                    uint4 lo;
+                    lo.x = Elem<T>::pack2(p[0] - h0.x, p[1] - h0.y);
+                    lo.y = Elem<T>::pack2(p[2] - h1.x, p[3] - h1.y);
+                    lo.z = Elem<T>::pack2(p[4] - h2.x, p[5] - h2.y);
+                    lo.w = Elem<T>::pack2(p[6] - h3.x, p[7] - h3.y);
+                    st_shared_v4(pb + kPBytes + (((uint32_t)c8 ^ sw) << 4), lo);
+                }
+            }
+            l_run += rs;
+            fence_proxy_async_smem();   // P (and the zeroed V rows) are read by the tensor cores
+            tc_fence_before();
+            mbar_arrive(&p_full[j & 1]);
+        }
+        // ---- normalise and write the row ----
+        if (!dead && warp_wait(&pv_done[(nst - 1) & 1], (uint32_t)((nst - 1) >> 1) & 1u)) {
+            tc_fence_after();
+            const float inv = 1.f / l_run;
+            uint4* dst = row_ok ? reinterpret_cast<uint4*>(static_cast<T*>(a.out) + q_offset(a, qs, hk, G, r))
+                                : nullptr;
+#pragma unroll
+            for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                float o[32];
+                tmem_ld32(lane_addr + kColO + c0, o);
+                if (row_ok) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 u;
+                        u.x = Elem<T>::pack2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                        u.y = Elem<T>::pack2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                        u.z = Elem<T>::pack2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                        u.w = Elem<T>::pack2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+                        dst[c0 / 8 + q4] = u;
+                    }
+                }
+            }
+        } else {
+            give_up();
+        }
+    }
+
+    // ---- teardown: nothing in flight on the tensor cores or the copy engine, then free ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && tid == 0) {
+        // let every copy still in flight land before the CTA's shared memory is released
+        const int n = *issued_count;
+        for (int st = 0; st < kTStages; ++st) {
+            int last = -1;
+            for (int i = st; i < n; i += kTStages) last = i;
+            if (last >= 0) (void)mbar_wait_bounded(&kv_full[st], (uint32_t)(last / kTStages) & 1u);
+        }
+    }
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::atomic<int> state{0};
+    if (state.load() == 0) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+        state.store(1);
+    }
+    return fn;
+}
+
+// A pool as [rows][128] 16-bit elements, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool tc_encode_map(const void* base, unsigned long long rows, int box_rows, CUtensorMap* out) {
+    auto fn = tc_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaStream_t stream) {
+    static std::atomic<unsigned long long> configured{0};
+    auto kernel = prefill_tc_kernel<T>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const long long tiles = ((long long)a.max_q * G + kTRows - 1) / kTRows;
+    if (tiles > 0x7fffffffLL || a.num_kv_heads > 65535 || a.num_seqs > 65535) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, a.num_kv_heads, a.num_seqs);
+    cfg.blockDim = dim3(kTThreads);
+    cfg.dynamicSmemBytes = kSmemTc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a, maps, R_log2);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const DecodeArgs& a, int dtype, cudaStream_t stream) {
+    static_assert(kSmemTc <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
+    const int R = a.block_size < kStageTokens ? a.block_size : kStageTokens;
+    int R_log2 = 0;
+    while ((1 << R_log2) < R) ++R_log2;
+    const unsigned long long rows = (unsigned long long)a.num_blocks * a.num_kv_heads * a.block_size;
+    if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
+    TcMaps maps;
+    if (!tc_encode_map(a.k_cache, rows, R, &maps.k) || !tc_encode_map(a.v_cache, rows, R, &maps.v))
+        return cudaErrorInvalidValue;
+    return dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, maps, R_log2, stream)
+                            : launch_tc<__half>(a, maps, R_log2, stream);
+}
+
+}  // namespace pa

@@ -19,11 +19,12 @@ def _clean_status():
     yield
 
 
-def _run(oracle, wl, new_tokens, seed, num_ctas=0, check_status=True):
+def _run(oracle, wl, new_tokens, seed, num_ctas=0, check_status=True, tiles="tc"):
     dev = torch.device("cuda")
     q, qs, max_q = workloads.multi_query_inputs(wl, new_tokens, seed)
     out = pa.multi_query(q.to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), wl.block_tables.to(dev),
-                         wl.context_lens.to(dev), qs.to(dev), wl.scale, wl.num_kv_heads, max_q, num_ctas=num_ctas)
+                         wl.context_lens.to(dev), qs.to(dev), wl.scale, wl.num_kv_heads, max_q, num_ctas=num_ctas,
+                         tiles=tiles)
     torch.cuda.synchronize()
     ref = oracle.multi_query(q, wl.k_cache[0], wl.v_cache[0], wl.block_tables, wl.context_lens, qs, wl.scale,
                              wl.num_kv_heads, wl.dtype == "bf16")
@@ -94,16 +95,21 @@ def test_counts_beyond_the_context_are_clamped_and_flagged(oracle):
     (2, [300, 31, 500], [300, 31, 1], 16, "f16"),                  # full prefills, 600 rows
     (3, [77, 0, 513, 900, 2], [37, 0, 1, 20, 2], 64, "f16"),       # ragged, an empty sequence
     (2, [260, 1024], [70, 130], 128, "bf16"),                      # 128-token blocks
+    (1, [4096, 700], [512, 300], 32, "f16"),                       # the chunked-prefill bench's shape
+    (4, [1000, 129, 2000], [40, 33, 64], 64, "bf16"),              # tiles of 128 rows, a ragged last
 ])
-def test_prefill_tiles_parity(oracle, G, lens, new, B, dtype):
-    """More than 16 query rows per (sequence, kv head): tensor-core tiles of 64 rows."""
+@pytest.mark.parametrize("tiles", ["tc", "mma"])
+def test_prefill_tiles_parity(oracle, G, lens, new, B, dtype, tiles):
+    """More than 16 query rows per (sequence, kv head): tcgen05 tiles of 128 rows (accumulators in
+    tensor memory) or mma.sync tiles of 64 rows."""
     wl = workloads.make_workload(f"pf_G{G}_B{B}", context_lens=lens, num_q_heads=2 * G, num_kv_heads=2,
                                  block_size=B, dtype=dtype, seed=G * 13 + B, max_context=max(lens) + B)
     assert max(new) * G > 16
-    _run(oracle, wl, new, seed=G + B)
+    _run(oracle, wl, new, seed=G + B, tiles=tiles)
 
 
-def test_prefill_counts_beyond_the_context_are_flagged(oracle):
+@pytest.mark.parametrize("tiles", ["tc", "mma"])
+def test_prefill_counts_beyond_the_context_are_flagged(oracle, tiles):
     lens = [10, 40]
     wl = workloads.make_workload("pf_bad", context_lens=lens, num_q_heads=8, num_kv_heads=1, block_size=16, seed=19)
     dev = torch.device("cuda")
@@ -111,7 +117,7 @@ def test_prefill_counts_beyond_the_context_are_flagged(oracle):
     qs = torch.tensor([0, 12, 24], dtype=torch.int32)
     # 12 new tokens claimed for a 10-token context: clamped to 10 and flagged
     out = pa.multi_query(q.to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), wl.block_tables.to(dev),
-                         wl.context_lens.to(dev), qs.to(dev), wl.scale, 1, 12)
+                         wl.context_lens.to(dev), qs.to(dev), wl.scale, 1, 12, tiles=tiles)
     torch.cuda.synchronize()
     assert pa.read_device_status(clear=True) & pa._native.DEV_BAD_CONTEXT
     ref = oracle.multi_query(q[12:24], wl.k_cache[0], wl.v_cache[0], wl.block_tables[1:2], wl.context_lens[1:2],
