@@ -8,17 +8,20 @@
 // logical blocks through block_tables, q.k, running-max softmax, weight V, normalise; the
 // chunked prefill of its closing section).
 //
-// One CTA per (128-row tile, kv head, sequence); rows r = i * G + g (new token i, group member g).
-//   warps 0-3  softmax: thread t owns row t of the tile (tensor-memory lane t)
-//   warp 4     producer: TMA copies of 64-token K and V stages into a 3-deep ring
-//   warp 5     MMA: allocates tensor memory; one thread issues
-//                S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
-//                O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major, V N-major)
-//              with S double-buffered in tensor memory, so S_{j+1} runs under the softmax of S_j.
+// One CTA per (256 query rows, kv head, sequence), two tiles of 128 rows; rows r = i * G + g (new
+// token i, group member g).
+//   warps 0-3, 4-7  softmax of tile 0, tile 1: thread t owns row t of its tile (tensor-memory lane t)
+//   warp 8          producer: TMA copies of 64-token K and V stages into a 3-deep ring
+//   warp 9          MMA: allocates tensor memory; one thread issues, per stage j and tile,
+//                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
+//                     O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major, V N-major)
+//                   with S double-buffered in tensor memory, so S_{j+1} of both tiles runs under
+//                   the softmax of S_j, and the two tiles share every K and V stage.
 // The softmax keeps a lazy exponent base per row (moved to the running max only when a score
 // exceeds it by more than 2^8, then O is rescaled in tensor memory), writes P = exp2(s - base)
-// to shared memory in the operand layout (bf16: a high and a low part, two MMAs), and at the end
-// normalises its O row.  Every wait is bounded; tensor memory is freed on every path.
+// to shared memory in the operand layout (fp16: two P buffers per tile; bf16: one, with a high
+// and a low part, two MMAs), and at the end normalises its O row.  Every wait is bounded;
+// tensor memory is freed on every path.
 #include "pa_internal.cuh"
 
 #include <cuda.h>
@@ -32,24 +35,29 @@ namespace pa {
 namespace {
 
 constexpr int kTRows = 128;                                  // query rows per tile: the MMA's M
-constexpr int kSoftWarps = 4;                                // one row per thread
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kTThreads = 6 * 32;
+constexpr int kTiles = 2;                                    // tiles per CTA, one softmax warpgroup each
+constexpr int kCtaRows = kTiles * kTRows;
+constexpr int kSoftWarps = 4 * kTiles;                       // one row per thread
+constexpr int kProdWarp = kSoftWarps;
+constexpr int kMmaWarp = kSoftWarps + 1;
+constexpr int kTThreads = (kSoftWarps + 2) * 32;
 constexpr int kTStages = 3;
 constexpr uint32_t kQHalf = kTRows * 128;                    // 16 KB: 128 rows x 64 dims
+constexpr uint32_t kQTile = 2 * kQHalf;
 constexpr uint32_t kKVHalf = kStageTokens * 128;             // 8 KB: 64 tokens x 64 dims
 constexpr uint32_t kKBytes = 2 * kKVHalf;                    // 16 KB of K per stage (V the same)
 constexpr uint32_t kStage = 2 * kKBytes;
 constexpr uint32_t kPBytes = kTRows * kStageTokens * 2;      // 16 KB: 128 rows x 64 tokens
-constexpr uint32_t kOffQ = 0;                                // [2 halves][128 rows][128 B]
-constexpr uint32_t kOffRing = 2 * kQHalf;                    // [stage][K, V][2 halves][64 tokens][128 B]
-constexpr uint32_t kOffP = kOffRing + kTStages * kStage;     // [2 buffers][high, low][128 rows][128 B]
-constexpr uint32_t kOffBar = kOffP + 4 * kPBytes;
-constexpr int kNumBars = 16;
+constexpr uint32_t kPTile = 2 * kPBytes;                     // fp16: two P buffers; bf16: one, high and low
+constexpr uint32_t kOffQ = 0;                                // [tile][2 halves][128 rows][128 B]
+constexpr uint32_t kOffRing = kTiles * kQTile;               // [stage][K, V][2 halves][64 tokens][128 B]
+constexpr uint32_t kOffP = kOffRing + kTStages * kStage;     // [tile][32 KB]
+constexpr uint32_t kOffBar = kOffP + kTiles * kPTile;
+constexpr int kNumBars = 24;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // tensor-memory address, abort flag, issued count
 constexpr size_t kSmemTc = 1024 /*alignment slack*/ + kOffMisc + 16;
-constexpr uint32_t kTmemCols = 256;                          // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kTmemCols = 512;                          // per tile: S buffers at +0, +64, O at +128
+constexpr uint32_t kTileCols = 256;
 constexpr uint32_t kColO = 128;
 constexpr float kLazyLog2 = 8.f;                             // exponent-base slack (weights below 2^8)
 
@@ -109,6 +117,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive fp32 columns of this thread's tensor-memory lane, one load.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,"
+        "%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -196,28 +225,29 @@ __global__ void __launch_bounds__(kTThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kOffBar);
     uint64_t* kv_full = bars;           // [3] a stage's K and V landed
     uint64_t* kv_empty = bars + 3;      // [3] the MMAs reading a stage are done
-    uint64_t* s_full = bars + 6;        // [2] S_j is in tensor memory
-    uint64_t* p_full = bars + 8;        // [2] P_j is in shared memory (128 arrivals)
-    uint64_t* pv_done = bars + 10;      // [2] O += P_j V_j is complete
-    uint64_t* q_ready = bars + 12;      // the Q tile is in shared memory (128 arrivals)
-    uint64_t* drain = bars + 13;        // every MMA issued is complete
+    uint64_t* s_full = bars + 6;        // [tile][2] S_j of the tile is in tensor memory
+    uint64_t* p_full = bars + 10;       // [tile][2] P_j of the tile is in shared memory (128 arrivals)
+    uint64_t* pv_done = bars + 14;      // [tile][2] O += P_j V_j of the tile is complete
+    uint64_t* q_ready = bars + 18;      // [tile] the tile's Q rows are in shared memory (128 arrivals)
+    uint64_t* drain = bars + 20;        // every MMA issued is complete
     volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + kOffMisc + 4);
     volatile int* issued_count = abort_flag + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    const int cta_tile = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
     const int G = a.num_q_heads / a.num_kv_heads;
     const int cap = a.max_blocks_per_seq * a.block_size;
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kPBufs = kSplitP ? 1 : 2;   // P buffers per tile (bf16 keeps a low part beside the high)
 
     grid_dependency_wait();
     int L = a.context_lens[s];
     if (L < 0 || L > cap) {
-        if (tid == 0 && tile == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+        if (tid == 0 && cta_tile == 0 && hk == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
         L = L < 0 ? 0 : cap;
     }
-    if (tid == 0 && tile == 0 && hk == 0) {
+    if (tid == 0 && cta_tile == 0 && hk == 0) {
         const int n_raw = a.q_start[s + 1] - a.q_start[s];
         const int r0_raw = a.q_start[s];
         if (n_raw < 0 || n_raw > L || n_raw > a.max_q || r0_raw < 0 || r0_raw + n_raw > a.q_rows)
@@ -225,10 +255,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
     const QSpan qs = q_span(a, s, L);
     const int rows = qs.n * G;
-    const int r0 = tile * kTRows;
+    const int r0 = cta_tile * kCtaRows;
     if (r0 >= rows) return;   // uniform for the CTA, before any tensor memory is held
-    const int r_last = min(r0 + kTRows, rows) - 1;
-    const int t_end = L - qs.n + r_last / G + 1;   // tokens the tile needs: up to its last row's position
+    const int ntiles = min(kTiles, (rows - r0 + kTRows - 1) / kTRows);   // tiles with rows (1 or 2)
+    const int r_last = min(r0 + kCtaRows, rows) - 1;
+    const int t_end = L - qs.n + r_last / G + 1;   // tokens the CTA needs: up to its last row's position
     const int nst = (t_end + kStageTokens - 1) / kStageTokens;
 
     if (tid == 0) {
@@ -238,12 +269,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 2 * kTiles; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], kSoftWarps * 32);
+            mbar_init(&p_full[b], 128);
             mbar_init(&pv_done[b], 1);
         }
-        mbar_init(q_ready, kSoftWarps * 32);
+        for (int t = 0; t < kTiles; ++t) mbar_init(&q_ready[t], 128);
         mbar_init(drain, 1);
         *abort_flag = 0;
         *issued_count = 0;
@@ -289,25 +320,29 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc<T>(kStageTokens, false);
             constexpr uint32_t kIdPV = idesc<T>(kHeadDim, true);
-            bool ok = mbar_wait_bounded(q_ready, 0u);
-            if (!ok) give_up();
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) ok = mbar_wait_bounded(&q_ready[t], 0u);
             tc_fence_after();
-            // S_j = Q K_j^T into S buffer j % 2: two 64-dim halves x four 16-dim steps
+            // S_j = Q K_j^T of every tile into its S buffer j % 2: two 64-dim halves x four 16-dim steps
             auto issue_s = [&](int j) -> bool {
                 const int st = j % kTStages;
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(j & 1) * kStageTokens;
                 const uint32_t kst = base + kOffRing + (uint32_t)st * kStage;
+                for (int t = 0; t < ntiles; ++t) {
+                    const uint32_t d = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
+                    const uint32_t qt = base + kOffQ + (uint32_t)t * kQTile;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma(d, sdesc(base + kOffQ + h * kQHalf + kk * 32, 16, 1024),
-                             sdesc(kst + h * kKVHalf + kk * 32, 16, 1024), kIdS, (h | kk) != 0 ? 1u : 0u);
-                umma_commit(&s_full[j & 1]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma(d, sdesc(qt + h * kQHalf + kk * 32, 16, 1024), sdesc(kst + h * kKVHalf + kk * 32, 16, 1024),
+                                 kIdS, (h | kk) != 0 ? 1u : 0u);
+                    umma_commit(&s_full[t * 2 + (j & 1)]);
+                }
                 return true;
             };
+            if (!ok) give_up();
             if (ok && !*abort_flag) ok = issue_s(0);
             for (int j = 0; j < nst && ok; ++j) {
                 if (*abort_flag) break;
@@ -315,35 +350,42 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     ok = false;
                     break;
                 }
-                if (!mbar_wait_bounded(&p_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // O += P_j V_j: four 16-token steps (and the low part of P for bf16)
+                // O += P_j V_j per tile: four 16-token steps (and the low part of P for bf16)
                 const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
-                const uint32_t pb = base + kOffP + (uint32_t)(j & 1) * 2u * kPBytes;
+                for (int t = 0; t < ntiles && ok; ++t) {
+                    if (!mbar_wait_bounded(&p_full[t * 2 + (j & 1)], (uint32_t)(j >> 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pb = base + kOffP + (uint32_t)t * kPTile + (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes;
+                    const uint32_t o = tmem + (uint32_t)t * kTileCols + kColO;
 #pragma unroll
-                for (int kt = 0; kt < 4; ++kt) {
-                    const uint64_t vd = sdesc(vst + kt * 2048, kKVHalf, 1024);
-                    umma(tmem + kColO, sdesc(pb + kt * 32, 16, 1024), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
-                    if (kSplitP) umma(tmem + kColO, sdesc(pb + kPBytes + kt * 32, 16, 1024), vd, kIdPV, 1u);
+                    for (int kt = 0; kt < 4; ++kt) {
+                        const uint64_t vd = sdesc(vst + kt * 2048, kKVHalf, 1024);
+                        umma(o, sdesc(pb + kt * 32, 16, 1024), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
+                        if (kSplitP) umma(o, sdesc(pb + kPBytes + kt * 32, 16, 1024), vd, kIdPV, 1u);
+                    }
+                    umma_commit(&pv_done[t * 2 + (j & 1)]);
                 }
-                umma_commit(&pv_done[j & 1]);
-                umma_commit(&kv_empty[j % kTStages]);
+                if (ok) umma_commit(&kv_empty[j % kTStages]);
             }
             if (!ok) give_up();
             // nothing of this CTA's may still run on the tensor cores when it frees its memory
             umma_commit(drain);
             (void)mbar_wait_bounded(drain, 0u);
         }
-    } else {
-        // ---------------- softmax: thread tid owns row r0 + tid (tensor-memory lane tid) ----------------
-        const int r = r0 + tid;
+    } else if (warp / 4 < ntiles) {
+        // ------- softmax: warpgroup t owns tile t; thread wt owns its row wt (tensor-memory lane wt) -------
+        const int t = warp / 4, wt = tid - t * 128;
+        const int r = r0 + t * kTRows + wt;
         const bool row_ok = r < rows;
         const int lim = row_ok ? L - qs.n + r / G : -1;   // newest position the row attends to
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        const uint32_t sw = (uint32_t)(tid & 7);          // 128-byte swizzle phase of this row
+        const uint32_t lane_addr = tmem + (uint32_t)t * kTileCols + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t sw = (uint32_t)(wt & 7);           // 128-byte swizzle phase of this row
+        uint64_t* t_s_full = s_full + 2 * t;
+        uint64_t* t_p_full = p_full + 2 * t;
+        uint64_t* t_pv_done = pv_done + 2 * t;
         // Q row into the K-major operand tile (two 64-dim halves); rows past the segment are zero
         {
             const uint4* src = row_ok ? reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
@@ -353,47 +395,60 @@ __global__ void __launch_bounds__(kTThreads, 1)
             for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_shared_v4(base + kOffQ + h * kQHalf + tid * 128 + ((c ^ sw) << 4),
+                    st_shared_v4(base + kOffQ + t * kQTile + h * kQHalf + wt * 128 + ((c ^ sw) << 4),
                                  row_ok ? src[h * 8 + c] : make_uint4(0, 0, 0, 0));
         }
         fence_proxy_async_smem();
-        mbar_arrive(q_ready);
+        mbar_arrive(&q_ready[t]);
 
         // waits and give-ups are decided per warp: the tensor-memory accesses are warp-wide
         auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
         };
+        const float sl = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool dead = false;
         for (int j = 0; j < nst && !dead; ++j) {
-            if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&s_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&t_s_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
                 dead = true;
                 break;
             }
             tc_fence_after();
             float x[64];
-            {
-                float v[32];
-                tmem_ld32(lane_addr + (uint32_t)(j & 1) * kStageTokens, v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = v[c];
-                tmem_ld32(lane_addr + (uint32_t)(j & 1) * kStageTokens + 32, v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
-            }
+            tmem_ld64(lane_addr + (uint32_t)(j & 1) * kStageTokens, x);
             const int t0 = j * kStageTokens;
+            // raw scores; the scale (log2 units) enters the exponent's FMA.  Stages every row of the
+            // warp sees whole skip the causal mask.
             float mx = -INFINITY;
+            if (__all_sync(0xffffffffu, t0 + kStageTokens - 1 <= lim)) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                x[c] = (t0 + c <= lim) ? x[c] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    x[c] = (t0 + c <= lim) ? x[c] : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
             }
-            if (j == nst - 1) {
+            if (sl > 0.f) {
+                mx *= sl;   // the scaled maximum (-inf stays)
+            } else {
+                // a non-positive scale reverses the order: scale first, then take the maximum
+                mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    x[c] = (x[c] == -INFINITY) ? -INFINITY : x[c] * sl;
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+            const float xs = (sl > 0.f) ? sl : 1.f;   // the factor still to apply to x
+            if (j == nst - 1 && t == 0) {
                 // the last stage: V rows from t_end on are masked, but they can hold pool slots past
                 // the context or stale data; zero them so that P = 0 never meets a non-finite V
+                // (tile 0 does it before its P arrives, and the MMA thread takes tile 0's P first)
                 const int nvalid = t_end - t0;
                 const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
-                for (int idx = tid; idx < (kStageTokens - nvalid) * 16; idx += kSoftWarps * 32) {
+                for (int idx = wt; idx < (kStageTokens - nvalid) * 16; idx += 128) {
                     const int t = nvalid + (idx >> 4);
                     st_shared_v4(vst + ((idx >> 3) & 1) * kKVHalf + t * 128 + (idx & 7) * 16, make_uint4(0, 0, 0, 0));
                 }
@@ -405,7 +460,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 // some row of the warp rescales O, which holds stages 0 .. j-1: wait (warp-wide) for
                 // O += P_{j-1} V_{j-1}; tensor-memory accesses are warp-wide, so every lane scales
                 // its O row (by 1 where the base stays)
-                if (!warp_wait(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
+                if (!warp_wait(&t_pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
                     dead = true;
                     break;
                 }
@@ -424,19 +479,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             if (move) m_run = mx;
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            // P buffer j % 2 was last read by O += P_{j-2} V_{j-2}
-            if (j >= 2 && !warp_wait(&pv_done[j & 1], (uint32_t)((j - 2) >> 1) & 1u)) {
+            // the P buffer was last read by O += P_{j - kPBufs} V_{j - kPBufs}
+            if (j >= kPBufs &&
+                !warp_wait(&t_pv_done[(j - kPBufs) & 1], (uint32_t)((j - kPBufs) >> 1) & 1u)) {
                 dead = true;
                 break;
             }
-            const uint32_t pb = base + kOffP + (uint32_t)(j & 1) * 2u * kPBytes + (uint32_t)tid * 128u;
+            const uint32_t pb = base + kOffP + (uint32_t)t * kPTile +
+                                (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes + (uint32_t)wt * 128u;
             float rs = 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    p[e] = exp2f(x[c8 * 8 + e] - m_use);
+                    p[e] = exp2f(fmaf(x[c8 * 8 + e], xs, -m_use));
                     rs += p[e];
                 }
                 uint4 hi;
@@ -459,10 +516,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             l_run += rs;
             fence_proxy_async_smem();   // P (and the zeroed V rows) are read by the tensor cores
             tc_fence_before();
-            mbar_arrive(&p_full[j & 1]);
+            mbar_arrive(&t_p_full[j & 1]);
         }
         // ---- normalise and write the row ----
-        if (!dead && warp_wait(&pv_done[(nst - 1) & 1], (uint32_t)((nst - 1) >> 1) & 1u)) {
+        if (!dead && warp_wait(&t_pv_done[(nst - 1) & 1], (uint32_t)((nst - 1) >> 1) & 1u)) {
             tc_fence_after();
             const float inv = 1.f / l_run;
             uint4* dst = row_ok ? reinterpret_cast<uint4*>(static_cast<T*>(a.out) + q_offset(a, qs, hk, G, r))
@@ -551,7 +608,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
         configured.fetch_or(bit);
     }
     const int G = a.num_q_heads / a.num_kv_heads;
-    const long long tiles = ((long long)a.max_q * G + kTRows - 1) / kTRows;
+    const long long tiles = ((long long)a.max_q * G + kCtaRows - 1) / kCtaRows;
     if (tiles > 0x7fffffffLL || a.num_kv_heads > 65535 || a.num_seqs > 65535) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, a.num_kv_heads, a.num_seqs);
