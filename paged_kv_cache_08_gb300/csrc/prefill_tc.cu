@@ -158,6 +158,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// 2^x on the special-function unit (approximate, subnormal results flushed to zero): the
+// softmax weights it produces lie in (0, 2^8], and weights below 2^-126 do not matter.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -419,17 +427,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const int t0 = j * kStageTokens;
             // raw scores; the scale (log2 units) enters the exponent's FMA.  Stages every row of the
             // warp sees whole skip the causal mask.
-            float mx = -INFINITY;
-            if (__all_sync(0xffffffffu, t0 + kStageTokens - 1 <= lim)) {
+            if (!__all_sync(0xffffffffu, t0 + kStageTokens - 1 <= lim)) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    x[c] = (t0 + c <= lim) ? x[c] : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
-                }
+                for (int c = 0; c < 64; ++c) x[c] = (t0 + c <= lim) ? x[c] : -INFINITY;
             }
+            // maximum as a tree (eight independent chains), not one 64-long dependency chain
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             if (sl > 0.f) {
                 mx *= sl;   // the scaled maximum (-inf stays)
             } else {
@@ -487,14 +495,14 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             const uint32_t pb = base + kOffP + (uint32_t)t * kPTile +
                                 (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes + (uint32_t)wt * 128u;
-            float rs = 0.f;
+            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial row sums
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    p[e] = exp2f(fmaf(x[c8 * 8 + e], xs, -m_use));
-                    rs += p[e];
+                    p[e] = ex2(fmaf(x[c8 * 8 + e], xs, -m_use));
+                    rs8[e] += p[e];
                 }
                 uint4 hi;
                 hi.x = Elem<T>::pack2(p[0], p[1]);
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     st_shared_v4(pb + kPBytes + (((uint32_t)c8 ^ sw) << 4), lo);
                 }
             }
-            l_run += rs;
+            l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             fence_proxy_async_smem();   // P (and the zeroed V rows) are read by the tensor cores
             tc_fence_before();
             mbar_arrive(&t_p_full[j & 1]);
