@@ -832,7 +832,10 @@ def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512
             "config": {"workload": f"prefill_{seqs}seq_ctx{context}_new{new_tokens}_mha32_f16_B32",
                        "l2": "1 GiB of K/V, above L2", "tiles": tiles},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(tflops / peak, 4), "traffic": None, "flops_per_launch": flops,
+                         "frac": round(tflops / peak, 4),
+                         "traffic": (profiled_traffic("paged_kv_cache_08_gb300/csrc/prefill_tc.cu", "prefill")
+                                     if tiles == "tc" else None),
+                         "flops_per_launch": flops,
                          "kernel": ("prefill_tc_kernel (tcgen05.mma, accumulators in tensor memory)" if tiles == "tc"
                                     else "prefill_mma_kernel (mma.sync m16n8k16)"), "peak_source": kind},
             "gpu_launches": args.steps, "clocks": clk.summary()}
