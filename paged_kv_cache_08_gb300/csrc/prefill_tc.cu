@@ -328,6 +328,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc<T>(kStageTokens, false);
             constexpr uint32_t kIdPV = idesc<T>(kHeadDim, true);
+            // descriptors of each operand region's first 16-byte unit; an MMA's operand is that plus
+            // its byte offset / 16 (every address stays below 256 KB, inside the 14-bit field)
+            const uint64_t dq0 = sdesc(base + kOffQ, 16, 1024);
+            const uint64_t dk0 = sdesc(base + kOffRing, 16, 1024);
+            const uint64_t dv0 = sdesc(base + kOffRing + kKBytes, kKVHalf, 1024);
+            const uint64_t dp0 = sdesc(base + kOffP, 16, 1024);
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) ok = mbar_wait_bounded(&q_ready[t], 0u);
             tc_fence_after();
@@ -336,15 +342,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 const int st = j % kTStages;
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
                 tc_fence_after();
-                const uint32_t kst = base + kOffRing + (uint32_t)st * kStage;
+                const uint64_t dk = dk0 + (uint64_t)(((uint32_t)st * kStage) >> 4);
                 for (int t = 0; t < ntiles; ++t) {
                     const uint32_t d = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
-                    const uint32_t qt = base + kOffQ + (uint32_t)t * kQTile;
+                    const uint64_t dq = dq0 + (uint64_t)(((uint32_t)t * kQTile) >> 4);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma(d, sdesc(qt + h * kQHalf + kk * 32, 16, 1024), sdesc(kst + h * kKVHalf + kk * 32, 16, 1024),
+                            umma(d, dq + (uint64_t)((h * kQHalf + kk * 32) >> 4), dk + (uint64_t)((h * kKVHalf + kk * 32) >> 4),
                                  kIdS, (h | kk) != 0 ? 1u : 0u);
                     umma_commit(&s_full[t * 2 + (j & 1)]);
                 }
@@ -359,20 +365,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     break;
                 }
                 // O += P_j V_j per tile: four 16-token steps (and the low part of P for bf16)
-                const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
+                const uint64_t dv = dv0 + (uint64_t)(((uint32_t)(j % kTStages) * kStage) >> 4);
                 for (int t = 0; t < ntiles && ok; ++t) {
                     if (!mbar_wait_bounded(&p_full[t * 2 + (j & 1)], (uint32_t)(j >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t pb = base + kOffP + (uint32_t)t * kPTile + (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes;
+                    const uint64_t dp =
+                        dp0 + (uint64_t)(((uint32_t)t * kPTile + (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes) >> 4);
                     const uint32_t o = tmem + (uint32_t)t * kTileCols + kColO;
 #pragma unroll
                     for (int kt = 0; kt < 4; ++kt) {
-                        const uint64_t vd = sdesc(vst + kt * 2048, kKVHalf, 1024);
-                        umma(o, sdesc(pb + kt * 32, 16, 1024), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
-                        if (kSplitP) umma(o, sdesc(pb + kPBytes + kt * 32, 16, 1024), vd, kIdPV, 1u);
+                        const uint64_t vd = dv + (uint64_t)((kt * 2048) >> 4);
+                        umma(o, dp + (uint64_t)((kt * 32) >> 4), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
+                        if (kSplitP) umma(o, dp + (uint64_t)((kPBytes + kt * 32) >> 4), vd, kIdPV, 1u);
                     }
                     umma_commit(&pv_done[t * 2 + (j & 1)]);
                 }
