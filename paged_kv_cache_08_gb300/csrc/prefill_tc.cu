@@ -12,7 +12,8 @@
 // token i, group member g).
 //   warps 0-3, 4-7  softmax of tile 0, tile 1: thread t owns row t of its tile (tensor-memory lane t)
 //   warp 8          producer: TMA copies of 64-token K and V stages into a 3-deep ring
-//   warp 9          MMA: allocates tensor memory; one thread issues, per stage j and tile,
+//   warps 9, 10     MMA of tile 0, tile 1 (warp 9 allocates tensor memory); one thread each issues,
+//                   per stage j,
 //                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
 //                     O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major, V N-major)
 //                   with S double-buffered in tensor memory, so S_{j+1} of both tiles runs under
@@ -39,8 +40,8 @@ constexpr int kTiles = 2;                                    // tiles per CTA, o
 constexpr int kCtaRows = kTiles * kTRows;
 constexpr int kSoftWarps = 4 * kTiles;                       // one row per thread
 constexpr int kProdWarp = kSoftWarps;
-constexpr int kMmaWarp = kSoftWarps + 1;
-constexpr int kTThreads = (kSoftWarps + 2) * 32;
+constexpr int kMmaWarp = kSoftWarps + 1;                     // + t: the MMA issuer of tile t
+constexpr int kTThreads = (kSoftWarps + 1 + kTiles) * 32;
 constexpr int kTStages = 3;
 constexpr uint32_t kQHalf = kTRows * 128;                    // 16 KB: 128 rows x 64 dims
 constexpr uint32_t kQTile = 2 * kQHalf;
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         prefetch_map(&maps.v);
         for (int i = 0; i < kTStages; ++i) {
             mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&kv_empty[i], ntiles);   // one commit per tile's issuer
         }
         for (int b = 0; b < 2 * kTiles; ++b) {
             mbar_init(&s_full[b], 1);
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
             mbar_init(&pv_done[b], 1);
         }
         for (int t = 0; t < kTiles; ++t) mbar_init(&q_ready[t], 128);
-        mbar_init(drain, 1);
+        mbar_init(drain, ntiles);
         *abort_flag = 0;
         *issued_count = 0;
         fence_mbar_init();
@@ -323,9 +324,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             *issued_count = i;
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue: one thread ----------------
-        if (lane == 0) {
+    } else if (warp >= kMmaWarp && warp < kMmaWarp + kTiles) {
+        // ---------------- MMA issue: one thread per tile, in warps on different schedulers ----------------
+        const int mt = warp - kMmaWarp;   // this issuer's tile
+        if (lane == 0 && mt < ntiles) {
             constexpr uint32_t kIdS = idesc<T>(kStageTokens, false);
             constexpr uint32_t kIdPV = idesc<T>(kHeadDim, true);
             // descriptors of each operand region's first 16-byte unit; an MMA's operand is that plus
@@ -334,16 +336,16 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const uint64_t dk0 = sdesc(base + kOffRing, 16, 1024);
             const uint64_t dv0 = sdesc(base + kOffRing + kKBytes, kKVHalf, 1024);
             const uint64_t dp0 = sdesc(base + kOffP, 16, 1024);
-            bool ok = true;
-            for (int t = 0; t < ntiles && ok; ++t) ok = mbar_wait_bounded(&q_ready[t], 0u);
+            bool ok = mbar_wait_bounded(&q_ready[mt], 0u);
             tc_fence_after();
-            // S_j = Q K_j^T of every tile into its S buffer j % 2: two 64-dim halves x four 16-dim steps
+            // S_j = Q K_j^T of the tile into its S buffer j % 2: two 64-dim halves x four 16-dim steps
             auto issue_s = [&](int j) -> bool {
                 const int st = j % kTStages;
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
                 tc_fence_after();
                 const uint64_t dk = dk0 + (uint64_t)(((uint32_t)st * kStage) >> 4);
-                for (int t = 0; t < ntiles; ++t) {
+                {
+                    const int t = mt;
                     const uint32_t d = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
                     const uint64_t dq = dq0 + (uint64_t)(((uint32_t)t * kQTile) >> 4);
 #pragma unroll
@@ -364,10 +366,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     ok = false;
                     break;
                 }
-                // O += P_j V_j per tile: four 16-token steps (and the low part of P for bf16)
+                // O += P_j V_j of the tile: four 16-token steps (and the low part of P for bf16)
                 const uint64_t dv = dv0 + (uint64_t)(((uint32_t)(j % kTStages) * kStage) >> 4);
-                for (int t = 0; t < ntiles && ok; ++t) {
+                {
+                    const int t = mt;
                     if (!mbar_wait_bounded(&p_full[t * 2 + (j & 1)], (uint32_t)(j >> 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    // the last stage's V rows past the context are zeroed by tile 0's softmax
+                    // before its P arrives
+                    if (t > 0 && j == nst - 1 && !mbar_wait_bounded(&p_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
             if (j == nst - 1 && t == 0) {
                 // the last stage: V rows from t_end on are masked, but they can hold pool slots past
                 // the context or stale data; zero them so that P = 0 never meets a non-finite V
-                // (tile 0 does it before its P arrives, and the MMA thread takes tile 0's P first)
+                // (tile 0 does it before its P arrives, which both issuers wait for at the last stage)
                 const int nvalid = t_end - t0;
                 const uint32_t vst = base + kOffRing + (uint32_t)(j % kTStages) * kStage + kKBytes;
                 for (int idx = wt; idx < (kStageTokens - nvalid) * 16; idx += 128) {
