@@ -113,9 +113,9 @@ int choose_path(int num_seqs, int group, int math, Path* path) {
 
 inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-int persist_ctas(int group, const pa_decode_options* opts) {
+int persist_ctas(int rows, int num_seqs, const pa_decode_options* opts) {
     if (opts && opts->num_ctas > 0) return opts->num_ctas;
-    return persist_ctas_per_sm(group) * sm_count();
+    return persist_ctas_per_sm(rows, num_seqs) * sm_count();
 }
 
 // CTA count the workspace layout is sized for: the requested count, or the largest default
@@ -536,7 +536,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     cudaError_t e;
 
     if (path == kPathPersist) {
-        const int ctas = persist_ctas(multi ? max_q * group : group, opts);
+        const int ctas = persist_ctas(multi ? max_q * group : group, num_seqs, opts);
         const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
         const size_t pieces = persist_pieces(persist_layout_ctas(opts));

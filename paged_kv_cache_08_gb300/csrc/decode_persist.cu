@@ -787,7 +787,7 @@ __device__ __forceinline__ void chunk_prefix_weighted(const DecodeArgs& a, int S
 }
 
 template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds>
-__global__ void __launch_bounds__(kThreads, (kG16 || kStages > 3) ? 1 : 2)
+__global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
     decode_persist_kernel(const DecodeArgs a, const __grid_constant__ MapsOf<kManyEnds> maps, const int R_log2) {
     using Lay = PLayout<kG16, kStages>;
     extern __shared__ unsigned char smem_raw[];
@@ -1497,7 +1497,12 @@ cudaError_t dispatch(const DecodeArgs& a, const MmaMapsTails& maps, int R_log2, 
 
 }  // namespace
 
-int persist_ctas_per_sm(int group) { return group <= 8 ? 2 : 1; }
+// Two CTAs per SM (the 3-stage ring) unless 9 to 16 query rows per segment and so many sequences
+// that two CTAs' shared memory (their prefix arrays included) no longer fits one SM.
+int persist_ctas_per_sm(int rows, int num_seqs) {
+    if (rows <= 8) return 2;
+    return 2 * (PLayout<true, 3>::total(num_seqs) + 1024) <= 228u * 1024u ? 2 : 1;
+}
 
 cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t stream) {
     const int R = a.block_size < kStageTokens ? a.block_size : kStageTokens;

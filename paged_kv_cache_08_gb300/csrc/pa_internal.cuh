@@ -287,7 +287,7 @@ bool fma_supports_group(int group);
 
 // Persistent load-balanced tensor-core kernel (G <= 16, num_seqs <= kPersistMaxSeqs); one launch.
 cudaError_t launch_decode_persist(const DecodeArgs& a, int dtype, cudaStream_t stream);
-int persist_ctas_per_sm(int group);
+int persist_ctas_per_sm(int rows, int num_seqs);
 
 // Several query tokens per sequence, any number: tiles of 64 query rows (prefill_mma.cu).
 cudaError_t launch_prefill_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
