@@ -11,7 +11,7 @@
 // One CTA per (256 query rows, kv head, sequence), two tiles of 128 rows; rows r = i * G + g (new
 // token i, group member g).
 //   warps 0-3, 4-7  softmax of tile 0, tile 1: thread t owns row t of its tile (tensor-memory lane t)
-//   warp 8          producer: TMA copies of 64-token K and V stages into a 3-deep ring
+//   warp 8          producer: TMA copies of 64-token K and V stages into a 4-deep ring (bf16: 3)
 //   warps 9, 10     MMA of tile 0, tile 1 (warp 9 allocates tensor memory); one thread each issues,
 //                   per stage j,
 //                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
@@ -20,9 +20,9 @@
 //                   the softmax of S_j, and the two tiles share every K and V stage.
 // The softmax keeps a lazy exponent base per row (moved to the running max only when a score
 // exceeds it by more than 2^8, then O is rescaled in tensor memory), writes P = exp2(s - base)
-// to shared memory in the operand layout (fp16: two P buffers per tile; bf16: one, with a high
-// and a low part, two MMAs), and at the end normalises its O row.  Every wait is bounded;
-// tensor memory is freed on every path.
+// to shared memory in the operand layout (one buffer per tile, rewritten once the previous PV
+// product is done; bf16 with a high and a low part, two MMAs), and at the end normalises its O
+// row.  Every wait is bounded; tensor memory is freed on every path.
 #include "pa_internal.cuh"
 
 #include <cuda.h>
@@ -42,21 +42,32 @@ constexpr int kSoftWarps = 4 * kTiles;                       // one row per thre
 constexpr int kProdWarp = kSoftWarps;
 constexpr int kMmaWarp = kSoftWarps + 1;                     // + t: the MMA issuer of tile t
 constexpr int kTThreads = (kSoftWarps + 1 + kTiles) * 32;
-constexpr int kTStages = 3;
 constexpr uint32_t kQHalf = kTRows * 128;                    // 16 KB: 128 rows x 64 dims
 constexpr uint32_t kQTile = 2 * kQHalf;
 constexpr uint32_t kKVHalf = kStageTokens * 128;             // 8 KB: 64 tokens x 64 dims
 constexpr uint32_t kKBytes = 2 * kKVHalf;                    // 16 KB of K per stage (V the same)
 constexpr uint32_t kStage = 2 * kKBytes;
 constexpr uint32_t kPBytes = kTRows * kStageTokens * 2;      // 16 KB: 128 rows x 64 tokens
-constexpr uint32_t kPTile = 2 * kPBytes;                     // fp16: two P buffers; bf16: one, high and low
 constexpr uint32_t kOffQ = 0;                                // [tile][2 halves][128 rows][128 B]
 constexpr uint32_t kOffRing = kTiles * kQTile;               // [stage][K, V][2 halves][64 tokens][128 B]
-constexpr uint32_t kOffP = kOffRing + kTStages * kStage;     // [tile][32 KB]
-constexpr uint32_t kOffBar = kOffP + kTiles * kPTile;
+constexpr int kMaxStages = 4;
 constexpr int kNumBars = 24;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // tensor-memory address, abort flag, issued count
-constexpr size_t kSmemTc = 1024 /*alignment slack*/ + kOffMisc + 16;
+
+// Shared memory by element type.  One P buffer per tile (the softmax of S_j writes it once
+// O += P_{j-1} V_{j-1} is done); bf16 keeps a low part beside the high one, so its K/V ring is
+// one stage shorter: fp16 Q 64 KB + 4 x 32 KB ring + 2 x 16 KB P, bf16 64 + 3 x 32 + 2 x 32.
+template <typename T>
+struct TcLayout {
+    static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+    static constexpr int kStages = kSplitP ? 3 : 4;
+    static constexpr uint32_t kPTile = kSplitP ? 2 * kPBytes : kPBytes;
+    static constexpr uint32_t kOffP = kOffRing + kStages * kStage;   // [tile][kPTile]
+    static constexpr uint32_t kOffBar = kOffP + kTiles * kPTile;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;      // tensor-memory address, abort flag, issued count
+    static constexpr size_t kSmem = 1024 /*alignment slack*/ + kOffMisc + 16;
+    static_assert(kStages <= kMaxStages, "barrier slots");
+    static_assert(kSmem <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
+};
 constexpr uint32_t kTmemCols = 512;                          // per tile: S buffers at +0, +64, O at +128
 constexpr uint32_t kTileCols = 256;
 constexpr uint32_t kColO = 128;
@@ -231,24 +242,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // 1024-aligned for the swizzle
     unsigned char* bp = smem_raw + (base - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kOffBar);
-    uint64_t* kv_full = bars;           // [3] a stage's K and V landed
-    uint64_t* kv_empty = bars + 3;      // [3] the MMAs reading a stage are done
-    uint64_t* s_full = bars + 6;        // [tile][2] S_j of the tile is in tensor memory
-    uint64_t* p_full = bars + 10;       // [tile][2] P_j of the tile is in shared memory (128 arrivals)
-    uint64_t* pv_done = bars + 14;      // [tile][2] O += P_j V_j of the tile is complete
-    uint64_t* q_ready = bars + 18;      // [tile] the tile's Q rows are in shared memory (128 arrivals)
-    uint64_t* drain = bars + 20;        // every MMA issued is complete
-    volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + kOffMisc + 4);
+    using Lay = TcLayout<T>;
+    constexpr int kTStages = Lay::kStages;
+    constexpr bool kSplitP = Lay::kSplitP;
+    constexpr uint32_t kPTile = Lay::kPTile;
+    constexpr uint32_t kOffP = Lay::kOffP;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + Lay::kOffBar);
+    uint64_t* kv_full = bars;                    // [stage] a stage's K and V landed
+    uint64_t* kv_empty = bars + kMaxStages;      // [stage] the MMAs reading a stage are done
+    uint64_t* s_full = bars + 2 * kMaxStages;    // [tile][2] S_j of the tile is in tensor memory
+    uint64_t* p_full = s_full + 4;               // [tile][2] P_j of the tile is in shared memory (128 arrivals)
+    uint64_t* pv_done = p_full + 4;              // [tile][2] O += P_j V_j of the tile is complete
+    uint64_t* q_ready = pv_done + 4;             // [tile] the tile's Q rows are in shared memory (128 arrivals)
+    uint64_t* drain = q_ready + kTiles;          // every MMA issued is complete
+    static_assert(2 * kMaxStages + 12 + kTiles + 1 <= kNumBars, "barrier slots");
+    volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + Lay::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + Lay::kOffMisc + 4);
     volatile int* issued_count = abort_flag + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta_tile = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
     const int G = a.num_q_heads / a.num_kv_heads;
     const int cap = a.max_blocks_per_seq * a.block_size;
-    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int kPBufs = kSplitP ? 1 : 2;   // P buffers per tile (bf16 keeps a low part beside the high)
 
     grid_dependency_wait();
     int L = a.context_lens[s];
@@ -382,7 +397,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t dp =
-                        dp0 + (uint64_t)(((uint32_t)t * kPTile + (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes) >> 4);
+                        dp0 + (uint64_t)(((uint32_t)t * kPTile) >> 4);
                     const uint32_t o = tmem + (uint32_t)t * kTileCols + kColO;
 #pragma unroll
                     for (int kt = 0; kt < 4; ++kt) {
@@ -503,14 +518,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             if (move) m_run = mx;
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            // the P buffer was last read by O += P_{j - kPBufs} V_{j - kPBufs}
-            if (j >= kPBufs &&
-                !warp_wait(&t_pv_done[(j - kPBufs) & 1], (uint32_t)((j - kPBufs) >> 1) & 1u)) {
+            // the P buffer was last read by O += P_{j-1} V_{j-1}
+            if (j >= 1 && !warp_wait(&t_pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
                 dead = true;
                 break;
             }
-            const uint32_t pb = base + kOffP + (uint32_t)t * kPTile +
-                                (uint32_t)((kPBufs == 2) ? (j & 1) : 0) * kPBytes + (uint32_t)wt * 128u;
+            const uint32_t pb = base + kOffP + (uint32_t)t * kPTile + (uint32_t)wt * 128u;
             float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial row sums
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
@@ -627,7 +640,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcLayout<T>::kSmem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
@@ -637,7 +650,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, a.num_kv_heads, a.num_seqs);
     cfg.blockDim = dim3(kTThreads);
-    cfg.dynamicSmemBytes = kSmemTc;
+    cfg.dynamicSmemBytes = TcLayout<T>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -652,7 +665,6 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
 }  // namespace
 
 cudaError_t launch_prefill_tc(const DecodeArgs& a, int dtype, cudaStream_t stream) {
-    static_assert(kSmemTc <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
     const int R = a.block_size < kStageTokens ? a.block_size : kStageTokens;
     int R_log2 = 0;
     while ((1 << R_log2) < R) ++R_log2;
