@@ -11,18 +11,19 @@
 // One CTA per (256 query rows, kv head, sequence), two tiles of 128 rows; rows r = i * G + g (new
 // token i, group member g).
 //   warps 0-3, 4-7  softmax of tile 0, tile 1: thread t owns row t of its tile (tensor-memory lane t)
-//   warp 8          producer: TMA copies of 64-token K and V stages into a 4-deep ring (bf16: 3)
+//   warp 8          producer: TMA copies of 64-token K and V stages into a 5-deep ring
 //   warps 9, 10     MMA of tile 0, tile 1 (warp 9 allocates tensor memory); one thread each issues,
 //                   per stage j,
-//                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands)
-//                     O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major, V N-major)
+//                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands in shared memory)
+//                     O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major in tensor memory, V
+//                                       N-major in shared memory)
 //                   with S double-buffered in tensor memory, so S_{j+1} of both tiles runs under
 //                   the softmax of S_j, and the two tiles share every K and V stage.
 // The softmax keeps a lazy exponent base per row (moved to the running max only when a score
 // exceeds it by more than 2^8, then O is rescaled in tensor memory), writes P = exp2(s - base)
-// to shared memory in the operand layout (one buffer per tile, rewritten once the previous PV
-// product is done; bf16 with a high and a low part, two MMAs), and at the end normalises its O
-// row.  Every wait is bounded; tensor memory is freed on every path.
+// over the first columns of S_j's tensor-memory buffer (bf16 with a high and a low part, two
+// MMAs), and at the end normalises its O row.  Every wait is bounded; tensor memory is freed on
+// every path.
 #include "pa_internal.cuh"
 
 #include <cuda.h>
@@ -47,27 +48,14 @@ constexpr uint32_t kQTile = 2 * kQHalf;
 constexpr uint32_t kKVHalf = kStageTokens * 128;             // 8 KB: 64 tokens x 64 dims
 constexpr uint32_t kKBytes = 2 * kKVHalf;                    // 16 KB of K per stage (V the same)
 constexpr uint32_t kStage = 2 * kKBytes;
-constexpr uint32_t kPBytes = kTRows * kStageTokens * 2;      // 16 KB: 128 rows x 64 tokens
 constexpr uint32_t kOffQ = 0;                                // [tile][2 halves][128 rows][128 B]
 constexpr uint32_t kOffRing = kTiles * kQTile;               // [stage][K, V][2 halves][64 tokens][128 B]
-constexpr int kMaxStages = 4;
-constexpr int kNumBars = 24;
-
-// Shared memory by element type.  One P buffer per tile (the softmax of S_j writes it once
-// O += P_{j-1} V_{j-1} is done); bf16 keeps a low part beside the high one, so its K/V ring is
-// one stage shorter: fp16 Q 64 KB + 4 x 32 KB ring + 2 x 16 KB P, bf16 64 + 3 x 32 + 2 x 32.
-template <typename T>
-struct TcLayout {
-    static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int kStages = kSplitP ? 3 : 4;
-    static constexpr uint32_t kPTile = kSplitP ? 2 * kPBytes : kPBytes;
-    static constexpr uint32_t kOffP = kOffRing + kStages * kStage;   // [tile][kPTile]
-    static constexpr uint32_t kOffBar = kOffP + kTiles * kPTile;
-    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;      // tensor-memory address, abort flag, issued count
-    static constexpr size_t kSmem = 1024 /*alignment slack*/ + kOffMisc + 16;
-    static_assert(kStages <= kMaxStages, "barrier slots");
-    static_assert(kSmem <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
-};
+constexpr int kTStages = 5;                                  // Q 64 KB + 5 x 32 KB ring
+constexpr int kNumBars = 2 * kTStages + 12 + kTiles + 1;
+constexpr uint32_t kOffBar = kOffRing + kTStages * kStage;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // tensor-memory address, abort flag, issued count
+constexpr size_t kSmemTc = 1024 /*alignment slack*/ + kOffMisc + 16;
+static_assert(kSmemTc <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
 constexpr uint32_t kTmemCols = 512;                          // per tile: S buffers at +0, +64, O at +128
 constexpr uint32_t kTileCols = 256;
 constexpr uint32_t kColO = 128;
@@ -103,6 +91,17 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t 
         "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A in tensor memory: row m of A in lane m, two 16-bit elements per 32-bit column
+// (the lower k in the low half), K-major.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t id,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(id), "r"(accumulate)
         : "memory");
 }
 
@@ -150,6 +149,17 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -242,22 +252,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // 1024-aligned for the swizzle
     unsigned char* bp = smem_raw + (base - raw);
-    using Lay = TcLayout<T>;
-    constexpr int kTStages = Lay::kStages;
-    constexpr bool kSplitP = Lay::kSplitP;
-    constexpr uint32_t kPTile = Lay::kPTile;
-    constexpr uint32_t kOffP = Lay::kOffP;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + Lay::kOffBar);
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kOffBar);
     uint64_t* kv_full = bars;                    // [stage] a stage's K and V landed
-    uint64_t* kv_empty = bars + kMaxStages;      // [stage] the MMAs reading a stage are done
-    uint64_t* s_full = bars + 2 * kMaxStages;    // [tile][2] S_j of the tile is in tensor memory
-    uint64_t* p_full = s_full + 4;               // [tile][2] P_j of the tile is in shared memory (128 arrivals)
+    uint64_t* kv_empty = bars + kTStages;        // [stage] the MMAs reading a stage are done
+    uint64_t* s_full = bars + 2 * kTStages;      // [tile][2] S_j of the tile is in tensor memory
+    uint64_t* p_full = s_full + 4;               // [tile][2] P_j of the tile is in tensor memory (128 arrivals)
     uint64_t* pv_done = p_full + 4;              // [tile][2] O += P_j V_j of the tile is complete
     uint64_t* q_ready = pv_done + 4;             // [tile] the tile's Q rows are in shared memory (128 arrivals)
     uint64_t* drain = q_ready + kTiles;          // every MMA issued is complete
-    static_assert(2 * kMaxStages + 12 + kTiles + 1 <= kNumBars, "barrier slots");
-    volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + Lay::kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + Lay::kOffMisc + 4);
+    volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(bp + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + kOffMisc + 4);
     volatile int* issued_count = abort_flag + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -350,7 +355,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const uint64_t dq0 = sdesc(base + kOffQ, 16, 1024);
             const uint64_t dk0 = sdesc(base + kOffRing, 16, 1024);
             const uint64_t dv0 = sdesc(base + kOffRing + kKBytes, kKVHalf, 1024);
-            const uint64_t dp0 = sdesc(base + kOffP, 16, 1024);
             bool ok = mbar_wait_bounded(&q_ready[mt], 0u);
             tc_fence_after();
             // S_j = Q K_j^T of the tile into its S buffer j % 2: two 64-dim halves x four 16-dim steps
@@ -396,14 +400,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t dp =
-                        dp0 + (uint64_t)(((uint32_t)t * kPTile) >> 4);
+                    // P_j over the first columns of S_j's buffer: 8 columns per 16 tokens (bf16: the
+                    // low part 32 columns on)
+                    const uint32_t pt = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
                     const uint32_t o = tmem + (uint32_t)t * kTileCols + kColO;
 #pragma unroll
                     for (int kt = 0; kt < 4; ++kt) {
                         const uint64_t vd = dv + (uint64_t)((kt * 2048) >> 4);
-                        umma(o, dp + (uint64_t)((kt * 32) >> 4), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
-                        if (kSplitP) umma(o, dp + (uint64_t)((kPBytes + kt * 32) >> 4), vd, kIdPV, 1u);
+                        umma_ts(o, pt + (uint32_t)(kt * 8), vd, kIdPV, (j > 0 || kt > 0) ? 1u : 0u);
+                        if (kSplitP) umma_ts(o, pt + 32u + (uint32_t)(kt * 8), vd, kIdPV, 1u);
                     }
                     umma_commit(&pv_done[t * 2 + (j & 1)]);
                 }
@@ -518,40 +523,29 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             if (move) m_run = mx;
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            // the P buffer was last read by O += P_{j-1} V_{j-1}
-            if (j >= 1 && !warp_wait(&t_pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
-                dead = true;
-                break;
-            }
-            const uint32_t pb = base + kOffP + (uint32_t)t * kPTile + (uint32_t)wt * 128u;
+            // P_j replaces S_j in its tensor-memory buffer (S_j is in registers; the next MMA to
+            // write the buffer, S_{j+2}, is issued after this P arrives and runs after O += P_j V_j)
             float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial row sums
+            uint32_t hi[32];
+            uint32_t lo[kSplitP ? 32 : 1];
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = ex2(fmaf(x[c8 * 8 + e], xs, -m_use));
-                    rs8[e] += p[e];
-                }
-                uint4 hi;
-                hi.x = Elem<T>::pack2(p[0], p[1]);
-                hi.y = Elem<T>::pack2(p[2], p[3]);
-                hi.z = Elem<T>::pack2(p[4], p[5]);
-                hi.w = Elem<T>::pack2(p[6], p[7]);
-                st_shared_v4(pb + (((uint32_t)c8 ^ sw) << 4), hi);
+            for (int c2 = 0; c2 < 32; ++c2) {
+                const float p0 = ex2(fmaf(x[2 * c2], xs, -m_use));
+                const float p1 = ex2(fmaf(x[2 * c2 + 1], xs, -m_use));
+                rs8[(2 * c2) & 7] += p0;
+                rs8[(2 * c2 + 1) & 7] += p1;
+                hi[c2] = Elem<T>::pack2(p0, p1);
                 if (kSplitP) {
-                    const float2 h0 = Elem<T>::to_float2(hi.x), h1 = Elem<T>::to_float2(hi.y);
-                    const float2 h2 = Elem<T>::to_float2(hi.z), h3 = Elem<T>::to_float2(hi.w);
-                    uint4 lo;
-                    lo.x = Elem<T>::pack2(p[0] - h0.x, p[1] - h0.y);
-                    lo.y = Elem<T>::pack2(p[2] - h1.x, p[3] - h1.y);
-                    lo.z = Elem<T>::pack2(p[4] - h2.x, p[5] - h2.y);
-                    lo.w = Elem<T>::pack2(p[6] - h3.x, p[7] - h3.y);
-                    st_shared_v4(pb + kPBytes + (((uint32_t)c8 ^ sw) << 4), lo);
+                    const float2 h = Elem<T>::to_float2(hi[c2]);
+                    lo[kSplitP ? c2 : 0] = Elem<T>::pack2(p0 - h.x, p1 - h.y);
                 }
             }
+            const uint32_t pcol = lane_addr + (uint32_t)(j & 1) * kStageTokens;
+            tmem_st32u(pcol, hi);
+            if (kSplitP) tmem_st32u(pcol + 32u, reinterpret_cast<const uint32_t (&)[32]>(lo));
             l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-            fence_proxy_async_smem();   // P (and the zeroed V rows) are read by the tensor cores
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            if (j == nst - 1) fence_proxy_async_smem();   // the zeroed V rows are read by the tensor cores
             tc_fence_before();
             mbar_arrive(&t_p_full[j & 1]);
         }
@@ -640,7 +634,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcLayout<T>::kSmem);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
@@ -650,7 +644,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const TcMaps& maps, int R_log2, cudaS
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, a.num_kv_heads, a.num_seqs);
     cfg.blockDim = dim3(kTThreads);
-    cfg.dynamicSmemBytes = TcLayout<T>::kSmem;
+    cfg.dynamicSmemBytes = kSmemTc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
