@@ -188,6 +188,35 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 lanes per instruction (the packed forms of the Blackwell FP32 pipe; each lane rounds
+// as the scalar instruction does) and a three-input maximum.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("{\n.reg .b64 ra, rb, rc;\nmov.b64 ra, {%1, %2};\nmov.b64 rb, {%3, %4};\nmov.b64 rc, {%5, %6};\n"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t d;
+    asm("{\n.reg .b64 ra, rb;\nmov.b64 ra, {%1, %2};\nmov.b64 rb, {%3, %4};\nadd.rn.f32x2 %0, ra, rb;\n}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -467,13 +496,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; ++c) x[c] = (t0 + c <= lim) ? x[c] : -INFINITY;
             }
-            // maximum as a tree (eight independent chains), not one 64-long dependency chain
+            // maximum as a tree (eight independent chains of three-input steps), not one 64-long
+            // dependency chain
             float m8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = x[e];
-#pragma unroll
-            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int e = 0; e < 8; ++e) {
+                float m = fmax3(x[e], x[e + 8], x[e + 16]);
+                m = fmax3(m, x[e + 24], x[e + 32]);
+                m = fmax3(m, x[e + 40], x[e + 48]);
+                m8[e] = fmaxf(m, x[e + 56]);
+            }
+            float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             if (sl > 0.f) {
                 mx *= sl;   // the scaled maximum (-inf stays)
             } else {
@@ -525,15 +558,16 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
             // P_j replaces S_j in its tensor-memory buffer (S_j is in registers; the next MMA to
             // write the buffer, S_{j+2}, is issued after this P arrives and runs after O += P_j V_j)
-            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight partial row sums
+            float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // eight partial row sums
             uint32_t hi[32];
             uint32_t lo[kSplitP ? 32 : 1];
+            const float2 xs2 = make_float2(xs, xs), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {
-                const float p0 = ex2(fmaf(x[2 * c2], xs, -m_use));
-                const float p1 = ex2(fmaf(x[2 * c2 + 1], xs, -m_use));
-                rs8[(2 * c2) & 7] += p0;
-                rs8[(2 * c2 + 1) & 7] += p1;
+                const float2 e2 = ffma2(make_float2(x[2 * c2], x[2 * c2 + 1]), xs2, nm2);
+                const float p0 = ex2(e2.x);
+                const float p1 = ex2(e2.y);
+                rs2[c2 & 3] = fadd2(rs2[c2 & 3], make_float2(p0, p1));
                 hi[c2] = Elem<T>::pack2(p0, p1);
                 if (kSplitP) {
                     const float2 h = Elem<T>::to_float2(hi[c2]);
@@ -543,7 +577,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const uint32_t pcol = lane_addr + (uint32_t)(j & 1) * kStageTokens;
             tmem_st32u(pcol, hi);
             if (kSplitP) tmem_st32u(pcol + 32u, reinterpret_cast<const uint32_t (&)[32]>(lo));
-            l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            l_run += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             if (j == nst - 1) fence_proxy_async_smem();   // the zeroed V rows are read by the tensor cores
             tc_fence_before();
