@@ -134,6 +134,16 @@ def test_large_and_small_scores(oracle, math):
     _check(oracle, wl, tokens_per_split=128, math=math)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.3])
+@pytest.mark.parametrize("math", ["auto"] + MATHS)
+def test_zero_and_negative_scale(oracle, scale, math):
+    """Scale 0 weighs every visible token equally; a negative scale reverses the order of the
+    scores, so the running maximum must be taken after scaling."""
+    wl = workloads.make_workload("scale_edge", context_lens=[300, 1, 1000, 64], num_q_heads=8, num_kv_heads=2,
+                                 block_size=16, seed=29, max_context=1024, scale=scale)
+    _check(oracle, wl, math=math)
+
+
 def test_side_stream(oracle):
     wl = workloads.make_workload("stream", context_lens=[33, 200], num_q_heads=12, num_kv_heads=2,
                                  block_size=16, seed=5, max_context=256)

@@ -108,6 +108,18 @@ def test_prefill_tiles_parity(oracle, G, lens, new, B, dtype, tiles):
     _run(oracle, wl, new, seed=G + B, tiles=tiles)
 
 
+@pytest.mark.parametrize("scale", [1.0, -0.25, 0.0])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("tiles", ["tc", "mma"])
+def test_prefill_peaky_zero_and_negative_scale(oracle, scale, dtype, tiles):
+    """Scale 1 makes the scores peaky (the exponent base moves in later stages and O is rescaled
+    in place), scale 0 weighs all visible tokens equally, a negative scale reverses their order."""
+    lens = [1500, 300]
+    wl = workloads.make_workload("pf_scale", context_lens=lens, num_q_heads=4, num_kv_heads=2, block_size=32,
+                                 dtype=dtype, seed=31, max_context=1536, scale=scale)
+    _run(oracle, wl, [200, 150], seed=32, tiles=tiles)
+
+
 @pytest.mark.parametrize("tiles", ["tc", "mma"])
 def test_prefill_counts_beyond_the_context_are_flagged(oracle, tiles):
     lens = [10, 40]
