@@ -1,5 +1,6 @@
 // Several new query tokens per sequence on the fifth-generation tensor cores: tcgen05.mma with
-// operands in shared memory and accumulators in tensor memory, tiles of 128 query rows.
+// Q, K and V in shared memory, the softmax weights P and the accumulators in tensor memory,
+// tiles of 128 query rows.
 //
 // What it computes (the same as the persistent kernel's several-token mode and the mma.sync
 // tiles): sequence s owns query rows q_start[s] .. q_start[s+1]-1, its n newest tokens, the last
