@@ -687,11 +687,11 @@ def run_multi_query(args, new_tokens: int = 2):
         for i in range(wl.layers):
             if fused:
                 pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
-                               workspace=ws, k_new=k_new[i], v_new=v_new[i])
+                               workspace=ws, k_new=k_new[i], v_new=v_new[i], num_ctas=args.num_ctas)
                 continue
             pa.cache_write(k_new[i], v_new[i], slots, wl.k_cache[i], wl.v_cache[i])
             pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
-                           workspace=ws)
+                           workspace=ws, num_ctas=args.num_ctas)
     step()
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
@@ -759,7 +759,7 @@ def run_config(args):
 
     def launch(i):
         pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], kcs[i], vcs[i], bt, lens, wl.scale, wl.num_kv_heads,
-                         out=outs[i], workspace=ws)
+                         out=outs[i], workspace=ws, num_ctas=args.num_ctas)
     for i in range(max(args.warmup, layers)):
         launch(i % layers)
     torch.cuda.synchronize()

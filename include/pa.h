@@ -91,7 +91,9 @@ typedef struct {
     int tokens_per_split;        /* split grids: 0 = library's choice; else a multiple of
                                     max(block_size, 64), at most 1024 * block_size */
     int math;                    /* a pa_math value */
-    int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once */
+    int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once
+                                    (16 fewer for the two-per-SM grid with early reads, so that a
+                                    chained launch's last CTAs find free slots) */
     int flags;                   /* PA_DECODE_NO_EARLY_READS: pa_decode_append reads nothing before
                                     the preceding kernel in the stream has finished */
     unsigned long long* timeline;/* persistent kernel trace, NULL = off; else device memory of

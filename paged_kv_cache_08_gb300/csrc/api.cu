@@ -113,9 +113,20 @@ int choose_path(int num_seqs, int group, int math, Path* path) {
 
 inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-int persist_ctas(int rows, int num_seqs, const pa_decode_options* opts) {
+// Launches with early reads run back to back, and the block scheduler hands a launch's CTAs
+// the slots of the previous launch's CTAs as they exit, in index order: with every slot of the
+// two-per-SM grid taken, the last CTAs start only as the previous launch's slowest ones finish,
+// with no time left to fill their ring before the dependency wait, and set the next launch's
+// end.  Leaving a few slots free lets them start earlier (measured on the 24-layer chain of 64
+// sequences: 304 CTAs 17.6 us per layer, 300 16.3, 288 16.1, 272 16.4; one launch alone changes
+// by about 1 %).
+constexpr int kEarlySpareSlots = 16;
+
+int persist_ctas(int rows, int num_seqs, bool early, const pa_decode_options* opts) {
     if (opts && opts->num_ctas > 0) return opts->num_ctas;
-    return persist_ctas_per_sm(rows, num_seqs) * sm_count();
+    const int per_sm = persist_ctas_per_sm(rows, num_seqs);
+    const int n = per_sm * sm_count();
+    return (early && per_sm == 2 && n > 4 * kEarlySpareSlots) ? n - kEarlySpareSlots : n;
 }
 
 // CTA count the workspace layout is sized for: the requested count, or the largest default
@@ -536,7 +547,8 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     cudaError_t e;
 
     if (path == kPathPersist) {
-        const int ctas = persist_ctas(multi ? max_q * group : group, num_seqs, opts);
+        const bool early = append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS));
+        const int ctas = persist_ctas(multi ? max_q * group : group, num_seqs, early, opts);
         const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
         const size_t pieces = persist_pieces(persist_layout_ctas(opts));
@@ -549,7 +561,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.timeline = opts ? opts->timeline : nullptr;
         a.k_new = k_new;
         a.v_new = v_new;
-        a.early = (append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS))) ? 1 : 0;
+        a.early = early ? 1 : 0;
         a.pf_k = opts ? opts->prefetch_k_cache : nullptr;
         a.pf_v = opts ? opts->prefetch_v_cache : nullptr;
         a.pf_own = (a.early && opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) ? 1 : 0;
