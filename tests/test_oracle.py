@@ -177,6 +177,38 @@ def pin_decode_vs_sdpa(o):
         np.testing.assert_allclose(got, want, rtol=0, atol=1e-12, err_msg=str(c))
 
 
+def pin_scales_vs_sdpa(o):
+    """The definition softmax(scale q.k) V holds for any real scale: 0 weighs every token equally,
+    a negative scale reverses the order of the scores, a scale of 1 on 128 dims makes the
+    weights peaky.  Decode and several query tokens per sequence against torch's fp64 attention
+    on the unpaged data."""
+    lens = [1, 30, 77, 16]
+    Hq, Hkv, D, B = 6, 2, 128, 16
+    G = Hq // Hkv
+    q, Kc, Vc, kc, vc, bt = _paged_problem(lens, Hq, Hkv, D, B, 55)
+    lt = np.array(lens, np.int32)
+    nq = [1, 7, 3, 16]
+    qm = _rand16((sum(nq), Hq, D), torch.Generator().manual_seed(56))
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    for scale in (0.0, -0.3, 1.0):
+        got = o.decode(q, kc, vc, bt, lt, scale, Hkv, False)
+        np.testing.assert_allclose(got, _sdpa_fp64(q, Kc, Vc, Hkv, scale), rtol=0, atol=1e-12,
+                                   err_msg=f"decode, scale {scale}")
+        got = o.multi_query(qm, kc, vc, bt, lt, qs, scale, Hkv, False)
+        for s, (L, n) in enumerate(zip(lens, nq)):
+            qq = qm[qs[s]:qs[s + 1]].to(torch.float64).permute(1, 0, 2)[None]
+            kk = Kc[s].to(torch.float64).repeat_interleave(G, dim=0)[None]
+            vv = Vc[s].to(torch.float64).repeat_interleave(G, dim=0)[None]
+            mask = torch.arange(L)[None, :] <= torch.arange(L - n, L)[:, None]
+            want = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)[0].permute(1, 0, 2)
+            assert np.max(np.abs(got[qs[s]:qs[s + 1]] - want.numpy())) < 1e-12, (scale, s)
+    # scale 0: every visible token weighs the same, so decode is the mean of the context's V rows
+    got = o.decode(q, kc, vc, bt, lt, 0.0, Hkv, False)
+    for s, L in enumerate(lens):
+        mean = Vc[s].to(torch.float64).mean(dim=1).repeat_interleave(G, dim=0).numpy()
+        np.testing.assert_allclose(got[s], mean, rtol=0, atol=1e-12)
+
+
 def pin_permutation_invariance(o):
     lens = [5, 23, 48, 1]
     Hq, Hkv, D, B = 4, 2, 128, 8
@@ -465,7 +497,7 @@ def pin_slotted_runs(o):
 
 
 PINS = [pin_f16_exhaustive, pin_bf16_exhaustive, pin_address_worked_example, pin_byte_ledger,
-        pin_decode_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write,
+        pin_decode_vs_sdpa, pin_scales_vs_sdpa, pin_permutation_invariance, pin_closed_forms, pin_cache_write,
         pin_copy_on_write_fork, pin_block_moves, pin_multi_query_vs_sdpa, pin_slotted_runs]
 
 
