@@ -391,6 +391,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             auto issue_s = [&](int j) -> bool {
                 const int st = j % kTStages;
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
+                // S_j overwrites the buffer from which O += P_{j-2} V_{j-2} reads its A operand; MMAs
+                // into different accumulators are not ordered by their issue order alone
+                if (j >= 2 && !mbar_wait_bounded(&pv_done[mt * 2 + (j & 1)], (uint32_t)((j - 2) >> 1) & 1u))
+                    return false;
                 tc_fence_after();
                 const uint64_t dk = dk0 + (uint64_t)(((uint32_t)st * kStage) >> 4);
                 {
