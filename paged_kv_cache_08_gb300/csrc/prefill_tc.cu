@@ -18,13 +18,17 @@
 //                     S_j  = Q K_j^T   (M 128, N 64, K 128: 8 MMAs, K-major operands in shared memory)
 //                     O   += P_j V_j   (M 128, N 128, K 64: 4 MMAs, P K-major in tensor memory, V
 //                                       N-major in shared memory)
-//                   with S double-buffered in tensor memory, so S_{j+1} of both tiles runs under
-//                   the softmax of S_j, and the two tiles share every K and V stage.
+//                   and the two tiles share every K and V stage.
+// Tensor memory per tile: one 64-column S buffer, 64 columns of P, a 128-column O.  The softmax
+// releases S_j as soon as its registers hold it (an mbarrier the issuer waits on), so S_{j+1} is
+// computed under the softmax of S_j; P_j goes to its own columns (fp16: two 32-column buffers
+// taken in turn; bf16: one buffer, the high part and the low part side by side), each reused only
+// after the PV product that last read it has completed (its mbarrier): MMAs into different
+// accumulators are not ordered by issue alone.
 // The softmax keeps a lazy exponent base per row (moved to the running max only when a score
 // exceeds it by more than 2^8, then O is rescaled in tensor memory), writes P = exp2(s - base)
-// over the first columns of S_j's tensor-memory buffer (bf16 with a high and a low part, two
-// MMAs), and at the end normalises its O row.  Every wait is bounded; tensor memory is freed on
-// every path.
+// (bf16 as a high and a low part, two MMAs) and at the end normalises its O row.  Every wait is
+// bounded; tensor memory is freed on every path.
 #include "pa_internal.cuh"
 
 #include <cuda.h>
@@ -57,8 +61,9 @@ constexpr uint32_t kOffBar = kOffRing + kTStages * kStage;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // tensor-memory address, abort flag, issued count
 constexpr size_t kSmemTc = 1024 /*alignment slack*/ + kOffMisc + 16;
 static_assert(kSmemTc <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
-constexpr uint32_t kTmemCols = 512;                          // per tile: S buffers at +0, +64, O at +128
+constexpr uint32_t kTmemCols = 512;                          // per tile: S at +0, P at +64, O at +128
 constexpr uint32_t kTileCols = 256;
+constexpr uint32_t kColP = 64;    // fp16: P buffers at +64, +96; bf16: one buffer, high +64, low +96
 constexpr uint32_t kColO = 128;
 constexpr float kLazyLog2 = 8.f;                             // exponent-base slack (weights below 2^8)
 
@@ -286,7 +291,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kOffBar);
     uint64_t* kv_full = bars;                    // [stage] a stage's K and V landed
     uint64_t* kv_empty = bars + kTStages;        // [stage] the MMAs reading a stage are done
-    uint64_t* s_full = bars + 2 * kTStages;      // [tile][2] S_j of the tile is in tensor memory
+    uint64_t* s_full = bars + 2 * kTStages;      // [tile] S_j of the tile is in tensor memory (phase j)
+    uint64_t* s_free = s_full + 2;               // [tile] the softmax holds S_j in registers (4 warps)
     uint64_t* p_full = s_full + 4;               // [tile][2] P_j of the tile is in tensor memory (128 arrivals)
     uint64_t* pv_done = p_full + 4;              // [tile][2] O += P_j V_j of the tile is complete
     uint64_t* q_ready = pv_done + 4;             // [tile] the tile's Q rows are in shared memory (128 arrivals)
@@ -329,7 +335,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             mbar_init(&kv_empty[i], ntiles);   // one commit per tile's issuer
         }
         for (int b = 0; b < 2 * kTiles; ++b) {
-            mbar_init(&s_full[b], 1);
+            if (b < kTiles) {
+                mbar_init(&s_full[b], 1);
+                mbar_init(&s_free[b], 4);
+            }
             mbar_init(&p_full[b], 128);
             mbar_init(&pv_done[b], 1);
         }
@@ -393,13 +402,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(j / kTStages) & 1u)) return false;
                 // S_j overwrites the buffer from which O += P_{j-2} V_{j-2} reads its A operand; MMAs
                 // into different accumulators are not ordered by their issue order alone
-                if (j >= 2 && !mbar_wait_bounded(&pv_done[mt * 2 + (j & 1)], (uint32_t)((j - 2) >> 1) & 1u))
-                    return false;
+                if (j >= 1 && !mbar_wait_bounded(&s_free[mt], (uint32_t)(j - 1) & 1u)) return false;
                 tc_fence_after();
                 const uint64_t dk = dk0 + (uint64_t)(((uint32_t)st * kStage) >> 4);
                 {
                     const int t = mt;
-                    const uint32_t d = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
+                    const uint32_t d = tmem + (uint32_t)t * kTileCols;
                     const uint64_t dq = dq0 + (uint64_t)(((uint32_t)t * kQTile) >> 4);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                         for (int kk = 0; kk < 4; ++kk)
                             umma(d, dq + (uint64_t)((h * kQHalf + kk * 32) >> 4), dk + (uint64_t)((h * kKVHalf + kk * 32) >> 4),
                                  kIdS, (h | kk) != 0 ? 1u : 0u);
-                    umma_commit(&s_full[t * 2 + (j & 1)]);
+                    umma_commit(&s_full[t]);
                 }
                 return true;
             };
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     tc_fence_after();
                     // P_j over the first columns of S_j's buffer: 8 columns per 16 tokens (bf16: the
                     // low part 32 columns on)
-                    const uint32_t pt = tmem + (uint32_t)t * kTileCols + (uint32_t)(j & 1) * kStageTokens;
+                    const uint32_t pt = tmem + (uint32_t)t * kTileCols + kColP + (kSplitP ? 0u : (uint32_t)(j & 1) * 32u);
                     const uint32_t o = tmem + (uint32_t)t * kTileCols + kColO;
 #pragma unroll
                     for (int kt = 0; kt < 4; ++kt) {
@@ -461,7 +469,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const int lim = row_ok ? L - qs.n + r / G : -1;   // newest position the row attends to
         const uint32_t lane_addr = tmem + (uint32_t)t * kTileCols + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t sw = (uint32_t)(wt & 7);           // 128-byte swizzle phase of this row
-        uint64_t* t_s_full = s_full + 2 * t;
+        uint64_t* t_s_full = s_full + t;
         uint64_t* t_p_full = p_full + 2 * t;
         uint64_t* t_pv_done = pv_done + 2 * t;
         // Q row into the K-major operand tile (two 64-dim halves); rows past the segment are zero
@@ -487,13 +495,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
         float m_run = -INFINITY, l_run = 0.f;
         bool dead = false;
         for (int j = 0; j < nst && !dead; ++j) {
-            if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&t_s_full[j & 1], (uint32_t)(j >> 1) & 1u)) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(t_s_full, (uint32_t)j & 1u)) {
                 dead = true;
                 break;
             }
             tc_fence_after();
             float x[64];
-            tmem_ld64(lane_addr + (uint32_t)(j & 1) * kStageTokens, x);
+            tmem_ld64(lane_addr, x);
+            // S_j is in registers: the buffer may take S_{j+1}
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[t]);
             const int t0 = j * kStageTokens;
             // raw scores; the scale (log2 units) enters the exponent's FMA.  Stages every row of the
             // warp sees whole skip the causal mask.
@@ -561,8 +573,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             if (move) m_run = mx;
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            // P_j replaces S_j in its tensor-memory buffer (S_j is in registers; the next MMA to
-            // write the buffer, S_{j+2}, is issued after this P arrives and runs after O += P_j V_j)
+            // P_j into its tensor-memory P buffer (fp16: two, alternating; bf16: one, high and low)
             float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // eight partial row sums
             uint32_t hi[32];
             uint32_t lo[kSplitP ? 32 : 1];
@@ -579,7 +590,16 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     lo[kSplitP ? c2 : 0] = Elem<T>::pack2(p0 - h.x, p1 - h.y);
                 }
             }
-            const uint32_t pcol = lane_addr + (uint32_t)(j & 1) * kStageTokens;
+            // the P buffer was last read by O += P_{j-k} V_{j-k}, k = the number of buffers
+            {
+                const int k = kSplitP ? 1 : 2;
+                if (j >= k && !warp_wait(&t_pv_done[(j - k) & 1], (uint32_t)((j - k) >> 1) & 1u)) {
+                    dead = true;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const uint32_t pcol = lane_addr + kColP + (kSplitP ? 0u : (uint32_t)(j & 1) * 32u);
             tmem_st32u(pcol, hi);
             if (kSplitP) tmem_st32u(pcol + 32u, reinterpret_cast<const uint32_t (&)[32]>(lo));
             l_run += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
