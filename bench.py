@@ -176,12 +176,9 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, prefetch: bool = False,
-                 prefetch_own: bool = False):
-        self.prefetch_own = prefetch_own
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0):
         self.fused = fused
         self.num_ctas = num_ctas
-        self.prefetch = prefetch
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
         self.wl = wl
@@ -211,18 +208,15 @@ class Step:
             pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
         if ev_pair is not None:
             ev_pair[0].record()
-        # the next layer's caches share this layer's block tables: their blocks are prefetched into
-        # L2 once this layer's copies are issued (the last layer of the step prefetches nothing)
-        nxt = (wl.k_cache[i + 1], wl.v_cache[i + 1]) if self.prefetch and i + 1 < wl.layers else None
         if self.fused:
+            # early reads: the kernel before each launch is the previous layer's, which writes
+            # other pools and never the tables or lengths
             pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
                              wl.scale, wl.num_kv_heads, out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
-                             prefetch=nxt, prefetch_own=self.prefetch_own)
+                             early_reads=True)
         else:
             pa.decode(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens, wl.scale, wl.num_kv_heads,
-                      out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas,
-                      prefetch=nxt if self.pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads) == 2
-                      else None)
+                      out=self.out[i], workspace=self.ws, num_ctas=self.num_ctas)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -292,7 +286,7 @@ def run_ours(args):
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, prefetch=args.prefetch, prefetch_own=args.prefetch_own)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -395,8 +389,7 @@ def run_e2e(st, wl, args, step_bytes):
     input buffer), runs the 24 layers and copies the outputs back (one copy).  Two buffer sets
     (and two captured graphs) let step k + 1's input copy and step k - 1's output copy run on
     copy streams while step k's kernels run; the timed region spans all copies of all steps."""
-    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas, prefetch=st.prefetch,
-               prefetch_own=st.prefetch_own)
+    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas)
     st2.capture()
     sets = [st, st2]
     host_in = st.inbuf.cpu().pin_memory()
@@ -687,7 +680,8 @@ def run_multi_query(args, new_tokens: int = 2):
         for i in range(wl.layers):
             if fused:
                 pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
-                               workspace=ws, k_new=k_new[i], v_new=v_new[i], num_ctas=args.num_ctas)
+                               workspace=ws, k_new=k_new[i], v_new=v_new[i], num_ctas=args.num_ctas,
+                               early_reads=True)
                 continue
             pa.cache_write(k_new[i], v_new[i], slots, wl.k_cache[i], wl.v_cache[i])
             pa.multi_query(q, wl.k_cache[i], wl.v_cache[i], bt, lens, qs, wl.scale, Hkv, max_q, out=outs[i],
@@ -934,10 +928,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
-    ap.add_argument("--prefetch", action="store_true",
-                    help="each layer asks the L2 to prefetch the next layer's blocks (slower on this step)")
-    ap.add_argument("--prefetch-own", action="store_true",
-                    help="each layer prefetches its own chunks beyond the copy pipeline before its dependency wait")
     ap.add_argument("--op", choices=["decode", "config", "copy_blocks", "swap", "multi_query", "prefill", "runs"],
                     default="decode",
                     help="decode step (default), one layer of another config (--config), or the block-copy, swap, "

@@ -45,6 +45,10 @@
  *       context_lens     int32 [num_seqs]; the length counts the newest token
  *       slot_mapping     int64 [num_tokens]; slot = physical_block * block_size + offset
  *   - Query head h attends with kv head h / (num_q_heads / num_kv_heads).
+ *   - The library looks up, once per device, the device addresses of its own static
+ *     device arrays (the status word, pa_decode_static's scratch) and keeps them for the
+ *     life of the process: resetting a device (cudaDeviceReset, or any reset of its
+ *     primary context) while the library is in use is not supported.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -92,10 +96,12 @@ typedef struct {
                                     max(block_size, 64), at most 1024 * block_size */
     int math;                    /* a pa_math value */
     int num_ctas;                /* persistent kernel: 0 = as many CTAs as fit on the GPU at once
-                                    (16 fewer for the two-per-SM grid with early reads, so that a
-                                    chained launch's last CTAs find free slots) */
-    int flags;                   /* PA_DECODE_NO_EARLY_READS: pa_decode_append reads nothing before
-                                    the preceding kernel in the stream has finished */
+                                    (16 fewer for the two-per-SM grid with PA_DECODE_EARLY_READS, so
+                                    that a chained launch's last CTAs find free slots) */
+    int flags;                   /* PA_DECODE_EARLY_READS: pa_decode_append / pa_multi_query_append may
+                                    read lengths, tables and cached rows before the preceding kernel
+                                    in the stream has finished (see pa_decode_append); off by
+                                    default.  PA_PREFILL_MMA_SYNC: see pa_multi_query. */
     unsigned long long* timeline;/* persistent kernel trace, NULL = off; else device memory of
                                     num_ctas * 16 uint64 per CTA: global-timer ns at 0 entry,
                                     1 dependency wait passed, 2 prefix sums done, 3 first block ids
@@ -105,13 +111,6 @@ typedef struct {
                                     waited for a free stage, 12 cut segments merged, 13 segment
                                     pieces finished, 14 chunks streamed, 15 SM id.  Entries of CTAs
                                     that own no chunk stay as set. */
-    /* Persistent kernel: another pool pair of the caches' shape that this call's block tables
-     * and lengths also address (the next layer's caches), or both NULL.  Once the last chunk of
-     * a CTA's share has landed, the CTA asks the L2 to prefetch the same blocks of these pools,
-     * so that a call on them that follows finds its rows there.  Read-only hints; 16-byte
-     * aligned. */
-    const void* prefetch_k_cache;
-    const void* prefetch_v_cache;
 } pa_decode_options;
 
 /* ------------------------------------------------------------------------------------
@@ -146,7 +145,7 @@ int pa_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
  * (else which bytes land is unspecified).  Asynchronous on `stream`; pinned host memory
  * must stay allocated, and host code must not touch it, until the copy has completed.
  * A pa_decode_append launched right after it that reads the destination pool must not
- * use early reads (PA_DECODE_NO_EARLY_READS).
+ * ask for early reads (PA_DECODE_EARLY_READS), which could read the rows before they land.
  * head_dim a positive multiple of 8; pools 16-byte aligned.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
  * ---------------------------------------------------------------------------------- */
@@ -212,10 +211,7 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
                      int num_seqs, int num_q_heads, int head_dim, int block_size, int num_blocks,
                      int max_blocks_per_seq, int dtype, void* stream);
 
-#define PA_DECODE_NO_EARLY_READS 1
-/* pa_decode_append with early reads: before waiting for the preceding kernel, each CTA also
- * asks the L2 to prefetch the blocks of its chunks that do not fit its copy pipeline. */
-#define PA_DECODE_PREFETCH_OWN 2
+#define PA_DECODE_EARLY_READS 1
 /* pa_multi_query beyond 16 query rows per (sequence, kv head): the mma.sync tiles of 64 rows
  * instead of the default tcgen05 tiles of 128 rows (same results within the parity tolerance). */
 #define PA_PREFILL_MMA_SYNC 4
@@ -230,12 +226,15 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
  * k_new, v_new: [num_seqs][num_kv_heads][head_dim].  Workspace as for pa_decode (same
  * size query, persistent kind).  Supported: the persistent kernel's shapes
  * (pa_decode_kernel_kind == PA_KERNEL_PERSISTENT_MMA); else PA_ERR_UNSUPPORTED.
- * Early reads: unless opts->flags has PA_DECODE_NO_EARLY_READS, the kernel may read
+ * Early reads (opt-in): with PA_DECODE_EARLY_READS in opts->flags the kernel may read
  * context_lens, block_tables and the cached rows of earlier tokens before the preceding
  * kernel in the stream has finished (so that, launched back to back, one layer's start
  * overlaps the previous layer's end); q, k_new and v_new are read, and out, the new slots
- * and the workspace written, only after it has finished.  The caller guarantees that the
- * preceding kernel does not write the caches, the tables or the lengths.
+ * and the workspace written, only after it has finished.  The caller then guarantees that
+ * the preceding kernel writes none of the caches, the tables or the lengths: a decode step
+ * whose preceding kernel produces q and the new K/V qualifies; a pa_copy_blocks or
+ * pa_gather_runs into the same pool (copy-on-write, defragmentation) does not.  Without the
+ * flag nothing is read before the preceding kernel has finished.
  * ---------------------------------------------------------------------------------- */
 int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
                      void* k_cache, void* v_cache,
@@ -261,7 +260,7 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  * PA_DEV_BAD_CONTEXT.
  * Kernels: while max_q_per_seq x (num_q_heads / num_kv_heads) <= 16 (and num_seqs <= 1024)
  * the persistent kernel, with a workspace as for pa_decode (same size query, persistent kind;
- * opts: num_ctas, timeline and the next-layer prefetch apply); beyond that, tcgen05 tiles of
+ * opts: num_ctas and timeline apply); beyond that, tcgen05 tiles of
  * 128 query rows per (sequence, kv head) with accumulators in tensor memory, one CTA each, no
  * workspace (chunked prefill; at most 65535 sequences and kv heads); opts->flags with
  * PA_PREFILL_MMA_SYNC selects mma.sync tiles of 64 rows instead.
@@ -287,10 +286,10 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
  * rows as q's.  A slot whose block id lies outside [0, num_blocks) is not written.
  * Supported: the persistent kernel's shapes (max_q_per_seq x (num_q_heads / num_kv_heads)
  * <= 16); beyond that PA_ERR_UNSUPPORTED (write the rows with pa_cache_write, then call
- * pa_multi_query).  Early reads as for pa_decode_append: unless opts->flags has
- * PA_DECODE_NO_EARLY_READS, context_lens, block_tables, query_start and the cached rows of
- * earlier tokens may be read before the preceding kernel in the stream has finished; q,
- * k_new and v_new are read, and out, the new slots and the workspace written, only after it.
+ * pa_multi_query).  Early reads as for pa_decode_append (opt-in, PA_DECODE_EARLY_READS):
+ * context_lens, block_tables, query_start and the cached rows of earlier tokens may then be
+ * read before the preceding kernel in the stream has finished; q, k_new and v_new are read,
+ * and out, the new slots and the workspace written, only after it.
  * Returns the codes of pa_decode.
  * ---------------------------------------------------------------------------------- */
 int pa_multi_query_append(void* out, const void* q, const void* k_new, const void* v_new,

@@ -51,19 +51,11 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
 
 
 def _opts(tokens_per_split: int, math: str, num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
-          flags: int = 0, prefetch=None, like: Optional[torch.Tensor] = None) -> DecodeOptions:
+          flags: int = 0) -> DecodeOptions:
     if math not in MATH:
         raise ValueError(f"math must be one of {sorted(MATH)}")
-    pk = pv = None
-    if prefetch is not None:
-        pk_t, pv_t = prefetch
-        for n, t in (("prefetch k", pk_t), ("prefetch v", pv_t)):
-            _need_cuda(n, t, like.dtype)
-            if t.shape != like.shape:
-                raise ValueError(f"{n} pool must have the caches' shape")
-        pk, pv = pk_t.data_ptr(), pv_t.data_ptr()
     return DecodeOptions(int(tokens_per_split), MATH[math], int(num_ctas), int(flags),
-                         timeline.data_ptr() if timeline is not None else None, pk, pv)
+                         timeline.data_ptr() if timeline is not None else None)
 
 
 def cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
@@ -161,13 +153,11 @@ def _workspace(device: torch.device, nbytes: int, kind: int, num_ctas: int) -> O
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, scale: float, num_kv_heads: int, out: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None, tokens_per_split: int = 0, math: str = "auto",
-           num_ctas: int = 0, timeline: Optional[torch.Tensor] = None, prefetch=None,
+           num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Paged decode attention.  q: [S, Hq, D]; caches [NB, Hkv, B, D]; block_tables int32
     [S, max_blocks]; context_lens int32 [S].  Returns out [S, Hq, D] in q's dtype.
-    ``timeline``: optional int64 CUDA tensor [num_ctas, 16] receiving the persistent kernel's trace.
-    ``prefetch``: optional (k, v) pools of the caches' shape (the next layer's) whose blocks of
-    this call the persistent kernel asks the L2 to prefetch."""
+    ``timeline``: optional int64 CUDA tensor [num_ctas, 16] receiving the persistent kernel's trace."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -188,7 +178,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(tokens_per_split, math, num_ctas, timeline, prefetch=prefetch, like=k_cache)
+    o = _opts(tokens_per_split, math, num_ctas, timeline)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))
@@ -206,12 +196,12 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
 def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                   num_kv_heads: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                  num_ctas: int = 0, early_reads: bool = True, timeline: Optional[torch.Tensor] = None,
-                  prefetch=None, prefetch_own: bool = False,
+                  num_ctas: int = 0, early_reads: bool = False, timeline: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Cache write of each sequence's newest token (position context_lens[s] - 1) and decode
-    attention, in one launch.  k_new, v_new: [S, Hkv, D].  See pa_decode_append in include/pa.h
-    for the early-read contract (disable with early_reads=False); ``prefetch`` as for decode."""
+    attention, in one launch.  k_new, v_new: [S, Hkv, D].  ``early_reads=True`` opts in to the
+    early-read contract of pa_decode_append (include/pa.h): the preceding kernel in the stream
+    must not write the caches, the tables or the lengths."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
         raise TypeError("q must be float16 or bfloat16")
@@ -232,8 +222,7 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
         out = torch.empty_like(q)
     else:
         _need_cuda("out", out, q.dtype)
-    flags = (0 if early_reads else _native.NO_EARLY_READS) | (_native.PREFETCH_OWN if prefetch_own else 0)
-    o = _opts(0, "mma", num_ctas, timeline, flags, prefetch=prefetch, like=k_cache)
+    o = _opts(0, "mma", num_ctas, timeline, _native.EARLY_READS if early_reads else 0)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         kind = lib().pa_decode_kernel_kind(S, Hq, Hkv, ctypes.byref(o))
@@ -253,14 +242,13 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                 max_q: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 num_ctas: int = 0, timeline: Optional[torch.Tensor] = None,
                 k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
-                early_reads: bool = True, prefetch=None, prefetch_own: bool = False, tiles: str = "tc",
+                early_reads: bool = False, tiles: str = "tc",
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Several new query tokens per sequence attending causally over the paged cache.
     q: [T, Hq, D]; sequence s owns rows query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its
     newest tokens; at most ``max_q`` per sequence.  See pa_multi_query in include/pa.h.
     With k_new / v_new ([T, Hkv, D], rows as q's) the same launch first writes them into the
-    slots of their positions (pa_multi_query_append; early reads, prefetch and prefetch_own as
-    for decode_append).  ``tiles``: beyond 16 query rows per (sequence, kv head), "tc" runs the
+    slots of their positions (pa_multi_query_append; ``early_reads`` as for decode_append).  ``tiles``: beyond 16 query rows per (sequence, kv head), "tc" runs the
     tcgen05 tiles of 128 rows, "mma" the mma.sync tiles of 64 rows."""
     _need_cuda("q", q)
     if q.dtype not in _DTYPE:
@@ -290,13 +278,11 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
             _need_cuda(n, t, q.dtype)
         if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape:
             raise ValueError("k_new / v_new must be [T, Hkv, D]")
-        flags = (0 if early_reads else _native.NO_EARLY_READS) | (_native.PREFETCH_OWN if prefetch_own else 0)
-        o = _opts(0, "mma", num_ctas, timeline, flags, prefetch=prefetch, like=k_cache)
+        o = _opts(0, "mma", num_ctas, timeline, _native.EARLY_READS if early_reads else 0)
     else:
         if tiles not in ("tc", "mma"):
             raise ValueError('tiles must be "tc" or "mma"')
-        o = _opts(0, "mma", num_ctas, timeline, _native.PREFILL_MMA_SYNC if tiles == "mma" else 0,
-                  prefetch=prefetch, like=k_cache)
+        o = _opts(0, "mma", num_ctas, timeline, _native.PREFILL_MMA_SYNC if tiles == "mma" else 0)
     need = int(lib().pa_decode_workspace_size_ex(S, Hq, Hkv, D, B, max_blocks, ctypes.byref(o)))
     if workspace is None:
         workspace = _workspace(q.device, need, 2, int(num_ctas))

@@ -23,7 +23,7 @@ c_u32p = ctypes.POINTER(ctypes.c_uint32)
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("tokens_per_split", c_int), ("math", c_int), ("num_ctas", c_int), ("flags", c_int),
-                ("timeline", c_vp), ("prefetch_k_cache", c_vp), ("prefetch_v_cache", c_vp)]
+                ("timeline", c_vp)]
 
 
 PA_OK = 0
@@ -32,8 +32,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "P
           -7: "PA_ERR_WORKSPACE", -8: "PA_ERR_SCRATCH_LIMIT"}
 DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
-NO_EARLY_READS = 1
-PREFETCH_OWN = 2
+EARLY_READS = 1
 PREFILL_MMA_SYNC = 4
 
 _SIGNATURES = {

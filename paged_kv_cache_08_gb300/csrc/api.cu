@@ -472,9 +472,6 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (opts && (opts->math < PA_MATH_AUTO || opts->math > PA_MATH_MMA_SPLIT || opts->num_ctas < 0))
         return PA_ERR_INVALID_ARG;
-    if (opts && (!aligned16(opts->prefetch_k_cache) || !aligned16(opts->prefetch_v_cache) ||
-                 (opts->prefetch_k_cache == nullptr) != (opts->prefetch_v_cache == nullptr)))
-        return PA_ERR_INVALID_ARG;
     if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !block_tables || !context_lens || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
@@ -547,7 +544,7 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
     cudaError_t e;
 
     if (path == kPathPersist) {
-        const bool early = append && !(opts && (opts->flags & PA_DECODE_NO_EARLY_READS));
+        const bool early = append && opts && (opts->flags & PA_DECODE_EARLY_READS);
         const int ctas = persist_ctas(multi ? max_q * group : group, num_seqs, early, opts);
         const size_t need = persist_workspace_bytes(num_seqs, num_kv_heads, group, persist_layout_ctas(opts));
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
@@ -562,9 +559,6 @@ static int decode_impl(void* out, const void* q, const void* k_new, const void* 
         a.k_new = k_new;
         a.v_new = v_new;
         a.early = early ? 1 : 0;
-        a.pf_k = opts ? opts->prefetch_k_cache : nullptr;
-        a.pf_v = opts ? opts->prefetch_v_cache : nullptr;
-        a.pf_own = (a.early && opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) ? 1 : 0;
         a.q_start = q_start;
         a.max_q = multi ? max_q : 1;
         a.q_rows = q_rows;
@@ -624,7 +618,6 @@ int pa_multi_query(void* out, const void* q, const void* k_cache, const void* v_
                    void* stream, const pa_decode_options* opts) {
     if (num_q_tokens < 0 || !query_start) return PA_ERR_INVALID_ARG;
     if (num_q_tokens == 0) return num_seqs >= 0 ? PA_OK : PA_ERR_INVALID_ARG;
-    if (opts && (opts->flags & PA_DECODE_PREFETCH_OWN)) return PA_ERR_INVALID_ARG;
     return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, dtype, workspace,
                        workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);

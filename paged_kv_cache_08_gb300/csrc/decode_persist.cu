@@ -187,10 +187,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -446,29 +442,6 @@ template <bool kMulti>
 __device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int L) {
     if (kMulti && span_of<kMulti>(a, s, L).n == 0) return 0;
     return (L + kStageTokens - 1) / kStageTokens;
-}
-
-// L2 prefetch of the blocks of chunks [g0, g1) of a range starting at b_c, in the pools (pk, pv):
-// lane j of a warp takes chunk g0 + j + 32 m; each (block, kv head) run of rows is one prefetch
-// per pool.
-template <bool kMulti>
-__device__ __forceinline__ void prefetch_range(const DecodeArgs& a, const int32_t* P, const int32_t* Lc, int S,
-                                               int Hkv, long long b_c, long long g0, long long g1, int R_log2,
-                                               int lane, const void* pk, const void* pv) {
-    const int B = a.block_size;
-    const uint32_t run = (uint32_t)(1 << R_log2) * kHeadDim * 2u;
-    for (long long gbase = g0; gbase < g1; gbase += 32) {
-        const ChunkDesc d = describe<kMulti>(a, P, Lc, S, Hkv, b_c, g1, gbase + lane);
-        const int within = (B > kStageTokens) ? (d.t0 % B) : 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (e < d.nblk && d.ids[e] >= 0) {
-                const size_t off = (((size_t)d.ids[e] * Hkv + d.h) * B + within) * kHeadDim * 2;
-                prefetch_l2(static_cast<const char*>(pk) + off, run);
-                prefetch_l2(static_cast<const char*>(pv) + off, run);
-            }
-        }
-    }
 }
 
 // Zero output rows of the empty sequences this CTA is responsible for (s = c, c + grid, ...).
@@ -798,7 +771,6 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
     uint64_t* empty = full + kStages;
     uint64_t* qbar = empty + kStages;   // q rows of the first kStages chunks (fetched after the dependency wait)
     uint64_t* pdone = qbar + 1;         // the consumers have published the piece the epilogue warp finishes
-    uint64_t* landed = qbar + 2;        // the range's last chunk has landed (the epilogue's prefetch cue)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Lay::kFlags);
     volatile int* issued_count = abort_flag + 1;
     volatile int* last_flag = abort_flag + 2;
@@ -844,7 +816,6 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
         }
         mbar_init(qbar, 1);
         mbar_init(pdone, kConsumerThreads);
-        mbar_init(landed, 1);
         *abort_flag = 0;
         *issued_count = 0;
         *last_flag = 0;
@@ -901,13 +872,8 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
         bool deps_done = false;
         // After the preceding kernel has finished (early mode), fetch the q rows of the first
         // stages onto their own barrier: they may be that kernel's output.
-        auto prefetch_chunks = [&](const void* pk, const void* pv, long long g0, long long g1) {
-            prefetch_range<kMulti>(a, P, Lc, S, Hkv, b_c, g0, g1, R_log2, lane, pk, pv);
-        };
         auto dependency_point = [&](int issued) {
             if (a.early) {
-                // the rest of the range will find its rows in L2 once stages free up
-                if (a.pf_own && b_c + kStages < b_e) prefetch_chunks(a.k_cache, a.v_cache, b_c + kStages, b_e);
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
@@ -1101,15 +1067,6 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
                 }
             }
         }
-        if (a.pf_k != nullptr) {
-            // Once the range's last chunk has landed, the memory system has room while this layer's
-            // tail runs: ask the L2 to prefetch the same chunks' blocks of the prefetch pools (the
-            // next layer), which that layer's copies will then find there.
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait_bounded(landed, 0u);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok && *abort_flag == 0) prefetch_range<kMulti>(a, P, Lc, S, Hkv, b_c, b_c, b_e, R_log2, lane, a.pf_k, a.pf_v);
-        }
     } else {
         // ================= consumer warps =================
         constexpr int kNT = kG16 ? 2 : 1;   // 8-row column tiles of the GQA group
@@ -1157,7 +1114,6 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
                 dead = true;
             }
             __syncwarp();
-            if (g == b_e - 1 && tid == 0) mbar_arrive(landed);
             if (a.timeline && tid == 0) {
                 const unsigned long long now = global_timer_ns();
                 wait_full_ns += now - tw;

@@ -73,9 +73,6 @@ struct DecodeArgs {
     const void* k_new;        // append mode: the new token's K and V rows [S][Hkv][D], written at
     const void* v_new;        //   position context_lens[s] - 1 before attention reads it; null = off
     int early;                // K/V of the first stages may be fetched before the preceding kernel ends
-    const void* pf_k;         // optional: pools whose blocks of this call's chunks are prefetched into L2
-    const void* pf_v;
-    int pf_own;               // early mode: prefetch this range's chunks beyond the ring into L2 before the wait
     int cut_unit, cut_seg;    // persistent path: weights of a chunk and of a segment end in the cut of the
                               // chunk list into CTA ranges (cut_seg == 0: equal chunk counts)
     const int32_t* q_start;   // several query tokens per sequence: rows q_start[s] .. q_start[s+1]-1 of q and

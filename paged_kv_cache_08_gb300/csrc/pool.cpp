@@ -1,8 +1,10 @@
 // Host block pool: the untimed bookkeeping that produces block tables and slot mappings.
 //
-// Free set: a bitmap of 32-bit words, bit = 1 when the block is free, lowest free block
-// first via count-trailing-zeros -- the allocator of "端侧 SLM 显存保活术：在 4GB 内存板卡上
-// 实现轻量 PagedAttention 与 KV 缓存分块", section "嵌入式轻量 Block 分配器设计".
+// Free set: a binary min-heap of the free block ids, so that an allocation takes the lowest
+// free id (the order the free-bitmap allocator of "端侧 SLM 显存保活术：在 4GB 内存板卡上实现
+// 轻量 PagedAttention 与 KV 缓存分块", section "嵌入式轻量 Block 分配器设计", hands blocks out in,
+// kept here as a requirement: the worked examples number their blocks that way) in O(log n),
+// and a release pushes the id back.  A block is free exactly when its reference count is 0.
 // Reference counts: shared prefix blocks ("共享前缀块（Prefix Caching）" on the same page)
 // and copy-on-write on append ("显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §四).
 // Token append and release follow the lifecycle diagram of that page's §三.
@@ -13,29 +15,33 @@
 #include <cstdlib>
 #include <new>
 #include <algorithm>
+#include <functional>
 #include <vector>
 
 #include "../../include/pa.h"
 
 struct pa_pool {
     int num_blocks;
-    std::vector<uint32_t> free_bits;  // bit set = free
+    std::vector<int32_t> free_heap;   // free ids, a min-heap under std::greater (front = lowest)
     std::vector<int32_t> refs;        // 0 = free
-    int num_free;
 };
 
 namespace {
 
 inline bool valid_id(const pa_pool* p, int id) { return p && id >= 0 && id < p->num_blocks; }
 
-inline void mark_used(pa_pool* p, int id) {
-    p->free_bits[id >> 5] &= ~(1u << (id & 31));
-    --p->num_free;
+// The lowest free id, taken out of the free set; -1 when the set is empty.
+inline int take_lowest_free(pa_pool* p) {
+    if (p->free_heap.empty()) return -1;
+    std::pop_heap(p->free_heap.begin(), p->free_heap.end(), std::greater<int32_t>());
+    const int id = p->free_heap.back();
+    p->free_heap.pop_back();
+    return id;
 }
 
-inline void mark_free(pa_pool* p, int id) {
-    p->free_bits[id >> 5] |= (1u << (id & 31));
-    ++p->num_free;
+inline void give_back(pa_pool* p, int id) {
+    p->free_heap.push_back(id);
+    std::push_heap(p->free_heap.begin(), p->free_heap.end(), std::greater<int32_t>());
 }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -50,11 +56,10 @@ pa_pool* pa_pool_create(int num_blocks) {
     if (!p) return nullptr;
     try {
         p->num_blocks = num_blocks;
-        p->free_bits.assign((size_t)ceil_div(num_blocks, 32), 0xFFFFFFFFu);
-        int tail = num_blocks & 31;  // bits past the last block never read as free
-        if (tail) p->free_bits.back() = (1u << tail) - 1u;
+        // 0, 1, ..., n-1 in increasing order is already a min-heap
+        p->free_heap.resize((size_t)num_blocks);
+        for (int i = 0; i < num_blocks; ++i) p->free_heap[(size_t)i] = i;
         p->refs.assign((size_t)num_blocks, 0);
-        p->num_free = num_blocks;
     } catch (...) {
         delete p;
         return nullptr;
@@ -66,17 +71,10 @@ void pa_pool_destroy(pa_pool* pool) { delete pool; }
 
 int pa_pool_alloc(pa_pool* pool) {
     if (!pool) return PA_ERR_INVALID_ARG;
-    const size_t words = pool->free_bits.size();
-    for (size_t w = 0; w < words; ++w) {
-        uint32_t bits = pool->free_bits[w];
-        if (bits) {
-            int id = (int)(w * 32) + __builtin_ctz(bits);
-            mark_used(pool, id);
-            pool->refs[id] = 1;
-            return id;
-        }
-    }
-    return PA_ERR_POOL_EXHAUSTED;
+    const int id = take_lowest_free(pool);
+    if (id < 0) return PA_ERR_POOL_EXHAUSTED;
+    pool->refs[id] = 1;
+    return id;
 }
 
 int pa_pool_incref(pa_pool* pool, int block_id) {
@@ -87,7 +85,7 @@ int pa_pool_incref(pa_pool* pool, int block_id) {
 int pa_pool_decref(pa_pool* pool, int block_id) {
     if (!valid_id(pool, block_id) || pool->refs[block_id] <= 0) return PA_ERR_BOUNDS;
     int r = --pool->refs[block_id];
-    if (r == 0) mark_free(pool, block_id);
+    if (r == 0) give_back(pool, block_id);
     return r;
 }
 
@@ -96,7 +94,7 @@ int pa_pool_refcount(const pa_pool* pool, int block_id) {
     return pool->refs[block_id];
 }
 
-int pa_pool_num_free(const pa_pool* pool) { return pool ? pool->num_free : PA_ERR_INVALID_ARG; }
+int pa_pool_num_free(const pa_pool* pool) { return pool ? (int)pool->free_heap.size() : PA_ERR_INVALID_ARG; }
 
 int pa_pool_num_blocks(const pa_pool* pool) { return pool ? pool->num_blocks : PA_ERR_INVALID_ARG; }
 
@@ -109,7 +107,7 @@ int pa_pool_assign(pa_pool* pool, int32_t* table_row, int max_blocks, int contex
     if (need > max_blocks || shared_blocks > need) return PA_ERR_BOUNDS;
     for (int i = 0; i < shared_blocks; ++i)
         if (!valid_id(pool, shared_row[i]) || pool->refs[shared_row[i]] <= 0) return PA_ERR_BOUNDS;
-    if (need - shared_blocks > pool->num_free) return PA_ERR_POOL_EXHAUSTED;
+    if (need - shared_blocks > (int)pool->free_heap.size()) return PA_ERR_POOL_EXHAUSTED;
     for (int i = 0; i < shared_blocks; ++i) {
         table_row[i] = shared_row[i];
         ++pool->refs[shared_row[i]];
@@ -167,7 +165,7 @@ int pa_pool_move_blocks(pa_pool* from, pa_pool* to, int32_t* table_row, int n, i
     if (!from || !to || n < 0 || (n > 0 && (!table_row || !src_ids || !dst_ids))) return PA_ERR_INVALID_ARG;
     for (int i = 0; i < n; ++i)
         if (!valid_id(from, table_row[i]) || from->refs[table_row[i]] <= 0) return PA_ERR_BOUNDS;
-    if (n > to->num_free) return PA_ERR_POOL_EXHAUSTED;
+    if (n > (int)to->free_heap.size()) return PA_ERR_POOL_EXHAUSTED;
     for (int i = 0; i < n; ++i) {
         const int id = pa_pool_alloc(to);   // cannot fail: n blocks are free
         src_ids[i] = table_row[i];

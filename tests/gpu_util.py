@@ -6,10 +6,13 @@ import torch
 import oracle as oracle_pkg
 import paged_kv_cache_08_gb300 as pa
 
-# Max-abs error allowed for fp16/bf16 outputs accumulated in fp32, on top of the output's own
-# rounding: an fp16/bf16 value v stands for every real number within half a unit in the last
-# place of v, and no kernel can do better than that (bf16 at |o| in [1, 2) already rounds by up
-# to 3.9e-3).  So an element passes when |out - ref| <= TOL + ulp(out) / 2.
+# Max-abs error allowed for fp16/bf16 outputs accumulated in fp32, against the fp64 oracle.
+# The raw error |out - ref| must stay within TOL, except where the output's own rounding alone
+# can exceed it: a bf16 value of magnitude >= 1 stands for every real number within half a unit
+# in its last place (up to 3.9e-3 in [1, 2)), which no kernel can beat, so there an element passes
+# when |out - ref| <= TOL + ulp(out) / 2.  Every fp16 output (half an ulp stays below 2e-3 up to
+# |o| < 8, and an output is a convex combination of V rows) and every bf16 output below 1 is
+# held to TOL itself.
 TOL = 2e-3
 
 
@@ -49,13 +52,23 @@ def half_ulp(out: torch.Tensor) -> np.ndarray:
     return (hi - lo) / 2
 
 
+def rounding_allowance(out: torch.Tensor) -> np.ndarray:
+    """Per element, the part of the output's own rounding that TOL does not cover: half an ulp
+    for bf16 outputs of magnitude >= 1, else 0."""
+    if out.dtype != torch.bfloat16:
+        return np.zeros(tuple(out.shape))
+    mag = np.abs(out.detach().float().cpu().numpy().astype(np.float64))
+    return np.where(mag >= 1.0, half_ulp(out), 0.0)
+
+
 def max_abs_err(out: torch.Tensor, ref: np.ndarray) -> float:
-    """Largest error beyond the output's own rounding (compare with TOL)."""
+    """Largest error against the fp64 reference, less the rounding allowance of bf16 outputs of
+    magnitude >= 1 (compare with TOL); for fp16 this is the raw max-abs error."""
     got = out.detach().float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all(), "non-finite output"
     if not ref.size:
         return 0.0
-    return float(np.max(np.abs(got - ref) - half_ulp(out)))
+    return float(np.max(np.abs(got - ref) - rounding_allowance(out)))
 
 
 def raw_max_abs_err(out: torch.Tensor, ref: np.ndarray) -> float:

@@ -5,8 +5,6 @@ must match bit for bit and the outputs within the parity tolerance.  A chain of
 layers in which each layer's query is the previous layer's output checks the
 early-read contract: the next launch may start before the previous one ends,
 but must read q only after it has finished."""
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -111,7 +109,7 @@ def test_append_layer_chain_reads_q_after_previous_layer(oracle):
     torch.cuda.synchronize()
     for i in range(layers):
         pa.decode_append(q, wl.k_new[i].to(dev), wl.v_new[i].to(dev), kcs[i], vcs[i], bt, lens, wl.scale,
-                         wl.num_kv_heads, out=outs[i])
+                         wl.num_kv_heads, out=outs[i], early_reads=True)
         q = outs[i]
     torch.cuda.synchronize()
     # the oracle's own chain: each layer's query is the previous oracle output rounded to fp16
@@ -132,45 +130,3 @@ def test_append_rejects_shapes_outside_the_persistent_kernel():
     wl = workloads.make_workload("g17", context_lens=[5], num_q_heads=17, num_kv_heads=1, block_size=16, seed=1)
     with pytest.raises(pa.PAError):
         _append(wl)
-
-
-def test_append_with_next_layer_prefetch(oracle):
-    """The L2 prefetches (the next layer's blocks; the range's own blocks beyond the copy
-    pipeline) are hints: results are bit-identical with and without them, and match the oracle
-    on both layers."""
-    wl = workloads.config(2, layers=2)
-    dev = torch.device("cuda")
-    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
-    outs = {}
-    for pf in (False, True):
-        kcs = [wl.k_cache[i].to(dev).clone() for i in range(2)]
-        vcs = [wl.v_cache[i].to(dev).clone() for i in range(2)]
-        res = []
-        for i in range(2):
-            nxt = (kcs[1], vcs[1]) if pf and i == 0 else None
-            res.append(pa.decode_append(wl.q[i].to(dev), wl.k_new[i].to(dev), wl.v_new[i].to(dev), kcs[i], vcs[i],
-                                        bt, lens, wl.scale, wl.num_kv_heads, prefetch=nxt, prefetch_own=pf))
-        torch.cuda.synchronize()
-        outs[pf] = (res, kcs, vcs)
-    for i in range(2):
-        assert torch.equal(outs[True][0][i].view(torch.int16), outs[False][0][i].view(torch.int16))
-        okc, ovc, ref = run_oracle(oracle, wl, i)
-        assert np.array_equal(u16(outs[True][1][i]), okc) and np.array_equal(u16(outs[True][2][i]), ovc)
-        err = max_abs_err(outs[True][0][i], ref)
-        assert err <= TOL, f"layer {i}: max abs error {err:.3e}"
-
-
-def test_prefetch_needs_both_pools():
-    wl = workloads.config(1)
-    dev = torch.device("cuda")
-    q = wl.q[0].to(dev)
-    kc, vc = wl.k_cache[0].to(dev), wl.v_cache[0].to(dev)
-    o = pa._native.DecodeOptions(0, 0, 0, 0, None, kc.data_ptr(), None)
-    out = torch.empty_like(q)
-    S, Hq, D = q.shape
-    rc = pa.lib().pa_decode_ex(out.data_ptr(), q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-                               wl.block_tables.to(dev).data_ptr(), wl.context_lens.to(dev).data_ptr(),
-                               ctypes.c_float(wl.scale), wl.num_kv_heads, S, Hq, D, wl.block_size, wl.num_blocks,
-                               wl.max_blocks_per_seq, 0, None, 0, torch.cuda.current_stream().cuda_stream,
-                               ctypes.byref(o))
-    assert rc == -1

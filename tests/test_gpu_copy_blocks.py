@@ -207,8 +207,9 @@ def test_copy_on_write_fork_end_to_end(oracle, fused):
     s_t, d_t = torch.tensor(src, dtype=torch.int32), torch.tensor(dst, dtype=torch.int32)
     pa.copy_blocks(gk, gv, gk, gv, s_t.to(dev), d_t.to(dev))
     if fused:
-        out = pa.decode_append(q.to(dev), k_new.to(dev), v_new.to(dev), gk, gv, tables.to(dev), ctx.to(dev), scale, H,
-                               early_reads=False)
+        # default options: no early reads, so the append reads the copied rows only after the
+        # copy kernel before it in the stream has finished
+        out = pa.decode_append(q.to(dev), k_new.to(dev), v_new.to(dev), gk, gv, tables.to(dev), ctx.to(dev), scale, H)
     else:
         pa.cache_write(k_new.to(dev), v_new.to(dev), torch.tensor(slots, dtype=torch.int64).to(dev), gk, gv)
         out = pa.decode(q.to(dev), gk, gv, tables.to(dev), ctx.to(dev), scale, H)

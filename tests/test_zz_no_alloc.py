@@ -4,8 +4,9 @@ It serves callers that cannot allocate device memory (a plugin inside a host
 framework that owns the GPU's memory pool, real-time deployments that forbid
 allocation after start-up): its scratch is a fixed device array inside the
 library.  Called through the C ABI twice in a row, its output must match
-pa_decode's (the entry point with a caller workspace) within the parity
-tolerance; a problem too large for the fixed array is refused.
+pa_decode's (the entry point with a caller workspace) and the fp64 oracle's,
+each within the parity tolerance; a problem too large for the fixed array is
+refused.
 
 This file is collected last on purpose, so that a run that stops at the first
 failure has already run every other test; it does not depend on them.
@@ -18,7 +19,7 @@ import torch
 
 import paged_kv_cache_08_gb300 as pa
 import workloads
-from gpu_util import TOL, half_ulp
+from gpu_util import TOL, half_ulp, max_abs_err
 
 pytestmark = pytest.mark.gpu
 
@@ -48,8 +49,16 @@ def _excess(a: torch.Tensor, b: torch.Tensor) -> float:
     return float(np.max(d - half_ulp(b)))
 
 
+def _oracle_decode(oracle, wl):
+    import oracle as oracle_pkg
+    kc = oracle_pkg.as_u16(wl.k_cache[0])
+    vc = oracle_pkg.as_u16(wl.v_cache[0])
+    return oracle.decode(wl.q[0], kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.num_kv_heads,
+                         wl.dtype == "bf16")
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_static_matches_workspace_entry_point_twice(dtype):
+def test_static_matches_workspace_entry_point_twice(oracle, dtype):
     dev = torch.device("cuda")
     # long and short contexts, so that the persistent kernel cuts sequences between CTAs and
     # merges their pieces through the scratch counters
@@ -57,6 +66,7 @@ def test_static_matches_workspace_entry_point_twice(dtype):
                                  num_q_heads=12, num_kv_heads=2, block_size=16, dtype=dtype, seed=41,
                                  max_context=2048)
     ref = _reference(wl, dev)
+    exact = _oracle_decode(oracle, wl)
     torch.cuda.synchronize()
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
@@ -65,6 +75,9 @@ def test_static_matches_workspace_entry_point_twice(dtype):
         torch.cuda.synchronize()
         err = _excess(out, ref)
         assert err <= TOL, f"call {call}: max abs difference {err:.3e} beyond rounding > {TOL}"
+        # against the fp64 oracle too, so that a fault both entry points share cannot pass
+        err = max_abs_err(out, exact)
+        assert err <= TOL, f"call {call}: max abs error against the oracle {err:.3e} > {TOL}"
 
 
 def test_static_refuses_problems_beyond_its_scratch():
