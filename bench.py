@@ -176,9 +176,10 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, planned: bool = True):
         self.fused = fused
         self.num_ctas = num_ctas
+        self.planned = planned and fused
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
         self.wl = wl
@@ -198,6 +199,13 @@ class Step:
         ws = pa.decode_workspace_size(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq,
                                       num_ctas=num_ctas)
         self.ws = pa.new_workspace(ws, device)
+        self.plan = None
+        if self.planned:
+            # the step's plan: built by the first launch of every step (inside the graph), read by
+            # every layer's decode
+            self.plan = pa.decode_plan(self.bt, self.lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size,
+                                       wl.num_blocks, num_ctas=num_ctas)
+            self.ws = pa.new_workspace(pa.planned_workspace_size(num_ctas), device)
         self.tps = pa.plan_tokens_per_split(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
         self.graph = None
         self.ev = None
@@ -208,7 +216,12 @@ class Step:
             pa.cache_write(wl.k_new[i], wl.v_new[i], self.slots, wl.k_cache[i], wl.v_cache[i])
         if ev_pair is not None:
             ev_pair[0].record()
-        if self.fused:
+        if self.planned:
+            # early reads from layer 1 on: the kernel before it is the previous layer's, which
+            # writes other pools and never the plan (layer 0 follows the plan kernel)
+            pa.decode_planned(wl.q[i], wl.k_cache[i], wl.v_cache[i], self.plan, wl.scale, k_new=wl.k_new[i],
+                              v_new=wl.v_new[i], out=self.out[i], workspace=self.ws, early_reads=i > 0)
+        elif self.fused:
             # early reads: the kernel before each launch is the previous layer's, which writes
             # other pools and never the tables or lengths
             pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], wl.k_cache[i], wl.v_cache[i], self.bt, self.lens,
@@ -220,7 +233,14 @@ class Step:
         if ev_pair is not None:
             ev_pair[1].record()
 
+    def make_plan(self):
+        wl = self.wl
+        self.pa.decode_plan(self.bt, self.lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks,
+                            plan=self.plan, num_ctas=self.num_ctas)
+
     def eager(self):
+        if self.planned:
+            self.make_plan()
         for i in range(self.wl.layers):
             self.launch_layer(i)
 
@@ -241,6 +261,8 @@ class Step:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(self.wl.layers)]
             torch.cuda._sleep(50_000_000)
+            if self.planned:
+                self.make_plan()
             for i in range(self.wl.layers):
                 self.launch_layer(i, evs[i])
             torch.cuda.synchronize()
@@ -285,8 +307,9 @@ def run_ours(args):
     wl = workloads.config(2, device=dev, layers=args.layers)
     import paged_kv_cache_08_gb300 as pa
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
-    fused = args.path == "fused" and kind == 2
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas)
+    fused = args.path in ("fused", "unplanned") and kind == 2
+    planned = args.path == "fused" and fused
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, planned=planned)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -295,7 +318,7 @@ def run_ours(args):
     st.capture()
     split_combine = kind != 2 and st.tps < wl.max_blocks_per_seq * wl.block_size
     # fused: one launch per layer; else cache write + decode (+ combine)
-    launches_per_step = wl.layers * (1 if fused else 2 + (1 if split_combine else 0))
+    launches_per_step = wl.layers * (1 if fused else 2 + (1 if split_combine else 0)) + (1 if planned else 0)
 
     for _ in range(args.warmup):
         st.replay()
@@ -329,17 +352,19 @@ def run_ours(args):
         iso_ms = statistics.mean(decode_ms)
         if fused:
             avg_ms = start.elapsed_time(stop) / (args.steps * wl.layers)
-            how = "timed-region events / launches in it"
+            how = ("timed-region events / decode launches in it (the step's plan launch included)" if planned
+                   else "timed-region events / launches in it")
         else:
             avg_ms = iso_ms
             how = "events around each launch, enqueued behind a spin kernel"
         kernel_bytes = d_bytes + (c_bytes if fused else 0)   # the fused kernel also moves the new rows
         achieved = kernel_bytes / (avg_ms * 1e-3) / 1e9
-        traffic = profiled_traffic("paged_kv_cache_08_gb300/csrc/decode_persist.cu") if kind == 2 else None
+        traffic = (profiled_traffic("paged_kv_cache_08_gb300/csrc/decode_planned.cu") if planned else
+                   profiled_traffic("paged_kv_cache_08_gb300/csrc/decode_persist.cu") if kind == 2 else None)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": kernel_bytes,
-                "kernel": "pa_decode_append" if fused else "pa_decode",
+                "kernel": "pa_decode_planned (append)" if planned else ("pa_decode_append" if fused else "pa_decode"),
                 "avg_launch_us": round(avg_ms * 1e3, 2), "avg_launch_from": how,
                 "isolated_launch_us": round(iso_ms * 1e3, 2),
                 "isolated_achieved": round(kernel_bytes / (iso_ms * 1e-3) / 1e9, 1),
@@ -363,7 +388,8 @@ def run_ours(args):
                        "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_blocks": wl.num_blocks,
                        "decode_kernel": {1: "split grid, CUDA cores", 2: "persistent, tensor cores",
                                          3: "split grid, tensor cores"}[kind],
-                       "step": ("pa_decode_append per layer (cache write fused)" if fused
+                       "step": ("pa_decode_plan once, then pa_decode_planned with the cache write per layer"
+                                if planned else "pa_decode_append per layer (cache write fused)" if fused
                                 else "pa_cache_write + pa_decode per layer"),
                        "l2": "inputs larger than L2: %d distinct layer caches (%.2f GB) read once per step"
                              % (wl.layers, 2 * sum(t.numel() * 2 for t in wl.k_cache) / 1e9),
@@ -389,7 +415,7 @@ def run_e2e(st, wl, args, step_bytes):
     input buffer), runs the 24 layers and copies the outputs back (one copy).  Two buffer sets
     (and two captured graphs) let step k + 1's input copy and step k - 1's output copy run on
     copy streams while step k's kernels run; the timed region spans all copies of all steps."""
-    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas)
+    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas, planned=st.planned)
     st2.capture()
     sets = [st, st2]
     host_in = st.inbuf.cpu().pin_memory()
@@ -926,7 +952,9 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "separate"], default="fused")
+    ap.add_argument("--path", choices=["fused", "unplanned", "separate"], default="fused",
+                    help="fused: one plan per step + pa_decode_planned (cache write fused) per layer; "
+                         "unplanned: pa_decode_append per layer; separate: pa_cache_write + pa_decode")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
     ap.add_argument("--op", choices=["decode", "config", "copy_blocks", "swap", "multi_query", "prefill", "runs"],
                     default="decode",

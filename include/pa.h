@@ -79,6 +79,7 @@ typedef enum {
 #define PA_DEV_BAD_CONTEXT  0x2u /* a context length < 0 or > max_blocks_per_seq*block_size was clamped */
 #define PA_DEV_BAD_SLOT     0x4u /* a slot >= num_blocks*block_size was skipped */
 #define PA_DEV_TIMEOUT      0x8u /* a copy pipeline wait gave up after about one second */
+#define PA_DEV_BAD_PLAN     0x10u /* pa_decode_planned: the plan was built for another shape or grid */
 
 /* Kernel choice of pa_decode_ex. */
 typedef enum {
@@ -244,6 +245,45 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
                      int max_blocks_per_seq, int dtype,
                      void* workspace, size_t workspace_bytes, void* stream,
                      const pa_decode_options* opts);
+
+/* ------------------------------------------------------------------------------------
+ * pa_decode_plan / pa_decode_planned  [P4 §五.1 decode kernel; P1 address formula; P4 §三
+ *                                     sequence diagram for the cache write of the new token]
+ * A decode step runs the same attention over every layer with the same block tables and
+ * lengths.  pa_decode_plan reads the tables and lengths once and writes a plan to device
+ * memory: the 64-token chunks of every (sequence, kv head) with the physical ids of the blocks
+ * each touches, and the share of the chunks each CTA of the decode launch streams.
+ * pa_decode_planned then computes, per layer, exactly what pa_decode (k_new == NULL) or
+ * pa_decode_append (k_new, v_new != NULL: the new token's rows written at position L - 1
+ * first) computes, reading the plan instead of the tables and lengths.
+ *   plan: device memory of pa_decode_plan_size(...) bytes, 16-byte aligned, caller-owned.
+ *     Valid while the tables' entries for positions < L and the lengths stay as they were
+ *     when it was built, and only for the same shape and options (num_ctas).
+ *   workspace: pa_decode_planned_workspace_size(opts) bytes, 16-byte aligned, ZERO-FILLED
+ *     before first use (pa_decode_workspace_init); every completed call leaves it zeroed for
+ *     the next (after a call that set PA_DEV_TIMEOUT, zero it again).  Calls that share a
+ *     workspace must not overlap on the GPU.
+ *   opts: num_ctas (<= the SM count; 0 = one CTA per SM), flags (PA_DECODE_EARLY_READS: the
+ *     plan and cached rows may be read before the preceding kernel ends; the preceding
+ *     kernel must then write none of the plan, the caches or the tables -- in particular a
+ *     pa_decode_planned right after pa_decode_plan must not ask for it), timeline.
+ * A plan that does not match the call's shape or grid makes the kernel write nothing and
+ * set PA_DEV_BAD_PLAN.  Supported: head_dim 128, block_size 16/32/64/128, num_q_heads /
+ * num_kv_heads <= 8, num_seqs <= 1024; else PA_ERR_UNSUPPORTED.
+ * Returns the codes of pa_decode.
+ * ---------------------------------------------------------------------------------- */
+size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_seq, const pa_decode_options* opts);
+int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, const int32_t* context_lens,
+                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, int max_blocks_per_seq, void* stream, const pa_decode_options* opts);
+size_t pa_decode_planned_workspace_size(const pa_decode_options* opts);
+int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new,
+                      void* k_cache, void* v_cache, const void* plan, float scale,
+                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, int max_blocks_per_seq, int dtype,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      const pa_decode_options* opts);
 
 /* ------------------------------------------------------------------------------------
  * pa_multi_query  [P4 §五.1 attention over the paged cache; P4's closing section on

@@ -24,7 +24,9 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "multi_query", "decode_runs", "gather_runs",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_planned", "DecodePlan",
+           "planned_workspace_size",
+           "multi_query", "decode_runs", "gather_runs",
            "SlotPool", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
@@ -234,6 +236,99 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_c
                                 context_lens.data_ptr(), float(scale), int(num_kv_heads), S, Hq, D, B, NB,
                                 max_blocks, _DTYPE[q.dtype], ws_ptr, ws_bytes, _stream_ptr(stream), ctypes.byref(o))
     _native.check("pa_decode_append", rc)
+    return out
+
+
+class DecodePlan:
+    """A decode step's plan (pa_decode_plan): device bytes plus the shape it was built for."""
+
+    def __init__(self, data: torch.Tensor, num_seqs: int, num_q_heads: int, num_kv_heads: int, block_size: int,
+                 num_blocks: int, max_blocks_per_seq: int, num_ctas: int):
+        self.data = data
+        self.num_seqs = num_seqs
+        self.num_q_heads = num_q_heads
+        self.num_kv_heads = num_kv_heads
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self.num_ctas = num_ctas
+
+
+def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_heads: int, num_kv_heads: int,
+                block_size: int, num_blocks: int, head_dim: int = 128, plan: Optional[DecodePlan] = None,
+                num_ctas: int = 0, stream: Optional[torch.cuda.Stream] = None) -> DecodePlan:
+    """Build (or rebuild in place, ``plan``) the plan of a decode step: one small kernel that reads
+    the block tables and lengths once for every layer's pa_decode_planned call."""
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if block_tables.dim() != 2 or block_tables.shape[0] != context_lens.numel():
+        raise ValueError("block_tables must be [S, max_blocks] with S = context_lens.numel()")
+    S, max_blocks = block_tables.shape
+    o = _opts(0, "auto", num_ctas)
+    need = int(lib().pa_decode_plan_size(S, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                                         ctypes.byref(o)))
+    if need == 0:
+        raise PAError("pa_decode_plan_size", -2)
+    if plan is None or plan.data.numel() < need:
+        data = torch.empty(need, dtype=torch.uint8, device=block_tables.device)
+        plan = DecodePlan(data, S, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks, int(num_ctas))
+    else:
+        plan.num_seqs, plan.num_q_heads, plan.num_kv_heads = S, num_q_heads, num_kv_heads
+        plan.block_size, plan.num_blocks, plan.max_blocks_per_seq, plan.num_ctas = (block_size, num_blocks,
+                                                                                     max_blocks, int(num_ctas))
+    rc = lib().pa_decode_plan(plan.data.data_ptr(), plan.data.numel(), block_tables.data_ptr(),
+                              context_lens.data_ptr(), S, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                              max_blocks, _stream_ptr(stream), ctypes.byref(o))
+    _native.check("pa_decode_plan", rc)
+    return plan
+
+
+def planned_workspace_size(num_ctas: int = 0) -> int:
+    """Bytes of workspace pa_decode_planned needs for a plan built with ``num_ctas``."""
+    o = _opts(0, "auto", num_ctas)
+    return int(lib().pa_decode_planned_workspace_size(ctypes.byref(o)))
+
+
+def decode_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, plan: DecodePlan, scale: float,
+                   k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   early_reads: bool = False, timeline: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention of one layer through a step's plan (pa_decode_planned); with k_new / v_new
+    ([S, Hkv, D]) the new token's rows are written at position L - 1 first, as decode_append."""
+    _need_cuda("q", q)
+    if q.dtype not in _DTYPE:
+        raise TypeError("q must be float16 or bfloat16")
+    _need_cuda("k_cache", k_cache, q.dtype)
+    _need_cuda("v_cache", v_cache, q.dtype)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if (S, Hq, Hkv, B, NB) != (plan.num_seqs, plan.num_q_heads, plan.num_kv_heads, plan.block_size,
+                               plan.num_blocks) or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("q / caches do not match the plan")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for n, t in (("k_new", k_new), ("v_new", v_new)):
+            _need_cuda(n, t, q.dtype)
+        if k_new.shape != (S, Hkv, D) or v_new.shape != k_new.shape:
+            raise ValueError("k_new / v_new must be [S, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    o = _opts(0, "auto", plan.num_ctas, timeline, _native.EARLY_READS if early_reads else 0)
+    need = planned_workspace_size(plan.num_ctas)
+    if workspace is None:
+        workspace = _workspace(q.device, need, 100, plan.num_ctas)
+    rc = lib().pa_decode_planned(out.data_ptr(), q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
+                                 v_new.data_ptr() if v_new is not None else None, k_cache.data_ptr(),
+                                 v_cache.data_ptr(), plan.data.data_ptr(), float(scale), S, Hq, Hkv, D, B, NB,
+                                 plan.max_blocks_per_seq, _DTYPE[q.dtype], workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream_ptr(stream), ctypes.byref(o))
+    _native.check("pa_decode_planned", rc)
     return out
 
 

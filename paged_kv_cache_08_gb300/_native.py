@@ -30,7 +30,7 @@ PA_OK = 0
 STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "PA_ERR_CUDA",
           -4: "PA_ERR_POOL_EXHAUSTED", -5: "PA_ERR_DEVICE_TIMEOUT", -6: "PA_ERR_BOUNDS",
           -7: "PA_ERR_WORKSPACE", -8: "PA_ERR_SCRATCH_LIMIT"}
-DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_PLAN = 0x1, 0x2, 0x4, 0x8, 0x10
 MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 EARLY_READS = 1
 PREFILL_MMA_SYNC = 4
@@ -63,6 +63,12 @@ _SIGNATURES = {
     "pa_slots_num_free": (c_int, [c_vp]),
     "pa_decode_static": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int, c_int,
                                  c_int, c_int, c_int, c_vp]),
+    "pa_decode_plan_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_plan": (c_int, [c_vp, c_size, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_vp,
+                               ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_planned_workspace_size": (c_size, [ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_planned": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int,
+                                  c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
     "pa_decode_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pa_decode_workspace_size_ex": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int,
                                              ctypes.POINTER(DecodeOptions)]),

@@ -20,7 +20,8 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libpa.so"
 
-CUDA_SOURCES = ["api.cu", "cache_write.cu", "copy_blocks.cu", "decode_fma.cu", "decode_mma.cu", "decode_persist.cu", "decode_static.cu",
+CUDA_SOURCES = ["api.cu", "cache_write.cu", "copy_blocks.cu", "decode_fma.cu", "decode_mma.cu", "decode_persist.cu", "decode_planned.cu",
+                "decode_static.cu",
                 "prefill_mma.cu", "prefill_tc.cu"]
 CXX_SOURCES = ["pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -636,6 +636,85 @@ int pa_multi_query_append(void* out, const void* q, const void* k_new, const voi
                        workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);
 }
 
+static int planned_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq) {
+    int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    if (num_q_heads / num_kv_heads > 8 || num_seqs > kPlanMaxSeqs || num_kv_heads > 32767) return PA_ERR_UNSUPPORTED;
+    // chunk indices and counts per segment are 16-bit in the plan
+    if ((long long)max_blocks_per_seq * block_size > 32767LL * kStageTokens) return PA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * num_kv_heads * (((long long)max_blocks_per_seq * block_size + kStageTokens - 1) /
+                                              kStageTokens) > 0x7fffffffLL)
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_seq, const pa_decode_options* opts) {
+    if (planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) != PA_OK)
+        return 0;
+    if (opts && opts->num_ctas < 0) return 0;
+    return planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts));
+}
+
+size_t pa_decode_planned_workspace_size(const pa_decode_options* opts) {
+    if (opts && opts->num_ctas < 0) return 0;
+    return planned_workspace_bytes(planned_ctas(opts));
+}
+
+int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, const int32_t* context_lens,
+                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   int max_blocks_per_seq, void* stream, const pa_decode_options* opts) {
+    int rc = planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    if (opts && opts->num_ctas < 0) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || !plan || !aligned16(plan)) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!block_tables || !context_lens || !aligned4(block_tables) || !aligned4(context_lens)))
+        return PA_ERR_INVALID_ARG;
+    const int ctas = planned_ctas(opts);
+    if (plan_bytes < planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas))
+        return PA_ERR_WORKSPACE;
+    cudaError_t e = launch_decode_plan(plan, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                       block_size, num_blocks, max_blocks_per_seq, ctas,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const void* plan, float scale, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
+                      size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    int rc = planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    if (opts && opts->num_ctas < 0) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !plan) return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(plan) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return PA_ERR_INVALID_ARG;
+    const int ctas = planned_ctas(opts);
+    const size_t need = planned_workspace_bytes(ctas);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    const bool early = opts && (opts->flags & PA_DECODE_EARLY_READS);
+    cudaError_t e = launch_decode_planned(out, q, k_new, v_new, k_cache, v_cache, plan, workspace, scale, num_seqs,
+                                          num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq,
+                                          dtype, ctas, early, opts ? opts->timeline : nullptr,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
               const int32_t* context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
               int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,

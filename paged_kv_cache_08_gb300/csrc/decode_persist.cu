@@ -35,10 +35,7 @@
 // epilogue warp (publish on a shared-memory barrier, move on) which does the arrival and, if
 // last, the merge while the stream continues.  The range's final piece is finished by the
 // consumers themselves, with all their threads, when nothing is left to stream.
-#include "pa_internal.cuh"
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "decode_common.cuh"
 
 #include <atomic>
 #include <climits>
@@ -122,75 +119,6 @@ struct MmaMapsTails {
 template <bool kManyEnds>
 using MapsOf = typename std::conditional<kManyEnds, MmaMapsTails, MmaMaps>::type;
 
-template <typename T>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1);
-
-template <>
-__device__ __forceinline__ void mma16816<__half>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                 uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-template <>
-__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Transpose of an 8x8 matrix of 16-bit elements held as one mma fragment register per lane.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     dst),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
 // Barrier of the 128 consumer threads (hardware named barrier 1).  Every consumer warp walks
@@ -198,38 +126,6 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 // then skips waits, math and global writes), so no warp can be left waiting here.
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-}
-
-// Arrival on a cut segment's counter: release publishes the partial stores that precede it (this
-// thread's, and the CTA's through the barrier before it); acquire orders the merge's reads after.
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ float4 ld_cg4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float2 ld_cg2(const float2* p) {
-    float2 v;
-    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-    return v;
-}
-
-// Shared-memory line (128 bytes) of token t (0..63 of the chunk), column half h: a chunk holds
-// 64 / R boxes of [2 halves][R rows][64 columns], R = min(block_size, 64).
-__device__ __forceinline__ uint32_t line_of(int t, int h, int R_log2) {
-    const int R = 1 << R_log2;
-    return (uint32_t)(((t >> R_log2) << (R_log2 + 1)) + h * R + (t & (R - 1)));
-}
-
-// Byte address of 16-byte chunk c (0..15 over the 128 columns) of token t, 128-byte swizzle.
-__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int t, int c, int R_log2) {
-    return base + line_of(t, c >> 3, R_log2) * 128u + ((uint32_t)((c & 7) ^ (t & 7)) << 4);
 }
 
 // The cut of the chunk list into the ranges of the C CTAs that take part.
@@ -1371,33 +1267,8 @@ __global__ void __launch_bounds__(kThreads, (kStages > 3) ? 1 : 2)
 
 // ---- host side ----
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::atomic<int> state{0};
-    if (state.load() == 0) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-        state.store(1);
-    }
-    return fn;
-}
-
 bool encode_map(const void* base, unsigned long long rows, int box_rows, CUtensorMap* out) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_pool_map(base, rows, box_rows, out);
 }
 
 template <typename T, bool kG16, int kStages, bool kMulti, bool kManyEnds = false>

@@ -1,0 +1,1228 @@
+// Paged decode attention with a per-step plan: one planning launch per decode step, then one
+// decode launch per layer that reads the plan instead of the block tables.
+//
+// What it computes is pa_decode's (and, with the new K/V rows, pa_decode_append's):
+// "显存虚拟化革命：PagedAttention 内存池管理与显存碎片终结", §五.1 -- for every sequence and query
+// head, walk the sequence's logical blocks through its block-table row, q.k for every cached
+// token, softmax with a running maximum, weight V, normalise at the end; the address rule of
+// "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块", section
+// "注意力寻址：非连续物理块的间接寻址内核".  Every layer of a decode step shares the block tables
+// and the lengths, so everything derived from them alone is computed once per step:
+//
+// The plan (decode_plan_kernel).  A segment is one (sequence, kv head), cut into 64-token
+// chunks; the chunks of all segments form one list (sequence-major, then kv head).  For every
+// chunk the plan holds its sequence, kv head, position in the segment, valid tokens and the
+// physical ids of the blocks it touches, read from the block table once.  The list is cut into
+// 2C equal contiguous ranges, two per CTA (C CTAs, one per SM): group 0 of a CTA streams its
+// range forwards, group 1 backwards.  So the range ends that border another CTA are streamed
+// first by both CTAs, and a segment cut there leaves pieces that are done early; the cut between
+// the two groups of one CTA is streamed last by both, and its two pieces meet in shared memory.
+// For a segment cut between CTAs the plan names the CTA that combines the pieces (the merger):
+// the first CTA whose piece finishes late (last in its group's order), else the first CTA.
+//
+// The decode launch (decode_planned_kernel), per CTA:
+//   warps 0-3, 4-7  consumers of group 0, 1: each warp owns 16 tokens of a 64-token stage and
+//                   runs S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 (the GQA group's
+//                   query rows on the 8-column side), online softmax with a lazy exponent base;
+//                   at a segment's end the four warps merge through the consumed stage and the
+//                   result goes to the output, to the other group (shared memory), to the
+//                   epilogue warp (shared memory) or, for another CTA's merger, to the workspace;
+//   warps 8, 9      producers of group 0, 1: read the group's chunk descriptors from the plan
+//                   (32 per load, one per lane) and issue the 2-D TMA copies (128-byte swizzle)
+//                   of K and V, the query rows at a segment's first chunk and, when appending,
+//                   the new token's K/V rows, into a 3-stage ring per group;
+//   warp 10         epilogue: publishes this CTA's pieces of cut segments (a release store of a
+//                   flag per piece after the consumers' partial stores) and, where this CTA is the
+//                   merger, folds the other CTAs' pieces in as their flags appear, then its own,
+//                   and writes the output.  The consumers never wait on another CTA.
+// Every wait is bounded (about one second); a wait that gives up sets PA_DEV_TIMEOUT.
+#include "decode_common.cuh"
+
+#include <atomic>
+#include <climits>
+#include <type_traits>
+
+namespace pa {
+
+namespace {
+
+constexpr int kGroups = 2;
+constexpr int kGroupWarps = 4;
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kConsWarps = kGroups * kGroupWarps;       // 8
+constexpr int kProdWarp0 = kConsWarps;                  // producers: warps 8, 9
+constexpr int kEpiWarp = kConsWarps + kGroups;          // 10
+constexpr int kPThreads = (kEpiWarp + 1) * 32;          // 352
+constexpr int kPStages = 3;
+constexpr int kRows = 8;                                // query rows per segment (the GQA group, G <= 8)
+constexpr uint32_t kKB = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
+constexpr uint32_t kKVB = 2 * kKB;
+constexpr uint32_t kQOff = kKVB;                        // q rows: 8 x 256 B
+constexpr uint32_t kNewOff = kQOff + kRows * kHeadDim * 2;   // new K row, new V row: 2 x 256 B
+constexpr uint32_t kMetaOff = kNewOff + 2 * kHeadDim * 2;    // stage metadata (64 B)
+constexpr uint32_t kStageB = 35 * 1024;                 // 1024-aligned stages
+static_assert(kMetaOff + 64 <= kStageB, "stage layout");
+constexpr uint32_t kRingB = kGroups * kPStages * kStageB;
+constexpr int kRedStride = kHeadDim + 4;                // padded rows of the merge scratch
+static_assert(kGroupWarps * 8 * kRedStride * 4 + kGroupWarps * 8 * 8 <= kKVB, "merge scratch fits a stage");
+constexpr uint32_t kSlotB = kRows * kHeadDim * 4 + kRows * 8;   // partial (o rows, then (m, l) per row)
+constexpr uint32_t kPairOff = kRingB;                   // the two groups' meeting slot
+constexpr uint32_t kHandOff = kPairOff + kSlotB;        // [2 sides] this CTA's piece for the epilogue
+constexpr uint32_t kBarOff = kHandOff + 2 * kSlotB;
+// barriers: full[2][3], empty[2][3], qbar[2], pair, ready[2]
+constexpr int kNumBars = 2 * kGroups * kPStages + kGroups + 1 + 2;
+constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+constexpr uint32_t kMiscB = 128;
+constexpr size_t kSmemPlanned = 1024 + kMiscOff + kMiscB;
+static_assert(kSmemPlanned <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
+constexpr float kLazyLog2 = 8.f;
+constexpr int kPlanMagic = 0x31504150;                  // "PAP1"
+
+// Flush modes of a segment's last chunk in a group's order.
+enum : int { kOut = 0, kPair = 1, kPublish = 2, kMerge = 3 };
+// Stage flags.
+enum : int { kBegin = 1, kEnd = 2, kNewRow = 4 };
+
+struct PlanHeader {
+    int magic;
+    int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq;
+    int num_ctas;     // C: two groups each
+    int num_chunks;   // N
+    int max_chunks;
+    int pad[6];
+};
+static_assert(sizeof(PlanHeader) == 64, "plan header");
+
+// One chunk of the list (32 bytes, two 16-byte loads).
+struct __align__(16) PlanChunk {
+    int ids[4];       // physical block of each block the chunk touches; -1: none or outside the pool
+    short s, h;       // sequence, kv head
+    short k, n;       // chunk of the segment, chunks of the segment
+    short nvalid;     // cached tokens of the chunk (1..64)
+    short gf, gl;     // first and last group holding the segment's chunks
+    short merger;     // CTA combining the segment's pieces; -1: the segment stays inside one CTA
+};
+static_assert(sizeof(PlanChunk) == 32, "plan chunk");
+
+// Byte offsets of the plan's sections: header, lengths [S], group bounds [2C + 1], chunks.
+struct PlanLayout {
+    size_t lens, bounds, chunks, total;
+};
+
+inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
+
+__host__ __device__ inline long long plan_max_chunks(int num_seqs, int num_kv_heads, int block_size,
+                                                     int max_blocks_per_seq) {
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    return (long long)num_seqs * num_kv_heads * ((cap + kStageTokens - 1) / kStageTokens);
+}
+
+PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
+    PlanLayout L;
+    L.lens = 256;
+    L.bounds = L.lens + al256((size_t)num_seqs * 4);
+    L.chunks = L.bounds + al256((size_t)(2 * ctas + 1) * 4);
+    L.total = L.chunks + (size_t)plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq) *
+                             sizeof(PlanChunk);
+    return L;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The plan
+// ---------------------------------------------------------------------------------------------
+
+struct PlanArgs {
+    unsigned char* plan;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    unsigned int* status;
+    int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq, ctas;
+    size_t lens_off, bounds_off, chunks_off;
+    long long max_chunks;
+};
+
+constexpr int kPlanThreads = 256;
+
+// Group bounds of the equal cut: group g streams chunks [N g / G2, N (g + 1) / G2).
+__device__ __forceinline__ long long cut_bound(long long N, int G2, int g) { return N * g / G2; }
+// The group holding chunk x (the largest g with cut_bound(g) <= x).
+__device__ __forceinline__ int group_of(long long N, int G2, long long x) {
+    return (int)(((x + 1) * (long long)G2 - 1) / N);
+}
+
+// Whether CTA c's piece of the segment [g0, g1) finishes late: a group streams its range from
+// one end, so a piece that starts its group's order (group 0's first chunks, group 1's last)
+// and is not the whole range is done early; any other piece is done at the group's end.
+__device__ __forceinline__ bool piece_is_late(long long N, int G2, int c, long long g0, long long g1) {
+    const long long b0 = cut_bound(N, G2, 2 * c), b1 = cut_bound(N, G2, 2 * c + 1), b2 = cut_bound(N, G2, 2 * c + 2);
+    if (b0 < b1 && g0 < b1 && g1 > b0 && !(g0 <= b0 && g1 < b1)) return true;
+    if (b1 < b2 && g0 < b2 && g1 > b1 && !(g1 >= b2 && g0 > b1)) return true;
+    return false;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArgs a) {
+    extern __shared__ int plan_smem[];
+    const int S = a.num_seqs, Hkv = a.num_kv_heads, B = a.block_size;
+    int* nch = plan_smem;             // [S] chunks per kv head of each sequence
+    int* P = nch + S;                 // [S + 1] exclusive prefix of nch
+    int* Ls = P + S + 1;              // [S] clamped lengths
+    __shared__ int warp_tot[kPlanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long cap = (long long)a.max_blocks_per_seq * B;
+
+    grid_dependency_wait();
+    // lengths and chunk counts; a thread owns a contiguous run of sequences
+    const int per = (S + kPlanThreads - 1) / kPlanThreads;
+    const int lo = min(S, tid * per), hi = min(S, lo + per);
+    int local = 0;
+    for (int s = lo; s < hi; ++s) {
+        int L = a.context_lens[s];
+        if (L < 0 || L > cap) {
+            if (blockIdx.x == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+            L = L < 0 ? 0 : (int)cap;
+        }
+        Ls[s] = L;
+        nch[s] = (L + kStageTokens - 1) / kStageTokens;
+        local += nch[s];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int run = incl - local, tot = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+        if (w < warp) run += warp_tot[w];
+        tot += warp_tot[w];
+    }
+    for (int s = lo; s < hi; ++s) {
+        P[s] = run;
+        run += nch[s];
+    }
+    if (tid == 0) P[S] = tot;
+    __syncthreads();
+
+    const long long N = (long long)Hkv * tot;
+    const int G2 = 2 * a.ctas;
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.plan);
+    int32_t* lens = reinterpret_cast<int32_t*>(a.plan + a.lens_off);
+    int32_t* bounds = reinterpret_cast<int32_t*>(a.plan + a.bounds_off);
+    PlanChunk* chunks = reinterpret_cast<PlanChunk*>(a.plan + a.chunks_off);
+    if (blockIdx.x == 0) {
+        for (int s = tid; s < S; s += kPlanThreads) lens[s] = Ls[s];
+        for (int g = tid; g <= G2; g += kPlanThreads) bounds[g] = (int32_t)(N > 0 ? cut_bound(N, G2, g) : 0);
+        if (tid == 0) {
+            PlanHeader h = {};
+            h.magic = kPlanMagic;
+            h.num_seqs = S;
+            h.num_q_heads = a.num_q_heads;
+            h.num_kv_heads = Hkv;
+            h.block_size = B;
+            h.num_blocks = a.num_blocks;
+            h.max_blocks_per_seq = a.max_blocks_per_seq;
+            h.num_ctas = a.ctas;
+            h.num_chunks = (int)N;
+            h.max_chunks = (int)a.max_chunks;
+            *hdr = h;
+        }
+    }
+    // one descriptor per chunk, grid-stride
+    for (long long g = (long long)blockIdx.x * kPlanThreads + tid; g < N; g += (long long)gridDim.x * kPlanThreads) {
+        // the sequence: largest s with Hkv * P[s] <= g
+        int l2 = 0, h2 = S - 1;
+        while (l2 < h2) {
+            const int mid = (l2 + h2 + 1) >> 1;
+            if ((long long)Hkv * P[mid] <= g) l2 = mid;
+            else h2 = mid - 1;
+        }
+        const int s = l2;
+        const int n = nch[s];
+        const int r = (int)(g - (long long)Hkv * P[s]);
+        const int h = r / n, k = r - h * n;
+        const int L = Ls[s];
+        const int t0 = k * kStageTokens, t1 = min(t0 + kStageTokens, L);
+        const int first = t0 / B, nblk = (t1 - 1) / B - first + 1;
+        PlanChunk d;
+        const int32_t* row = a.block_tables + (size_t)s * a.max_blocks_per_seq + first;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            d.ids[e] = -1;
+            if (e < nblk) {
+                const int id = row[e];
+                if (id >= 0 && id < a.num_blocks) d.ids[e] = id;
+                else flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            }
+        }
+        d.s = (short)s;
+        d.h = (short)h;
+        d.k = (short)k;
+        d.n = (short)n;
+        d.nvalid = (short)(t1 - t0);
+        const long long g0 = g - k, g1 = g0 + n;
+        const int gf = group_of(N, G2, g0), gl = group_of(N, G2, g1 - 1);
+        d.gf = (short)gf;
+        d.gl = (short)gl;
+        int merger = -1;
+        if (gf / 2 != gl / 2) {
+            merger = gf / 2;
+            for (int c = gf / 2; c <= gl / 2; ++c)
+                if (piece_is_late(N, G2, c, g0, g1)) {
+                    merger = c;
+                    break;
+                }
+        }
+        d.merger = (short)merger;
+        const uint4* src = reinterpret_cast<const uint4*>(&d);
+        uint4* dst = reinterpret_cast<uint4*>(chunks + g);
+        dst[0] = src[0];
+        dst[1] = src[1];
+    }
+    grid_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------------------------
+// The decode launch
+// ---------------------------------------------------------------------------------------------
+
+struct PlannedArgs {
+    void* out;                  // [S][Hq][D]
+    const void* q;              // [S][Hq][D]
+    const void* k_new;          // append: [S][Hkv][D] rows written at position L - 1; null = off
+    const void* v_new;
+    const void* k_cache;        // [NB][Hkv][B][D]
+    const void* v_cache;
+    const unsigned char* plan;
+    float* part_o;              // [2C][8][D] unnormalised partial outputs of cut segments
+    float2* part_ml;            // [2C][8] (running max in log2 units, sum)
+    int* part_flag;             // [2C] 1 once the partial is published; 0 between launches
+    unsigned int* status;
+    unsigned long long* timeline;
+    float scale_log2;
+    int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq;
+    int early;
+    size_t lens_off, bounds_off, chunks_off;
+};
+
+struct MmaMapsP {
+    CUtensorMap k;
+    CUtensorMap v;
+};
+
+struct StageMeta {
+    int s, h, k, n;
+    int nvalid;
+    int flags;        // kBegin / kEnd / kNewRow
+    int mode;         // flush mode at kEnd
+    int post;         // after the two groups have met (kPair): kOut, kPublish or kMerge
+    int side;         // which of the CTA's two cut segments (0: the one holding its first chunk)
+    int new_phys;     // block of the new token (-1: none, -2: outside the pool)
+    int new_off;      // its row within the block
+    int pad[5];
+};
+static_assert(sizeof(StageMeta) == 64, "stage metadata");
+
+__device__ __forceinline__ void group_sync(int grp) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void load_chunk(const PlanChunk* src, PlanChunk& d) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+    uint4* q = reinterpret_cast<uint4*>(&d);
+    q[0] = __ldcg(p);
+    q[1] = __ldcg(p + 1);
+}
+
+// A running combination of partial results (m, l, o) of one query row, 8 columns per thread.
+struct Fold8 {
+    float M, den, num[8];
+    __device__ __forceinline__ void init() {
+        M = -INFINITY;
+        den = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) num[j] = 0.f;
+    }
+    __device__ __forceinline__ void add(float m, float l, const float (&o)[8]) {
+        const float Mn = fmaxf(M, m);
+        const float a = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+        const float b = exp2f(m - Mn);
+        den = den * a + l * b;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) num[j] = num[j] * a + o[j] * b;
+        M = Mn;
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8], float inv) {
+    uint4 u;
+    u.x = Elem<T>::pack2(v[0] * inv, v[1] * inv);
+    u.y = Elem<T>::pack2(v[2] * inv, v[3] * inv);
+    u.z = Elem<T>::pack2(v[4] * inv, v[5] * inv);
+    u.w = Elem<T>::pack2(v[6] * inv, v[7] * inv);
+    return u;
+}
+
+// Partial slot (global or shared): o [8][D] fp32, then (m, l) [8].
+__device__ __forceinline__ void slot_store(float* o, float2* ml, int r, int d0, const Fold8& f, bool write_ml) {
+    *reinterpret_cast<float4*>(o + r * kHeadDim + d0) = make_float4(f.num[0], f.num[1], f.num[2], f.num[3]);
+    *reinterpret_cast<float4*>(o + r * kHeadDim + d0 + 4) = make_float4(f.num[4], f.num[5], f.num[6], f.num[7]);
+    if (write_ml) ml[r] = make_float2(f.M, f.den);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPThreads, 1)
+    decode_planned_kernel(const PlannedArgs a, const __grid_constant__ MmaMapsP maps, const int R_log2) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* bp = smem_raw + (base - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kBarOff);
+    uint64_t* full = bars;                                  // [2][3]
+    uint64_t* empty = bars + kGroups * kPStages;            // [2][3]
+    uint64_t* qbar = bars + 2 * kGroups * kPStages;         // [2] deferred q / new rows of the first stages
+    uint64_t* pair_bar = qbar + kGroups;                    // the first group's piece is in the pair slot
+    uint64_t* ready = pair_bar + 1;                         // [2] this CTA's piece of cut segment `side`
+    volatile int* misc = reinterpret_cast<volatile int*>(bp + kMiscOff);
+    volatile int* abort_flag = misc;
+    volatile int* pair_count = misc + 1;
+    volatile int* pair_role = misc + 2;                     // [2]
+    volatile int* issued = misc + 4;                        // [2]
+    volatile int* qdef = misc + 8;                          // [2][3]: deferred q row (s * Hkv + h) or -1
+    volatile int* ndef = misc + 16;                         // [2][3]: deferred new rows (s * Hkv + h) or -1
+    float* pair_o = reinterpret_cast<float*>(bp + kPairOff);
+    float2* pair_ml = reinterpret_cast<float2*>(bp + kPairOff + kRows * kHeadDim * 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv, B = a.block_size;
+    const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.plan);
+    const int32_t* bounds = reinterpret_cast<const int32_t*>(a.plan + a.bounds_off);
+    const PlanChunk* chunks = reinterpret_cast<const PlanChunk*>(a.plan + a.chunks_off);
+    const bool append = a.k_new != nullptr;
+
+    if (tid == 0) {
+        trace(a.timeline, c, 0);
+        prefetch_map(&maps.k);
+        prefetch_map(&maps.v);
+        for (int i = 0; i < kGroups * kPStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kGroupThreads);
+        }
+        for (int i = 0; i < kGroups; ++i) mbar_init(&qbar[i], 1);
+        mbar_init(pair_bar, kGroupThreads);
+        mbar_init(&ready[0], kGroupThreads);
+        mbar_init(&ready[1], kGroupThreads);
+        *abort_flag = 0;
+        *pair_count = 0;
+        for (int i = 0; i < kGroups * kPStages; ++i) {
+            qdef[i] = -1;
+            ndef[i] = -1;
+        }
+        fence_mbar_init();
+    }
+    if (!a.early) grid_dependency_wait();
+    // the plan must match the launch (checked by every thread on its own: no barrier needed)
+    PlanHeader hd;
+    {
+        const int4* hp = reinterpret_cast<const int4*>(hdr);
+        int4* hq = reinterpret_cast<int4*>(&hd);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hq[j] = __ldcg(hp + j);
+    }
+    const bool plan_ok = hd.magic == kPlanMagic && hd.num_seqs == a.num_seqs && hd.num_q_heads == Hq &&
+                         hd.num_kv_heads == Hkv && hd.block_size == B && hd.num_blocks == a.num_blocks &&
+                         hd.max_blocks_per_seq == a.max_blocks_per_seq && hd.num_ctas == (int)gridDim.x;
+    const int b0 = plan_ok ? __ldcg(bounds + 2 * c) : 0, b1 = plan_ok ? __ldcg(bounds + 2 * c + 1) : 0,
+              b2 = plan_ok ? __ldcg(bounds + 2 * c + 2) : 0;
+    __syncthreads();
+    if (!plan_ok) {
+        if (a.early) grid_dependency_wait();
+        grid_launch_dependents();
+        if (tid == 0 && c == 0) flag_status(a.status, PA_DEV_BAD_PLAN);
+        return;
+    }
+    if (!a.early) grid_launch_dependents();
+
+    if (warp >= kProdWarp0 && warp < kEpiWarp) {
+        // ============================ producer of one group ============================
+        const int grp = warp - kProdWarp0;
+        const int lo = grp ? b1 : b0, hi = grp ? b2 : b1;
+        const int cnt = hi - lo;
+        auto chunk_at = [&](int p) { return grp ? hi - 1 - p : lo + p; };
+        uint64_t* gfull = full + grp * kPStages;
+        uint64_t* gempty = empty + grp * kPStages;
+        const uint32_t ring = base + (uint32_t)grp * kPStages * kStageB;
+        const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
+        const int R = 1 << R_log2;
+        bool deps_done = !a.early;
+        auto dependency_point = [&](int n_issued) {
+            grid_dependency_wait();
+            grid_launch_dependents();
+            if (lane == 0) {
+                const int n = min(n_issued, kPStages);
+                uint32_t bytes = 0;
+                for (int e = 0; e < n; ++e) {
+                    if (qdef[grp * kPStages + e] >= 0) bytes += group_bytes;
+                    if (ndef[grp * kPStages + e] >= 0) bytes += 4u * kHeadDim;
+                }
+                mbar_arrive_expect_tx(&qbar[grp], bytes);
+                for (int e = 0; e < n; ++e) {
+                    const uint32_t dst = ring + (uint32_t)e * kStageB;
+                    const int sh = qdef[grp * kPStages + e];
+                    if (sh >= 0)
+                        bulk_g2s(dst + kQOff, static_cast<const T*>(a.q) + ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim,
+                                 group_bytes, &qbar[grp]);
+                    const int nh = ndef[grp * kPStages + e];
+                    if (nh >= 0) {
+                        bulk_g2s(dst + kNewOff, static_cast<const T*>(a.k_new) + (size_t)nh * kHeadDim, 2u * kHeadDim,
+                                 &qbar[grp]);
+                        bulk_g2s(dst + kNewOff + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)nh * kHeadDim,
+                                 2u * kHeadDim, &qbar[grp]);
+                    }
+                }
+            }
+            __syncwarp();
+        };
+        PlanChunk cur;
+        if (lane < cnt) load_chunk(chunks + chunk_at(lane), cur);
+        if (grp == 0 && lane == 0) trace(a.timeline, c, 3);
+        bool ok = true;
+        int i = 0;
+        for (int pb = 0; pb < cnt && ok; pb += 32) {
+            PlanChunk nxt;
+            if (pb + 32 + lane < cnt) load_chunk(chunks + chunk_at(pb + 32 + lane), nxt);
+            const int m = min(32, cnt - pb);
+            for (int j = 0; j < m; ++j, ++i) {
+                const int st = i % kPStages;
+                if (i == kPStages && !deps_done) {
+                    dependency_point(i);
+                    deps_done = true;
+                }
+                if (i >= kPStages) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait_bounded(&gempty[st], (uint32_t)((i / kPStages) - 1) & 1u);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) {
+                        if (lane == 0) {
+                            flag_status(a.status, PA_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                }
+                // chunk j of this batch, from lane j
+                const uint4 w0 = reinterpret_cast<const uint4*>(&cur)[0];
+                const uint4 w1 = reinterpret_cast<const uint4*>(&cur)[1];
+                PlanChunk d;
+                uint4* dw = reinterpret_cast<uint4*>(&d);
+                dw[0] = make_uint4(__shfl_sync(0xffffffffu, w0.x, j), __shfl_sync(0xffffffffu, w0.y, j),
+                                   __shfl_sync(0xffffffffu, w0.z, j), __shfl_sync(0xffffffffu, w0.w, j));
+                dw[1] = make_uint4(__shfl_sync(0xffffffffu, w1.x, j), __shfl_sync(0xffffffffu, w1.y, j),
+                                   __shfl_sync(0xffffffffu, w1.z, j), __shfl_sync(0xffffffffu, w1.w, j));
+                if (lane == 0) {
+                    if (*abort_flag) {
+                        ok = false;
+                    } else {
+                        const int g = chunk_at(pb + j);
+                        const int s = d.s, h = d.h, k = d.k, n = d.n, nvalid = d.nvalid;
+                        const int g0 = g - k, g1 = g0 + n;
+                        int flags = 0;
+                        if (grp == 0) {
+                            if (k == 0 || g == lo) flags |= kBegin;
+                            if (k == n - 1 || g == hi - 1) flags |= kEnd;
+                        } else {
+                            if (k == n - 1 || g == hi - 1) flags |= kBegin;
+                            if (k == 0 || g == lo) flags |= kEnd;
+                        }
+                        int mode = kOut, post = kOut, side = 0;
+                        if (flags & kEnd) {
+                            const bool in_group = g0 >= lo && g1 <= hi;
+                            const bool cross_cta = d.gf / 2 != d.gl / 2;
+                            const bool spans_pair = g0 < b1 && g1 > b1 && b0 < b1 && b1 < b2;
+                            side = (g0 <= b0) ? 0 : 1;
+                            const int role = cross_cta ? (d.merger == c ? kMerge : kPublish) : kOut;
+                            if (in_group) {
+                                mode = kOut;
+                            } else if (spans_pair) {
+                                mode = kPair;
+                                post = role;
+                            } else {
+                                mode = role;
+                            }
+                        }
+                        const bool newrow = append && (k == n - 1);
+                        int new_phys = -1, new_off = 0;
+                        if (newrow) {
+                            const int t0 = k * kStageTokens, tl = t0 + nvalid - 1;
+                            const int e = tl / B - t0 / B;
+                            int id = -2;
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                if (q4 == e) id = d.ids[q4] >= 0 ? d.ids[q4] : -2;
+                            new_phys = id;
+                            new_off = tl % B;
+                            flags |= kNewRow;
+                        }
+                        const uint32_t dst = ring + (uint32_t)st * kStageB;
+                        StageMeta* meta = reinterpret_cast<StageMeta*>(bp + (dst - base) + kMetaOff);
+                        meta->s = s;
+                        meta->h = h;
+                        meta->k = k;
+                        meta->n = n;
+                        meta->nvalid = nvalid;
+                        meta->flags = flags;
+                        meta->mode = mode;
+                        meta->post = post;
+                        meta->side = side;
+                        meta->new_phys = new_phys;
+                        meta->new_off = new_off;
+                        const bool defer = !deps_done;   // q and the new rows come after the dependency wait
+                        const int sh = s * Hkv + h;
+                        if (defer) {
+                            qdef[grp * kPStages + i] = (flags & kBegin) ? sh : -1;
+                            ndef[grp * kPStages + i] = newrow ? sh : -1;
+                        }
+                        const int t0 = k * kStageTokens;
+                        const int within = (B > kStageTokens) ? (t0 % B) : 0;
+                        const int nblk = (t0 + nvalid - 1) / B - t0 / B + 1;
+                        uint32_t bytes = 0;
+                        if ((flags & kBegin) && !defer) bytes += group_bytes;
+                        if (newrow && !defer) bytes += 4u * kHeadDim;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (e < nblk && d.ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
+                        if (i >= kPStages) fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&gfull[st], bytes);   // release: the metadata above
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (e < nblk && d.ids[e] >= 0) {
+                                const int row = (d.ids[e] * Hkv + h) * B + within;
+                                const uint32_t box = dst + (uint32_t)(e * 2 * R) * 128u;
+                                tma_load_2d(box, &maps.k, 0, row, &gfull[st]);
+                                tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &gfull[st]);
+                                tma_load_2d(box + kKB, &maps.v, 0, row, &gfull[st]);
+                                tma_load_2d(box + kKB + (uint32_t)R * 128u, &maps.v, 64, row, &gfull[st]);
+                            }
+                        }
+                        if (grp == 0 && i == 0) trace(a.timeline, c, 4);
+                        if ((flags & kBegin) && !defer)
+                            bulk_g2s(dst + kQOff, static_cast<const T*>(a.q) + ((size_t)s * Hq + h * G) * kHeadDim,
+                                     group_bytes, &gfull[st]);
+                        if (newrow && !defer) {
+                            bulk_g2s(dst + kNewOff, static_cast<const T*>(a.k_new) + (size_t)sh * kHeadDim,
+                                     2u * kHeadDim, &gfull[st]);
+                            bulk_g2s(dst + kNewOff + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)sh * kHeadDim,
+                                     2u * kHeadDim, &gfull[st]);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            cur = nxt;
+        }
+        if (!deps_done) dependency_point(i);
+        if (lane == 0) issued[grp] = i;
+    } else if (warp == kEpiWarp) {
+        // ============================ epilogue ============================
+        if (a.early) {
+            grid_dependency_wait();   // outputs, partials and flags belong after this point
+            grid_launch_dependents();
+        }
+        // zero the output rows of empty sequences (sequence s handled by CTA s mod C)
+        {
+            const int32_t* lens = reinterpret_cast<const int32_t*>(a.plan + a.lens_off);
+            for (int s = c; s < a.num_seqs; s += (int)gridDim.x)
+                if (__ldcg(lens + s) == 0) {
+                    uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + (size_t)s * Hq * kHeadDim);
+                    for (int e = lane; e < Hq * kHeadDim / 8; e += 32) o[e] = make_uint4(0, 0, 0, 0);
+                }
+        }
+        if (b0 < b2) {
+            // this CTA's cut segments: the one holding its first chunk (side 0) and, if another,
+            // the one holding its last (side 1)
+            int n_ev = 0;
+            int ev_s[2], ev_h[2], ev_g0[2], ev_cf[2], ev_cl[2], ev_merge[2], ev_side[2];
+            for (int side = 0; side < 2; ++side) {
+                const int g = side == 0 ? b0 : b2 - 1;
+                PlanChunk pc;
+                load_chunk(chunks + g, pc);
+                const int k = pc.k;
+                const int g0 = g - k;
+                if (side == 1 && n_ev > 0 && ev_g0[0] == g0) continue;   // the same segment
+                const int gf = pc.gf, gl = pc.gl;
+                if (gf / 2 == gl / 2) continue;                           // not cut between CTAs
+                ev_s[n_ev] = pc.s;
+                ev_h[n_ev] = pc.h;
+                ev_g0[n_ev] = g0;
+                ev_cf[n_ev] = gf / 2;
+                ev_cl[n_ev] = gl / 2;
+                ev_merge[n_ev] = pc.merger == c;
+                ev_side[n_ev] = (g0 <= b0) ? 0 : 1;
+                ++n_ev;
+            }
+            // lane layout for folds: row r = lane / 4, columns cb .. cb + 31
+            const int r = lane >> 2, cb = (lane & 3) * 32;
+            float accM[2], accD[2], accN[2][32];
+            int cursor[2];     // next remote CTA to fold (merge), 0 / 1 done (publish)
+            bool local_done[2], done[2];
+            for (int e = 0; e < 2; ++e) {
+                accM[e] = -INFINITY;
+                accD[e] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) accN[e][j] = 0.f;
+                cursor[e] = e < n_ev ? ev_cf[e] : 0;
+                local_done[e] = false;
+                done[e] = e >= n_ev;
+            }
+            auto fold = [&](int e, float m, float l, const float (&o)[32]) {
+                const float Mn = fmaxf(accM[e], m);
+                const float x = (accM[e] == -INFINITY) ? 0.f : exp2f(accM[e] - Mn);
+                const float y = exp2f(m - Mn);
+                accD[e] = accD[e] * x + l * y;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) accN[e][j] = accN[e][j] * x + o[j] * y;
+                accM[e] = Mn;
+            };
+            const unsigned long long t_start = global_timer_ns();
+            bool gave_up = false;
+            while (!(done[0] && done[1])) {
+                if (*abort_flag) break;
+                bool progress = false;
+                for (int e = 0; e < n_ev; ++e) {
+                    if (done[e]) continue;
+                    const int side = ev_side[e];
+                    if (!ev_merge[e]) {
+                        // publisher: the consumers have stored this CTA's partial; release it
+                        if (mbar_test(&ready[side], 0u)) {
+                            if (lane == 0) {
+                                trace(a.timeline, c, side ? 11 : 1);
+                                st_release_gpu(&a.part_flag[2 * c + side], 1);
+                                trace(a.timeline, c, side ? 13 : 2);
+                            }
+                            done[e] = true;
+                            progress = true;
+                        }
+                        continue;
+                    }
+                    // merger: fold the other CTAs' pieces as their flags appear, in CTA order
+                    while (cursor[e] <= ev_cl[e]) {
+                        const int cc = cursor[e];
+                        const int cb0 = __ldcg(bounds + 2 * cc);
+                        if (cc == c || cb0 == __ldcg(bounds + 2 * cc + 2)) {   // this CTA, or a CTA without chunks
+                            ++cursor[e];
+                            continue;
+                        }
+                        const int slot = 2 * cc + ((ev_g0[e] <= cb0) ? 0 : 1);
+                        if (ld_acquire_gpu(&a.part_flag[slot]) == 0) break;
+                        const float2 ml = a.part_ml[(size_t)slot * kRows + r];
+                        float o[32];
+                        const float* src = a.part_o + ((size_t)slot * kRows + r) * kHeadDim + cb;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(src + j);
+                            o[j] = v.x;
+                            o[j + 1] = v.y;
+                            o[j + 2] = v.z;
+                            o[j + 3] = v.w;
+                        }
+                        fold(e, ml.x, ml.y, o);
+                        __syncwarp();
+                        if (lane == 0) a.part_flag[slot] = 0;   // ready for the next launch
+                        ++cursor[e];
+                        progress = true;
+                    }
+                    if (!local_done[e] && mbar_test(&ready[side], 0u)) {
+                        const float* so = reinterpret_cast<const float*>(bp + kHandOff + side * kSlotB);
+                        const float2* sml = reinterpret_cast<const float2*>(bp + kHandOff + side * kSlotB +
+                                                                            kRows * kHeadDim * 4);
+                        const float2 ml = sml[r];
+                        float o[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = so[r * kHeadDim + cb + j];
+                        fold(e, ml.x, ml.y, o);
+                        local_done[e] = true;
+                        progress = true;
+                        if (lane == 0) trace(a.timeline, c, side ? 11 : 1);
+                    }
+                    if (local_done[e] && cursor[e] > ev_cl[e]) {
+                        if (r < G) {
+                            const float inv = 1.f / accD[e];
+                            uint4* dst = reinterpret_cast<uint4*>(
+                                static_cast<T*>(a.out) + ((size_t)ev_s[e] * Hq + (size_t)ev_h[e] * G + r) * kHeadDim + cb);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                float v8[8];
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) v8[j] = accN[e][q4 * 8 + j];
+                                dst[q4] = pack8<T>(v8, inv);
+                            }
+                        }
+                        if (lane == 0 && a.timeline) {
+                            a.timeline[(size_t)c * kTimelineSlots + 12] += 1;
+                            trace(a.timeline, c, side ? 13 : 2);
+                        }
+                        done[e] = true;
+                        progress = true;
+                    }
+                }
+                if (!progress) {
+                    if (global_timer_ns() - t_start > kWaitLimitNs) {
+                        gave_up = true;
+                        break;
+                    }
+                    __nanosleep(128);   // leave the issue slots to the consumers sharing this scheduler
+                }
+            }
+            if (gave_up && lane == 0) {
+                flag_status(a.status, PA_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        if (lane == 0) trace(a.timeline, c, 10);
+    } else {
+        // ============================ consumers of one group ============================
+        const int grp = warp / kGroupWarps, wq = warp % kGroupWarps, tg = tid - grp * kGroupThreads;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int t_warp = wq * 16;
+        const int lo = grp ? b1 : b0, hi = grp ? b2 : b1;
+        const int cnt = hi - lo;
+        uint64_t* gfull = full + grp * kPStages;
+        uint64_t* gempty = empty + grp * kPStages;
+        const uint32_t ring = base + (uint32_t)grp * kPStages * kStageB;
+        unsigned char* ring_p = bp + (size_t)grp * kPStages * kStageB;
+        const int tokA = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int chA = lane >> 4;
+        const int tokV = t_warp + (lane & 7) + ((lane >> 4) << 3);
+        const int chV = (lane >> 3) & 1;
+        float m_run[2], l_run[2], o[8][4];
+        uint32_t qb[8][2];
+        if (a.early) {
+            grid_dependency_wait();   // q, the new rows and every output belong after this point
+            grid_launch_dependents();
+        }
+        // A warp that gave up on a wait is "dead": it keeps walking the group's chunks without
+        // waiting or writing.  Warps die only on the group's shared barriers (a stage that never
+        // lands times every warp of the group out at the same chunk), so all four keep taking
+        // the same named-barrier path through the segment ends.
+        bool dead = false;
+        for (int i = 0; i < cnt; ++i) {
+            const int st = i % kPStages;
+            if (!dead && !__all_sync(0xffffffffu, mbar_wait_bounded(&gfull[st], (uint32_t)(i / kPStages) & 1u))) {
+                if (lane == 0) {
+                    flag_status(a.status, PA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                dead = true;
+            }
+            if (grp == 0 && tid == 0 && a.timeline) {
+                if (i == 0) trace(a.timeline, c, 5);
+                if (i == cnt - 1) trace(a.timeline, c, 6);
+            }
+            const uint32_t kbase = ring + (uint32_t)st * kStageB;
+            const uint32_t vbase = kbase + kKB;
+            unsigned char* stage_p = ring_p + (size_t)st * kStageB;
+            const StageMeta* meta = reinterpret_cast<const StageMeta*>(stage_p + kMetaOff);
+            const int flags = dead ? 0 : meta->flags;
+            const int nvalid = dead ? 0 : meta->nvalid;
+            if ((flags & (kBegin | kNewRow)) && a.early && i < kPStages) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&qbar[grp], 0u))) {
+                    if (lane == 0) {
+                        flag_status(a.status, PA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    dead = true;
+                }
+            }
+            if ((flags & kBegin) && !dead) {
+                const uint32_t* qs = reinterpret_cast<const uint32_t*>(stage_p + kQOff);
+                const int row = gid;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int wcol = (ks * 16 + tig * 2) >> 1;
+                    qb[ks][0] = (row < G) ? qs[row * 64 + wcol] : 0u;
+                    qb[ks][1] = (row < G) ? qs[row * 64 + wcol + 4] : 0u;
+                }
+                m_run[0] = m_run[1] = -INFINITY;
+                l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            }
+            if (t_warp < nvalid && !dead) {
+                if (nvalid < t_warp + 16) {
+                    // V rows past the context: stale pool rows must not meet P = 0 as non-finite values
+                    uint4* vz = reinterpret_cast<uint4*>(stage_p + kKB);
+                    for (int idx = lane; idx < (t_warp + 16 - nvalid) * 16; idx += 32) {
+                        const int t = nvalid + (idx >> 4);
+                        const int cc = idx & 15;
+                        vz[line_of(t, cc >> 3, R_log2) * 8 + (cc & 7)] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const int tn = nvalid - 1;
+                if ((flags & kNewRow) && (tn >> 4) == wq) {
+                    // the new K/V row: into the staged tile and into its cache slot
+                    const int cc = lane & 15;
+                    const bool isv = lane >= 16;
+                    const uint4 val = *reinterpret_cast<const uint4*>(stage_p + kNewOff + (isv ? 2u * kHeadDim : 0u) +
+                                                                      cc * 16);
+                    st_shared_v4(chunk_addr(isv ? vbase : kbase, tn, cc, R_log2), val);
+                    const int phys = meta->new_phys;
+                    if (phys >= 0) {
+                        const size_t row = ((size_t)phys * Hkv + meta->h) * B + (size_t)meta->new_off;
+                        T* cache = const_cast<T*>(static_cast<const T*>(isv ? a.v_cache : a.k_cache));
+                        *reinterpret_cast<uint4*>(cache + row * kHeadDim + cc * 8) = val;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                // S^T = K Q^T over the warp's 16 tokens, two accumulator chains
+                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(chunk_addr(kbase, tokA, 2 * ks + chA, R_log2), a0, a1, a2, a3);
+                    if (ks & 1) mma16816<T>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    else mma16816<T>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+                const bool in0 = t_warp + gid < nvalid, in1 = t_warp + gid + 8 < nvalid;
+                constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+                float xs[4];
+                bool move = false;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    xs[j] = in0 ? (sc[j] + sc2[j]) * a.scale_log2 : -INFINITY;
+                    xs[2 + j] = in1 ? (sc[2 + j] + sc2[2 + j]) * a.scale_log2 : -INFINITY;
+                    move = move || xs[j] > m_run[j] + kLazyLog2 || xs[2 + j] > m_run[j] + kLazyLog2;
+                }
+                if (__any_sync(0xffffffffu, move)) {
+                    float alpha[2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float mx = fmaxf(xs[j], xs[2 + j]);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[j], mx);
+                        alpha[j] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[j] - m_new);
+                        m_run[j] = m_new;
+                        l_run[j] *= alpha[j];
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        o[mt][0] *= alpha[0];
+                        o[mt][1] *= alpha[1];
+                        o[mt][2] *= alpha[0];
+                        o[mt][3] *= alpha[1];
+                    }
+                }
+                float pv[4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float m_use = (m_run[j] == -INFINITY) ? 0.f : m_run[j];
+                    pv[j] = exp2f(xs[j] - m_use);
+                    pv[2 + j] = exp2f(xs[2 + j] - m_use);
+                    l_run[j] += pv[j] + pv[2 + j];
+                }
+                const uint32_t h0 = Elem<T>::pack2(pv[0], pv[1]), h1 = Elem<T>::pack2(pv[2], pv[3]);
+                const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
+                uint32_t pl0 = 0, pl1 = 0;
+                if (kSplitP) {
+                    const float2 r0 = Elem<T>::to_float2(h0), r1 = Elem<T>::to_float2(h1);
+                    pl0 = movmatrix_trans(Elem<T>::pack2(pv[0] - r0.x, pv[1] - r0.y));
+                    pl1 = movmatrix_trans(Elem<T>::pack2(pv[2] - r1.x, pv[3] - r1.y));
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(chunk_addr(vbase, tokV, 2 * mt + chV, R_log2), a0, a1, a2, a3);
+                    mma16816<T>(o[mt], a0, a1, a2, a3, pb0, pb1);
+                    if (kSplitP) mma16816<T>(o[mt], a0, a1, a2, a3, pl0, pl1);
+                }
+            }
+
+            if (flags & kEnd) {
+                // ---- the segment's last chunk in this group's order: merge the four warps ----
+                float lr[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float v = l_run[j];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    lr[j] = v;
+                }
+                float* red_o = reinterpret_cast<float*>(stage_p);                                  // [4][8][kRedStride]
+                float2* red_ml = reinterpret_cast<float2*>(red_o + kGroupWarps * 8 * kRedStride);  // [4][8]
+                group_sync(grp);   // every warp is past its reads of the stage
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int row = tig * 2 + j;
+                    float* dst = &red_o[(wq * 8 + row) * kRedStride + gid];
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        dst[mt * 16] = o[mt][j];
+                        dst[mt * 16 + 8] = o[mt][2 + j];
+                    }
+                    if (gid == 0) red_ml[wq * 8 + row] = make_float2(m_run[j], lr[j]);
+                }
+                group_sync(grp);
+                const int r = tg >> 4, d0 = (tg & 15) * 8;
+                Fold8 f;
+                f.init();
+                {
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w2 = 0; w2 < kGroupWarps; ++w2) M = fmaxf(M, red_ml[w2 * 8 + r].x);
+                    f.M = M;
+#pragma unroll
+                    for (int w2 = 0; w2 < kGroupWarps; ++w2) {
+                        const float2 ml = red_ml[w2 * 8 + r];
+                        // a warp without a valid token (m = -inf) weighs 0
+                        const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                        f.den = fmaf(wgt, ml.y, f.den);
+                        const float4 x0 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0]);
+                        const float4 x1 = *reinterpret_cast<const float4*>(&red_o[(w2 * 8 + r) * kRedStride + d0 + 4]);
+                        f.num[0] = fmaf(wgt, x0.x, f.num[0]);
+                        f.num[1] = fmaf(wgt, x0.y, f.num[1]);
+                        f.num[2] = fmaf(wgt, x0.z, f.num[2]);
+                        f.num[3] = fmaf(wgt, x0.w, f.num[3]);
+                        f.num[4] = fmaf(wgt, x1.x, f.num[4]);
+                        f.num[5] = fmaf(wgt, x1.y, f.num[5]);
+                        f.num[6] = fmaf(wgt, x1.z, f.num[6]);
+                        f.num[7] = fmaf(wgt, x1.w, f.num[7]);
+                    }
+                }
+                const int s = meta->s, h = meta->h, side = meta->side;
+                int mode = dead ? -1 : meta->mode;
+                if (mode == kPair) {
+                    // the two groups of this CTA meet: the first to arrive leaves its piece in the
+                    // pair slot, the second folds it in and carries on with the segment
+                    if (tg == 0) pair_role[grp] = atomicAdd(const_cast<int*>(pair_count), 1);
+                    group_sync(grp);
+                    if (pair_role[grp] == 0) {
+                        slot_store(pair_o, pair_ml, r, d0, f, (tg & 15) == 0);
+                        mbar_arrive(pair_bar);
+                        mode = -1;
+                    } else {
+                        if (!mbar_wait_bounded(pair_bar, 0u)) {
+                            flag_status(a.status, PA_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                            mode = -1;
+                        } else {
+                            const float2 ml = pair_ml[r];
+                            float ov[8];
+                            const float4 x0 = *reinterpret_cast<const float4*>(pair_o + r * kHeadDim + d0);
+                            const float4 x1 = *reinterpret_cast<const float4*>(pair_o + r * kHeadDim + d0 + 4);
+                            ov[0] = x0.x; ov[1] = x0.y; ov[2] = x0.z; ov[3] = x0.w;
+                            ov[4] = x1.x; ov[5] = x1.y; ov[6] = x1.z; ov[7] = x1.w;
+                            f.add(ml.x, ml.y, ov);
+                            mode = meta->post;
+                        }
+                    }
+                }
+                if (mode == kOut) {
+                    if (r < G) {
+                        const float inv = 1.f / f.den;
+                        *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)s * Hq + (size_t)h * G + r) * kHeadDim +
+                                                  d0) = pack8<T>(f.num, inv);
+                    }
+                } else if (mode == kPublish) {
+                    const size_t slot = (size_t)2 * c + side;
+                    slot_store(a.part_o + slot * kRows * kHeadDim, a.part_ml + slot * kRows, r, d0, f, (tg & 15) == 0);
+                    mbar_arrive(&ready[side]);   // the epilogue warp releases the flag after these stores
+                } else if (mode == kMerge) {
+                    float* so = reinterpret_cast<float*>(bp + kHandOff + side * kSlotB);
+                    float2* sml = reinterpret_cast<float2*>(bp + kHandOff + side * kSlotB + kRows * kHeadDim * 4);
+                    slot_store(so, sml, r, d0, f, (tg & 15) == 0);
+                    mbar_arrive(&ready[side]);
+                }
+                group_sync(grp);   // the scratch (this stage) is free again
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(&gempty[st]);
+        }
+        if (grp == 0 && tid == 0) trace(a.timeline, c, 7);
+        if (grp == 1 && tg == 0) trace(a.timeline, c, 9);
+    }
+
+    __syncthreads();
+    if (tid == 0 && a.timeline) {
+        trace(a.timeline, c, 8);
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        trace_put(a.timeline, c, 14, (unsigned long long)(b2 - b0));
+        trace_put(a.timeline, c, 15, smid);
+    }
+    if (*abort_flag && tid == 0) {
+        // let every copy still in flight land before the CTA's shared memory is released
+        for (int grp = 0; grp < kGroups; ++grp) {
+            const int n = issued[grp];
+            for (int st = 0; st < kPStages; ++st) {
+                int last = -1;
+                for (int i = st; i < n; i += kPStages) last = i;
+                if (last >= 0) (void)mbar_wait_bounded(&full[grp * kPStages + st], (uint32_t)(last / kPStages) & 1u);
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_planned_impl(const PlannedArgs& a, const MmaMapsP& maps, int R_log2, int ctas, cudaStream_t stream) {
+    static std::atomic<unsigned long long> configured{0};
+    auto kernel = decode_planned_kernel<T>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemPlanned);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kSmemPlanned;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a, maps, R_log2);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
+
+}  // namespace
+
+int planned_ctas(const pa_decode_options* opts) {
+    const int sms = sm_count_current();
+    if (opts && opts->num_ctas > 0) return opts->num_ctas < sms ? opts->num_ctas : sms;
+    return sms;
+}
+
+size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
+    return plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas).total;
+}
+
+size_t planned_workspace_bytes(int ctas) {
+    const size_t slots = (size_t)2 * ctas;
+    return al256(slots * kRows * kHeadDim * sizeof(float)) + al256(slots * kRows * sizeof(float2)) +
+           al256(slots * sizeof(int));
+}
+
+cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                               int max_blocks_per_seq, int ctas, cudaStream_t stream) {
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    PlanArgs a;
+    a.plan = static_cast<unsigned char*>(plan);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.status = device_status_ptr();
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.ctas = ctas;
+    a.lens_off = L.lens;
+    a.bounds_off = L.bounds;
+    a.chunks_off = L.chunks;
+    a.max_chunks = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
+    long long blocks = (a.max_chunks + kPlanThreads - 1) / kPlanThreads;
+    const long long cap = 4LL * sm_count_current();
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    const size_t smem = (size_t)(3 * num_seqs + 1) * sizeof(int);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_plan_kernel, a);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+}
+
+cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                  const void* v_cache, const void* plan, void* workspace, float scale, int num_seqs,
+                                  int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                  int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                  unsigned long long* timeline, cudaStream_t stream) {
+    const int R = block_size < kStageTokens ? block_size : kStageTokens;
+    int R_log2 = 0;
+    while ((1 << R_log2) < R) ++R_log2;
+    const unsigned long long rows = (unsigned long long)num_blocks * num_kv_heads * block_size;
+    if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
+    MmaMapsP maps;
+    if (!encode_pool_map(k_cache, rows, R, &maps.k) || !encode_pool_map(v_cache, rows, R, &maps.v))
+        return cudaErrorInvalidValue;
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    PlannedArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.plan = static_cast<const unsigned char*>(plan);
+    const size_t slots = (size_t)2 * ctas;
+    char* w = static_cast<char*>(workspace);
+    a.part_o = reinterpret_cast<float*>(w);
+    a.part_ml = reinterpret_cast<float2*>(w + al256(slots * kRows * kHeadDim * sizeof(float)));
+    a.part_flag = reinterpret_cast<int*>(w + al256(slots * kRows * kHeadDim * sizeof(float)) +
+                                         al256(slots * kRows * sizeof(float2)));
+    a.status = device_status_ptr();
+    a.timeline = timeline;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.early = early ? 1 : 0;
+    a.lens_off = L.lens;
+    a.bounds_off = L.bounds;
+    a.chunks_off = L.chunks;
+    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16>(a, maps, R_log2, ctas, stream)
+                            : launch_planned_impl<__half>(a, maps, R_log2, ctas, stream);
+}
+
+}  // namespace pa

@@ -291,6 +291,20 @@ cudaError_t launch_prefill_mma(const DecodeArgs& a, int dtype, cudaStream_t stre
 // Several query tokens per sequence beyond 16 rows on tcgen05 tiles of 128 rows.
 cudaError_t launch_prefill_tc(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
+// Planned decode (decode_planned.cu): the per-step plan and the per-layer launch that reads it.
+constexpr int kPlanMaxSeqs = 1024;      // sequences the plan kernel keeps in shared memory
+int planned_ctas(const pa_decode_options* opts);
+size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas);
+size_t planned_workspace_bytes(int ctas);
+cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                               int max_blocks_per_seq, int ctas, cudaStream_t stream);
+cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                  const void* v_cache, const void* plan, void* workspace, float scale, int num_seqs,
+                                  int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                  int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                  unsigned long long* timeline, cudaStream_t stream);
+
 // Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.
 cudaError_t launch_decode_split_mma(const DecodeArgs& a, int dtype, cudaStream_t stream);
 bool mma_supports_group(int group);
