@@ -205,7 +205,7 @@ class Step:
             # every layer's decode
             self.plan = pa.decode_plan(self.bt, self.lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size,
                                        wl.num_blocks, num_ctas=num_ctas)
-            self.ws = pa.new_workspace(pa.planned_workspace_size(num_ctas), device)
+            self.ws = pa.new_planned_workspace(num_ctas, device)
         self.tps = pa.plan_tokens_per_split(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
         self.graph = None
         self.ev = None
@@ -374,6 +374,18 @@ def run_ours(args):
     # e2e through the public API with host buffers: H2D of the step's inputs, D2H of its outputs
     e2e = run_e2e(st, wl, args, step_bytes) if rank == 0 else None
 
+    # every configuration, one layer timed alone, with its raw error against the oracle
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        del st
+        torch.cuda.empty_cache()
+        per_config = {}
+        with ClockSampler(local) as clk_pc:
+            for cfg, B in PER_CONFIG:
+                key = f"config{cfg}" + (f"_B{B}" if B else "")
+                per_config[key] = time_config(cfg, B, dev, 30, 3, args.num_ctas, errors=not args.no_cpu_baseline)
+        per_config["clocks"] = clk_pc.summary()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, budget_s=args.cpu_seconds)
@@ -401,6 +413,7 @@ def run_ours(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "per_config": per_config,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
@@ -756,64 +769,133 @@ def run_multi_query(args, new_tokens: int = 2):
     print(json.dumps(line), flush=True)
 
 
-def run_config(args):
-    """One decode layer of another seeded configuration, timed alone: the cache write of each
-    sequence's new token plus decode attention (pa_decode_append), the L2 flushed (a 512 MB
-    write) before every timed launch, mean of ``--steps`` launches by CUDA events (each event
-    pair resolves about 2 us; the mean of many resolves finer).  Config 2
-    rotates over 4 layer caches; config 5 is served from L2 by design (its shared prefix is
-    read by all 128 sequences), so its bytes are logical ones."""
-    import paged_kv_cache_08_gb300 as pa
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    cfg = args.config
-    layers = 4 if cfg == 2 else 1
-    wl = workloads.config(cfg, device=dev, layers=layers, block_size=args.block_size)
-    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
-    kcs = [wl.k_cache[i].clone() for i in range(layers)]
-    vcs = [wl.v_cache[i].clone() for i in range(layers)]
-    outs = [torch.empty_like(wl.q[i]) for i in range(layers)]
-    ws = pa.new_workspace(pa.decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                                                   wl.block_size, wl.max_blocks_per_seq), dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+def _half_ulp(t: torch.Tensor):
+    """Half the spacing from |t| to the next representable magnitude of t's 16-bit dtype."""
+    import numpy as np
+    bits = t.detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint32) & 0x7FFF
+    if t.dtype == torch.bfloat16:
+        lo = (bits << 16).view(np.float32).astype(np.float64)
+        hi = ((bits + 1) << 16).view(np.float32).astype(np.float64)
+    else:
+        lo = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+        hi = (bits + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    return (hi - lo) / 2
 
-    def launch(i):
-        pa.decode_append(wl.q[i], wl.k_new[i], wl.v_new[i], kcs[i], vcs[i], bt, lens, wl.scale, wl.num_kv_heads,
-                         out=outs[i], workspace=ws, num_ctas=args.num_ctas)
-    for i in range(max(args.warmup, layers)):
-        launch(i % layers)
-    torch.cuda.synchronize()
-    times = []
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clk:
-        for r in range(args.steps):
+
+def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: int = 0, errors: bool = True):
+    """One decode layer (the cache write of each sequence's new token plus attention) of a seeded
+    configuration, timed alone: the step's plan built first (pa_decode_plan, timed separately),
+    then ``steps`` pa_decode_planned launches, each after a 512 MB write that flushes the L2, by
+    CUDA events (mean; one event pair resolves about 2 us, the mean of many finer).  The per-layer
+    persistent launch (pa_decode_append) is timed the same way beside it.  With ``errors`` the
+    output of one launch on fresh caches is compared with the fp64 oracle's on the host: the raw
+    max-abs error, and the error beyond the output dtype's own rounding (bf16)."""
+    import numpy as np
+    import paged_kv_cache_08_gb300 as pa
+    wl = workloads.config(cfg, device=dev, layers=1, block_size=block_size)
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    q, kn, vn = wl.q[0], wl.k_new[0], wl.v_new[0]
+    kc0, vc0 = wl.k_cache[0], wl.v_cache[0]
+    kc, vc = kc0.clone(), vc0.clone()
+    out = torch.empty_like(q)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
             flush.zero_()
+            a, b = ev(), ev()
             a.record()
-            launch(r % layers)
+            fn()
             b.record()
             torch.cuda.synchronize()
-            times.append(a.elapsed_time(b))
-    ms = statistics.fmean(times)
+            ts.append(a.elapsed_time(b))
+        return statistics.fmean(ts), statistics.median(ts)
+
+    res = {}
+    plan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, num_ctas=num_ctas)
+    ws = pa.new_planned_workspace(num_ctas, dev)
+
+    def planned():
+        pa.decode_planned(q, kc, vc, plan, wl.scale, k_new=kn, v_new=vn, out=out, workspace=ws)
+
+    def replan():
+        pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, plan=plan,
+                       num_ctas=num_ctas)
+    uws = pa.new_workspace(pa.decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                                    wl.block_size, wl.max_blocks_per_seq), dev)
+
+    def unplanned():
+        pa.decode_append(q, kn, vn, kc, vc, bt, lens, wl.scale, wl.num_kv_heads, out=out, workspace=uws)
+    for fn in (planned, unplanned, replan):
+        for _ in range(max(3, warmup)):
+            fn()
+    torch.cuda.synchronize()
+    ms, med = timed(planned, steps)
+    ms_u, _ = timed(unplanned, steps)
+    ms_p, _ = timed(replan, max(10, steps // 3))
     nbytes = decode_bytes(wl) + cache_write_bytes(wl)
-    gbs = nbytes / (ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak_gbs()
-    B = wl.block_size
-    line = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": f"config{cfg}_{wl.num_seqs}seq_gqa{wl.num_q_heads}x{wl.num_kv_heads}_{wl.dtype}_B{B}",
-                       "step": "one pa_decode_append launch, timed alone (mean)", "layers_rotated": layers,
-                       "median_ms": round(statistics.median(times), 5),
-                       "l2": "flushed (512 MB write) before every timed launch",
-                       "kv_tokens_per_s": round(float(wl.context_lens.sum()) / (ms * 1e-3), 1)},
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4),
-                         "traffic": profiled_traffic("paged_kv_cache_08_gb300/csrc/decode_persist.cu",
-                                                     f"config{cfg}" + (f"_B{B}" if cfg == 5 else "")),
-                         "algorithmic_bytes_per_launch": nbytes,
-                         "kernel": "pa_decode_append", "peak_source": f"{peak_kind} copy bandwidth"},
-            "gpu_launches": args.steps, "clocks": clk.summary()}
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res.update({"workload": f"config{cfg}_{wl.num_seqs}seq_gqa{wl.num_q_heads}x{wl.num_kv_heads}_{wl.dtype}"
+                            f"_B{wl.block_size}",
+                "dtype": wl.dtype, "us": round(ms * 1e3, 2), "median_us": round(med * 1e3, 2),
+                "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+                "frac_of_8TBs_spec": round(gbs / SPEC_PEAK_GBS, 4), "algorithmic_bytes": nbytes,
+                "kv_tokens_per_s": round(float(wl.context_lens.sum()) / (ms * 1e-3), 1),
+                "kernel": "pa_decode_planned (append)", "plan_us": round(ms_p * 1e3, 2),
+                "per_layer_persistent_us": round(ms_u * 1e3, 2),
+                "per_layer_persistent_gbs": round(nbytes / (ms_u * 1e-3) / 1e9, 1),
+                "peak": peak, "peak_source": f"{peak_kind} copy bandwidth",
+                "l2": "flushed (512 MB write) before every timed launch"})
+    if errors:
+        import oracle as oracle_pkg
+        o = oracle_pkg.get()
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        planned()
+        torch.cuda.synchronize()
+        host = _host_layer(wl, 0)
+        okc = oracle_pkg.as_u16(host.k_cache[0]).copy()
+        ovc = oracle_pkg.as_u16(host.v_cache[0]).copy()
+        t0 = time.perf_counter()
+        slots = o.slot_mapping(host.block_tables, host.context_lens, host.block_size)
+        o.cache_write(host.k_new[0], host.v_new[0], slots, okc, ovc)
+        ref = o.decode(host.q[0], okc, ovc, host.block_tables, host.context_lens, host.scale, host.num_kv_heads,
+                       host.dtype == "bf16")
+        o_s = time.perf_counter() - t0
+        got = out.float().cpu().numpy().astype(np.float64)
+        d = np.abs(got - ref)
+        allow = _half_ulp(out) if out.dtype == torch.bfloat16 else 0.0
+        res.update({"max_abs_err_raw": float(d.max()) if d.size else 0.0,
+                    "max_abs_err_beyond_rounding": float((d - allow).max()) if d.size else 0.0,
+                    "cache_bit_exact": bool(np.array_equal(oracle_pkg.as_u16(kc.cpu()), okc) and
+                                            np.array_equal(oracle_pkg.as_u16(vc.cpu()), ovc)),
+                    "oracle_s": round(o_s, 3), "oracle_cores": o.num_threads()})
+    del wl, kc, vc, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+PER_CONFIG = [(1, None), (2, None), (3, None), (4, None), (5, 16), (5, 32), (5, 64), (5, 128)]
+
+
+def run_config(args):
+    """``--op config``: one configuration through time_config, as one JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    with ClockSampler(0) as clk:
+        r = time_config(args.config, args.block_size, dev, args.steps, args.warmup, args.num_ctas,
+                        errors=not args.no_cpu_baseline)
+    line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(r["us"] / 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
+            "config": {"workload": r["workload"], "step": "one pa_decode_planned launch (plan prebuilt), timed alone"},
+            "roofline": {"bound": "hbm", "achieved": r["value"], "peak": r["peak"], "unit": "GB/s", "frac": r["frac"],
+                         "traffic": None, "algorithmic_bytes_per_launch": r["algorithmic_bytes"],
+                         "kernel": r["kernel"], "peak_source": r["peak_source"]},
+            "detail": r, "gpu_launches": args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 
@@ -952,6 +1034,8 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing every configuration's single layer (and its oracle error) after the step")
     ap.add_argument("--path", choices=["fused", "unplanned", "separate"], default="fused",
                     help="fused: one plan per step + pa_decode_planned (cache write fused) per layer; "
                          "unplanned: pa_decode_append per layer; separate: pa_cache_write + pa_decode")

@@ -256,13 +256,14 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  * pa_decode_planned then computes, per layer, exactly what pa_decode (k_new == NULL) or
  * pa_decode_append (k_new, v_new != NULL: the new token's rows written at position L - 1
  * first) computes, reading the plan instead of the tables and lengths.
- *   plan: device memory of pa_decode_plan_size(...) bytes, 16-byte aligned, caller-owned.
+ *   plan: device memory of pa_decode_plan_size(...) bytes, 16-byte aligned, caller-owned;
+ *     plan_bytes (its size) must cover the call's shape (else PA_ERR_WORKSPACE).
  *     Valid while the tables' entries for positions < L and the lengths stay as they were
  *     when it was built, and only for the same shape and options (num_ctas).
- *   workspace: pa_decode_planned_workspace_size(opts) bytes, 16-byte aligned, ZERO-FILLED
- *     before first use (pa_decode_workspace_init); every completed call leaves it zeroed for
- *     the next (after a call that set PA_DEV_TIMEOUT, zero it again).  Calls that share a
- *     workspace must not overlap on the GPU.
+ *   workspace: pa_decode_planned_workspace_size(opts) bytes, 16-byte aligned, caller-owned,
+ *     FILLED WITH 0xFF BYTES before first use (pa_decode_planned_workspace_init); every
+ *     completed call leaves it so for the next (after a call that set PA_DEV_TIMEOUT, fill it
+ *     again).  Calls that share a workspace must not overlap on the GPU.
  *   opts: num_ctas (<= the SM count; 0 = one CTA per SM), flags (PA_DECODE_EARLY_READS: the
  *     plan and cached rows may be read before the preceding kernel ends; the preceding
  *     kernel must then write none of the plan, the caches or the tables -- in particular a
@@ -278,8 +279,10 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                    int num_blocks, int max_blocks_per_seq, void* stream, const pa_decode_options* opts);
 size_t pa_decode_planned_workspace_size(const pa_decode_options* opts);
+/* Fill `bytes` of a pa_decode_planned workspace with 0xFF on `stream` (cudaMemsetAsync). */
+int pa_decode_planned_workspace_init(void* workspace, size_t bytes, void* stream);
 int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new,
-                      void* k_cache, void* v_cache, const void* plan, float scale,
+                      void* k_cache, void* v_cache, const void* plan, size_t plan_bytes, float scale,
                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       int num_blocks, int max_blocks_per_seq, int dtype,
                       void* workspace, size_t workspace_bytes, void* stream,

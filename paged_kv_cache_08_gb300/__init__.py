@@ -25,7 +25,7 @@ from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
 __all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_planned", "DecodePlan",
-           "planned_workspace_size",
+           "planned_workspace_size", "new_planned_workspace",
            "multi_query", "decode_runs", "gather_runs",
            "SlotPool", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
@@ -289,6 +289,12 @@ def planned_workspace_size(num_ctas: int = 0) -> int:
     return int(lib().pa_decode_planned_workspace_size(ctypes.byref(o)))
 
 
+def new_planned_workspace(num_ctas: int = 0, device=None) -> torch.Tensor:
+    """A pa_decode_planned workspace, filled with 0xFF bytes as the kernel expects."""
+    return torch.full((max(planned_workspace_size(num_ctas), 16),), 255, dtype=torch.uint8,
+                      device=device or "cuda")
+
+
 def decode_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, plan: DecodePlan, scale: float,
                    k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
@@ -320,12 +326,16 @@ def decode_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     o = _opts(0, "auto", plan.num_ctas, timeline, _native.EARLY_READS if early_reads else 0)
-    need = planned_workspace_size(plan.num_ctas)
     if workspace is None:
-        workspace = _workspace(q.device, need, 100, plan.num_ctas)
+        key = ("planned", q.device.index if q.device.index is not None else torch.cuda.current_device(),
+               plan.num_ctas)
+        workspace = _workspaces.get(key)
+        if workspace is None:
+            workspace = _workspaces[key] = new_planned_workspace(plan.num_ctas, q.device)
     rc = lib().pa_decode_planned(out.data_ptr(), q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
                                  v_new.data_ptr() if v_new is not None else None, k_cache.data_ptr(),
-                                 v_cache.data_ptr(), plan.data.data_ptr(), float(scale), S, Hq, Hkv, D, B, NB,
+                                 v_cache.data_ptr(), plan.data.data_ptr(), plan.data.numel(), float(scale), S, Hq,
+                                 Hkv, D, B, NB,
                                  plan.max_blocks_per_seq, _DTYPE[q.dtype], workspace.data_ptr(),
                                  workspace.numel() * workspace.element_size(), _stream_ptr(stream), ctypes.byref(o))
     _native.check("pa_decode_planned", rc)

@@ -67,7 +67,8 @@ _SIGNATURES = {
     "pa_decode_plan": (c_int, [c_vp, c_size, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_vp,
                                ctypes.POINTER(DecodeOptions)]),
     "pa_decode_planned_workspace_size": (c_size, [ctypes.POINTER(DecodeOptions)]),
-    "pa_decode_planned": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32, c_int, c_int, c_int, c_int,
+    "pa_decode_planned_workspace_init": (c_int, [c_vp, c_size, c_vp]),
+    "pa_decode_planned": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_f32, c_int, c_int, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),
     "pa_decode_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pa_decode_workspace_size_ex": (c_size, [c_int, c_int, c_int, c_int, c_int, c_int,

@@ -662,6 +662,16 @@ size_t pa_decode_planned_workspace_size(const pa_decode_options* opts) {
     return planned_workspace_bytes(planned_ctas(opts));
 }
 
+int pa_decode_planned_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (bytes == 0) return PA_OK;
+    if (!workspace) return PA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(workspace, 0xFF, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, const int32_t* context_lens,
                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
                    int max_blocks_per_seq, void* stream, const pa_decode_options* opts) {
@@ -685,7 +695,7 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
 }
 
 int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                      const void* plan, float scale, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      const void* plan, size_t plan_bytes, float scale, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                       int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
                       size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
@@ -701,6 +711,8 @@ int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v
         !aligned16(k_new) || !aligned16(v_new))
         return PA_ERR_INVALID_ARG;
     const int ctas = planned_ctas(opts);
+    if (plan_bytes < planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas))
+        return PA_ERR_WORKSPACE;
     const size_t need = planned_workspace_bytes(ctas);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
     const bool early = opts && (opts->flags & PA_DECODE_EARLY_READS);

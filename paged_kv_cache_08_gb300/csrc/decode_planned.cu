@@ -71,15 +71,15 @@ constexpr uint32_t kHandOff = kPairOff + kSlotB;        // [2 sides] this CTA's 
 constexpr uint32_t kBarOff = kHandOff + 2 * kSlotB;
 // barriers: full[2][3], empty[2][3], qbar[2], pair, ready[2]
 constexpr int kNumBars = 2 * kGroups * kPStages + kGroups + 1 + 2;
-constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+constexpr uint32_t kMiscOff = (kBarOff + kNumBars * 8 + 15u) & ~15u;
 constexpr uint32_t kMiscB = 128;
-constexpr size_t kSmemPlanned = 1024 + kMiscOff + kMiscB;
+constexpr uint32_t kHdrOff = kMiscOff + kMiscB;          // copy of this CTA's plan header (128 B)
+constexpr size_t kSmemPlanned = 1024 + kHdrOff + 128;
+static_assert(kHdrOff % 16 == 0 && kPairOff % 16 == 0 && kHandOff % 16 == 0, "16-byte aligned smem sections");
 static_assert(kSmemPlanned <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
 constexpr float kLazyLog2 = 8.f;
 constexpr int kPlanMagic = 0x31504150;                  // "PAP1"
 
-// Flush modes of a segment's last chunk in a group's order.
-enum : int { kOut = 0, kPair = 1, kPublish = 2, kMerge = 3 };
 // Stage flags.
 enum : int { kBegin = 1, kEnd = 2, kNewRow = 4 };
 
@@ -104,9 +104,33 @@ struct __align__(16) PlanChunk {
 };
 static_assert(sizeof(PlanChunk) == 32, "plan chunk");
 
-// Byte offsets of the plan's sections: header, lengths [S], group bounds [2C + 1], chunks.
+// A cut segment seen from one CTA: the segment holding the CTA's first chunk (side 0) or, if
+// another, its last chunk (side 1), when that segment also has chunks in other CTAs.
+struct PlanEvent {
+    int exists;
+    int g0;             // the segment's first chunk in the list
+    int s, h;
+    int cf, cl;         // first and last CTA holding its chunks
+    int merger;         // 1: this CTA combines the pieces
+    int by_consumers;   // 1: this CTA's piece ends one of its groups' order, the consumers finish it
+    int nrem;           // merger: the other CTAs' published pieces
+    int rem[5];         // merger: their workspace slots (the first five; beyond, from the bounds)
+};
+static_assert(sizeof(PlanEvent) == 56, "plan event");
+
+// Per CTA: its range and its cut segments, then each group's chunks in the order it streams them.
+struct CtaHeader {
+    int b0, b1, b2;     // group 0 streams [b0, b1) forwards, group 1 [b1, b2) backwards
+    int pad;
+    PlanEvent ev[2];
+};
+static_assert(sizeof(CtaHeader) == 128, "CTA header");
+
+// Byte offsets of the plan's sections: header, lengths [S], group bounds [2C + 1], then per CTA
+// its header and two groups of `cap` chunk slots.
 struct PlanLayout {
-    size_t lens, bounds, chunks, total;
+    size_t lens, bounds, cta, cta_bytes, total;
+    int cap;            // chunk slots per group (the largest group of the equal cut)
 };
 
 inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
@@ -119,11 +143,15 @@ __host__ __device__ inline long long plan_max_chunks(int num_seqs, int num_kv_he
 
 PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
     PlanLayout L;
+    const long long maxc = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
+    // the weighted cut gives a group at most (its share of the weight + one chunk) / the lightest
+    // chunk's weight; chunk weights lie within a factor of two, so twice the equal share is room enough
+    L.cap = 2 * (int)((maxc + 2 * ctas - 1) / (2 * ctas)) + 4;
     L.lens = 256;
     L.bounds = L.lens + al256((size_t)num_seqs * 4);
-    L.chunks = L.bounds + al256((size_t)(2 * ctas + 1) * 4);
-    L.total = L.chunks + (size_t)plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq) *
-                             sizeof(PlanChunk);
+    L.cta = L.bounds + al256((size_t)(2 * ctas + 1) * 4);
+    L.cta_bytes = sizeof(CtaHeader) + (size_t)2 * L.cap * sizeof(PlanChunk);
+    L.total = L.cta + (size_t)ctas * L.cta_bytes;
     return L;
 }
 
@@ -137,44 +165,72 @@ struct PlanArgs {
     const int32_t* context_lens;
     unsigned int* status;
     int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq, ctas;
-    size_t lens_off, bounds_off, chunks_off;
+    size_t lens_off, bounds_off, cta_off, cta_bytes;
+    int cap;
     long long max_chunks;
 };
 
 constexpr int kPlanThreads = 256;
 
-// Group bounds of the equal cut: group g streams chunks [N g / G2, N (g + 1) / G2).
-__device__ __forceinline__ long long cut_bound(long long N, int G2, int g) { return N * g / G2; }
-// The group holding chunk x (the largest g with cut_bound(g) <= x).
-__device__ __forceinline__ int group_of(long long N, int G2, long long x) {
-    return (int)(((x + 1) * (long long)G2 - 1) / N);
+// The cut of the chunk list into the 2C group ranges weighs each chunk by what it costs a group:
+// the K/V rows its boxes fetch (a partly valid last block still costs its whole box), a fixed
+// share for the consumers' per-chunk work and, at a segment's last chunk, the four warps' merge
+// and output (row units).  Ranges of many short contexts then get fewer chunks than ranges of
+// long ones.
+constexpr int kWChunk = 16;
+constexpr int kWEnd = 32;
+
+// Weight of one (sequence, kv head) segment of L tokens with boxes of R rows.
+__device__ __forceinline__ long long segment_weight(int L, int R) {
+    if (L <= 0) return 0;
+    const int n = (L + kStageTokens - 1) / kStageTokens;
+    const int last = L - (n - 1) * kStageTokens;                  // valid rows of the last chunk
+    const int last_rows = ((last + R - 1) / R) * R;
+    return (long long)(n - 1) * (kStageTokens + kWChunk) + last_rows + kWChunk + kWEnd;
+}
+
+// The group holding chunk x: the largest g with bnd[g] <= x (bnd ascending, bnd[G2] = N).
+__device__ __forceinline__ int group_of(const int32_t* bnd, int G2, long long x) {
+    int lo = 0, hi = G2 - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (bnd[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 // Whether CTA c's piece of the segment [g0, g1) finishes late: a group streams its range from
 // one end, so a piece that starts its group's order (group 0's first chunks, group 1's last)
 // and is not the whole range is done early; any other piece is done at the group's end.
-__device__ __forceinline__ bool piece_is_late(long long N, int G2, int c, long long g0, long long g1) {
-    const long long b0 = cut_bound(N, G2, 2 * c), b1 = cut_bound(N, G2, 2 * c + 1), b2 = cut_bound(N, G2, 2 * c + 2);
+__device__ __forceinline__ bool piece_is_late(const int32_t* bnd, int c, long long g0, long long g1) {
+    const long long b0 = bnd[2 * c], b1 = bnd[2 * c + 1], b2 = bnd[2 * c + 2];
     if (b0 < b1 && g0 < b1 && g1 > b0 && !(g0 <= b0 && g1 < b1)) return true;
     if (b1 < b2 && g0 < b2 && g1 > b1 && !(g1 >= b2 && g0 > b1)) return true;
     return false;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArgs a) {
-    extern __shared__ int plan_smem[];
+    extern __shared__ long long plan_smem[];
     const int S = a.num_seqs, Hkv = a.num_kv_heads, B = a.block_size;
-    int* nch = plan_smem;             // [S] chunks per kv head of each sequence
-    int* P = nch + S;                 // [S + 1] exclusive prefix of nch
-    int* Ls = P + S + 1;              // [S] clamped lengths
+    const int G2 = 2 * a.ctas;
+    long long* PW = plan_smem;                                     // [S + 1] exclusive prefix of weights
+    int* nch = reinterpret_cast<int*>(PW + S + 1);                 // [S] chunks per kv head of each sequence
+    int* P = nch + S;                                              // [S + 1] exclusive prefix of nch
+    int* Ls = P + S + 1;                                           // [S] clamped lengths
+    int32_t* bnd = Ls + S;                                         // [2C + 1] group bounds
     __shared__ int warp_tot[kPlanThreads / 32];
+    __shared__ long long warp_wt[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long cap = (long long)a.max_blocks_per_seq * B;
+    const int R = B < kStageTokens ? B : kStageTokens;
 
     grid_dependency_wait();
-    // lengths and chunk counts; a thread owns a contiguous run of sequences
+    // lengths, chunk counts and weights; a thread owns a contiguous run of sequences
     const int per = (S + kPlanThreads - 1) / kPlanThreads;
     const int lo = min(S, tid * per), hi = min(S, lo + per);
     int local = 0;
+    long long local_w = 0;
     for (int s = lo; s < hi; ++s) {
         int L = a.context_lens[s];
         if (L < 0 || L > cap) {
@@ -184,36 +240,87 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         Ls[s] = L;
         nch[s] = (L + kStageTokens - 1) / kStageTokens;
         local += nch[s];
+        local_w += (long long)Hkv * segment_weight(L, R);
     }
     int incl = local;
+    long long incl_w = local_w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const long long vw = __shfl_up_sync(0xffffffffu, incl_w, o);
+        if (lane >= o) {
+            incl += v;
+            incl_w += vw;
+        }
     }
-    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 31) {
+        warp_tot[warp] = incl;
+        warp_wt[warp] = incl_w;
+    }
     __syncthreads();
     int run = incl - local, tot = 0;
+    long long run_w = incl_w - local_w, tot_w = 0;
     for (int w = 0; w < kPlanThreads / 32; ++w) {
-        if (w < warp) run += warp_tot[w];
+        if (w < warp) {
+            run += warp_tot[w];
+            run_w += warp_wt[w];
+        }
         tot += warp_tot[w];
+        tot_w += warp_wt[w];
     }
     for (int s = lo; s < hi; ++s) {
         P[s] = run;
+        PW[s] = run_w;
         run += nch[s];
+        run_w += (long long)Hkv * segment_weight(Ls[s], R);
     }
-    if (tid == 0) P[S] = tot;
+    if (tid == 0) {
+        P[S] = tot;
+        PW[S] = tot_w;
+    }
     __syncthreads();
 
     const long long N = (long long)Hkv * tot;
-    const int G2 = 2 * a.ctas;
+    // group bounds: group g starts at the first chunk whose starting weight reaches W g / G2
+    for (int g = tid; g <= G2; g += kPlanThreads) {
+        const long long T = tot_w * g / G2;
+        long long b = N;
+        if (T < tot_w) {
+            int l2 = 0, h2 = S - 1;   // the sequence holding weight position T (empty ones skipped)
+            while (l2 < h2) {
+                const int mid = (l2 + h2 + 1) >> 1;
+                if (PW[mid] <= T) l2 = mid;
+                else h2 = mid - 1;
+            }
+            const int n = nch[l2];
+            const long long ws = segment_weight(Ls[l2], R);
+            const long long o = T - PW[l2];
+            const long long h = o / ws, rem = o - h * ws;
+            const long long k = (rem + kStageTokens + kWChunk - 1) / (kStageTokens + kWChunk);   // ceil
+            b = (long long)Hkv * P[l2] + h * n + (k < n ? k : n);
+        }
+        bnd[g] = (int32_t)b;
+    }
+    __syncthreads();
+
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(a.plan);
     int32_t* lens = reinterpret_cast<int32_t*>(a.plan + a.lens_off);
     int32_t* bounds = reinterpret_cast<int32_t*>(a.plan + a.bounds_off);
-    PlanChunk* chunks = reinterpret_cast<PlanChunk*>(a.plan + a.chunks_off);
+    auto cta_header = [&](int c) { return reinterpret_cast<CtaHeader*>(a.plan + a.cta_off + (size_t)c * a.cta_bytes); };
     if (blockIdx.x == 0) {
         for (int s = tid; s < S; s += kPlanThreads) lens[s] = Ls[s];
-        for (int g = tid; g <= G2; g += kPlanThreads) bounds[g] = (int32_t)(N > 0 ? cut_bound(N, G2, g) : 0);
+        for (int g = tid; g <= G2; g += kPlanThreads) bounds[g] = bnd[g];
+        for (int c = tid; c < a.ctas; c += kPlanThreads) {
+            CtaHeader* ch = cta_header(c);
+            ch->b0 = bnd[2 * c];
+            ch->b1 = bnd[2 * c + 1];
+            ch->b2 = bnd[2 * c + 2];
+            ch->pad = 0;
+            if (bnd[2 * c] == bnd[2 * c + 2]) {   // no chunks: no events (nothing else writes them)
+                ch->ev[0].exists = 0;
+                ch->ev[1].exists = 0;
+            }
+        }
         if (tid == 0) {
             PlanHeader h = {};
             h.magic = kPlanMagic;
@@ -262,23 +369,57 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         d.n = (short)n;
         d.nvalid = (short)(t1 - t0);
         const long long g0 = g - k, g1 = g0 + n;
-        const int gf = group_of(N, G2, g0), gl = group_of(N, G2, g1 - 1);
+        const int gf = group_of(bnd, G2, g0), gl = group_of(bnd, G2, g1 - 1);
         d.gf = (short)gf;
         d.gl = (short)gl;
         int merger = -1;
         if (gf / 2 != gl / 2) {
             merger = gf / 2;
             for (int c = gf / 2; c <= gl / 2; ++c)
-                if (piece_is_late(N, G2, c, g0, g1)) {
+                if (piece_is_late(bnd, c, g0, g1)) {
                     merger = c;
                     break;
                 }
         }
         d.merger = (short)merger;
+        // stored where its group streams it: group 0 forwards from b0, group 1 backwards from b2 - 1
+        const int grp = group_of(bnd, G2, g);
+        const int c = grp / 2, side_g = grp & 1;
+        const long long b0 = bnd[2 * c], b1 = bnd[2 * c + 1], b2 = bnd[2 * c + 2];
+        const long long pos = side_g ? (b2 - 1 - g) : (g - b0);
+        CtaHeader* ch = cta_header(c);
+        PlanChunk* slots = reinterpret_cast<PlanChunk*>(reinterpret_cast<unsigned char*>(ch) + sizeof(CtaHeader));
         const uint4* src = reinterpret_cast<const uint4*>(&d);
-        uint4* dst = reinterpret_cast<uint4*>(chunks + g);
+        uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)side_g * a.cap + pos);
         dst[0] = src[0];
         dst[1] = src[1];
+        // the CTA's cut segments: written by the threads of its first and last chunks
+        for (int side = 0; side < 2; ++side) {
+            if (g != (side == 0 ? b0 : b2 - 1)) continue;
+            PlanEvent ev = {};
+            const bool cross = gf / 2 != gl / 2;
+            ev.exists = cross && (side == 0 || g0 > b0) ? 1 : 0;   // side 1: another segment than side 0's
+            ev.g0 = (int)g0;
+            ev.s = s;
+            ev.h = h;
+            ev.cf = gf / 2;
+            ev.cl = gl / 2;
+            ev.merger = merger == c ? 1 : 0;
+            // the piece ends a group's order: it reaches b1 (side 0) or starts by b1 (side 1), or
+            // the other group is empty
+            ev.by_consumers = side == 0 ? ((b0 < b1) ? (g1 >= b1) : 1) : ((b1 < b2) ? (g0 <= b1) : 1);
+            int nrem = 0;
+            if (ev.merger) {
+                for (int cc = gf / 2; cc <= gl / 2; ++cc) {
+                    const long long cb0 = bnd[2 * cc], cb2 = bnd[2 * cc + 2];
+                    if (cc == c || cb0 == cb2) continue;
+                    if (nrem < 5) ev.rem[nrem] = 2 * cc + (g0 <= cb0 ? 0 : 1);
+                    ++nrem;
+                }
+            }
+            ev.nrem = nrem;
+            ch->ev[side] = ev;
+        }
     }
     grid_launch_dependents();
 }
@@ -296,27 +437,43 @@ struct PlannedArgs {
     const void* v_cache;
     const unsigned char* plan;
     float* part_o;              // [2C][8][D] unnormalised partial outputs of cut segments
-    float2* part_ml;            // [2C][8] (running max in log2 units, sum)
-    int* part_flag;             // [2C] 1 once the partial is published; 0 between launches
+    float2* part_ml;            // [2C][8] (running max in log2 units, sum); every word holds kEmptyWord
+                                // between launches, so that a word another CTA reads is either empty
+                                // or the published value (32-bit words are read and written whole)
     unsigned int* status;
     unsigned long long* timeline;
     float scale_log2;
     int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq;
     int early;
-    size_t lens_off, bounds_off, chunks_off;
+    int cap;                    // chunk slots per group in the plan
+    size_t lens_off, bounds_off, cta_off, cta_bytes;
 };
 
+// Tensor maps of the two pools: boxes of R = min(block_size, 64) rows.
 struct MmaMapsP {
-    CUtensorMap k;
-    CUtensorMap v;
+    CUtensorMap k, v;
 };
+
+// Flush modes of a segment's last chunk in a group's order.
+//   kOut          the segment lies in this group: write the output
+//   kPair         it spans both groups of this CTA: meet the other group in shared memory
+//   kPublish      another CTA merges: store the partial into this CTA's workspace slot (the
+//                 stored words are the publication: the merger waits for them to stop being empty)
+//   kMerge        this CTA merges, its piece ends early: hand it to the epilogue warp
+//   kMergeHere    this CTA merges at the end of this group's order: fold the others' pieces here
+enum : int { kOutM = 0, kPairM = 1, kPublishM = 2, kMergeM = 3, kMergeHereM = 5 };
+
+// The value of every workspace word between launches: a NaN bit pattern no arithmetic here
+// produces (fp32 operations return the canonical 0x7fffffff, and NaN inputs keep part of their
+// fp16/bf16 payload), so a word that differs from it holds a published value.
+constexpr uint32_t kEmptyWord = 0xffffffffu;
 
 struct StageMeta {
     int s, h, k, n;
     int nvalid;
     int flags;        // kBegin / kEnd / kNewRow
     int mode;         // flush mode at kEnd
-    int post;         // after the two groups have met (kPair): kOut, kPublish or kMerge
+    int post;         // after the two groups have met (kPairM): kOutM, kPublishM or kMergeHereM
     int side;         // which of the CTA's two cut segments (0: the one holding its first chunk)
     int new_phys;     // block of the new token (-1: none, -2: outside the pool)
     int new_off;      // its row within the block
@@ -326,6 +483,21 @@ static_assert(sizeof(StageMeta) == 64, "stage metadata");
 
 __device__ __forceinline__ void group_sync(int grp) {
     asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
+}
+
+// A barrier of the group's 128 consumer threads that also returns whether `v` holds in all of
+// them, so that the group takes one decision together.
+__device__ __forceinline__ bool group_all(int grp, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(1 + grp), "n"(kGroupThreads)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
@@ -340,15 +512,32 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// GPU-scope relaxed accesses of the workspace: each 32-bit element is read or written whole.
+__device__ __forceinline__ uint4 ld_relaxed4(const void* p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
     return v;
 }
-
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint2 ld_relaxed2(const void* p) {
+    uint2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
 }
+__device__ __forceinline__ void st_relaxed4(void* p, uint4 v) {
+    asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_relaxed2(void* p, uint2 v) {
+    asm volatile("st.relaxed.gpu.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ bool full4(uint4 v) {
+    return v.x != kEmptyWord && v.y != kEmptyWord && v.z != kEmptyWord && v.w != kEmptyWord;
+}
+
 
 __device__ __forceinline__ void load_chunk(const PlanChunk* src, PlanChunk& d) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
@@ -394,6 +583,64 @@ __device__ __forceinline__ void slot_store(float* o, float2* ml, int r, int d0, 
     if (write_ml) ml[r] = make_float2(f.M, f.den);
 }
 
+__device__ __forceinline__ void slot_load(const float* o, const float2* ml, int r, int d0, float& m, float& l,
+                                          float (&v)[8]) {
+    const float2 x = ml[r];
+    m = x.x;
+    l = x.y;
+    const float4 a0 = *reinterpret_cast<const float4*>(o + r * kHeadDim + d0);
+    const float4 a1 = *reinterpret_cast<const float4*>(o + r * kHeadDim + d0 + 4);
+    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+}
+
+// Publish this thread's share of a partial (row r, columns d0 .. d0 + 7; (m, l) by one thread of
+// the row) into a workspace slot.
+__device__ __forceinline__ void publish8(float* o, float2* ml, int r, int d0, const Fold8& f, bool write_ml) {
+    float* dst = o + r * kHeadDim + d0;
+    st_relaxed4(dst, make_uint4(__float_as_uint(f.num[0]), __float_as_uint(f.num[1]), __float_as_uint(f.num[2]),
+                                __float_as_uint(f.num[3])));
+    st_relaxed4(dst + 4, make_uint4(__float_as_uint(f.num[4]), __float_as_uint(f.num[5]), __float_as_uint(f.num[6]),
+                                    __float_as_uint(f.num[7])));
+    if (write_ml) st_relaxed2(ml + r, make_uint2(__float_as_uint(f.M), __float_as_uint(f.den)));
+}
+
+// Fetch this thread's share of a published partial into (m, l, v) once every word of it has been
+// written; false if some word is still empty.
+__device__ __forceinline__ bool fetch8(const float* o, const float2* ml, int r, int d0, float& m, float& l,
+                                       float (&v)[8]) {
+    const uint4 a0 = ld_relaxed4(o + r * kHeadDim + d0);
+    const uint4 a1 = ld_relaxed4(o + r * kHeadDim + d0 + 4);
+    const uint2 x = ld_relaxed2(ml + r);
+    if (!full4(a0) || !full4(a1) || x.x == kEmptyWord || x.y == kEmptyWord) return false;
+    m = __uint_as_float(x.x);
+    l = __uint_as_float(x.y);
+    v[0] = __uint_as_float(a0.x); v[1] = __uint_as_float(a0.y); v[2] = __uint_as_float(a0.z); v[3] = __uint_as_float(a0.w);
+    v[4] = __uint_as_float(a1.x); v[5] = __uint_as_float(a1.y); v[6] = __uint_as_float(a1.z); v[7] = __uint_as_float(a1.w);
+    return true;
+}
+
+// Return a consumed share to empty for the next launch.
+__device__ __forceinline__ void clear8(float* o, float2* ml, int r, int d0, bool write_ml) {
+    const uint4 e = make_uint4(kEmptyWord, kEmptyWord, kEmptyWord, kEmptyWord);
+    st_relaxed4(o + r * kHeadDim + d0, e);
+    st_relaxed4(o + r * kHeadDim + d0 + 4, e);
+    if (write_ml) st_relaxed2(ml + r, make_uint2(kEmptyWord, kEmptyWord));
+}
+
+// The k-th other CTA's workspace slot for a merge event: from the plan's list for the first
+// five, else counted out of the bounds (CTA order, skipping this CTA and CTAs without chunks).
+__device__ __forceinline__ int remote_slot(const PlanEvent& ev, const int32_t* bounds, int c, int k) {
+    if (k < 5) return ev.rem[k];
+    int seen = 0;
+    for (int cc = ev.cf; cc <= ev.cl; ++cc) {
+        const int cb0 = __ldcg(bounds + 2 * cc);
+        if (cc == c || cb0 == __ldcg(bounds + 2 * cc + 2)) continue;
+        if (seen++ == k) return 2 * cc + (ev.g0 <= cb0 ? 0 : 1);
+    }
+    return 0;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_planned_kernel(const PlannedArgs a, const __grid_constant__ MmaMapsP maps, const int R_log2) {
@@ -414,15 +661,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     volatile int* issued = misc + 4;                        // [2]
     volatile int* qdef = misc + 8;                          // [2][3]: deferred q row (s * Hkv + h) or -1
     volatile int* ndef = misc + 16;                         // [2][3]: deferred new rows (s * Hkv + h) or -1
+    // this CTA's header, copied by each producer before its first stage is released
+    CtaHeader* sh_hdr = reinterpret_cast<CtaHeader*>(bp + kHdrOff);
     float* pair_o = reinterpret_cast<float*>(bp + kPairOff);
     float2* pair_ml = reinterpret_cast<float2*>(bp + kPairOff + kRows * kHeadDim * 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv, B = a.block_size;
-    const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.plan);
     const int32_t* bounds = reinterpret_cast<const int32_t*>(a.plan + a.bounds_off);
-    const PlanChunk* chunks = reinterpret_cast<const PlanChunk*>(a.plan + a.chunks_off);
+    const unsigned char* cta_area = a.plan + a.cta_off + (size_t)c * a.cta_bytes;
+    const CtaHeader* g_hdr = reinterpret_cast<const CtaHeader*>(cta_area);
+    const PlanChunk* slots = reinterpret_cast<const PlanChunk*>(cta_area + sizeof(CtaHeader));
     const bool append = a.k_new != nullptr;
 
     if (tid == 0) {
@@ -445,22 +695,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         fence_mbar_init();
     }
-    if (!a.early) grid_dependency_wait();
-    // the plan must match the launch (checked by every thread on its own: no barrier needed)
-    PlanHeader hd;
-    {
-        const int4* hp = reinterpret_cast<const int4*>(hdr);
-        int4* hq = reinterpret_cast<int4*>(&hd);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) hq[j] = __ldcg(hp + j);
-    }
-    const bool plan_ok = hd.magic == kPlanMagic && hd.num_seqs == a.num_seqs && hd.num_q_heads == Hq &&
-                         hd.num_kv_heads == Hkv && hd.block_size == B && hd.num_blocks == a.num_blocks &&
-                         hd.max_blocks_per_seq == a.max_blocks_per_seq && hd.num_ctas == (int)gridDim.x;
-    const int b0 = plan_ok ? __ldcg(bounds + 2 * c) : 0, b1 = plan_ok ? __ldcg(bounds + 2 * c + 1) : 0,
-              b2 = plan_ok ? __ldcg(bounds + 2 * c + 2) : 0;
     __syncthreads();
+    if (!a.early) grid_dependency_wait();
+    // Every warp reads the plan's header (is it this launch's?) and this CTA's range together in
+    // one round trip; the producers also read their first descriptors in it.
+    const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.plan);
+    const int h_magic = __ldcg(&hdr->magic), h_seqs = __ldcg(&hdr->num_seqs), h_qh = __ldcg(&hdr->num_q_heads),
+              h_kvh = __ldcg(&hdr->num_kv_heads), h_bs = __ldcg(&hdr->block_size), h_nb = __ldcg(&hdr->num_blocks),
+              h_mb = __ldcg(&hdr->max_blocks_per_seq), h_c = __ldcg(&hdr->num_ctas);
+    const int b0 = __ldcg(&g_hdr->b0), b1 = __ldcg(&g_hdr->b1), b2 = __ldcg(&g_hdr->b2);
+    const bool is_prod = warp >= kProdWarp0 && warp < kEpiWarp;
+    const int pgrp = warp - kProdWarp0;
+    const int plo = pgrp ? b1 : b0, phi = pgrp ? b2 : b1;   // producer's group range (valid for producers)
+    PlanChunk cur;
+    if (is_prod && lane < min(32, a.cap)) load_chunk(slots + (size_t)pgrp * a.cap + lane, cur);
+    uint4 hdr_part = make_uint4(0, 0, 0, 0);   // producers: lane j < 8 holds bytes 16 j .. of the CTA header
+    if (is_prod && lane < 8) hdr_part = __ldcg(reinterpret_cast<const uint4*>(g_hdr) + lane);
+    const bool plan_ok = h_magic == kPlanMagic && h_seqs == a.num_seqs && h_qh == Hq && h_kvh == Hkv && h_bs == B &&
+                         h_nb == a.num_blocks && h_mb == a.max_blocks_per_seq && h_c == (int)gridDim.x &&
+                         b0 <= b1 && b1 <= b2 && b1 - b0 <= a.cap && b2 - b1 <= a.cap;
     if (!plan_ok) {
+        // the same decision in every thread (same bytes read); nothing was started
         if (a.early) grid_dependency_wait();
         grid_launch_dependents();
         if (tid == 0 && c == 0) flag_status(a.status, PA_DEV_BAD_PLAN);
@@ -468,10 +723,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     if (!a.early) grid_launch_dependents();
 
-    if (warp >= kProdWarp0 && warp < kEpiWarp) {
+    if (is_prod) {
         // ============================ producer of one group ============================
-        const int grp = warp - kProdWarp0;
-        const int lo = grp ? b1 : b0, hi = grp ? b2 : b1;
+        const int grp = pgrp, lo = plo, hi = phi;
         const int cnt = hi - lo;
         auto chunk_at = [&](int p) { return grp ? hi - 1 - p : lo + p; };
         uint64_t* gfull = full + grp * kPStages;
@@ -479,6 +733,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t ring = base + (uint32_t)grp * kPStages * kStageB;
         const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
         const int R = 1 << R_log2;
+        // the CTA header into shared memory (both producers write the same bytes): consumers read it
+        // after a stage of this producer has landed
+        if (lane < 8) reinterpret_cast<uint4*>(sh_hdr)[lane] = hdr_part;
+        __syncwarp();
         bool deps_done = !a.early;
         auto dependency_point = [&](int n_issued) {
             grid_dependency_wait();
@@ -495,7 +753,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const uint32_t dst = ring + (uint32_t)e * kStageB;
                     const int sh = qdef[grp * kPStages + e];
                     if (sh >= 0)
-                        bulk_g2s(dst + kQOff, static_cast<const T*>(a.q) + ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim,
+                        bulk_g2s(dst + kQOff,
+                                 static_cast<const T*>(a.q) + ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim,
                                  group_bytes, &qbar[grp]);
                     const int nh = ndef[grp * kPStages + e];
                     if (nh >= 0) {
@@ -508,14 +767,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             __syncwarp();
         };
-        PlanChunk cur;
-        if (lane < cnt) load_chunk(chunks + chunk_at(lane), cur);
         if (grp == 0 && lane == 0) trace(a.timeline, c, 3);
         bool ok = true;
         int i = 0;
         for (int pb = 0; pb < cnt && ok; pb += 32) {
             PlanChunk nxt;
-            if (pb + 32 + lane < cnt) load_chunk(chunks + chunk_at(pb + 32 + lane), nxt);
+            if (pb + 32 + lane < cnt) load_chunk(slots + (size_t)grp * a.cap + pb + 32 + lane, nxt);
             const int m = min(32, cnt - pb);
             for (int j = 0; j < m; ++j, ++i) {
                 const int st = i % kPStages;
@@ -549,7 +806,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (*abort_flag) {
                         ok = false;
                     } else {
-                        const int g = chunk_at(pb + j);
+                        const int p = pb + j;
+                        const int g = chunk_at(p);
                         const int s = d.s, h = d.h, k = d.k, n = d.n, nvalid = d.nvalid;
                         const int g0 = g - k, g1 = g0 + n;
                         int flags = 0;
@@ -560,18 +818,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             if (k == n - 1 || g == hi - 1) flags |= kBegin;
                             if (k == 0 || g == lo) flags |= kEnd;
                         }
-                        int mode = kOut, post = kOut, side = 0;
+                        int mode = kOutM, post = kOutM, side = 0;
                         if (flags & kEnd) {
                             const bool in_group = g0 >= lo && g1 <= hi;
                             const bool cross_cta = d.gf / 2 != d.gl / 2;
                             const bool spans_pair = g0 < b1 && g1 > b1 && b0 < b1 && b1 < b2;
+                            const bool here = p == cnt - 1;   // the group's last chunk: nothing after it to stream
                             side = (g0 <= b0) ? 0 : 1;
-                            const int role = cross_cta ? (d.merger == c ? kMerge : kPublish) : kOut;
+                            const int role =
+                                cross_cta ? (d.merger == c ? (here ? kMergeHereM : kMergeM) : kPublishM) : kOutM;
                             if (in_group) {
-                                mode = kOut;
+                                mode = kOutM;
                             } else if (spans_pair) {
-                                mode = kPair;
-                                post = role;
+                                mode = kPairM;   // pair pieces end both groups' orders
+                                post = cross_cta ? (d.merger == c ? kMergeHereM : kPublishM) : kOutM;
                             } else {
                                 mode = role;
                             }
@@ -618,7 +878,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         for (int e = 0; e < 4; ++e)
                             if (e < nblk && d.ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
                         if (i >= kPStages) fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(&gfull[st], bytes);   // release: the metadata above
+                        mbar_arrive_expect_tx(&gfull[st], bytes);   // release: the metadata and header above
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             if (e < nblk && d.ids[e] >= 0) {
@@ -637,8 +897,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         if (newrow && !defer) {
                             bulk_g2s(dst + kNewOff, static_cast<const T*>(a.k_new) + (size_t)sh * kHeadDim,
                                      2u * kHeadDim, &gfull[st]);
-                            bulk_g2s(dst + kNewOff + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)sh * kHeadDim,
-                                     2u * kHeadDim, &gfull[st]);
+                            bulk_g2s(dst + kNewOff + 2u * kHeadDim,
+                                     static_cast<const T*>(a.v_new) + (size_t)sh * kHeadDim, 2u * kHeadDim,
+                                     &gfull[st]);
                         }
                     }
                 }
@@ -664,146 +925,96 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int e = lane; e < Hq * kHeadDim / 8; e += 32) o[e] = make_uint4(0, 0, 0, 0);
                 }
         }
-        if (b0 < b2) {
-            // this CTA's cut segments: the one holding its first chunk (side 0) and, if another,
-            // the one holding its last (side 1)
-            int n_ev = 0;
-            int ev_s[2], ev_h[2], ev_g0[2], ev_cf[2], ev_cl[2], ev_merge[2], ev_side[2];
+        // the cut segments this CTA merges whose pieces all end early (no CTA holds a late piece
+        // of them): fold the other CTAs' pieces as their words appear, and this CTA's own
+        PlanEvent ev[2];
+        bool todo[2];
+        for (int side = 0; side < 2; ++side) {
+            // 8-byte loads: the second event sits at a multiple of 8 bytes only
+            const int2* src = reinterpret_cast<const int2*>(&g_hdr->ev[side]);
+            int2* dstv = reinterpret_cast<int2*>(&ev[side]);
+#pragma unroll
+            for (int j = 0; j < 7; ++j) dstv[j] = __ldcg(src + j);
+            todo[side] = b0 < b2 && ev[side].exists && ev[side].merger && !ev[side].by_consumers;
+        }
+        // four fold lanes per row: lane = 4 r + q owns row r, columns 32 q .. 32 q + 31, as four
+        // 8-column shares
+        const int r = lane >> 2, cq = (lane & 3) * 32;
+        Fold8 acc[2][4];
+        int cursor[2];
+        bool local_done[2];
+        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[e][j].init();
+            cursor[e] = 0;
+            local_done[e] = false;
+        }
+        const unsigned long long t_start = global_timer_ns();
+        bool gave_up = false;
+        while (todo[0] || todo[1]) {
+            if (*abort_flag) break;
+            bool progress = false;
             for (int side = 0; side < 2; ++side) {
-                const int g = side == 0 ? b0 : b2 - 1;
-                PlanChunk pc;
-                load_chunk(chunks + g, pc);
-                const int k = pc.k;
-                const int g0 = g - k;
-                if (side == 1 && n_ev > 0 && ev_g0[0] == g0) continue;   // the same segment
-                const int gf = pc.gf, gl = pc.gl;
-                if (gf / 2 == gl / 2) continue;                           // not cut between CTAs
-                ev_s[n_ev] = pc.s;
-                ev_h[n_ev] = pc.h;
-                ev_g0[n_ev] = g0;
-                ev_cf[n_ev] = gf / 2;
-                ev_cl[n_ev] = gl / 2;
-                ev_merge[n_ev] = pc.merger == c;
-                ev_side[n_ev] = (g0 <= b0) ? 0 : 1;
-                ++n_ev;
-            }
-            // lane layout for folds: row r = lane / 4, columns cb .. cb + 31
-            const int r = lane >> 2, cb = (lane & 3) * 32;
-            float accM[2], accD[2], accN[2][32];
-            int cursor[2];     // next remote CTA to fold (merge), 0 / 1 done (publish)
-            bool local_done[2], done[2];
-            for (int e = 0; e < 2; ++e) {
-                accM[e] = -INFINITY;
-                accD[e] = 0.f;
+                if (!todo[side]) continue;
+                const PlanEvent& E = ev[side];
+                // the other CTAs' pieces in order, each once all of its words are there
+                while (cursor[side] < E.nrem) {
+                    const int slot = remote_slot(E, bounds, c, cursor[side]);
+                    float* po = a.part_o + (size_t)slot * kRows * kHeadDim;
+                    float2* pml = a.part_ml + (size_t)slot * kRows;
+                    float m[4], l[4], v[4][8];
+                    bool got = true;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) accN[e][j] = 0.f;
-                cursor[e] = e < n_ev ? ev_cf[e] : 0;
-                local_done[e] = false;
-                done[e] = e >= n_ev;
-            }
-            auto fold = [&](int e, float m, float l, const float (&o)[32]) {
-                const float Mn = fmaxf(accM[e], m);
-                const float x = (accM[e] == -INFINITY) ? 0.f : exp2f(accM[e] - Mn);
-                const float y = exp2f(m - Mn);
-                accD[e] = accD[e] * x + l * y;
+                    for (int j = 0; j < 4; ++j) got = fetch8(po, pml, r, cq + 8 * j, m[j], l[j], v[j]) && got;
+                    if (!__all_sync(0xffffffffu, got)) break;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) accN[e][j] = accN[e][j] * x + o[j] * y;
-                accM[e] = Mn;
-            };
-            const unsigned long long t_start = global_timer_ns();
-            bool gave_up = false;
-            while (!(done[0] && done[1])) {
-                if (*abort_flag) break;
-                bool progress = false;
-                for (int e = 0; e < n_ev; ++e) {
-                    if (done[e]) continue;
-                    const int side = ev_side[e];
-                    if (!ev_merge[e]) {
-                        // publisher: the consumers have stored this CTA's partial; release it
-                        if (mbar_test(&ready[side], 0u)) {
-                            if (lane == 0) {
-                                trace(a.timeline, c, side ? 11 : 1);
-                                st_release_gpu(&a.part_flag[2 * c + side], 1);
-                                trace(a.timeline, c, side ? 13 : 2);
-                            }
-                            done[e] = true;
-                            progress = true;
-                        }
-                        continue;
+                    for (int j = 0; j < 4; ++j) {
+                        acc[side][j].add(m[j], l[j], v[j]);
+                        clear8(po, pml, r, cq + 8 * j, j == 0 && (lane & 3) == 0);
                     }
-                    // merger: fold the other CTAs' pieces as their flags appear, in CTA order
-                    while (cursor[e] <= ev_cl[e]) {
-                        const int cc = cursor[e];
-                        const int cb0 = __ldcg(bounds + 2 * cc);
-                        if (cc == c || cb0 == __ldcg(bounds + 2 * cc + 2)) {   // this CTA, or a CTA without chunks
-                            ++cursor[e];
-                            continue;
-                        }
-                        const int slot = 2 * cc + ((ev_g0[e] <= cb0) ? 0 : 1);
-                        if (ld_acquire_gpu(&a.part_flag[slot]) == 0) break;
-                        const float2 ml = a.part_ml[(size_t)slot * kRows + r];
-                        float o[32];
-                        const float* src = a.part_o + ((size_t)slot * kRows + r) * kHeadDim + cb;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 v = *reinterpret_cast<const float4*>(src + j);
-                            o[j] = v.x;
-                            o[j + 1] = v.y;
-                            o[j + 2] = v.z;
-                            o[j + 3] = v.w;
-                        }
-                        fold(e, ml.x, ml.y, o);
-                        __syncwarp();
-                        if (lane == 0) a.part_flag[slot] = 0;   // ready for the next launch
-                        ++cursor[e];
-                        progress = true;
-                    }
-                    if (!local_done[e] && mbar_test(&ready[side], 0u)) {
-                        const float* so = reinterpret_cast<const float*>(bp + kHandOff + side * kSlotB);
-                        const float2* sml = reinterpret_cast<const float2*>(bp + kHandOff + side * kSlotB +
-                                                                            kRows * kHeadDim * 4);
-                        const float2 ml = sml[r];
-                        float o[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = so[r * kHeadDim + cb + j];
-                        fold(e, ml.x, ml.y, o);
-                        local_done[e] = true;
-                        progress = true;
-                        if (lane == 0) trace(a.timeline, c, side ? 11 : 1);
-                    }
-                    if (local_done[e] && cursor[e] > ev_cl[e]) {
-                        if (r < G) {
-                            const float inv = 1.f / accD[e];
-                            uint4* dst = reinterpret_cast<uint4*>(
-                                static_cast<T*>(a.out) + ((size_t)ev_s[e] * Hq + (size_t)ev_h[e] * G + r) * kHeadDim + cb);
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                float v8[8];
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) v8[j] = accN[e][q4 * 8 + j];
-                                dst[q4] = pack8<T>(v8, inv);
-                            }
-                        }
-                        if (lane == 0 && a.timeline) {
-                            a.timeline[(size_t)c * kTimelineSlots + 12] += 1;
-                            trace(a.timeline, c, side ? 13 : 2);
-                        }
-                        done[e] = true;
-                        progress = true;
-                    }
+                    ++cursor[side];
+                    progress = true;
                 }
-                if (!progress) {
-                    if (global_timer_ns() - t_start > kWaitLimitNs) {
-                        gave_up = true;
-                        break;
+                if (!local_done[side] && mbar_test(&ready[side], 0u)) {
+                    const float* so = reinterpret_cast<const float*>(bp + kHandOff + side * kSlotB);
+                    const float2* sml =
+                        reinterpret_cast<const float2*>(bp + kHandOff + side * kSlotB + kRows * kHeadDim * 4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float m2, l2, v2[8];
+                        slot_load(so, sml, r, cq + 8 * j, m2, l2, v2);
+                        acc[side][j].add(m2, l2, v2);
                     }
-                    __nanosleep(128);   // leave the issue slots to the consumers sharing this scheduler
+                    local_done[side] = true;
+                    progress = true;
+                    if (lane == 0) trace(a.timeline, c, 11);
+                }
+                if (local_done[side] && cursor[side] >= E.nrem) {
+                    if (r < G) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.out) +
+                                                              ((size_t)E.s * Hq + (size_t)E.h * G + r) * kHeadDim + cq);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) dst[j] = pack8<T>(acc[side][j].num, 1.f / acc[side][j].den);
+                    }
+                    if (lane == 0 && a.timeline) {
+                        a.timeline[(size_t)c * kTimelineSlots + 12] += 1;
+                        trace(a.timeline, c, 13);
+                    }
+                    todo[side] = false;
+                    progress = true;
                 }
             }
-            if (gave_up && lane == 0) {
-                flag_status(a.status, PA_DEV_TIMEOUT);
-                *abort_flag = 1;
+            if (!progress) {
+                if (global_timer_ns() - t_start > kWaitLimitNs) {
+                    gave_up = true;
+                    break;
+                }
+                __nanosleep(128);   // leave the issue slots to the consumers sharing this scheduler
             }
+        }
+        if (gave_up && lane == 0) {
+            flag_status(a.status, PA_DEV_TIMEOUT);
+            *abort_flag = 1;
         }
         if (lane == 0) trace(a.timeline, c, 10);
     } else {
@@ -826,6 +1037,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (a.early) {
             grid_dependency_wait();   // q, the new rows and every output belong after this point
             grid_launch_dependents();
+            if (tid == 0) trace(a.timeline, c, 1);
         }
         // A warp that gave up on a wait is "dead": it keeps walking the group's chunks without
         // waiting or writing.  Warps die only on the group's shared barriers (a stage that never
@@ -1022,7 +1234,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 const int s = meta->s, h = meta->h, side = meta->side;
                 int mode = dead ? -1 : meta->mode;
-                if (mode == kPair) {
+                if (mode == kPairM) {
                     // the two groups of this CTA meet: the first to arrive leaves its piece in the
                     // pair slot, the second folds it in and carries on with the segment
                     if (tg == 0) pair_role[grp] = atomicAdd(const_cast<int*>(pair_count), 1);
@@ -1031,34 +1243,80 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         slot_store(pair_o, pair_ml, r, d0, f, (tg & 15) == 0);
                         mbar_arrive(pair_bar);
                         mode = -1;
-                    } else {
-                        if (!mbar_wait_bounded(pair_bar, 0u)) {
+                    } else if (!group_all(grp, mbar_wait_bounded(pair_bar, 0u))) {
+                        if (tg == 0) {
                             flag_status(a.status, PA_DEV_TIMEOUT);
                             *abort_flag = 1;
-                            mode = -1;
-                        } else {
-                            const float2 ml = pair_ml[r];
-                            float ov[8];
-                            const float4 x0 = *reinterpret_cast<const float4*>(pair_o + r * kHeadDim + d0);
-                            const float4 x1 = *reinterpret_cast<const float4*>(pair_o + r * kHeadDim + d0 + 4);
-                            ov[0] = x0.x; ov[1] = x0.y; ov[2] = x0.z; ov[3] = x0.w;
-                            ov[4] = x1.x; ov[5] = x1.y; ov[6] = x1.z; ov[7] = x1.w;
-                            f.add(ml.x, ml.y, ov);
-                            mode = meta->post;
                         }
+                        mode = -1;
+                    } else {
+                        float m2, l2, v2[8];
+                        slot_load(pair_o, pair_ml, r, d0, m2, l2, v2);
+                        f.add(m2, l2, v2);
+                        mode = meta->post;
                     }
                 }
-                if (mode == kOut) {
+                if (mode == kMergeHereM) {
+                    // the last piece of a segment this CTA merges: fold the other CTAs' pieces here,
+                    // up to four at a time with all their loads in flight, each once every word of it
+                    // has been published
+                    const PlanEvent& E = sh_hdr->ev[side];
+                    const int nrem = E.nrem;
+                    const unsigned long long t0 = global_timer_ns();
+                    bool ok = true;
+                    for (int k0 = 0; k0 < nrem && ok; k0 += 4) {
+                        const int kn = min(4, nrem - k0);
+                        int slot[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) slot[j] = j < kn ? remote_slot(E, bounds, c, k0 + j) : 0;
+                        unsigned done_mask = 0, want = (1u << kn) - 1u;
+                        while (done_mask != want) {
+                            float m2[4], l2[4], v2[4][8];
+                            bool got[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                got[j] = false;
+                                if (j < kn && !(done_mask & (1u << j)))
+                                    got[j] = fetch8(a.part_o + (size_t)slot[j] * kRows * kHeadDim,
+                                                    a.part_ml + (size_t)slot[j] * kRows, r, d0, m2[j], l2[j], v2[j]);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (got[j]) {
+                                    f.add(m2[j], l2[j], v2[j]);
+                                    done_mask |= 1u << j;
+                                }
+                            if (done_mask != want && global_timer_ns() - t0 > kWaitLimitNs) break;
+                        }
+                        ok = done_mask == want;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (done_mask & (1u << j))
+                                clear8(a.part_o + (size_t)slot[j] * kRows * kHeadDim, a.part_ml + (size_t)slot[j] * kRows,
+                                       r, d0, (tg & 15) == 0);
+                    }
+                    if (!group_all(grp, ok)) {
+                        if (tg == 0) {
+                            flag_status(a.status, PA_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        mode = -1;
+                    } else {
+                        mode = kOutM;
+                    }
+                    if (tg == 0 && a.timeline) a.timeline[(size_t)c * kTimelineSlots + 12] += 1;
+                }
+                if (mode == kOutM) {
                     if (r < G) {
                         const float inv = 1.f / f.den;
                         *reinterpret_cast<uint4*>(static_cast<T*>(a.out) + ((size_t)s * Hq + (size_t)h * G + r) * kHeadDim +
                                                   d0) = pack8<T>(f.num, inv);
                     }
-                } else if (mode == kPublish) {
+                } else if (mode == kPublishM) {
+                    // the stored words are the publication (the merger waits until none is empty)
                     const size_t slot = (size_t)2 * c + side;
-                    slot_store(a.part_o + slot * kRows * kHeadDim, a.part_ml + slot * kRows, r, d0, f, (tg & 15) == 0);
-                    mbar_arrive(&ready[side]);   // the epilogue warp releases the flag after these stores
-                } else if (mode == kMerge) {
+                    publish8(a.part_o + slot * kRows * kHeadDim, a.part_ml + slot * kRows, r, d0, f, (tg & 15) == 0);
+                } else if (mode == kMergeM) {
                     float* so = reinterpret_cast<float*>(bp + kHandOff + side * kSlotB);
                     float2* sml = reinterpret_cast<float2*>(bp + kHandOff + side * kSlotB + kRows * kHeadDim * 4);
                     slot_store(so, sml, r, d0, f, (tg & 15) == 0);
@@ -1136,8 +1394,7 @@ size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int ma
 
 size_t planned_workspace_bytes(int ctas) {
     const size_t slots = (size_t)2 * ctas;
-    return al256(slots * kRows * kHeadDim * sizeof(float)) + al256(slots * kRows * sizeof(float2)) +
-           al256(slots * sizeof(int));
+    return al256(slots * kRows * kHeadDim * sizeof(float)) + al256(slots * kRows * sizeof(float2));
 }
 
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
@@ -1158,13 +1415,16 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
     a.ctas = ctas;
     a.lens_off = L.lens;
     a.bounds_off = L.bounds;
-    a.chunks_off = L.chunks;
+    a.cta_off = L.cta;
+    a.cta_bytes = L.cta_bytes;
+    a.cap = L.cap;
     a.max_chunks = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
     long long blocks = (a.max_chunks + kPlanThreads - 1) / kPlanThreads;
     const long long cap = 4LL * sm_count_current();
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    const size_t smem = (size_t)(3 * num_seqs + 1) * sizeof(int);
+    const size_t smem = (size_t)(num_seqs + 1) * sizeof(long long) + (size_t)(3 * num_seqs + 1) * sizeof(int) +
+                        (size_t)(2 * ctas + 1) * sizeof(int32_t);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kPlanThreads);
@@ -1206,8 +1466,7 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     char* w = static_cast<char*>(workspace);
     a.part_o = reinterpret_cast<float*>(w);
     a.part_ml = reinterpret_cast<float2*>(w + al256(slots * kRows * kHeadDim * sizeof(float)));
-    a.part_flag = reinterpret_cast<int*>(w + al256(slots * kRows * kHeadDim * sizeof(float)) +
-                                         al256(slots * kRows * sizeof(float2)));
+
     a.status = device_status_ptr();
     a.timeline = timeline;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -1218,9 +1477,11 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     a.num_blocks = num_blocks;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.early = early ? 1 : 0;
+    a.cap = L.cap;
     a.lens_off = L.lens;
     a.bounds_off = L.bounds;
-    a.chunks_off = L.chunks;
+    a.cta_off = L.cta;
+    a.cta_bytes = L.cta_bytes;
     return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16>(a, maps, R_log2, ctas, stream)
                             : launch_planned_impl<__half>(a, maps, R_log2, ctas, stream);
 }

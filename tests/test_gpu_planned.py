@@ -172,8 +172,8 @@ def test_plan_for_another_grid_is_refused_on_the_device():
     wl = workloads.make_workload("plan_bad", context_lens=[100, 200], num_q_heads=4, num_kv_heads=2, block_size=16,
                                  seed=3, max_context=256)
     dev = torch.device("cuda")
-    plan = pa.decode_plan(wl.block_tables.to(dev), wl.context_lens.to(dev), 4, 2, 16, wl.num_blocks, num_ctas=5)
-    plan.num_ctas = 6   # launch another grid with the same bytes
+    plan = pa.decode_plan(wl.block_tables.to(dev), wl.context_lens.to(dev), 4, 2, 16, wl.num_blocks, num_ctas=6)
+    plan.num_ctas = 5   # launch another grid with the same bytes (large enough for it)
     out = torch.full_like(wl.q[0].to(dev), 7.0)
     pa.decode_planned(wl.q[0].to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), plan, wl.scale, out=out)
     torch.cuda.synchronize()
