@@ -176,9 +176,11 @@ class Step:
     ``fused``: one pa_decode_append launch per layer (cache write of the new token + decode);
     otherwise pa_cache_write followed by pa_decode."""
 
-    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, planned: bool = True):
+    def __init__(self, wl, device, fused: bool = True, num_ctas: int = 0, planned: bool = True,
+                 adaptive: bool = False):
         self.fused = fused
         self.num_ctas = num_ctas
+        self.adaptive = adaptive
         self.planned = planned and fused
         import paged_kv_cache_08_gb300 as pa
         self.pa = pa
@@ -204,7 +206,7 @@ class Step:
             # the step's plan: built by the first launch of every step (inside the graph), read by
             # every layer's decode
             self.plan = pa.decode_plan(self.bt, self.lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size,
-                                       wl.num_blocks, num_ctas=num_ctas)
+                                       wl.num_blocks, num_ctas=num_ctas, adaptive=adaptive)
             self.ws = pa.new_planned_workspace(num_ctas, device)
         self.tps = pa.plan_tokens_per_split(S, Hq, wl.num_kv_heads, D, wl.block_size, wl.max_blocks_per_seq)
         self.graph = None
@@ -236,7 +238,7 @@ class Step:
     def make_plan(self):
         wl = self.wl
         self.pa.decode_plan(self.bt, self.lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks,
-                            plan=self.plan, num_ctas=self.num_ctas)
+                            plan=self.plan, num_ctas=self.num_ctas, adaptive=self.adaptive)
 
     def eager(self):
         if self.planned:
@@ -309,7 +311,7 @@ def run_ours(args):
     kind = pa.kernel_kind(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads)
     fused = args.path in ("fused", "unplanned") and kind == 2
     planned = args.path == "fused" and fused
-    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, planned=planned)
+    st = Step(wl, dev, fused=fused, num_ctas=args.num_ctas, planned=planned, adaptive=args.adaptive)
     d_bytes = decode_bytes(wl)
     c_bytes = cache_write_bytes(wl)
     step_bytes = wl.layers * (d_bytes + c_bytes)
@@ -332,12 +334,17 @@ def run_ours(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        st.pa.read_device_status(clear=True)
         start.record()
         for _ in range(args.steps):
             st.replay()
         stop.record()
         torch.cuda.synchronize()
+        timed_status = st.pa.read_device_status(clear=True)
         decode_ms = st.decode_launch_ms()
+    if timed_status:
+        print(f"bench: the device status word read {timed_status:#x} after the timed region "
+              "(a kernel skipped an index or gave up a wait): the number is not valid", file=sys.stderr)
     total_ms = max_over_ranks(start.elapsed_time(stop), dev)
     ms_per_step = total_ms / args.steps
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -383,7 +390,8 @@ def run_ours(args):
         with ClockSampler(local) as clk_pc:
             for cfg, B in PER_CONFIG:
                 key = f"config{cfg}" + (f"_B{B}" if B else "")
-                per_config[key] = time_config(cfg, B, dev, 30, 3, args.num_ctas, errors=not args.no_cpu_baseline)
+                per_config[key] = time_config(cfg, B, dev, 30, 3, args.num_ctas, errors=not args.no_cpu_baseline,
+                                               adaptive=args.adaptive)
         per_config["clocks"] = clk_pc.summary()
 
     cpu = None
@@ -415,6 +423,7 @@ def run_ours(args):
             "e2e": e2e,
             "per_config": per_config,
             "gpu_launches": launches_per_step * args.steps,
+            "device_status": timed_status,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -428,7 +437,7 @@ def run_e2e(st, wl, args, step_bytes):
     input buffer), runs the 24 layers and copies the outputs back (one copy).  Two buffer sets
     (and two captured graphs) let step k + 1's input copy and step k - 1's output copy run on
     copy streams while step k's kernels run; the timed region spans all copies of all steps."""
-    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas, planned=st.planned)
+    st2 = Step(wl, st.dev, fused=st.fused, num_ctas=st.num_ctas, planned=st.planned, adaptive=st.adaptive)
     st2.capture()
     sets = [st, st2]
     host_in = st.inbuf.cpu().pin_memory()
@@ -782,14 +791,17 @@ def _half_ulp(t: torch.Tensor):
     return (hi - lo) / 2
 
 
-def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: int = 0, errors: bool = True):
+def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: int = 0, errors: bool = True,
+                adaptive: bool = False):
     """One decode layer (the cache write of each sequence's new token plus attention) of a seeded
     configuration, timed alone: the step's plan built first (pa_decode_plan, timed separately),
     then ``steps`` pa_decode_planned launches, each after a 512 MB write that flushes the L2, by
     CUDA events (mean; one event pair resolves about 2 us, the mean of many finer).  The per-layer
     persistent launch (pa_decode_append) is timed the same way beside it.  With ``errors`` the
     output of one launch on fresh caches is compared with the fp64 oracle's on the host: the raw
-    max-abs error, and the error beyond the output dtype's own rounding (bf16)."""
+    max-abs error, and the error beyond the output dtype's own rounding (bf16).  With ``adaptive``
+    the plan is rebuilt after each warm-up launch, so that the CTAs' shares follow the rates the
+    launches measured, and the timed launches use the last plan."""
     import numpy as np
     import paged_kv_cache_08_gb300 as pa
     wl = workloads.config(cfg, device=dev, layers=1, block_size=block_size)
@@ -814,7 +826,8 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
         return statistics.fmean(ts), statistics.median(ts)
 
     res = {}
-    plan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, num_ctas=num_ctas)
+    plan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, num_ctas=num_ctas,
+                          adaptive=adaptive)
     ws = pa.new_planned_workspace(num_ctas, dev)
 
     def planned():
@@ -822,7 +835,7 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
 
     def replan():
         pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, plan=plan,
-                       num_ctas=num_ctas)
+                       num_ctas=num_ctas, adaptive=adaptive)
     uws = pa.new_workspace(pa.decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                                                     wl.block_size, wl.max_blocks_per_seq), dev)
 
@@ -831,9 +844,19 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
     for fn in (planned, unplanned, replan):
         for _ in range(max(3, warmup)):
             fn()
+    if adaptive:
+        for _ in range(max(24, warmup)):
+            flush.zero_()
+            planned()
+            replan()
     torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    pa.read_device_status(clear=True)
     ms, med = timed(planned, steps)
     ms_u, _ = timed(unplanned, steps)
+    status = pa.read_device_status(clear=True)
+    if status:
+        print(f"bench: device status {status:#x} after timing config {cfg}: not valid", file=sys.stderr)
     ms_p, _ = timed(replan, max(10, steps // 3))
     nbytes = decode_bytes(wl) + cache_write_bytes(wl)
     peak, peak_kind = measured_peak_gbs()
@@ -847,8 +870,8 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
                 "kernel": "pa_decode_planned (append)", "plan_us": round(ms_p * 1e3, 2),
                 "per_layer_persistent_us": round(ms_u * 1e3, 2),
                 "per_layer_persistent_gbs": round(nbytes / (ms_u * 1e-3) / 1e9, 1),
-                "peak": peak, "peak_source": f"{peak_kind} copy bandwidth",
-                "l2": "flushed (512 MB write) before every timed launch"})
+                "peak": peak, "peak_source": f"{peak_kind} copy bandwidth", "adaptive_plan": adaptive,
+                "device_status": status, "l2": "flushed (512 MB write) before every timed launch"})
     if errors:
         import oracle as oracle_pkg
         o = oracle_pkg.get()
@@ -887,7 +910,7 @@ def run_config(args):
     torch.cuda.set_device(dev)
     with ClockSampler(0) as clk:
         r = time_config(args.config, args.block_size, dev, args.steps, args.warmup, args.num_ctas,
-                        errors=not args.no_cpu_baseline)
+                        errors=not args.no_cpu_baseline, adaptive=args.adaptive)
     line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(r["us"] / 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
@@ -1040,6 +1063,8 @@ def main():
                     help="fused: one plan per step + pa_decode_planned (cache write fused) per layer; "
                          "unplanned: pa_decode_append per layer; separate: pa_cache_write + pa_decode")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent kernel grid (0 = library default)")
+    ap.add_argument("--adaptive", action="store_true",
+                    help="plans whose CTA shares follow the CTAs' measured streaming rates (PA_PLAN_ADAPTIVE)")
     ap.add_argument("--op", choices=["decode", "config", "copy_blocks", "swap", "multi_query", "prefill", "runs"],
                     default="decode",
                     help="decode step (default), one layer of another config (--config), or the block-copy, swap, "

@@ -216,6 +216,9 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
 /* pa_multi_query beyond 16 query rows per (sequence, kv head): the mma.sync tiles of 64 rows
  * instead of the default tcgen05 tiles of 128 rows (same results within the parity tolerance). */
 #define PA_PREFILL_MMA_SYNC 4
+/* pa_decode_plan: shares of the decode launch's CTAs that follow their measured streaming rates
+ * (see pa_decode_plan). */
+#define PA_PLAN_ADAPTIVE 8
 
 /* ------------------------------------------------------------------------------------
  * pa_decode_append  [P4 §三 sequence diagram + §五.1; P1 address formula]
@@ -268,6 +271,20 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  *     plan and cached rows may be read before the preceding kernel ends; the preceding
  *     kernel must then write none of the plan, the caches or the tables -- in particular a
  *     pa_decode_planned right after pa_decode_plan must not ask for it), timeline.
+ * Adaptive plans (PA_PLAN_ADAPTIVE in pa_decode_plan's opts->flags): SMs stream at different
+ * rates, so by default every CTA gets the same weight of chunks; an adaptive plan instead
+ * gives CTA c a share proportional to its rate measured by earlier pa_decode_planned calls on
+ * plans built into the same buffer (each such call folds one measurement per CTA into the
+ * buffer's rates, an exponential average; the first adaptive build into a buffer, or one for
+ * another CTA count, uses equal shares).  Such calls therefore write to the plan buffer, and
+ * two of them on one buffer must not overlap on the GPU.  Outputs are the same function of
+ * the inputs whatever the shares (within the parity tolerance: the split points move).  The
+ * rates section is the one part of the plan that a pa_decode_planned with early reads may read
+ * while the preceding pa_decode_planned on the same plan writes it: such a race only loses one
+ * measurement.  Measured on GB300: one layer launched alone and repeated gains 3-8 % (configs 3
+ * and 4 of the benchmark); in a chain of layers with early reads the CTAs' order on the SMs
+ * changes from layer to layer, the rates follow the launch order rather than the SMs, and the
+ * chain loses about 15 % -- leave adaptive plans off there.
  * A plan that does not match the call's shape or grid makes the kernel write nothing and
  * set PA_DEV_BAD_PLAN.  Supported: head_dim 128, block_size 16/32/64/128, num_q_heads /
  * num_kv_heads <= 8, num_seqs <= 1024; else PA_ERR_UNSUPPORTED.
@@ -278,11 +295,20 @@ size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int 
 int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, const int32_t* context_lens,
                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                    int num_blocks, int max_blocks_per_seq, void* stream, const pa_decode_options* opts);
+/* Where a plan of this shape keeps the two sections a caller may read back (for inspection):
+ * *bounds_offset: int32 [2 * num_ctas + 1], the first chunk of each CTA's two groups in the
+ * plan's chunk order (the last entry = the number of chunks); *rates_offset: float [num_ctas], the
+ * CTAs' measured streaming rates of an adaptive plan (weight per SM cycle; 0 = no measurement;
+ * meaningful only after a pa_decode_planned call on an adaptive plan).  *num_ctas: the grid the
+ * plan is built for.  Returns PA_OK or the shape's error code. */
+int pa_decode_plan_sections(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, const pa_decode_options* opts, int* num_ctas,
+                            size_t* bounds_offset, size_t* rates_offset);
 size_t pa_decode_planned_workspace_size(const pa_decode_options* opts);
 /* Fill `bytes` of a pa_decode_planned workspace with 0xFF on `stream` (cudaMemsetAsync). */
 int pa_decode_planned_workspace_init(void* workspace, size_t bytes, void* stream);
 int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new,
-                      void* k_cache, void* v_cache, const void* plan, size_t plan_bytes, float scale,
+                      void* k_cache, void* v_cache, void* plan, size_t plan_bytes, float scale,
                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       int num_blocks, int max_blocks_per_seq, int dtype,
                       void* workspace, size_t workspace_bytes, void* stream,

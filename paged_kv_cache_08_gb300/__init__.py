@@ -24,7 +24,7 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_planned", "DecodePlan",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_planned", "DecodePlan", "plan_bounds", "plan_rates",
            "planned_workspace_size", "new_planned_workspace",
            "multi_query", "decode_runs", "gather_runs",
            "SlotPool", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
@@ -256,21 +256,27 @@ class DecodePlan:
 
 def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_heads: int, num_kv_heads: int,
                 block_size: int, num_blocks: int, head_dim: int = 128, plan: Optional[DecodePlan] = None,
-                num_ctas: int = 0, stream: Optional[torch.cuda.Stream] = None) -> DecodePlan:
+                num_ctas: int = 0, adaptive: bool = False,
+                stream: Optional[torch.cuda.Stream] = None) -> DecodePlan:
     """Build (or rebuild in place, ``plan``) the plan of a decode step: one small kernel that reads
-    the block tables and lengths once for every layer's pa_decode_planned call."""
+    the block tables and lengths once for every layer's pa_decode_planned call.  ``adaptive``:
+    the CTAs' shares follow the streaming rates that earlier decode_planned calls measured into
+    the same plan buffer (PA_PLAN_ADAPTIVE)."""
     _need_cuda("block_tables", block_tables, torch.int32)
     _need_cuda("context_lens", context_lens, torch.int32)
     if block_tables.dim() != 2 or block_tables.shape[0] != context_lens.numel():
         raise ValueError("block_tables must be [S, max_blocks] with S = context_lens.numel()")
     S, max_blocks = block_tables.shape
     o = _opts(0, "auto", num_ctas)
+    if adaptive:
+        o.flags |= _native.PLAN_ADAPTIVE
     need = int(lib().pa_decode_plan_size(S, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
                                          ctypes.byref(o)))
     if need == 0:
         raise PAError("pa_decode_plan_size", -2)
     if plan is None or plan.data.numel() < need:
-        data = torch.empty(need, dtype=torch.uint8, device=block_tables.device)
+        # zeroed: an adaptive build finds no stale rates in a fresh buffer
+        data = torch.zeros(need, dtype=torch.uint8, device=block_tables.device)
         plan = DecodePlan(data, S, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks, int(num_ctas))
     else:
         plan.num_seqs, plan.num_q_heads, plan.num_kv_heads = S, num_q_heads, num_kv_heads
@@ -281,6 +287,30 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
                               max_blocks, _stream_ptr(stream), ctypes.byref(o))
     _native.check("pa_decode_plan", rc)
     return plan
+
+
+def _plan_sections(plan: DecodePlan):
+    o = _opts(0, "auto", plan.num_ctas)
+    ctas, b_off, r_off = ctypes.c_int(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
+    rc = lib().pa_decode_plan_sections(plan.num_seqs, plan.num_q_heads, plan.num_kv_heads, 128, plan.block_size,
+                                       plan.max_blocks_per_seq, ctypes.byref(o), ctypes.byref(ctas),
+                                       ctypes.byref(b_off), ctypes.byref(r_off))
+    _native.check("pa_decode_plan_sections", rc)
+    return ctas.value, b_off.value, r_off.value
+
+
+def plan_bounds(plan: DecodePlan) -> torch.Tensor:
+    """The plan's group bounds (int32 [2 C + 1], on the host): CTA c streams chunks
+    [b[2c], b[2c+1]) forwards and [b[2c+1], b[2c+2]) backwards."""
+    C, off, _ = _plan_sections(plan)
+    return plan.data[off:off + 4 * (2 * C + 1)].cpu().view(torch.int32).clone()
+
+
+def plan_rates(plan: DecodePlan) -> torch.Tensor:
+    """The CTAs' measured streaming rates kept in an adaptive plan's buffer (float [C], host;
+    weight per SM cycle, 0 = no measurement)."""
+    C, _, off = _plan_sections(plan)
+    return plan.data[off:off + 4 * C].cpu().view(torch.float32).clone()
 
 
 def planned_workspace_size(num_ctas: int = 0) -> int:

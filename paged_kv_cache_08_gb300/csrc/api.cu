@@ -657,6 +657,18 @@ size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int 
     return planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts));
 }
 
+int pa_decode_plan_sections(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, const pa_decode_options* opts, int* num_ctas,
+                            size_t* bounds_offset, size_t* rates_offset) {
+    int rc = planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    if ((opts && opts->num_ctas < 0) || !num_ctas || !bounds_offset || !rates_offset) return PA_ERR_INVALID_ARG;
+    *num_ctas = planned_ctas(opts);
+    planned_plan_offsets(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, *num_ctas, bounds_offset,
+                         rates_offset);
+    return PA_OK;
+}
+
 size_t pa_decode_planned_workspace_size(const pa_decode_options* opts) {
     if (opts && opts->num_ctas < 0) return 0;
     return planned_workspace_bytes(planned_ctas(opts));
@@ -686,7 +698,7 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
         return PA_ERR_WORKSPACE;
     cudaError_t e = launch_decode_plan(plan, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                        block_size, num_blocks, max_blocks_per_seq, ctas,
-                                       static_cast<cudaStream_t>(stream));
+                                       opts && (opts->flags & PA_PLAN_ADAPTIVE), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;
@@ -695,7 +707,7 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
 }
 
 int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                      const void* plan, size_t plan_bytes, float scale, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      void* plan, size_t plan_bytes, float scale, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                       int block_size, int num_blocks, int max_blocks_per_seq, int dtype, void* workspace,
                       size_t workspace_bytes, void* stream, const pa_decode_options* opts) {
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;

@@ -39,6 +39,7 @@
 #include "decode_common.cuh"
 
 #include <atomic>
+#include <cstddef>
 #include <climits>
 #include <type_traits>
 
@@ -89,9 +90,29 @@ struct PlanHeader {
     int num_ctas;     // C: two groups each
     int num_chunks;   // N
     int max_chunks;
-    int pad[6];
+    int adaptive;     // 0: equal shares; kAdaptiveFirst / kAdaptiveFold: see PlanRates
+    int pad[5];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header");
+
+// Adaptive shares.  SMs stream the same bytes at different rates (on GB300 the per-SM finishing
+// times of equal ranges of one layer differ by up to 14 %, and the same SMs stay slow from launch
+// to launch), so a plan built with PA_PLAN_ADAPTIVE gives CTA c a share of the weight proportional
+// to rate[c]: every decode launch on the plan measures each CTA's rate (the weight of its range
+// per SM cycle of the CTA's life) and folds it into rate[c] (an exponential average); the next
+// pa_decode_plan into the same buffer reads the rates.  The section outlives rebuilds; the first
+// adaptive build into a buffer (or one for another grid) cuts equal shares.
+struct PlanRates {
+    int magic;
+    int ctas;
+    int pad[2];
+    float rate[1];   // [ctas]; <= 0: no measurement
+};
+constexpr int kRatesMagic = 0x52415031;   // "RAP1"
+constexpr int kAdaptiveFold = 1;          // PlanHeader::adaptive: the rates hold measurements
+constexpr int kAdaptiveFirst = 2;         //   ... they hold none yet: launches write theirs
+constexpr float kRateAlpha = 0.125f;      // weight of a new measurement in the average
+constexpr float kRateMax = 1.0e4f;        // rates are row units per SM cycle (about 0.1): above is garbage
 
 // One chunk of the list (32 bytes, two 16-byte loads).
 struct __align__(16) PlanChunk {
@@ -121,7 +142,8 @@ static_assert(sizeof(PlanEvent) == 56, "plan event");
 // Per CTA: its range and its cut segments, then each group's chunks in the order it streams them.
 struct CtaHeader {
     int b0, b1, b2;     // group 0 streams [b0, b1) forwards, group 1 [b1, b2) backwards
-    int pad;
+    float weight;       // adaptive plans: the weight of [b0, b2), negative while the rates hold no
+                        // measurement; 0: not adaptive
     PlanEvent ev[2];
 };
 static_assert(sizeof(CtaHeader) == 128, "CTA header");
@@ -129,8 +151,8 @@ static_assert(sizeof(CtaHeader) == 128, "CTA header");
 // Byte offsets of the plan's sections: header, lengths [S], group bounds [2C + 1], then per CTA
 // its header and two groups of `cap` chunk slots.
 struct PlanLayout {
-    size_t lens, bounds, cta, cta_bytes, total;
-    int cap;            // chunk slots per group (the largest group of the equal cut)
+    size_t lens, bounds, cta, cta_bytes, rates, total;
+    int cap;            // chunk slots per group
 };
 
 inline size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
@@ -144,14 +166,16 @@ __host__ __device__ inline long long plan_max_chunks(int num_seqs, int num_kv_he
 PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
     PlanLayout L;
     const long long maxc = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
-    // the weighted cut gives a group at most (its share of the weight + one chunk) / the lightest
-    // chunk's weight; chunk weights lie within a factor of two, so twice the equal share is room enough
-    L.cap = 2 * (int)((maxc + 2 * ctas - 1) / (2 * ctas)) + 4;
+    // A group gets at most (its share of the weight + one chunk) / the lightest chunk's weight.
+    // Chunks weigh 64 to 112 (at most 1.75x their mean) and a share is at most 1.5x the equal one
+    // (adaptive shares are bounded so): 1.5 x 1.75 < 3 equal shares of chunks, plus rounding.
+    L.cap = 3 * (int)((maxc + 2 * ctas - 1) / (2 * ctas)) + 6;
     L.lens = 256;
     L.bounds = L.lens + al256((size_t)num_seqs * 4);
     L.cta = L.bounds + al256((size_t)(2 * ctas + 1) * 4);
     L.cta_bytes = sizeof(CtaHeader) + (size_t)2 * L.cap * sizeof(PlanChunk);
-    L.total = L.cta + (size_t)ctas * L.cta_bytes;
+    L.rates = al256(L.cta + (size_t)ctas * L.cta_bytes);
+    L.total = L.rates + al256(16 + (size_t)ctas * sizeof(float));
     return L;
 }
 
@@ -165,8 +189,9 @@ struct PlanArgs {
     const int32_t* context_lens;
     unsigned int* status;
     int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq, ctas;
-    size_t lens_off, bounds_off, cta_off, cta_bytes;
+    size_t lens_off, bounds_off, cta_off, cta_bytes, rates_off;
     int cap;
+    int adaptive;
     long long max_chunks;
 };
 
@@ -210,6 +235,56 @@ __device__ __forceinline__ bool piece_is_late(const int32_t* bnd, int c, long lo
     return false;
 }
 
+// Block-wide sums over kPlanThreads threads (every thread gets the result; `scratch` is reused
+// only after a barrier).
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* scratch, int lane, int warp) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float2 t = make_float2(0.f, 0.f);
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+        t.x += scratch[w].x;
+        t.y += scratch[w].y;
+    }
+    return t;
+}
+
+// Block-wide maximum (every thread gets it).
+__device__ __forceinline__ float block_max(float v, float2* scratch, int lane, int warp) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) scratch[warp].x = v;
+    __syncthreads();
+    float t = scratch[0].x;
+    for (int w = 1; w < kPlanThreads / 32; ++w) t = fmaxf(t, scratch[w].x);
+    return t;
+}
+
+// Block-wide exclusive prefix sum of v in thread order, and the total.
+__device__ __forceinline__ void block_scan(float v, float2* scratch, int lane, int warp, float& excl, float& total) {
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[warp].x = incl;
+    __syncthreads();
+    excl = incl - v;
+    total = 0.f;
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+        if (w < warp) excl += scratch[w].x;
+        total += scratch[w].x;
+    }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArgs a) {
     extern __shared__ long long plan_smem[];
     const int S = a.num_seqs, Hkv = a.num_kv_heads, B = a.block_size;
@@ -219,8 +294,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
     int* P = nch + S;                                              // [S + 1] exclusive prefix of nch
     int* Ls = P + S + 1;                                           // [S] clamped lengths
     int32_t* bnd = Ls + S;                                         // [2C + 1] group bounds
+    float* rc = reinterpret_cast<float*>(bnd + G2 + 1);            // [C + 1] adaptive: share before CTA c
     __shared__ int warp_tot[kPlanThreads / 32];
     __shared__ long long warp_wt[kPlanThreads / 32];
+    __shared__ float2 warp_f2[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long cap = (long long)a.max_blocks_per_seq * B;
     const int R = B < kStageTokens ? B : kStageTokens;
@@ -281,9 +358,71 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
     __syncthreads();
 
     const long long N = (long long)Hkv * tot;
-    // group bounds: group g starts at the first chunk whose starting weight reaches W g / G2
+    // CTA shares: equal, or (adaptive, once rates were measured) proportional to the CTAs'
+    // measured rates, each clamped to within a factor of two of their mean (a CTA without a
+    // measurement counts as the mean); rc[c] = the share before CTA c, rc[C] = 1.  No block of
+    // this kernel writes the rates, so all blocks take the same shares.
+    const PlanRates* rates = reinterpret_cast<const PlanRates*>(a.plan + a.rates_off);
+    const int C = a.ctas;
+    const bool rates_ok = a.adaptive && rates->magic == kRatesMagic && rates->ctas == C;
+    if (rates_ok) {   // (the same branch in every thread: nothing writes the rates during this kernel)
+        const int per_c = (C + kPlanThreads - 1) / kPlanThreads;
+        const int clo = min(C, tid * per_c), chi = min(C, clo + per_c);
+        float mine[4];   // C <= 4 * kPlanThreads (checked by the host)
+        float sum = 0.f, cnt = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float r = -1.f;
+            if (clo + j < chi) {
+                r = rates->rate[clo + j];
+                if (!(r > 0.f && r < kRateMax)) r = -1.f;   // unmeasured (0, negative, NaN, garbage)
+            }
+            mine[j] = r;
+            if (r > 0.f) {
+                sum += r;
+                cnt += 1.f;
+            }
+        }
+        float2 tw = block_sum2(make_float2(sum, cnt), warp_f2, lane, warp);
+        const float mean = tw.y > 0.f ? tw.x / tw.y : 1.f;
+        float run_r = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float r = clo + j >= chi ? 0.f : mine[j] > 0.f ? fminf(fmaxf(mine[j], 0.5f * mean), 2.f * mean) : mean;
+            mine[j] = r;
+            run_r += r;
+        }
+        float excl = 0.f, total = 0.f;
+        block_scan(run_r, warp_f2, lane, warp, excl, total);
+        // no share above 1.5x the equal one (the plan's slots per group assume it): mix the rates'
+        // shares with equal ones, beta = 0.5 / (largest ratio - 1) where that ratio exceeds 1.5
+        float top = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (clo + j < chi) top = fmaxf(top, mine[j] * (float)C / total);
+        top = block_max(top, warp_f2, lane, warp);
+        const float beta = top > 1.5f ? 0.5f / (top - 1.f) : 1.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (clo + j < chi) rc[clo + j] = (1.f - beta) * (float)(clo + j) / (float)C + beta * excl / total;
+            excl += mine[j];
+        }
+        if (tid == 0) rc[C] = 1.f;
+        __syncthreads();
+    }
+    // group bounds: group g starts at the first chunk whose starting weight reaches its share of
+    // the total, W g / G2 (adaptive: its CTA's share, split in half between the two groups)
     for (int g = tid; g <= G2; g += kPlanThreads) {
-        const long long T = tot_w * g / G2;
+        long long T;
+        if (rates_ok) {
+            const int cg = g >> 1;
+            double f = (g & 1) ? 0.5 * ((double)rc[cg] + (double)rc[cg + 1]) : (double)rc[min(cg, C)];
+            f = f >= 0.0 ? (f <= 1.0 ? f : 1.0) : 0.0;   // (NaN -> 0: cannot arise from sanitised rates)
+            T = (g == G2) ? tot_w : (long long)(f * (double)tot_w);
+            if (T > tot_w) T = tot_w;
+        } else {
+            T = tot_w * g / G2;
+        }
         long long b = N;
         if (T < tot_w) {
             int l2 = 0, h2 = S - 1;   // the sequence holding weight position T (empty ones skipped)
@@ -307,6 +446,21 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
     int32_t* lens = reinterpret_cast<int32_t*>(a.plan + a.lens_off);
     int32_t* bounds = reinterpret_cast<int32_t*>(a.plan + a.bounds_off);
     auto cta_header = [&](int c) { return reinterpret_cast<CtaHeader*>(a.plan + a.cta_off + (size_t)c * a.cta_bytes); };
+    // starting weight of chunk x (x == N: the total): the sequence is the last whose first chunk is
+    // at or before x (empty sequences share the next one's first chunk, so that one is found)
+    auto chunk_start_weight = [&](long long x) -> long long {
+        if (x >= N) return tot_w;
+        int l2 = 0, h2 = S - 1;
+        while (l2 < h2) {
+            const int mid = (l2 + h2 + 1) >> 1;
+            if ((long long)Hkv * P[mid] <= x) l2 = mid;
+            else h2 = mid - 1;
+        }
+        const int n = nch[l2];
+        const long long o = x - (long long)Hkv * P[l2];
+        const long long h = o / n, k = o - h * n;
+        return PW[l2] + h * segment_weight(Ls[l2], R) + k * (kStageTokens + kWChunk);
+    };
     if (blockIdx.x == 0) {
         for (int s = tid; s < S; s += kPlanThreads) lens[s] = Ls[s];
         for (int g = tid; g <= G2; g += kPlanThreads) bounds[g] = bnd[g];
@@ -315,7 +469,12 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
             ch->b0 = bnd[2 * c];
             ch->b1 = bnd[2 * c + 1];
             ch->b2 = bnd[2 * c + 2];
-            ch->pad = 0;
+            if (a.adaptive) {
+                const float w = fmaxf(1.f, (float)(chunk_start_weight(bnd[2 * c + 2]) - chunk_start_weight(bnd[2 * c])));
+                ch->weight = rates_ok ? w : -w;
+            } else {
+                ch->weight = 0.f;
+            }
             if (bnd[2 * c] == bnd[2 * c + 2]) {   // no chunks: no events (nothing else writes them)
                 ch->ev[0].exists = 0;
                 ch->ev[1].exists = 0;
@@ -333,6 +492,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
             h.num_ctas = a.ctas;
             h.num_chunks = (int)N;
             h.max_chunks = (int)a.max_chunks;
+            h.adaptive = a.adaptive ? (rates_ok ? kAdaptiveFold : kAdaptiveFirst) : 0;
             *hdr = h;
         }
     }
@@ -442,6 +602,7 @@ struct PlannedArgs {
                                 // or the published value (32-bit words are read and written whole)
     unsigned int* status;
     unsigned long long* timeline;
+    PlanRates* rates;           // the plan's rates section (adaptive plans: updated at the end)
     float scale_log2;
     int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq;
     int early;
@@ -661,6 +822,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     volatile int* issued = misc + 4;                        // [2]
     volatile int* qdef = misc + 8;                          // [2][3]: deferred q row (s * Hkv + h) or -1
     volatile int* ndef = misc + 16;                         // [2][3]: deferred new rows (s * Hkv + h) or -1
+    // misc + 29: this CTA's rate before the launch (bits, copied by thread 0), + 30: the SM clock
+    // when the CTA started (adaptive plans)
     // this CTA's header, copied by each producer before its first stage is released
     CtaHeader* sh_hdr = reinterpret_cast<CtaHeader*>(bp + kHdrOff);
     float* pair_o = reinterpret_cast<float*>(bp + kPairOff);
@@ -689,6 +852,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(&ready[1], kGroupThreads);
         *abort_flag = 0;
         *pair_count = 0;
+        misc[30] = (int)clock();
+        // this CTA's rate so far (adaptive plans fold it at the end), copied without a register;
+        // this thread waits for the copy at the end of its consumer loop
+        cp_async4(smem_u32(const_cast<int*>(misc + 29)), &a.rates->rate[c]);   // adaptive plans time the CTA's life from here
         for (int i = 0; i < kGroups * kPStages; ++i) {
             qdef[i] = -1;
             ndef[i] = -1;
@@ -719,6 +886,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (a.early) grid_dependency_wait();
         grid_launch_dependents();
         if (tid == 0 && c == 0) flag_status(a.status, PA_DEV_BAD_PLAN);
+        if (tid == 0) cp_async_wait_all();
         return;
     }
     if (!a.early) grid_launch_dependents();
@@ -1263,7 +1431,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const PlanEvent& E = sh_hdr->ev[side];
                     const int nrem = E.nrem;
                     const unsigned long long t0 = global_timer_ns();
-                    bool ok = true;
+                    bool ok = true;   // the same in every thread of the group
                     for (int k0 = 0; k0 < nrem && ok; k0 += 4) {
                         const int kn = min(4, nrem - k0);
                         int slot[4];
@@ -1288,14 +1456,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 }
                             if (done_mask != want && global_timer_ns() - t0 > kWaitLimitNs) break;
                         }
-                        ok = done_mask == want;
+                        // A row's (m, l) words are read by its 16 threads and cleared by one of them:
+                        // clear only once every thread of the group has stopped reading the batch.
+                        ok = group_all(grp, done_mask == want);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             if (done_mask & (1u << j))
                                 clear8(a.part_o + (size_t)slot[j] * kRows * kHeadDim, a.part_ml + (size_t)slot[j] * kRows,
                                        r, d0, (tg & 15) == 0);
                     }
-                    if (!group_all(grp, ok)) {
+                    if (!ok) {
                         if (tg == 0) {
                             flag_status(a.status, PA_DEV_TIMEOUT);
                             *abort_flag = 1;
@@ -1327,11 +1497,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             mbar_arrive(&gempty[st]);
         }
+        if (tid == 0) cp_async_wait_all();   // the rate copied at the start
         if (grp == 0 && tid == 0) trace(a.timeline, c, 7);
         if (grp == 1 && tg == 0) trace(a.timeline, c, 9);
     }
 
     __syncthreads();
+    if (tid == kEpiWarp * 32 && sh_hdr->weight != 0.f && !*abort_flag) {
+        // adaptive plan: this CTA's rate, the weight of its range per SM cycle of its life
+        const float w = fabsf(sh_hdr->weight);
+        const unsigned span = (unsigned)clock() - (unsigned)misc[30];
+        const float r = (sh_hdr->b2 > sh_hdr->b0 && span > 0u && span < 0x40000000u) ? w / (float)span : 0.f;
+        const float old_rate = __int_as_float(misc[29]);
+        if (sh_hdr->weight < 0.f) {   // the rates hold no measurement yet
+            a.rates->rate[c] = r;   // 0: no measurement
+            if (c == 0) {
+                a.rates->magic = kRatesMagic;
+                a.rates->ctas = (int)gridDim.x;
+            }
+        } else if (r > 0.f) {
+            a.rates->rate[c] = old_rate > 0.f && old_rate < kRateMax ? old_rate + kRateAlpha * (r - old_rate) : r;
+        }
+    }
     if (tid == 0 && a.timeline) {
         trace(a.timeline, c, 8);
         unsigned int smid;
@@ -1392,6 +1579,13 @@ size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int ma
     return plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas).total;
 }
 
+void planned_plan_offsets(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
+                          size_t* bounds_offset, size_t* rates_offset) {
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    *bounds_offset = L.bounds;
+    *rates_offset = L.rates + offsetof(PlanRates, rate);
+}
+
 size_t planned_workspace_bytes(int ctas) {
     const size_t slots = (size_t)2 * ctas;
     return al256(slots * kRows * kHeadDim * sizeof(float)) + al256(slots * kRows * sizeof(float2));
@@ -1399,7 +1593,8 @@ size_t planned_workspace_bytes(int ctas) {
 
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
-                               int max_blocks_per_seq, int ctas, cudaStream_t stream) {
+                               int max_blocks_per_seq, int ctas, bool adaptive, cudaStream_t stream) {
+    if (ctas < 1 || ctas > 4 * kPlanThreads) return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
     PlanArgs a;
     a.plan = static_cast<unsigned char*>(plan);
@@ -1417,14 +1612,16 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
     a.bounds_off = L.bounds;
     a.cta_off = L.cta;
     a.cta_bytes = L.cta_bytes;
+    a.rates_off = L.rates;
     a.cap = L.cap;
+    a.adaptive = adaptive ? 1 : 0;
     a.max_chunks = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
     long long blocks = (a.max_chunks + kPlanThreads - 1) / kPlanThreads;
     const long long cap = 4LL * sm_count_current();
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const size_t smem = (size_t)(num_seqs + 1) * sizeof(long long) + (size_t)(3 * num_seqs + 1) * sizeof(int) +
-                        (size_t)(2 * ctas + 1) * sizeof(int32_t);
+                        (size_t)(2 * ctas + 1) * sizeof(int32_t) + (size_t)(ctas + 1) * sizeof(float);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kPlanThreads);
@@ -1435,13 +1632,17 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_plan_kernel, a);
     if (e == cudaSuccess) note_launches(1);
     return e;
 }
 
 cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                  const void* v_cache, const void* plan, void* workspace, float scale, int num_seqs,
+                                  const void* v_cache, void* plan, void* workspace, float scale, int num_seqs,
                                   int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
                                   int max_blocks_per_seq, int dtype, int ctas, bool early,
                                   unsigned long long* timeline, cudaStream_t stream) {
@@ -1462,6 +1663,7 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.plan = static_cast<const unsigned char*>(plan);
+    a.rates = reinterpret_cast<PlanRates*>(static_cast<unsigned char*>(plan) + L.rates);
     const size_t slots = (size_t)2 * ctas;
     char* w = static_cast<char*>(workspace);
     a.part_o = reinterpret_cast<float*>(w);

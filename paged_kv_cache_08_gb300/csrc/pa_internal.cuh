@@ -296,11 +296,13 @@ constexpr int kPlanMaxSeqs = 1024;      // sequences the plan kernel keeps in sh
 int planned_ctas(const pa_decode_options* opts);
 size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas);
 size_t planned_workspace_bytes(int ctas);
+void planned_plan_offsets(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
+                          size_t* bounds_offset, size_t* rates_offset);
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
-                               int max_blocks_per_seq, int ctas, cudaStream_t stream);
+                               int max_blocks_per_seq, int ctas, bool adaptive, cudaStream_t stream);
 cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                  const void* v_cache, const void* plan, void* workspace, float scale, int num_seqs,
+                                  const void* v_cache, void* plan, void* workspace, float scale, int num_seqs,
                                   int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
                                   int max_blocks_per_seq, int dtype, int ctas, bool early,
                                   unsigned long long* timeline, cudaStream_t stream);

@@ -82,3 +82,22 @@ def test_plan_and_workspace(lib):
     assert pa.kernel_kind(2000, 4, 2) == 3           # too many sequences for the on-chip prefix sums
     with pytest.raises(pa.PAError):
         pa.kernel_kind(3, 17, 1)                     # G = 17: no kernel
+
+
+def test_plan_sections_lie_inside_the_plan(lib):
+    """pa_decode_plan_sections: the bounds and rates sections of a plan sit inside the bytes that
+    pa_decode_plan_size asks for, and follow the grid the options name."""
+    import ctypes
+    import paged_kv_cache_08_gb300._native as nat
+    for ctas_req, ctas_want in ((10, 10), (1, 1)):
+        o = nat.DecodeOptions(0, 0, ctas_req, nat.PLAN_ADAPTIVE, None)
+        size = lib.pa_decode_plan_size(4, 12, 2, 128, 16, 64, ctypes.byref(o))
+        C, b, r = ctypes.c_int(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
+        assert lib.pa_decode_plan_sections(4, 12, 2, 128, 16, 64, ctypes.byref(o), ctypes.byref(C), ctypes.byref(b),
+                                           ctypes.byref(r)) == 0
+        assert C.value == ctas_want
+        assert b.value % 4 == 0 and r.value % 16 == 0
+        assert b.value + 4 * (2 * C.value + 1) <= r.value and r.value + 4 * C.value <= size
+    o = nat.DecodeOptions(0, 0, -1, 0, None)
+    assert lib.pa_decode_plan_sections(4, 12, 2, 128, 16, 64, ctypes.byref(o), ctypes.byref(C), ctypes.byref(b),
+                                       ctypes.byref(r)) != 0

@@ -186,3 +186,35 @@ def test_planned_rejects_groups_above_8():
     dev = torch.device("cuda")
     with pytest.raises(pa.PAError):
         pa.decode_plan(wl.block_tables.to(dev), wl.context_lens.to(dev), 12, 1, 16, wl.num_blocks)
+
+
+def test_adaptive_plan_follows_measured_rates(oracle):
+    """Adaptive plans rebuilt into one buffer between launches: the first build cuts equal
+    shares, later ones cut by the rates the launches measured; every launch stays correct and
+    the measured rates are positive and finite."""
+    wl = workloads.make_workload("plan_adapt", context_lens=[5, 900, 64, 2000, 333, 1, 1200, 700, 4000],
+                                 num_q_heads=12, num_kv_heads=2, block_size=16, seed=41, max_context=4096)
+    dev = torch.device("cuda")
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    okc = oracle_pkg.as_u16(wl.k_cache[0])
+    ovc = oracle_pkg.as_u16(wl.v_cache[0])
+    ref = oracle.decode(wl.q[0], okc, ovc, wl.block_tables, wl.context_lens, wl.scale, wl.num_kv_heads, False)
+    for num_ctas in (0, 7):
+        plan = None
+        bounds = []
+        for it in range(6):
+            plan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks,
+                                  plan=plan, num_ctas=num_ctas, adaptive=True)
+            for _ in range(3):
+                out = pa.decode_planned(wl.q[0].to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), plan,
+                                        wl.scale)
+                torch.cuda.synchronize()
+                err = max_abs_err(out, ref)
+                assert err <= TOL, f"ctas {num_ctas}, build {it}: max abs error {err:.3e}"
+            bounds.append(pa.plan_bounds(plan).tolist())
+        rates = pa.plan_rates(plan)
+        assert rates.numel() == (bounds[0].__len__() - 1) // 2
+        r = rates[rates > 0]
+        assert r.numel() > 0 and torch.isfinite(r).all()
+        # the list length grows by the cuts that fall inside chunks (at most one per group bound)
+        assert all(b[0] == 0 and b == sorted(b) and abs(b[-1] - bounds[0][-1]) < len(b) for b in bounds)
