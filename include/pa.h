@@ -271,7 +271,10 @@ int pa_decode_append(void* out, const void* q, const void* k_new, const void* v_
  *     plan and cached rows may be read before the preceding kernel ends; the preceding
  *     kernel must then write none of the plan, the caches or the tables -- in particular a
  *     pa_decode_planned right after pa_decode_plan must not ask for it), timeline.
- * Adaptive plans (PA_PLAN_ADAPTIVE in pa_decode_plan's opts->flags): SMs stream at different
+ * Adaptive plans (PA_PLAN_ADAPTIVE in opts->flags, given alike to pa_decode_plan_size,
+ * pa_decode_plan, pa_decode_plan_sections and every pa_decode_planned on the plan: the plan's
+ * layout and the decode kernel depend on it; a mismatch makes the kernel set PA_DEV_BAD_PLAN
+ * and write nothing): SMs stream at different
  * rates, so by default every CTA gets the same weight of chunks; an adaptive plan instead
  * gives CTA c a share proportional to its rate measured by earlier pa_decode_planned calls on
  * plans built into the same buffer (each such call folds one measurement per CTA into the

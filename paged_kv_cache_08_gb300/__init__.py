@@ -243,8 +243,9 @@ class DecodePlan:
     """A decode step's plan (pa_decode_plan): device bytes plus the shape it was built for."""
 
     def __init__(self, data: torch.Tensor, num_seqs: int, num_q_heads: int, num_kv_heads: int, block_size: int,
-                 num_blocks: int, max_blocks_per_seq: int, num_ctas: int):
+                 num_blocks: int, max_blocks_per_seq: int, num_ctas: int, adaptive: bool = False):
         self.data = data
+        self.adaptive = adaptive
         self.num_seqs = num_seqs
         self.num_q_heads = num_q_heads
         self.num_kv_heads = num_kv_heads
@@ -267,9 +268,7 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
     if block_tables.dim() != 2 or block_tables.shape[0] != context_lens.numel():
         raise ValueError("block_tables must be [S, max_blocks] with S = context_lens.numel()")
     S, max_blocks = block_tables.shape
-    o = _opts(0, "auto", num_ctas)
-    if adaptive:
-        o.flags |= _native.PLAN_ADAPTIVE
+    o = _opts(0, "auto", num_ctas, flags=_native.PLAN_ADAPTIVE if adaptive else 0)
     need = int(lib().pa_decode_plan_size(S, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
                                          ctypes.byref(o)))
     if need == 0:
@@ -277,11 +276,13 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
     if plan is None or plan.data.numel() < need:
         # zeroed: an adaptive build finds no stale rates in a fresh buffer
         data = torch.zeros(need, dtype=torch.uint8, device=block_tables.device)
-        plan = DecodePlan(data, S, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks, int(num_ctas))
+        plan = DecodePlan(data, S, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks, int(num_ctas),
+                          adaptive)
     else:
         plan.num_seqs, plan.num_q_heads, plan.num_kv_heads = S, num_q_heads, num_kv_heads
         plan.block_size, plan.num_blocks, plan.max_blocks_per_seq, plan.num_ctas = (block_size, num_blocks,
                                                                                      max_blocks, int(num_ctas))
+        plan.adaptive = adaptive
     rc = lib().pa_decode_plan(plan.data.data_ptr(), plan.data.numel(), block_tables.data_ptr(),
                               context_lens.data_ptr(), S, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                               max_blocks, _stream_ptr(stream), ctypes.byref(o))
@@ -290,7 +291,7 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
 
 
 def _plan_sections(plan: DecodePlan):
-    o = _opts(0, "auto", plan.num_ctas)
+    o = _opts(0, "auto", plan.num_ctas, flags=_native.PLAN_ADAPTIVE if plan.adaptive else 0)
     ctas, b_off, r_off = ctypes.c_int(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
     rc = lib().pa_decode_plan_sections(plan.num_seqs, plan.num_q_heads, plan.num_kv_heads, 128, plan.block_size,
                                        plan.max_blocks_per_seq, ctypes.byref(o), ctypes.byref(ctas),
@@ -355,7 +356,8 @@ def decode_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(0, "auto", plan.num_ctas, timeline, _native.EARLY_READS if early_reads else 0)
+    o = _opts(0, "auto", plan.num_ctas, timeline,
+              (_native.EARLY_READS if early_reads else 0) | (_native.PLAN_ADAPTIVE if plan.adaptive else 0))
     if workspace is None:
         key = ("planned", q.device.index if q.device.index is not None else torch.cuda.current_device(),
                plan.num_ctas)

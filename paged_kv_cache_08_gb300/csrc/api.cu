@@ -636,6 +636,8 @@ int pa_multi_query_append(void* out, const void* q, const void* k_new, const voi
                        workspace_bytes, stream, opts, query_start, max_q_per_seq, num_q_tokens);
 }
 
+static bool plan_adaptive(const pa_decode_options* opts) { return opts && (opts->flags & PA_PLAN_ADAPTIVE); }
+
 static int planned_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq) {
     int rc = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
@@ -654,7 +656,8 @@ size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int 
     if (planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) != PA_OK)
         return 0;
     if (opts && opts->num_ctas < 0) return 0;
-    return planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts));
+    return planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts),
+                              plan_adaptive(opts));
 }
 
 int pa_decode_plan_sections(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -664,8 +667,8 @@ int pa_decode_plan_sections(int num_seqs, int num_q_heads, int num_kv_heads, int
     if (rc != PA_OK) return rc;
     if ((opts && opts->num_ctas < 0) || !num_ctas || !bounds_offset || !rates_offset) return PA_ERR_INVALID_ARG;
     *num_ctas = planned_ctas(opts);
-    planned_plan_offsets(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, *num_ctas, bounds_offset,
-                         rates_offset);
+    planned_plan_offsets(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, *num_ctas, plan_adaptive(opts),
+                         bounds_offset, rates_offset);
     return PA_OK;
 }
 
@@ -694,11 +697,12 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
     if (num_seqs > 0 && (!block_tables || !context_lens || !aligned4(block_tables) || !aligned4(context_lens)))
         return PA_ERR_INVALID_ARG;
     const int ctas = planned_ctas(opts);
-    if (plan_bytes < planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas))
+    if (plan_bytes <
+        planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, plan_adaptive(opts)))
         return PA_ERR_WORKSPACE;
     cudaError_t e = launch_decode_plan(plan, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                        block_size, num_blocks, max_blocks_per_seq, ctas,
-                                       opts && (opts->flags & PA_PLAN_ADAPTIVE), static_cast<cudaStream_t>(stream));
+                                       plan_adaptive(opts), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;
@@ -723,14 +727,15 @@ int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v
         !aligned16(k_new) || !aligned16(v_new))
         return PA_ERR_INVALID_ARG;
     const int ctas = planned_ctas(opts);
-    if (plan_bytes < planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas))
+    if (plan_bytes <
+        planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, plan_adaptive(opts)))
         return PA_ERR_WORKSPACE;
     const size_t need = planned_workspace_bytes(ctas);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
     const bool early = opts && (opts->flags & PA_DECODE_EARLY_READS);
     cudaError_t e = launch_decode_planned(out, q, k_new, v_new, k_cache, v_cache, plan, workspace, scale, num_seqs,
                                           num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq,
-                                          dtype, ctas, early, opts ? opts->timeline : nullptr,
+                                          dtype, ctas, early, plan_adaptive(opts), opts ? opts->timeline : nullptr,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -80,6 +80,7 @@ static_assert(kHdrOff % 16 == 0 && kPairOff % 16 == 0 && kHandOff % 16 == 0, "16
 static_assert(kSmemPlanned <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
 constexpr float kLazyLog2 = 8.f;
 constexpr int kPlanMagic = 0x31504150;                  // "PAP1"
+constexpr int kPlanMagicAdaptive = 0x41504150;          // "PAPA": an adaptive plan (another layout)
 
 // Stage flags.
 enum : int { kBegin = 1, kEnd = 2, kNewRow = 4 };
@@ -91,7 +92,8 @@ struct PlanHeader {
     int num_chunks;   // N
     int max_chunks;
     int adaptive;     // 0: equal shares; kAdaptiveFirst / kAdaptiveFold: see PlanRates
-    int pad[5];
+    int cap;          // chunk slots per group (the layout: larger for adaptive plans)
+    int pad[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header");
 
@@ -163,13 +165,14 @@ __host__ __device__ inline long long plan_max_chunks(int num_seqs, int num_kv_he
     return (long long)num_seqs * num_kv_heads * ((cap + kStageTokens - 1) / kStageTokens);
 }
 
-PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
+PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas, bool adaptive) {
     PlanLayout L;
     const long long maxc = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
     // A group gets at most (its share of the weight + one chunk) / the lightest chunk's weight.
-    // Chunks weigh 64 to 112 (at most 1.75x their mean) and a share is at most 1.5x the equal one
-    // (adaptive shares are bounded so): 1.5 x 1.75 < 3 equal shares of chunks, plus rounding.
-    L.cap = 3 * (int)((maxc + 2 * ctas - 1) / (2 * ctas)) + 6;
+    // Chunks weigh 64 to 112 (at most 1.75x their mean): equal shares need fewer than two equal
+    // shares of chunks, adaptive ones (at most 1.5x the equal share) fewer than three.
+    const int eq = (int)((maxc + 2 * ctas - 1) / (2 * ctas));
+    L.cap = adaptive ? 3 * eq + 6 : 2 * eq + 4;
     L.lens = 256;
     L.bounds = L.lens + al256((size_t)num_seqs * 4);
     L.cta = L.bounds + al256((size_t)(2 * ctas + 1) * 4);
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         }
         if (tid == 0) {
             PlanHeader h = {};
-            h.magic = kPlanMagic;
+            h.magic = a.adaptive ? kPlanMagicAdaptive : kPlanMagic;   // (the layouts differ)
             h.num_seqs = S;
             h.num_q_heads = a.num_q_heads;
             h.num_kv_heads = Hkv;
@@ -493,6 +496,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
             h.num_chunks = (int)N;
             h.max_chunks = (int)a.max_chunks;
             h.adaptive = a.adaptive ? (rates_ok ? kAdaptiveFold : kAdaptiveFirst) : 0;
+            h.cap = a.cap;
             *hdr = h;
         }
     }
@@ -802,7 +806,7 @@ __device__ __forceinline__ int remote_slot(const PlanEvent& ev, const int32_t* b
     return 0;
 }
 
-template <typename T>
+template <typename T, bool kAdaptive>
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_planned_kernel(const PlannedArgs a, const __grid_constant__ MmaMapsP maps, const int R_log2) {
     extern __shared__ unsigned char smem_raw[];
@@ -852,10 +856,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(&ready[1], kGroupThreads);
         *abort_flag = 0;
         *pair_count = 0;
-        misc[30] = (int)clock();
-        // this CTA's rate so far (adaptive plans fold it at the end), copied without a register;
-        // this thread waits for the copy at the end of its consumer loop
-        cp_async4(smem_u32(const_cast<int*>(misc + 29)), &a.rates->rate[c]);   // adaptive plans time the CTA's life from here
+        if (kAdaptive) {
+            misc[30] = (int)clock();
+            // this CTA's rate so far (folded at the end), copied without a register; this thread
+            // waits for the copy at the end of its consumer loop
+            cp_async4(smem_u32(const_cast<int*>(misc + 29)), &a.rates->rate[c]);
+        }   // adaptive plans time the CTA's life from here
         for (int i = 0; i < kGroups * kPStages; ++i) {
             qdef[i] = -1;
             ndef[i] = -1;
@@ -878,15 +884,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (is_prod && lane < min(32, a.cap)) load_chunk(slots + (size_t)pgrp * a.cap + lane, cur);
     uint4 hdr_part = make_uint4(0, 0, 0, 0);   // producers: lane j < 8 holds bytes 16 j .. of the CTA header
     if (is_prod && lane < 8) hdr_part = __ldcg(reinterpret_cast<const uint4*>(g_hdr) + lane);
-    const bool plan_ok = h_magic == kPlanMagic && h_seqs == a.num_seqs && h_qh == Hq && h_kvh == Hkv && h_bs == B &&
-                         h_nb == a.num_blocks && h_mb == a.max_blocks_per_seq && h_c == (int)gridDim.x &&
+    const bool plan_ok = h_magic == (kAdaptive ? kPlanMagicAdaptive : kPlanMagic) && h_seqs == a.num_seqs &&
+                         h_qh == Hq && h_kvh == Hkv && h_bs == B && h_nb == a.num_blocks && h_mb == a.max_blocks_per_seq && h_c == (int)gridDim.x &&
                          b0 <= b1 && b1 <= b2 && b1 - b0 <= a.cap && b2 - b1 <= a.cap;
     if (!plan_ok) {
         // the same decision in every thread (same bytes read); nothing was started
         if (a.early) grid_dependency_wait();
         grid_launch_dependents();
         if (tid == 0 && c == 0) flag_status(a.status, PA_DEV_BAD_PLAN);
-        if (tid == 0) cp_async_wait_all();
+        if (kAdaptive && tid == 0) cp_async_wait_all();
         return;
     }
     if (!a.early) grid_launch_dependents();
@@ -1497,13 +1503,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             mbar_arrive(&gempty[st]);
         }
-        if (tid == 0) cp_async_wait_all();   // the rate copied at the start
+        if (kAdaptive && tid == 0) cp_async_wait_all();   // the rate copied at the start
         if (grp == 0 && tid == 0) trace(a.timeline, c, 7);
         if (grp == 1 && tg == 0) trace(a.timeline, c, 9);
     }
 
     __syncthreads();
-    if (tid == kEpiWarp * 32 && sh_hdr->weight != 0.f && !*abort_flag) {
+    if (kAdaptive && tid == kEpiWarp * 32 && sh_hdr->weight != 0.f && !*abort_flag) {
         // adaptive plan: this CTA's rate, the weight of its range per SM cycle of its life
         const float w = fabsf(sh_hdr->weight);
         const unsigned span = (unsigned)clock() - (unsigned)misc[30];
@@ -1539,10 +1545,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
-template <typename T>
+template <typename T, bool kAdaptive>
 cudaError_t launch_planned_impl(const PlannedArgs& a, const MmaMapsP& maps, int R_log2, int ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_planned_kernel<T>;
+    auto kernel = decode_planned_kernel<T, kAdaptive>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1575,13 +1581,14 @@ int planned_ctas(const pa_decode_options* opts) {
     return sms;
 }
 
-size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
-    return plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas).total;
+size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
+                          bool adaptive) {
+    return plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, adaptive).total;
 }
 
 void planned_plan_offsets(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
-                          size_t* bounds_offset, size_t* rates_offset) {
-    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+                          bool adaptive, size_t* bounds_offset, size_t* rates_offset) {
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, adaptive);
     *bounds_offset = L.bounds;
     *rates_offset = L.rates + offsetof(PlanRates, rate);
 }
@@ -1595,7 +1602,7 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
                                int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
                                int max_blocks_per_seq, int ctas, bool adaptive, cudaStream_t stream) {
     if (ctas < 1 || ctas > 4 * kPlanThreads) return cudaErrorInvalidValue;
-    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, adaptive);
     PlanArgs a;
     a.plan = static_cast<unsigned char*>(plan);
     a.block_tables = block_tables;
@@ -1644,7 +1651,7 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
 cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                                   const void* v_cache, void* plan, void* workspace, float scale, int num_seqs,
                                   int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
-                                  int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                  int max_blocks_per_seq, int dtype, int ctas, bool early, bool adaptive,
                                   unsigned long long* timeline, cudaStream_t stream) {
     const int R = block_size < kStageTokens ? block_size : kStageTokens;
     int R_log2 = 0;
@@ -1654,7 +1661,7 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     MmaMapsP maps;
     if (!encode_pool_map(k_cache, rows, R, &maps.k) || !encode_pool_map(v_cache, rows, R, &maps.v))
         return cudaErrorInvalidValue;
-    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, adaptive);
     PlannedArgs a;
     a.out = out;
     a.q = q;
@@ -1684,8 +1691,11 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     a.bounds_off = L.bounds;
     a.cta_off = L.cta;
     a.cta_bytes = L.cta_bytes;
-    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16>(a, maps, R_log2, ctas, stream)
-                            : launch_planned_impl<__half>(a, maps, R_log2, ctas, stream);
+    if (adaptive)
+        return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, true>(a, maps, R_log2, ctas, stream)
+                                : launch_planned_impl<__half, true>(a, maps, R_log2, ctas, stream);
+    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, false>(a, maps, R_log2, ctas, stream)
+                            : launch_planned_impl<__half, false>(a, maps, R_log2, ctas, stream);
 }
 
 }  // namespace pa

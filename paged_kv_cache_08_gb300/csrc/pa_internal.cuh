@@ -294,17 +294,18 @@ cudaError_t launch_prefill_tc(const DecodeArgs& a, int dtype, cudaStream_t strea
 // Planned decode (decode_planned.cu): the per-step plan and the per-layer launch that reads it.
 constexpr int kPlanMaxSeqs = 1024;      // sequences the plan kernel keeps in shared memory
 int planned_ctas(const pa_decode_options* opts);
-size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas);
+size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
+                          bool adaptive);
 size_t planned_workspace_bytes(int ctas);
 void planned_plan_offsets(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
-                          size_t* bounds_offset, size_t* rates_offset);
+                          bool adaptive, size_t* bounds_offset, size_t* rates_offset);
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
                                int max_blocks_per_seq, int ctas, bool adaptive, cudaStream_t stream);
 cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                                   const void* v_cache, void* plan, void* workspace, float scale, int num_seqs,
                                   int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
-                                  int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                  int max_blocks_per_seq, int dtype, int ctas, bool early, bool adaptive,
                                   unsigned long long* timeline, cudaStream_t stream);
 
 // Tensor-core split pass (any G <= 16); builds the TMA tensor maps of the two caches.

@@ -218,3 +218,18 @@ def test_adaptive_plan_follows_measured_rates(oracle):
         assert r.numel() > 0 and torch.isfinite(r).all()
         # the list length grows by the cuts that fall inside chunks (at most one per group bound)
         assert all(b[0] == 0 and b == sorted(b) and abs(b[-1] - bounds[0][-1]) < len(b) for b in bounds)
+
+
+def test_adaptive_plan_used_without_the_flag_is_refused_on_the_device():
+    """The layout of an adaptive plan differs: a launch that does not name PA_PLAN_ADAPTIVE finds
+    another slot count in the plan's header, writes nothing and flags PA_DEV_BAD_PLAN."""
+    wl = workloads.make_workload("plan_mismatch", context_lens=[100, 2000, 700], num_q_heads=8, num_kv_heads=2,
+                                 block_size=16, seed=4, max_context=2048)
+    dev = torch.device("cuda")
+    plan = pa.decode_plan(wl.block_tables.to(dev), wl.context_lens.to(dev), 8, 2, 16, wl.num_blocks, adaptive=True)
+    plan.adaptive = False
+    out = torch.full_like(wl.q[0].to(dev), 7.0)
+    pa.decode_planned(wl.q[0].to(dev), wl.k_cache[0].to(dev), wl.v_cache[0].to(dev), plan, wl.scale, out=out)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) == pa._native.DEV_BAD_PLAN
+    assert torch.all(out == 7.0)
