@@ -969,10 +969,13 @@ def run_prefill(args, seqs: int = 16, context: int = 4096, new_tokens: int = 512
 
 def run_runs(args):
     """Slotted contexts: the decode bench's 24-layer 1.1B shape with every 16-token block of every
-    context read as two runs cut at a seeded random offset (about 2 x 4300 runs per layer), on
-    pa_decode_runs; then the compaction of one layer's runs into fresh whole blocks
-    (pa_gather_runs).  Bytes: the decode ledger with 12 bytes per run in place of 4 per table
-    entry; the compaction moves every context row of K and V once (read + written)."""
+    context read as two runs cut at a seeded random offset (about 2 x 4300 runs per layer).  The
+    step is one pa_decode_plan_runs (the token table and the cut, once for all layers) and one
+    pa_decode_planned per layer (early reads from layer 1 on), in a CUDA graph; the one-call
+    pa_decode_runs per layer (three launches each) is timed beside it, and the compaction of one
+    layer's runs into fresh whole blocks (pa_gather_runs).  Bytes: the decode ledger with 12 bytes
+    per run in place of 4 per table entry; the compaction moves every context row of K and V once
+    (read + written)."""
     import paged_kv_cache_08_gb300 as pa
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -996,19 +999,33 @@ def run_runs(args):
     max_ctx = int(wl.context_lens.max())
     outs = [torch.empty_like(wl.q[i]) for i in range(wl.layers)]
     S, Hq, D, Hkv = wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.num_kv_heads
-    ws = pa.new_workspace(pa.lib().pa_decode_runs_workspace_size(S, Hq, Hkv, D, B, max_ctx), dev)
+    ws = pa.new_runs_workspace(wl.q[0], Hkv, B, max_ctx)
+    plan = pa.decode_plan_runs(runs_t, seq_t, Hq, Hkv, B, wl.num_blocks, max_ctx)
+    pws = pa.new_planned_workspace(0, dev)
 
     def step():
+        pa.decode_plan_runs(runs_t, seq_t, Hq, Hkv, B, wl.num_blocks, max_ctx, plan=plan)
+        for i in range(wl.layers):
+            pa.decode_planned(wl.q[i], wl.k_cache[i], wl.v_cache[i], plan, wl.scale, out=outs[i], workspace=pws,
+                              early_reads=i > 0)
+
+    def step_one_call():
         for i in range(wl.layers):
             pa.decode_runs(wl.q[i], wl.k_cache[i], wl.v_cache[i], runs_t, seq_t, wl.scale, Hkv, max_ctx, out=outs[i],
                            workspace=ws)
-    step()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
+    graphs = []
+    for fn in (step, step_one_call):
+        fn()
+        torch.cuda.synchronize()
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            fn()
+        graphs.append(g_)
+    pa.read_device_status(clear=True)
     with ClockSampler(0) as clk:
-        ms = _event_ms(lambda _: graph.replay(), args.steps, args.warmup)
+        ms = _event_ms(lambda _: graphs[0].replay(), args.steps, args.warmup)
+    ms_one = _event_ms(lambda _: graphs[1].replay(), args.steps, args.warmup)
+    status = pa.read_device_status(clear=True)
     lens64 = wl.context_lens.to(torch.int64)
     per_layer = int(lens64.sum()) * Hkv * D * 2 * 2 + 2 * S * Hq * D * 2 + 12 * len(runs) + 4 * (S + 1)
     gbs = wl.layers * per_layer / (ms * 1e-3) / 1e9
@@ -1041,10 +1058,15 @@ def run_runs(args):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "traffic": None, "algorithmic_bytes_per_layer": per_layer,
                          "avg_layer_us": round(ms * 1e3 / wl.layers, 2),
-                         "kernel": "decode_split_fma_kernel (runs) + combine", "peak_source": f"{peak_kind} copy bandwidth"},
+                         "kernel": "decode_planned_kernel (runs: one bulk copy per K and V row)",
+                         "peak_source": f"{peak_kind} copy bandwidth"},
+            "one_call_per_layer": {"us_per_layer": round(ms_one * 1e3 / wl.layers, 2),
+                                   "gbs": round(wl.layers * per_layer / (ms_one * 1e-3) / 1e9, 1),
+                                   "how": "pa_decode_runs per layer: token table, plan and decode each time"},
+            "device_status": status,
             "compaction": {"moves": len(moves), "us": round(cms * 1e3, 2),
                            "gbs": round(moved / (cms * 1e-3) / 1e9, 1), "frac": round(moved / (cms * 1e-3) / 1e9 / peak, 4)},
-            "gpu_launches": wl.layers * 2 * args.steps, "clocks": clk.summary()}
+            "gpu_launches": (wl.layers + 2) * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 

@@ -219,6 +219,9 @@ int pa_decode_static(void* out, const void* q, const void* k_cache, const void* 
 /* pa_decode_plan: shares of the decode launch's CTAs that follow their measured streaming rates
  * (see pa_decode_plan). */
 #define PA_PLAN_ADAPTIVE 8
+/* pa_decode_plan_size / pa_decode_plan_sections / pa_decode_planned: the plan is a runs plan
+ * (pa_decode_plan_runs). */
+#define PA_PLAN_RUNS 16
 
 /* ------------------------------------------------------------------------------------
  * pa_decode_append  [P4 §三 sequence diagram + §五.1; P1 address formula]
@@ -308,6 +311,23 @@ int pa_decode_plan_sections(int num_seqs, int num_q_heads, int num_kv_heads, int
                             int max_blocks_per_seq, const pa_decode_options* opts, int* num_ctas,
                             size_t* bounds_offset, size_t* rates_offset);
 size_t pa_decode_planned_workspace_size(const pa_decode_options* opts);
+/* ------------------------------------------------------------------------------------
+ * pa_decode_plan_runs  [P2 "Slotted Block 分槽与微块共享架构": (block_id, slot_offset, length)
+ *                       triples; P4 §五.1 attention]
+ * The plan of a decode step whose contexts are given as runs (as pa_decode_runs: sequence s reads
+ * runs seq_runs[s] .. seq_runs[s+1]-1 of `runs`, int32 [R][3]; a run that leaves its block or the
+ * pool counts as empty and sets PA_DEV_BAD_BLOCK_ID; contexts longer than max_context are cut and
+ * set PA_DEV_BAD_CONTEXT).  One warp per sequence writes its tokens' rows into a token table in
+ * the plan, then the plan kernel cuts the chunks as pa_decode_plan does.  Two launches.
+ *   plan: pa_decode_plan_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+ *     max_blocks_per_seq = ceil(max_context / block_size), opts with PA_PLAN_RUNS) bytes.
+ * Then pa_decode_planned with PA_PLAN_RUNS in opts->flags, the same max_blocks_per_seq and no
+ * new rows (k_new = v_new = NULL) decodes one layer: every token's K and V row is one bulk copy
+ * into a padded shared-memory row.  Not adaptive.  Returns the codes of pa_decode_plan.
+ * ---------------------------------------------------------------------------------- */
+int pa_decode_plan_runs(void* plan, size_t plan_bytes, const int32_t* runs, const int32_t* seq_runs, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        int max_context, void* stream, const pa_decode_options* opts);
 /* Fill `bytes` of a pa_decode_planned workspace with 0xFF on `stream` (cudaMemsetAsync). */
 int pa_decode_planned_workspace_init(void* workspace, size_t bytes, void* stream);
 int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v_new,
@@ -383,9 +403,16 @@ int pa_multi_query_append(void* out, const void* q, const void* k_new, const voi
  *   out[s][h][:] = sum_t softmax_t(scale * q[s][h] . K[t]) * V[t][:]   (L == 0: zero row).
  * max_context bounds every L (longer contexts are cut there and set PA_DEV_BAD_CONTEXT).  A run
  * that leaves its block or the pool counts as empty and sets PA_DEV_BAD_BLOCK_ID.
- * Runs on the split CUDA-core kernel (each run piece one bulk copy of contiguous rows):
- * num_q_heads / num_kv_heads in {1, 2, 3, 4, 6, 8}, block_size 16/32/64/128, head_dim 128.
- * workspace: pa_decode_runs_workspace_size(...) bytes (0: none needed).
+ * Up to 1024 sequences (and max_context up to 2^21): three launches on the stream -- one warp
+ * per sequence lays its tokens' rows out in a token table, the decode plan kernel cuts the
+ * 64-token chunks among the SMs, and the planned decode kernel copies every token's K and V row
+ * (one bulk copy each) into padded shared-memory rows.  Beyond that the split CUDA-core kernel
+ * runs (each run piece one bulk copy of contiguous rows).  num_q_heads / num_kv_heads in
+ * {1, 2, 3, 4, 6, 8}, block_size 16/32/64/128, head_dim 128.
+ * workspace: pa_decode_runs_workspace_size(...) bytes, 16-byte aligned (0: none needed), FILLED
+ * WITH 0xFF BYTES before its first use (pa_decode_planned_workspace_init); every completed call
+ * leaves it fit for the next (after a call that set PA_DEV_TIMEOUT, fill it again).  Calls that
+ * share a workspace must not overlap on the GPU.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or PA_ERR_CUDA.
  * ---------------------------------------------------------------------------------- */
 int pa_decode_runs(void* out, const void* q, const void* k_cache, const void* v_cache,

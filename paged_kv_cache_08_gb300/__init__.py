@@ -24,9 +24,9 @@ import torch
 from . import _native
 from ._native import PAError, DecodeOptions, MATH
 
-__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_planned", "DecodePlan", "plan_bounds", "plan_rates",
+__all__ = ["cache_write", "copy_blocks", "decode", "decode_append", "decode_plan", "decode_plan_runs", "decode_planned", "DecodePlan", "plan_bounds", "plan_rates",
            "planned_workspace_size", "new_planned_workspace",
-           "multi_query", "decode_runs", "gather_runs",
+           "multi_query", "decode_runs", "new_runs_workspace", "gather_runs",
            "SlotPool", "decode_workspace_size", "plan_tokens_per_split", "kernel_kind",
            "new_workspace", "BlockPool",
            "build_slot_mapping", "read_device_status", "kernel_launch_count", "PAError", "lib"]
@@ -243,9 +243,11 @@ class DecodePlan:
     """A decode step's plan (pa_decode_plan): device bytes plus the shape it was built for."""
 
     def __init__(self, data: torch.Tensor, num_seqs: int, num_q_heads: int, num_kv_heads: int, block_size: int,
-                 num_blocks: int, max_blocks_per_seq: int, num_ctas: int, adaptive: bool = False):
+                 num_blocks: int, max_blocks_per_seq: int, num_ctas: int, adaptive: bool = False,
+                 runs: bool = False):
         self.data = data
         self.adaptive = adaptive
+        self.runs = runs
         self.num_seqs = num_seqs
         self.num_q_heads = num_q_heads
         self.num_kv_heads = num_kv_heads
@@ -282,7 +284,7 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
         plan.num_seqs, plan.num_q_heads, plan.num_kv_heads = S, num_q_heads, num_kv_heads
         plan.block_size, plan.num_blocks, plan.max_blocks_per_seq, plan.num_ctas = (block_size, num_blocks,
                                                                                      max_blocks, int(num_ctas))
-        plan.adaptive = adaptive
+        plan.adaptive, plan.runs = adaptive, False
     rc = lib().pa_decode_plan(plan.data.data_ptr(), plan.data.numel(), block_tables.data_ptr(),
                               context_lens.data_ptr(), S, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                               max_blocks, _stream_ptr(stream), ctypes.byref(o))
@@ -290,8 +292,47 @@ def decode_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, num_q_he
     return plan
 
 
+def _plan_flags(plan: DecodePlan) -> int:
+    return (_native.PLAN_ADAPTIVE if plan.adaptive else 0) | (_native.PLAN_RUNS if plan.runs else 0)
+
+
+def decode_plan_runs(runs: torch.Tensor, seq_runs: torch.Tensor, num_q_heads: int, num_kv_heads: int,
+                     block_size: int, num_blocks: int, max_context: int, head_dim: int = 128,
+                     plan: Optional[DecodePlan] = None, num_ctas: int = 0,
+                     stream: Optional[torch.cuda.Stream] = None) -> DecodePlan:
+    """The plan of a decode step over contexts given as runs (block_id, slot_offset, length):
+    runs int32 [R, 3], sequence s reading runs seq_runs[s] .. seq_runs[s+1]-1 (pa_decode_plan_runs).
+    decode_planned then decodes each layer through it (no cache write)."""
+    _need_cuda("runs", runs, torch.int32)
+    _need_cuda("seq_runs", seq_runs, torch.int32)
+    S = seq_runs.numel() - 1
+    if S < 1 or (runs.numel() and runs.shape[-1] != 3):
+        raise ValueError("seq_runs must have S + 1 entries and runs 3 columns")
+    max_blocks = (int(max_context) + block_size - 1) // block_size
+    o = _opts(0, "auto", num_ctas, flags=_native.PLAN_RUNS)
+    need = int(lib().pa_decode_plan_size(S, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                                         ctypes.byref(o)))
+    if need == 0:
+        raise PAError("pa_decode_plan_size", -2)
+    if plan is None or plan.data.numel() < need:
+        data = torch.zeros(need, dtype=torch.uint8, device=runs.device)
+        plan = DecodePlan(data, S, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks, int(num_ctas),
+                          False, True)
+    else:
+        plan.num_seqs, plan.num_q_heads, plan.num_kv_heads = S, num_q_heads, num_kv_heads
+        plan.block_size, plan.num_blocks, plan.max_blocks_per_seq, plan.num_ctas = (block_size, num_blocks,
+                                                                                     max_blocks, int(num_ctas))
+        plan.adaptive, plan.runs = False, True
+    rc = lib().pa_decode_plan_runs(plan.data.data_ptr(), plan.data.numel(),
+                                   runs.data_ptr() if runs.numel() else seq_runs.data_ptr(), seq_runs.data_ptr(), S,
+                                   num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, int(max_context),
+                                   _stream_ptr(stream), ctypes.byref(o))
+    _native.check("pa_decode_plan_runs", rc)
+    return plan
+
+
 def _plan_sections(plan: DecodePlan):
-    o = _opts(0, "auto", plan.num_ctas, flags=_native.PLAN_ADAPTIVE if plan.adaptive else 0)
+    o = _opts(0, "auto", plan.num_ctas, flags=_plan_flags(plan))
     ctas, b_off, r_off = ctypes.c_int(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
     rc = lib().pa_decode_plan_sections(plan.num_seqs, plan.num_q_heads, plan.num_kv_heads, 128, plan.block_size,
                                        plan.max_blocks_per_seq, ctypes.byref(o), ctypes.byref(ctas),
@@ -356,8 +397,7 @@ def decode_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
         _need_cuda("out", out, q.dtype)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    o = _opts(0, "auto", plan.num_ctas, timeline,
-              (_native.EARLY_READS if early_reads else 0) | (_native.PLAN_ADAPTIVE if plan.adaptive else 0))
+    o = _opts(0, "auto", plan.num_ctas, timeline, (_native.EARLY_READS if early_reads else 0) | _plan_flags(plan))
     if workspace is None:
         key = ("planned", q.device.index if q.device.index is not None else torch.cuda.current_device(),
                plan.num_ctas)
@@ -441,6 +481,27 @@ def multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
     return out
 
 
+_runs_workspaces = {}
+
+
+def _runs_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """One pa_decode_runs workspace per device, filled with 0xFF bytes once (every completed call
+    leaves it so)."""
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _runs_workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.full((nbytes,), 255, dtype=torch.uint8, device=device)
+        _runs_workspaces[key] = ws
+    return ws
+
+
+def new_runs_workspace(q: torch.Tensor, num_kv_heads: int, block_size: int, max_context: int) -> torch.Tensor:
+    """A pa_decode_runs workspace for q's shape, filled with 0xFF bytes as the kernels expect."""
+    S, Hq, D = q.shape
+    need = int(lib().pa_decode_runs_workspace_size(S, Hq, num_kv_heads, D, block_size, int(max_context)))
+    return torch.full((max(need, 16),), 255, dtype=torch.uint8, device=q.device)
+
+
 def decode_runs(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, runs: torch.Tensor,
                 seq_runs: torch.Tensor, scale: float, num_kv_heads: int, max_context: int,
                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
@@ -466,7 +527,7 @@ def decode_runs(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, r
         _need_cuda("out", out, q.dtype)
     need = int(lib().pa_decode_runs_workspace_size(S, Hq, Hkv, D, B, int(max_context)))
     if workspace is None and need:
-        workspace = _workspace(q.device, need, -1, 0)
+        workspace = _runs_workspace(q.device, need)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().pa_decode_runs(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),

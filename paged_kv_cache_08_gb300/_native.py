@@ -35,6 +35,7 @@ MATH = {"auto": 0, "fma": 1, "mma": 2, "mma_split": 3}
 EARLY_READS = 1
 PREFILL_MMA_SYNC = 4
 PLAN_ADAPTIVE = 8
+PLAN_RUNS = 16
 
 _SIGNATURES = {
     "pa_cache_write": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp]),
@@ -70,6 +71,8 @@ _SIGNATURES = {
     "pa_decode_plan_sections": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(DecodeOptions),
                                         ctypes.POINTER(c_int), ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
     "pa_decode_planned_workspace_size": (c_size, [ctypes.POINTER(DecodeOptions)]),
+    "pa_decode_plan_runs": (c_int, [c_vp, c_size, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_vp,
+                                    ctypes.POINTER(DecodeOptions)]),
     "pa_decode_planned_workspace_init": (c_int, [c_vp, c_size, c_vp]),
     "pa_decode_planned": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_f32, c_int, c_int, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_vp, c_size, c_vp, ctypes.POINTER(DecodeOptions)]),

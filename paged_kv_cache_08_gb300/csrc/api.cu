@@ -322,11 +322,40 @@ static int runs_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_d
     return PA_OK;
 }
 
+static int planned_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq);
+
+// A runs plan: the block-table plan's shapes, and a token table of num_seqs x max_context rows.
+static int runs_planned_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq) {
+    int rc = planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+    if (rc != PA_OK) return rc;
+    const long long stride = ((long long)max_blocks_per_seq * block_size + kStageTokens - 1) / kStageTokens * kStageTokens;
+    if ((long long)num_seqs * stride > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// The one-shot pa_decode_runs on the planned kernel: its workspace holds the runs plan and the
+// decode's partial slots.
+static bool runs_one_shot(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int max_context, size_t* plan_bytes, size_t* total) {
+    if (num_seqs <= 0 || max_context <= 0) return false;
+    const int maxb = (max_context + block_size - 1) / block_size;
+    if (runs_planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, maxb) != PA_OK) return false;
+    const int ctas = planned_ctas(nullptr);
+    *plan_bytes = planned_runs_plan_bytes(num_seqs, num_kv_heads, block_size, maxb, ctas);
+    *total = ((*plan_bytes + 255) & ~size_t(255)) + planned_workspace_bytes(ctas);
+    return true;
+}
+
 size_t pa_decode_runs_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                      int max_context) {
     int tps, maxb, ms;
     if (runs_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context, &tps, &maxb, &ms) != PA_OK)
         return 0;
+    size_t pb, total;
+    if (runs_one_shot(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context, &pb, &total))
+        return total;
     return ms > 1 ? workspace_bytes_for(num_seqs, num_q_heads, ms) : 0;
 }
 
@@ -344,6 +373,25 @@ int pa_decode_runs(void* out, const void* q, const void* k_cache, const void* v_
         !aligned4(seq_runs))
         return PA_ERR_INVALID_ARG;
     if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    size_t pb, total;
+    if (runs_one_shot(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context, &pb, &total)) {
+        if (!workspace || workspace_bytes < total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+        const int ctas = planned_ctas(nullptr);
+        const int maxb = (max_context + block_size - 1) / block_size;
+        void* plan = workspace;
+        void* ws = static_cast<char*>(workspace) + ((pb + 255) & ~size_t(255));
+        cudaError_t e = launch_decode_plan_runs(plan, runs, seq_runs, num_seqs, num_q_heads, num_kv_heads, block_size,
+                                                num_blocks, maxb, max_context, ctas, st);
+        if (e == cudaSuccess)
+            e = launch_decode_planned_runs(out, q, k_cache, v_cache, plan, ws, scale, num_seqs, num_q_heads,
+                                           num_kv_heads, block_size, num_blocks, maxb, dtype, ctas, false, nullptr, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        return PA_OK;
+    }
     const size_t need = ms > 1 ? workspace_bytes_for(num_seqs, num_q_heads, ms) : 0;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PA_ERR_WORKSPACE;
     DecodeArgs a;
@@ -368,7 +416,6 @@ int pa_decode_runs(void* out, const void* q, const void* k_cache, const void* v_
     a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + n_part * kHeadDim * sizeof(float))
                      : nullptr;
     a.status = device_status_ptr();
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_decode_split_fma(a, dtype, num_q_heads / num_kv_heads, st);
     if (e == cudaSuccess && ms > 1) e = launch_decode_combine(a, dtype, st);
     if (e != cudaSuccess) {
@@ -637,6 +684,7 @@ int pa_multi_query_append(void* out, const void* q, const void* k_new, const voi
 }
 
 static bool plan_adaptive(const pa_decode_options* opts) { return opts && (opts->flags & PA_PLAN_ADAPTIVE); }
+static bool plan_runs(const pa_decode_options* opts) { return opts && (opts->flags & PA_PLAN_RUNS); }
 
 static int planned_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq) {
@@ -656,6 +704,12 @@ size_t pa_decode_plan_size(int num_seqs, int num_q_heads, int num_kv_heads, int 
     if (planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) != PA_OK)
         return 0;
     if (opts && opts->num_ctas < 0) return 0;
+    if (plan_runs(opts)) {
+        if (plan_adaptive(opts) ||
+            runs_planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) != PA_OK)
+            return 0;
+        return planned_runs_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts));
+    }
     return planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, planned_ctas(opts),
                               plan_adaptive(opts));
 }
@@ -692,7 +746,7 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
                    int max_blocks_per_seq, void* stream, const pa_decode_options* opts) {
     int rc = planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
     if (rc != PA_OK) return rc;
-    if (opts && opts->num_ctas < 0) return PA_ERR_INVALID_ARG;
+    if ((opts && opts->num_ctas < 0) || plan_runs(opts)) return PA_ERR_INVALID_ARG;
     if (num_blocks <= 0 || !plan || !aligned16(plan)) return PA_ERR_INVALID_ARG;
     if (num_seqs > 0 && (!block_tables || !context_lens || !aligned4(block_tables) || !aligned4(context_lens)))
         return PA_ERR_INVALID_ARG;
@@ -703,6 +757,28 @@ int pa_decode_plan(void* plan, size_t plan_bytes, const int32_t* block_tables, c
     cudaError_t e = launch_decode_plan(plan, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                        block_size, num_blocks, max_blocks_per_seq, ctas,
                                        plan_adaptive(opts), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode_plan_runs(void* plan, size_t plan_bytes, const int32_t* runs, const int32_t* seq_runs, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        int max_context, void* stream, const pa_decode_options* opts) {
+    if (max_context <= 0 || num_seqs <= 0) return PA_ERR_INVALID_ARG;
+    const int maxb = (max_context + block_size - 1) / block_size;
+    int rc = runs_planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, maxb);
+    if (rc != PA_OK) return rc;
+    if ((opts && opts->num_ctas < 0) || plan_adaptive(opts)) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || !plan || !aligned16(plan) || !runs || !seq_runs || !aligned4(runs) || !aligned4(seq_runs))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const int ctas = planned_ctas(opts);
+    if (plan_bytes < planned_runs_plan_bytes(num_seqs, num_kv_heads, block_size, maxb, ctas)) return PA_ERR_WORKSPACE;
+    cudaError_t e = launch_decode_plan_runs(plan, runs, seq_runs, num_seqs, num_q_heads, num_kv_heads, block_size,
+                                            num_blocks, maxb, max_context, ctas, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;
@@ -727,16 +803,27 @@ int pa_decode_planned(void* out, const void* q, const void* k_new, const void* v
         !aligned16(k_new) || !aligned16(v_new))
         return PA_ERR_INVALID_ARG;
     const int ctas = planned_ctas(opts);
-    if (plan_bytes <
-        planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, plan_adaptive(opts)))
-        return PA_ERR_WORKSPACE;
+    const bool runs = plan_runs(opts);
+    if (runs && (k_new != nullptr || plan_adaptive(opts))) return PA_ERR_INVALID_ARG;
+    if (runs) {
+        rc = runs_planned_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq);
+        if (rc != PA_OK) return rc;
+    }
+    const size_t plan_need =
+        runs ? planned_runs_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas)
+             : planned_plan_bytes(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, plan_adaptive(opts));
+    if (plan_bytes < plan_need) return PA_ERR_WORKSPACE;
     const size_t need = planned_workspace_bytes(ctas);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
     const bool early = opts && (opts->flags & PA_DECODE_EARLY_READS);
-    cudaError_t e = launch_decode_planned(out, q, k_new, v_new, k_cache, v_cache, plan, workspace, scale, num_seqs,
-                                          num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq,
-                                          dtype, ctas, early, plan_adaptive(opts), opts ? opts->timeline : nullptr,
-                                          static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e =
+        runs ? launch_decode_planned_runs(out, q, k_cache, v_cache, plan, workspace, scale, num_seqs, num_q_heads,
+                                          num_kv_heads, block_size, num_blocks, max_blocks_per_seq, dtype, ctas, early,
+                                          opts ? opts->timeline : nullptr, st)
+             : launch_decode_planned(out, q, k_new, v_new, k_cache, v_cache, plan, workspace, scale, num_seqs,
+                                     num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq, dtype,
+                                     ctas, early, plan_adaptive(opts), opts ? opts->timeline : nullptr, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PA_ERR_CUDA;

@@ -40,6 +40,7 @@
 
 #include <atomic>
 #include <cstddef>
+#include <cstring>
 #include <climits>
 #include <type_traits>
 
@@ -54,33 +55,55 @@ constexpr int kConsWarps = kGroups * kGroupWarps;       // 8
 constexpr int kProdWarp0 = kConsWarps;                  // producers: warps 8, 9
 constexpr int kEpiWarp = kConsWarps + kGroups;          // 10
 constexpr int kPThreads = (kEpiWarp + 1) * 32;          // 352
-constexpr int kPStages = 3;
 constexpr int kRows = 8;                                // query rows per segment (the GQA group, G <= 8)
-constexpr uint32_t kKB = kStageTokens * kHeadDim * 2;   // 16 KB of K per stage (V the same)
-constexpr uint32_t kKVB = 2 * kKB;
-constexpr uint32_t kQOff = kKVB;                        // q rows: 8 x 256 B
-constexpr uint32_t kNewOff = kQOff + kRows * kHeadDim * 2;   // new K row, new V row: 2 x 256 B
-constexpr uint32_t kMetaOff = kNewOff + 2 * kHeadDim * 2;    // stage metadata (64 B)
-constexpr uint32_t kStageB = 35 * 1024;                 // 1024-aligned stages
-static_assert(kMetaOff + 64 <= kStageB, "stage layout");
-constexpr uint32_t kRingB = kGroups * kPStages * kStageB;
 constexpr int kRedStride = kHeadDim + 4;                // padded rows of the merge scratch
-static_assert(kGroupWarps * 8 * kRedStride * 4 + kGroupWarps * 8 * 8 <= kKVB, "merge scratch fits a stage");
 constexpr uint32_t kSlotB = kRows * kHeadDim * 4 + kRows * 8;   // partial (o rows, then (m, l) per row)
-constexpr uint32_t kPairOff = kRingB;                   // the two groups' meeting slot
-constexpr uint32_t kHandOff = kPairOff + kSlotB;        // [2 sides] this CTA's piece for the epilogue
-constexpr uint32_t kBarOff = kHandOff + 2 * kSlotB;
-// barriers: full[2][3], empty[2][3], qbar[2], pair, ready[2]
-constexpr int kNumBars = 2 * kGroups * kPStages + kGroups + 1 + 2;
-constexpr uint32_t kMiscOff = (kBarOff + kNumBars * 8 + 15u) & ~15u;
 constexpr uint32_t kMiscB = 128;
-constexpr uint32_t kHdrOff = kMiscOff + kMiscB;          // copy of this CTA's plan header (128 B)
-constexpr size_t kSmemPlanned = 1024 + kHdrOff + 128;
-static_assert(kHdrOff % 16 == 0 && kPairOff % 16 == 0 && kHandOff % 16 == 0, "16-byte aligned smem sections");
-static_assert(kSmemPlanned <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
+// Runs stages: a chunk's 64 tokens as 8 octets of 8 consecutive tokens; octet k is 8 rows of 256
+// bytes in a row at k * 2064 (16 bytes of pad per octet).  Staged row t (the consumers' index)
+// holds token 8 (t mod 8) + t / 8, so the 8 rows one ldmatrix reads lie in 8 different octets,
+// 16 bytes apart in the bank map (no conflict), and the rows of one octet, consecutive tokens, take
+// one bulk copy wherever they are consecutive rows of the pool.
+constexpr uint32_t kOctB = 8 * kHeadDim * 2 + 16;        // 2064
+
+// Shared-memory layout of a decode CTA: per group 3 stages of 35 KB.  Block-table plans: K and V
+// as TMA boxes with the 128-byte swizzle.  Runs plans (contexts given as slot runs): K and V as the
+// quads above, filled by bulk copies; no new-token rows (runs plans do not append).
+template <bool kRuns>
+struct Lay {
+    static constexpr int kPStages = 3;
+    static constexpr uint32_t kKB = kRuns ? 8 * kOctB : kStageTokens * kHeadDim * 2;   // K per stage (V the same)
+    static constexpr uint32_t kKVB = 2 * kKB;
+    static constexpr uint32_t kQOff = kKVB;                          // q rows: 8 x 256 B
+    static constexpr uint32_t kNewOff = kQOff + kRows * kHeadDim * 2;   // new K row, new V row: 2 x 256 B
+    static constexpr uint32_t kMetaOff = kNewOff + (kRuns ? 0u : 2u * kHeadDim * 2);   // stage metadata (64 B)
+    static constexpr uint32_t kStageB = 35 * 1024;                   // 1024-aligned stages
+    static constexpr uint32_t kRingB = kGroups * kPStages * kStageB;
+    static constexpr uint32_t kPairOff = kRingB;                     // the two groups' meeting slot
+    static constexpr uint32_t kHandOff = kPairOff + kSlotB;          // [2 sides] this CTA's piece for the epilogue
+    static constexpr uint32_t kBarOff = kHandOff + 2 * kSlotB;
+    // barriers: full[2][stages], empty[2][stages], qbar[2], pair, ready[2]
+    static constexpr int kNumBars = 2 * kGroups * kPStages + kGroups + 1 + 2;
+    static constexpr uint32_t kMiscOff = (kBarOff + kNumBars * 8 + 15u) & ~15u;
+    static constexpr uint32_t kHdrOff = kMiscOff + kMiscB;           // copy of this CTA's plan header (128 B)
+    static constexpr size_t kSmem = 1024 + kHdrOff + 128;
+    static_assert(kMetaOff + 64 <= kStageB, "stage layout");
+    static_assert(kGroupWarps * 8 * kRedStride * 4 + kGroupWarps * 8 * 8 <= kKVB, "merge scratch fits a stage");
+    static_assert(kHdrOff % 16 == 0 && kPairOff % 16 == 0 && kHandOff % 16 == 0, "16-byte aligned smem sections");
+    static_assert(kSmem <= 227 * 1024, "one CTA's shared memory must fit in 227 KB");
+};
+
+// Byte address of 16-byte chunk c (0..15 over the 128 columns) of staged token t: swizzled
+// boxes, or padded rows for runs.
+template <bool kRuns>
+__device__ __forceinline__ uint32_t kv_addr(uint32_t base, int t, int c, int R_log2) {
+    if (kRuns) return base + (uint32_t)(t & 7) * kOctB + (uint32_t)(t >> 3) * (kHeadDim * 2) + ((uint32_t)c << 4);
+    return chunk_addr(base, t, c, R_log2);
+}
 constexpr float kLazyLog2 = 8.f;
 constexpr int kPlanMagic = 0x31504150;                  // "PAP1"
 constexpr int kPlanMagicAdaptive = 0x41504150;          // "PAPA": an adaptive plan (another layout)
+constexpr int kPlanMagicRuns = 0x52504150;              // "PAPR": a plan of runs (token table, no block ids)
 
 // Stage flags.
 enum : int { kBegin = 1, kEnd = 2, kNewRow = 4 };
@@ -195,6 +218,7 @@ struct PlanArgs {
     size_t lens_off, bounds_off, cta_off, cta_bytes, rates_off;
     int cap;
     int adaptive;
+    int tok_stride;   // runs plans: the token table's stride per sequence (0: block-table plan)
     long long max_chunks;
 };
 
@@ -303,7 +327,8 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
     __shared__ float2 warp_f2[kPlanThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long cap = (long long)a.max_blocks_per_seq * B;
-    const int R = B < kStageTokens ? B : kStageTokens;
+    // rows a chunk's last block costs: whole boxes of R rows, or (runs) exactly its rows
+    const int R = a.tok_stride ? 1 : (B < kStageTokens ? B : kStageTokens);
 
     grid_dependency_wait();
     // lengths, chunk counts and weights; a thread owns a contiguous run of sequences
@@ -485,7 +510,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         }
         if (tid == 0) {
             PlanHeader h = {};
-            h.magic = a.adaptive ? kPlanMagicAdaptive : kPlanMagic;   // (the layouts differ)
+            h.magic = a.tok_stride ? kPlanMagicRuns : a.adaptive ? kPlanMagicAdaptive : kPlanMagic;   // (layouts differ)
             h.num_seqs = S;
             h.num_q_heads = a.num_q_heads;
             h.num_kv_heads = Hkv;
@@ -517,14 +542,19 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         const int t0 = k * kStageTokens, t1 = min(t0 + kStageTokens, L);
         const int first = t0 / B, nblk = (t1 - 1) / B - first + 1;
         PlanChunk d;
-        const int32_t* row = a.block_tables + (size_t)s * a.max_blocks_per_seq + first;
+        if (a.tok_stride) {   // runs: where the chunk's tokens start in the token table
+            d.ids[0] = (int)((long long)s * a.tok_stride + t0);
+            d.ids[1] = d.ids[2] = d.ids[3] = -1;
+        } else {
+            const int32_t* row = a.block_tables + (size_t)s * a.max_blocks_per_seq + first;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            d.ids[e] = -1;
-            if (e < nblk) {
-                const int id = row[e];
-                if (id >= 0 && id < a.num_blocks) d.ids[e] = id;
-                else flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            for (int e = 0; e < 4; ++e) {
+                d.ids[e] = -1;
+                if (e < nblk) {
+                    const int id = row[e];
+                    if (id >= 0 && id < a.num_blocks) d.ids[e] = id;
+                    else flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                }
             }
         }
         d.s = (short)s;
@@ -607,6 +637,8 @@ struct PlannedArgs {
     unsigned int* status;
     unsigned long long* timeline;
     PlanRates* rates;           // the plan's rates section (adaptive plans: updated at the end)
+    const int32_t* tok;         // runs plans: per token of a sequence, (block * Hkv) * B + slot; a chunk
+                                // descriptor's ids[0] indexes its first token
     float scale_log2;
     int num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq;
     int early;
@@ -806,20 +838,21 @@ __device__ __forceinline__ int remote_slot(const PlanEvent& ev, const int32_t* b
     return 0;
 }
 
-template <typename T, bool kAdaptive>
+template <typename T, bool kAdaptive, bool kRuns>
 __global__ void __launch_bounds__(kPThreads, 1)
     decode_planned_kernel(const PlannedArgs a, const __grid_constant__ MmaMapsP maps, const int R_log2) {
+    using Y = Lay<kRuns>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* bp = smem_raw + (base - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + kBarOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bp + Y::kBarOff);
     uint64_t* full = bars;                                  // [2][3]
-    uint64_t* empty = bars + kGroups * kPStages;            // [2][3]
-    uint64_t* qbar = bars + 2 * kGroups * kPStages;         // [2] deferred q / new rows of the first stages
+    uint64_t* empty = bars + kGroups * Y::kPStages;            // [2][3]
+    uint64_t* qbar = bars + 2 * kGroups * Y::kPStages;         // [2] deferred q / new rows of the first stages
     uint64_t* pair_bar = qbar + kGroups;                    // the first group's piece is in the pair slot
     uint64_t* ready = pair_bar + 1;                         // [2] this CTA's piece of cut segment `side`
-    volatile int* misc = reinterpret_cast<volatile int*>(bp + kMiscOff);
+    volatile int* misc = reinterpret_cast<volatile int*>(bp + Y::kMiscOff);
     volatile int* abort_flag = misc;
     volatile int* pair_count = misc + 1;
     volatile int* pair_role = misc + 2;                     // [2]
@@ -829,9 +862,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // misc + 29: this CTA's rate before the launch (bits, copied by thread 0), + 30: the SM clock
     // when the CTA started (adaptive plans)
     // this CTA's header, copied by each producer before its first stage is released
-    CtaHeader* sh_hdr = reinterpret_cast<CtaHeader*>(bp + kHdrOff);
-    float* pair_o = reinterpret_cast<float*>(bp + kPairOff);
-    float2* pair_ml = reinterpret_cast<float2*>(bp + kPairOff + kRows * kHeadDim * 4);
+    CtaHeader* sh_hdr = reinterpret_cast<CtaHeader*>(bp + Y::kHdrOff);
+    float* pair_o = reinterpret_cast<float*>(bp + Y::kPairOff);
+    float2* pair_ml = reinterpret_cast<float2*>(bp + Y::kPairOff + kRows * kHeadDim * 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
@@ -844,9 +877,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (tid == 0) {
         trace(a.timeline, c, 0);
-        prefetch_map(&maps.k);
-        prefetch_map(&maps.v);
-        for (int i = 0; i < kGroups * kPStages; ++i) {
+        if (!kRuns) {
+            prefetch_map(&maps.k);
+            prefetch_map(&maps.v);
+        }
+        for (int i = 0; i < kGroups * Y::kPStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kGroupThreads);
         }
@@ -862,7 +897,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // waits for the copy at the end of its consumer loop
             cp_async4(smem_u32(const_cast<int*>(misc + 29)), &a.rates->rate[c]);
         }   // adaptive plans time the CTA's life from here
-        for (int i = 0; i < kGroups * kPStages; ++i) {
+        for (int i = 0; i < kGroups * Y::kPStages; ++i) {
             qdef[i] = -1;
             ndef[i] = -1;
         }
@@ -884,7 +919,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (is_prod && lane < min(32, a.cap)) load_chunk(slots + (size_t)pgrp * a.cap + lane, cur);
     uint4 hdr_part = make_uint4(0, 0, 0, 0);   // producers: lane j < 8 holds bytes 16 j .. of the CTA header
     if (is_prod && lane < 8) hdr_part = __ldcg(reinterpret_cast<const uint4*>(g_hdr) + lane);
-    const bool plan_ok = h_magic == (kAdaptive ? kPlanMagicAdaptive : kPlanMagic) && h_seqs == a.num_seqs &&
+    const bool plan_ok = h_magic == (kRuns ? kPlanMagicRuns : kAdaptive ? kPlanMagicAdaptive : kPlanMagic) &&
+                         h_seqs == a.num_seqs &&
                          h_qh == Hq && h_kvh == Hkv && h_bs == B && h_nb == a.num_blocks && h_mb == a.max_blocks_per_seq && h_c == (int)gridDim.x &&
                          b0 <= b1 && b1 <= b2 && b1 - b0 <= a.cap && b2 - b1 <= a.cap;
     if (!plan_ok) {
@@ -902,9 +938,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int grp = pgrp, lo = plo, hi = phi;
         const int cnt = hi - lo;
         auto chunk_at = [&](int p) { return grp ? hi - 1 - p : lo + p; };
-        uint64_t* gfull = full + grp * kPStages;
-        uint64_t* gempty = empty + grp * kPStages;
-        const uint32_t ring = base + (uint32_t)grp * kPStages * kStageB;
+        uint64_t* gfull = full + grp * Y::kPStages;
+        uint64_t* gempty = empty + grp * Y::kPStages;
+        const uint32_t ring = base + (uint32_t)grp * Y::kPStages * Y::kStageB;
         const uint32_t group_bytes = (uint32_t)G * kHeadDim * 2u;
         const int R = 1 << R_log2;
         // the CTA header into shared memory (both producers write the same bytes): consumers read it
@@ -916,25 +952,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
             grid_dependency_wait();
             grid_launch_dependents();
             if (lane == 0) {
-                const int n = min(n_issued, kPStages);
+                const int n = min(n_issued, Y::kPStages);
                 uint32_t bytes = 0;
                 for (int e = 0; e < n; ++e) {
-                    if (qdef[grp * kPStages + e] >= 0) bytes += group_bytes;
-                    if (ndef[grp * kPStages + e] >= 0) bytes += 4u * kHeadDim;
+                    if (qdef[grp * Y::kPStages + e] >= 0) bytes += group_bytes;
+                    if (ndef[grp * Y::kPStages + e] >= 0) bytes += 4u * kHeadDim;
                 }
                 mbar_arrive_expect_tx(&qbar[grp], bytes);
                 for (int e = 0; e < n; ++e) {
-                    const uint32_t dst = ring + (uint32_t)e * kStageB;
-                    const int sh = qdef[grp * kPStages + e];
+                    const uint32_t dst = ring + (uint32_t)e * Y::kStageB;
+                    const int sh = qdef[grp * Y::kPStages + e];
                     if (sh >= 0)
-                        bulk_g2s(dst + kQOff,
+                        bulk_g2s(dst + Y::kQOff,
                                  static_cast<const T*>(a.q) + ((size_t)(sh / Hkv) * Hq + (sh % Hkv) * G) * kHeadDim,
                                  group_bytes, &qbar[grp]);
-                    const int nh = ndef[grp * kPStages + e];
+                    const int nh = ndef[grp * Y::kPStages + e];
                     if (nh >= 0) {
-                        bulk_g2s(dst + kNewOff, static_cast<const T*>(a.k_new) + (size_t)nh * kHeadDim, 2u * kHeadDim,
+                        bulk_g2s(dst + Y::kNewOff, static_cast<const T*>(a.k_new) + (size_t)nh * kHeadDim, 2u * kHeadDim,
                                  &qbar[grp]);
-                        bulk_g2s(dst + kNewOff + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)nh * kHeadDim,
+                        bulk_g2s(dst + Y::kNewOff + 2u * kHeadDim, static_cast<const T*>(a.v_new) + (size_t)nh * kHeadDim,
                                  2u * kHeadDim, &qbar[grp]);
                     }
                 }
@@ -942,6 +978,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
             __syncwarp();
         };
         if (grp == 0 && lane == 0) trace(a.timeline, c, 3);
+        // runs: the token entries of this lane's octet (tokens 8 (lane mod 8) .. + 7; lanes 0-15) of
+        // the chunk about to be issued
+        int tokq[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (kRuns && cnt > 0) {
+            const uint4 c0 = reinterpret_cast<const uint4*>(&cur)[0];
+            const uint4 c1 = reinterpret_cast<const uint4*>(&cur)[1];
+            const int idx = (int)__shfl_sync(0xffffffffu, c0.x, 0);
+            const int nv0 = (int)(short)(__shfl_sync(0xffffffffu, c1.z, 0) & 0xffffu);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                tokq[e] = lane < 16 && 8 * (lane & 7) + e < nv0 ? __ldg(a.tok + idx + 8 * (lane & 7) + e) : 0;
+        }
         bool ok = true;
         int i = 0;
         for (int pb = 0; pb < cnt && ok; pb += 32) {
@@ -949,14 +997,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (pb + 32 + lane < cnt) load_chunk(slots + (size_t)grp * a.cap + pb + 32 + lane, nxt);
             const int m = min(32, cnt - pb);
             for (int j = 0; j < m; ++j, ++i) {
-                const int st = i % kPStages;
-                if (i == kPStages && !deps_done) {
+                const int st = i % Y::kPStages;
+                if (i == Y::kPStages && !deps_done) {
                     dependency_point(i);
                     deps_done = true;
                 }
-                if (i >= kPStages) {
+                if (i >= Y::kPStages) {
                     bool w = true;
-                    if (lane == 0) w = mbar_wait_bounded(&gempty[st], (uint32_t)((i / kPStages) - 1) & 1u);
+                    if (lane == 0) w = mbar_wait_bounded(&gempty[st], (uint32_t)((i / Y::kPStages) - 1) & 1u);
                     w = __shfl_sync(0xffffffffu, w, 0);
                     if (!w) {
                         if (lane == 0) {
@@ -1023,8 +1071,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             new_off = tl % B;
                             flags |= kNewRow;
                         }
-                        const uint32_t dst = ring + (uint32_t)st * kStageB;
-                        StageMeta* meta = reinterpret_cast<StageMeta*>(bp + (dst - base) + kMetaOff);
+                        const uint32_t dst = ring + (uint32_t)st * Y::kStageB;
+                        StageMeta* meta = reinterpret_cast<StageMeta*>(bp + (dst - base) + Y::kMetaOff);
                         meta->s = s;
                         meta->h = h;
                         meta->k = k;
@@ -1039,8 +1087,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         const bool defer = !deps_done;   // q and the new rows come after the dependency wait
                         const int sh = s * Hkv + h;
                         if (defer) {
-                            qdef[grp * kPStages + i] = (flags & kBegin) ? sh : -1;
-                            ndef[grp * kPStages + i] = newrow ? sh : -1;
+                            qdef[grp * Y::kPStages + i] = (flags & kBegin) ? sh : -1;
+                            ndef[grp * Y::kPStages + i] = newrow ? sh : -1;
                         }
                         const int t0 = k * kStageTokens;
                         const int within = (B > kStageTokens) ? (t0 % B) : 0;
@@ -1048,30 +1096,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         uint32_t bytes = 0;
                         if ((flags & kBegin) && !defer) bytes += group_bytes;
                         if (newrow && !defer) bytes += 4u * kHeadDim;
+                        if (kRuns) {
+                            bytes += 4u * kHeadDim * (uint32_t)nvalid;   // a K and a V row per token
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (e < nblk && d.ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
-                        if (i >= kPStages) fence_proxy_async_smem();
+                            for (int e = 0; e < 4; ++e)
+                                if (e < nblk && d.ids[e] >= 0) bytes += 4u * (uint32_t)R * 128u;
+                        }
+                        if (i >= Y::kPStages) fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&gfull[st], bytes);   // release: the metadata and header above
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            if (e < nblk && d.ids[e] >= 0) {
+                            if (!kRuns && e < nblk && d.ids[e] >= 0) {
                                 const int row = (d.ids[e] * Hkv + h) * B + within;
                                 const uint32_t box = dst + (uint32_t)(e * 2 * R) * 128u;
                                 tma_load_2d(box, &maps.k, 0, row, &gfull[st]);
                                 tma_load_2d(box + (uint32_t)R * 128u, &maps.k, 64, row, &gfull[st]);
-                                tma_load_2d(box + kKB, &maps.v, 0, row, &gfull[st]);
-                                tma_load_2d(box + kKB + (uint32_t)R * 128u, &maps.v, 64, row, &gfull[st]);
+                                tma_load_2d(box + Y::kKB, &maps.v, 0, row, &gfull[st]);
+                                tma_load_2d(box + Y::kKB + (uint32_t)R * 128u, &maps.v, 64, row, &gfull[st]);
                             }
                         }
                         if (grp == 0 && i == 0) trace(a.timeline, c, 4);
                         if ((flags & kBegin) && !defer)
-                            bulk_g2s(dst + kQOff, static_cast<const T*>(a.q) + ((size_t)s * Hq + h * G) * kHeadDim,
+                            bulk_g2s(dst + Y::kQOff, static_cast<const T*>(a.q) + ((size_t)s * Hq + h * G) * kHeadDim,
                                      group_bytes, &gfull[st]);
                         if (newrow && !defer) {
-                            bulk_g2s(dst + kNewOff, static_cast<const T*>(a.k_new) + (size_t)sh * kHeadDim,
+                            bulk_g2s(dst + Y::kNewOff, static_cast<const T*>(a.k_new) + (size_t)sh * kHeadDim,
                                      2u * kHeadDim, &gfull[st]);
-                            bulk_g2s(dst + kNewOff + 2u * kHeadDim,
+                            bulk_g2s(dst + Y::kNewOff + 2u * kHeadDim,
                                      static_cast<const T*>(a.v_new) + (size_t)sh * kHeadDim, 2u * kHeadDim,
                                      &gfull[st]);
                         }
@@ -1079,6 +1131,45 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                if (kRuns && lane < 16) {
+                    // lane l copies octet l mod 8 of the chunk (its K rows; lanes 8-15 its V rows):
+                    // one bulk copy per stretch of tokens that are consecutive pool rows
+                    const int nv = (int)(short)(d.nvalid), hh = d.h, oc = lane & 7;
+                    const uint32_t dst = ring + (uint32_t)st * Y::kStageB + (lane >= 8 ? Y::kKB : 0u) +
+                                         (uint32_t)oc * kOctB;
+                    const T* pool = static_cast<const T*>(lane >= 8 ? a.v_cache : a.k_cache);
+                    if (i >= Y::kPStages) fence_proxy_async_smem();
+                    bool valid[8], start[8];
+                    int len[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        valid[e] = 8 * oc + e < nv;
+                        start[e] = valid[e] && (e == 0 || tokq[e] != tokq[e - 1] + 1);
+                    }
+#pragma unroll
+                    for (int e = 7; e >= 0; --e)
+                        len[e] = !valid[e] ? 0 : (e < 7 && valid[e + 1] && !start[e + 1]) ? len[e + 1] + 1 : 1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (start[e])
+                            bulk_g2s(dst + (uint32_t)e * (kHeadDim * 2),
+                                     pool + ((size_t)tokq[e] + (size_t)hh * B) * kHeadDim,
+                                     (uint32_t)len[e] * (kHeadDim * 2), &gfull[st]);
+                }
+                if (kRuns) {
+                    // the next chunk's token entries, in flight while this one lands
+                    if (pb + j + 1 < cnt) {
+                        const uint4 n0 = reinterpret_cast<const uint4*>(j + 1 < m ? &cur : &nxt)[0];
+                        const uint4 n1 = reinterpret_cast<const uint4*>(j + 1 < m ? &cur : &nxt)[1];
+                        const int src_lane = j + 1 < m ? j + 1 : 0;
+                        const int idx = (int)__shfl_sync(0xffffffffu, n0.x, src_lane);
+                        const int nvn = (int)(short)(__shfl_sync(0xffffffffu, n1.z, src_lane) & 0xffffu);
+                        const int oc = lane & 7;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            tokq[e] = lane < 16 && 8 * oc + e < nvn ? __ldg(a.tok + idx + 8 * oc + e) : 0;
+                    }
+                }
             }
             cur = nxt;
         }
@@ -1150,9 +1241,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     progress = true;
                 }
                 if (!local_done[side] && mbar_test(&ready[side], 0u)) {
-                    const float* so = reinterpret_cast<const float*>(bp + kHandOff + side * kSlotB);
+                    const float* so = reinterpret_cast<const float*>(bp + Y::kHandOff + side * kSlotB);
                     const float2* sml =
-                        reinterpret_cast<const float2*>(bp + kHandOff + side * kSlotB + kRows * kHeadDim * 4);
+                        reinterpret_cast<const float2*>(bp + Y::kHandOff + side * kSlotB + kRows * kHeadDim * 4);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         float m2, l2, v2[8];
@@ -1198,10 +1289,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int t_warp = wq * 16;
         const int lo = grp ? b1 : b0, hi = grp ? b2 : b1;
         const int cnt = hi - lo;
-        uint64_t* gfull = full + grp * kPStages;
-        uint64_t* gempty = empty + grp * kPStages;
-        const uint32_t ring = base + (uint32_t)grp * kPStages * kStageB;
-        unsigned char* ring_p = bp + (size_t)grp * kPStages * kStageB;
+        uint64_t* gfull = full + grp * Y::kPStages;
+        uint64_t* gempty = empty + grp * Y::kPStages;
+        const uint32_t ring = base + (uint32_t)grp * Y::kPStages * Y::kStageB;
+        unsigned char* ring_p = bp + (size_t)grp * Y::kPStages * Y::kStageB;
         const int tokA = t_warp + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int chA = lane >> 4;
         const int tokV = t_warp + (lane & 7) + ((lane >> 4) << 3);
@@ -1219,8 +1310,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // the same named-barrier path through the segment ends.
         bool dead = false;
         for (int i = 0; i < cnt; ++i) {
-            const int st = i % kPStages;
-            if (!dead && !__all_sync(0xffffffffu, mbar_wait_bounded(&gfull[st], (uint32_t)(i / kPStages) & 1u))) {
+            const int st = i % Y::kPStages;
+            if (!dead && !__all_sync(0xffffffffu, mbar_wait_bounded(&gfull[st], (uint32_t)(i / Y::kPStages) & 1u))) {
                 if (lane == 0) {
                     flag_status(a.status, PA_DEV_TIMEOUT);
                     *abort_flag = 1;
@@ -1231,13 +1322,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (i == 0) trace(a.timeline, c, 5);
                 if (i == cnt - 1) trace(a.timeline, c, 6);
             }
-            const uint32_t kbase = ring + (uint32_t)st * kStageB;
-            const uint32_t vbase = kbase + kKB;
-            unsigned char* stage_p = ring_p + (size_t)st * kStageB;
-            const StageMeta* meta = reinterpret_cast<const StageMeta*>(stage_p + kMetaOff);
+            const uint32_t kbase = ring + (uint32_t)st * Y::kStageB;
+            const uint32_t vbase = kbase + Y::kKB;
+            unsigned char* stage_p = ring_p + (size_t)st * Y::kStageB;
+            const StageMeta* meta = reinterpret_cast<const StageMeta*>(stage_p + Y::kMetaOff);
             const int flags = dead ? 0 : meta->flags;
             const int nvalid = dead ? 0 : meta->nvalid;
-            if ((flags & (kBegin | kNewRow)) && a.early && i < kPStages) {
+            if ((flags & (kBegin | kNewRow)) && a.early && i < Y::kPStages) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&qbar[grp], 0u))) {
                     if (lane == 0) {
                         flag_status(a.status, PA_DEV_TIMEOUT);
@@ -1247,7 +1338,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             if ((flags & kBegin) && !dead) {
-                const uint32_t* qs = reinterpret_cast<const uint32_t*>(stage_p + kQOff);
+                const uint32_t* qs = reinterpret_cast<const uint32_t*>(stage_p + Y::kQOff);
                 const int row = gid;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -1260,10 +1351,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
             }
-            if (t_warp < nvalid && !dead) {
-                if (nvalid < t_warp + 16) {
+            // runs stages: this warp's row x (0..15) holds token 8 (x mod 8) + 2 wq + x / 8
+            if ((kRuns ? 2 * wq < nvalid : t_warp < nvalid) && !dead) {
+                if (kRuns) {
+                    if (nvalid < 64) {
+                        // V rows past the context: stale rows must not meet P = 0 as non-finite values
+                        uint4* vz = reinterpret_cast<uint4*>(stage_p + Y::kKB);
+                        for (int idx = lane; idx < 16 * 16; idx += 32) {
+                            const int x = idx >> 4;
+                            if (8 * (x & 7) + 2 * wq + (x >> 3) >= nvalid)
+                                vz[((uint32_t)(x & 7) * kOctB + (uint32_t)(2 * wq + (x >> 3)) * (kHeadDim * 2)) / 16 +
+                                   (idx & 15)] = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                } else if (nvalid < t_warp + 16) {
                     // V rows past the context: stale pool rows must not meet P = 0 as non-finite values
-                    uint4* vz = reinterpret_cast<uint4*>(stage_p + kKB);
+                    uint4* vz = reinterpret_cast<uint4*>(stage_p + Y::kKB);
                     for (int idx = lane; idx < (t_warp + 16 - nvalid) * 16; idx += 32) {
                         const int t = nvalid + (idx >> 4);
                         const int cc = idx & 15;
@@ -1277,9 +1382,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     // the new K/V row: into the staged tile and into its cache slot
                     const int cc = lane & 15;
                     const bool isv = lane >= 16;
-                    const uint4 val = *reinterpret_cast<const uint4*>(stage_p + kNewOff + (isv ? 2u * kHeadDim : 0u) +
+                    const uint4 val = *reinterpret_cast<const uint4*>(stage_p + Y::kNewOff + (isv ? 2u * kHeadDim : 0u) +
                                                                       cc * 16);
-                    st_shared_v4(chunk_addr(isv ? vbase : kbase, tn, cc, R_log2), val);
+                    st_shared_v4(kv_addr<kRuns>(isv ? vbase : kbase, tn, cc, R_log2), val);
                     const int phys = meta->new_phys;
                     if (phys >= 0) {
                         const size_t row = ((size_t)phys * Hkv + meta->h) * B + (size_t)meta->new_off;
@@ -1294,11 +1399,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(chunk_addr(kbase, tokA, 2 * ks + chA, R_log2), a0, a1, a2, a3);
+                    ldsm_x4(kv_addr<kRuns>(kbase, tokA, 2 * ks + chA, R_log2), a0, a1, a2, a3);
                     if (ks & 1) mma16816<T>(sc2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                     else mma16816<T>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
-                const bool in0 = t_warp + gid < nvalid, in1 = t_warp + gid + 8 < nvalid;
+                const bool in0 = kRuns ? 8 * gid + 2 * wq < nvalid : t_warp + gid < nvalid;
+                const bool in1 = kRuns ? 8 * gid + 2 * wq + 1 < nvalid : t_warp + gid + 8 < nvalid;
                 constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
                 float xs[4];
                 bool move = false;
@@ -1348,7 +1454,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(chunk_addr(vbase, tokV, 2 * mt + chV, R_log2), a0, a1, a2, a3);
+                    ldsm_x4_t(kv_addr<kRuns>(vbase, tokV, 2 * mt + chV, R_log2), a0, a1, a2, a3);
                     mma16816<T>(o[mt], a0, a1, a2, a3, pb0, pb1);
                     if (kSplitP) mma16816<T>(o[mt], a0, a1, a2, a3, pl0, pl1);
                 }
@@ -1493,8 +1599,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     const size_t slot = (size_t)2 * c + side;
                     publish8(a.part_o + slot * kRows * kHeadDim, a.part_ml + slot * kRows, r, d0, f, (tg & 15) == 0);
                 } else if (mode == kMergeM) {
-                    float* so = reinterpret_cast<float*>(bp + kHandOff + side * kSlotB);
-                    float2* sml = reinterpret_cast<float2*>(bp + kHandOff + side * kSlotB + kRows * kHeadDim * 4);
+                    float* so = reinterpret_cast<float*>(bp + Y::kHandOff + side * kSlotB);
+                    float2* sml = reinterpret_cast<float2*>(bp + Y::kHandOff + side * kSlotB + kRows * kHeadDim * 4);
                     slot_store(so, sml, r, d0, f, (tg & 15) == 0);
                     mbar_arrive(&ready[side]);
                 }
@@ -1536,32 +1642,82 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // let every copy still in flight land before the CTA's shared memory is released
         for (int grp = 0; grp < kGroups; ++grp) {
             const int n = issued[grp];
-            for (int st = 0; st < kPStages; ++st) {
+            for (int st = 0; st < Y::kPStages; ++st) {
                 int last = -1;
-                for (int i = st; i < n; i += kPStages) last = i;
-                if (last >= 0) (void)mbar_wait_bounded(&full[grp * kPStages + st], (uint32_t)(last / kPStages) & 1u);
+                for (int i = st; i < n; i += Y::kPStages) last = i;
+                if (last >= 0) (void)mbar_wait_bounded(&full[grp * Y::kPStages + st], (uint32_t)(last / Y::kPStages) & 1u);
             }
         }
     }
 }
 
-template <typename T, bool kAdaptive>
+// ---------------------------------------------------------------------------------------------
+// Contexts given as runs (block, slot offset, length): one warp per sequence lays its tokens out in
+// a token table, (block * Hkv) * B + slot per token, and sums its length; the plan kernel then
+// cuts chunks as for a block table and the decode's producers copy each token's K and V row.
+// ---------------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) runs_prep_kernel(const int32_t* runs, const int32_t* seq_runs, int num_seqs,
+                                                         int num_kv_heads, int block_size, int num_blocks,
+                                                         int max_context, int stride, int32_t* lens, int32_t* tok,
+                                                         unsigned int* status) {
+    const int s = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (s >= num_seqs) return;
+    int r0 = seq_runs[s], r1 = seq_runs[s + 1];
+    if (r0 < 0 || r1 < r0) {   // a malformed run range: an empty context
+        if (lane == 0) flag_status(status, PA_DEV_BAD_BLOCK_ID);
+        r0 = r1 = 0;
+    }
+    int pos = 0;
+    for (int rb = r0; rb < r1; rb += 32) {
+        const int r = rb + lane;
+        int blk = 0, off = 0, len = 0;
+        if (r < r1) {
+            blk = runs[3 * r];
+            off = runs[3 * r + 1];
+            len = runs[3 * r + 2];
+            if (blk < 0 || blk >= num_blocks || off < 0 || len < 0 || off + len > block_size) {
+                flag_status(status, PA_DEV_BAD_BLOCK_ID);   // the run counts as empty
+                len = 0;
+            }
+        }
+        int incl = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int start = pos + incl - len;
+        const int base = (blk * num_kv_heads) * block_size + off;
+        for (int t = 0; t < len && start + t < max_context; ++t) tok[(size_t)s * stride + start + t] = base + t;
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        if (pos > max_context) {
+            flag_status(status, PA_DEV_BAD_CONTEXT);
+            pos = max_context;
+        }
+        lens[s] = pos;
+    }
+}
+
+template <typename T, bool kAdaptive, bool kRuns>
 cudaError_t launch_planned_impl(const PlannedArgs& a, const MmaMapsP& maps, int R_log2, int ctas, cudaStream_t stream) {
     static std::atomic<unsigned long long> configured{0};
-    auto kernel = decode_planned_kernel<T, kAdaptive>;
+    auto kernel = decode_planned_kernel<T, kAdaptive, kRuns>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemPlanned);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay<kRuns>::kSmem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kSmemPlanned;
+    cfg.dynamicSmemBytes = Lay<kRuns>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1598,9 +1754,22 @@ size_t planned_workspace_bytes(int ctas) {
     return al256(slots * kRows * kHeadDim * sizeof(float)) + al256(slots * kRows * sizeof(float2));
 }
 
+static cudaError_t launch_plan_kernel(void* plan, const int32_t* block_tables, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                                      int num_blocks, int max_blocks_per_seq, int ctas, bool adaptive,
+                                      int tok_stride, cudaStream_t stream);
+
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
                                int max_blocks_per_seq, int ctas, bool adaptive, cudaStream_t stream) {
+    return launch_plan_kernel(plan, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, block_size,
+                              num_blocks, max_blocks_per_seq, ctas, adaptive, 0, stream);
+}
+
+static cudaError_t launch_plan_kernel(void* plan, const int32_t* block_tables, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                                      int num_blocks, int max_blocks_per_seq, int ctas, bool adaptive,
+                                      int tok_stride, cudaStream_t stream) {
     if (ctas < 1 || ctas > 4 * kPlanThreads) return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, adaptive);
     PlanArgs a;
@@ -1622,6 +1791,7 @@ cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const in
     a.rates_off = L.rates;
     a.cap = L.cap;
     a.adaptive = adaptive ? 1 : 0;
+    a.tok_stride = tok_stride;
     a.max_chunks = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
     long long blocks = (a.max_chunks + kPlanThreads - 1) / kPlanThreads;
     const long long cap = 4LL * sm_count_current();
@@ -1671,6 +1841,7 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     a.v_cache = v_cache;
     a.plan = static_cast<const unsigned char*>(plan);
     a.rates = reinterpret_cast<PlanRates*>(static_cast<unsigned char*>(plan) + L.rates);
+    a.tok = nullptr;
     const size_t slots = (size_t)2 * ctas;
     char* w = static_cast<char*>(workspace);
     a.part_o = reinterpret_cast<float*>(w);
@@ -1692,10 +1863,93 @@ cudaError_t launch_decode_planned(void* out, const void* q, const void* k_new, c
     a.cta_off = L.cta;
     a.cta_bytes = L.cta_bytes;
     if (adaptive)
-        return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, true>(a, maps, R_log2, ctas, stream)
-                                : launch_planned_impl<__half, true>(a, maps, R_log2, ctas, stream);
-    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, false>(a, maps, R_log2, ctas, stream)
-                            : launch_planned_impl<__half, false>(a, maps, R_log2, ctas, stream);
+        return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, true, false>(a, maps, R_log2, ctas, stream)
+                                : launch_planned_impl<__half, true, false>(a, maps, R_log2, ctas, stream);
+    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, false, false>(a, maps, R_log2, ctas, stream)
+                            : launch_planned_impl<__half, false, false>(a, maps, R_log2, ctas, stream);
+}
+
+// Runs plans: the plan, then the prep kernel's lengths and token table.
+struct RunsLayout {
+    PlanLayout plan;
+    size_t lens, tok, total;
+    int stride;
+};
+
+static RunsLayout runs_layout(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
+    RunsLayout R;
+    const long long max_context = (long long)max_blocks_per_seq * block_size;
+    R.stride = (int)((max_context + kStageTokens - 1) / kStageTokens * kStageTokens);
+    R.plan = plan_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas, false);
+    R.lens = al256(R.plan.total);
+    R.tok = R.lens + al256((size_t)num_seqs * 4);
+    R.total = R.tok + al256((size_t)num_seqs * R.stride * 4);
+    return R;
+}
+
+size_t planned_runs_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas) {
+    return runs_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas).total;
+}
+
+cudaError_t launch_decode_plan_runs(void* plan, const int32_t* runs, const int32_t* seq_runs, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                    int max_blocks_per_seq, int max_context, int ctas, cudaStream_t stream) {
+    const RunsLayout RL = runs_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    unsigned char* buf = static_cast<unsigned char*>(plan);
+    int32_t* lens = reinterpret_cast<int32_t*>(buf + RL.lens);
+    int32_t* tok = reinterpret_cast<int32_t*>(buf + RL.tok);
+    const unsigned warps_per_block = 8;
+    runs_prep_kernel<<<(unsigned)((num_seqs + warps_per_block - 1) / warps_per_block), 32 * warps_per_block, 0,
+                       stream>>>(runs, seq_runs, num_seqs, num_kv_heads, block_size, num_blocks, max_context,
+                                 RL.stride, lens, tok, device_status_ptr());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    return launch_plan_kernel(buf, nullptr, lens, num_seqs, num_q_heads, num_kv_heads, block_size, num_blocks,
+                              max_blocks_per_seq, ctas, false, RL.stride, stream);
+}
+
+cudaError_t launch_decode_planned_runs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const void* plan, void* workspace, float scale, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                       int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                       unsigned long long* timeline, cudaStream_t stream) {
+    const RunsLayout RL = runs_layout(num_seqs, num_kv_heads, block_size, max_blocks_per_seq, ctas);
+    const PlanLayout& L = RL.plan;
+    const unsigned char* buf = static_cast<const unsigned char*>(plan);
+    PlannedArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.plan = buf;
+    a.rates = nullptr;
+    a.tok = reinterpret_cast<const int32_t*>(buf + RL.tok);
+    const size_t slots = (size_t)2 * ctas;
+    char* w = static_cast<char*>(workspace);
+    a.part_o = reinterpret_cast<float*>(w);
+    a.part_ml = reinterpret_cast<float2*>(w + al256(slots * kRows * kHeadDim * sizeof(float)));
+    a.status = device_status_ptr();
+    a.timeline = timeline;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.early = early ? 1 : 0;
+    a.cap = L.cap;
+    a.lens_off = L.lens;
+    a.bounds_off = L.bounds;
+    a.cta_off = L.cta;
+    a.cta_bytes = L.cta_bytes;
+    MmaMapsP maps;
+    std::memset(&maps, 0, sizeof(maps));   // (the runs form copies rows, no tensor maps)
+    return dtype == PA_BF16 ? launch_planned_impl<__nv_bfloat16, false, true>(a, maps, 6, ctas, stream)
+                            : launch_planned_impl<__half, false, true>(a, maps, 6, ctas, stream);
 }
 
 }  // namespace pa

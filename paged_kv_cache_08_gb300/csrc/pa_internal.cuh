@@ -297,6 +297,15 @@ int planned_ctas(const pa_decode_options* opts);
 size_t planned_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
                           bool adaptive);
 size_t planned_workspace_bytes(int ctas);
+size_t planned_runs_plan_bytes(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas);
+cudaError_t launch_decode_plan_runs(void* plan, const int32_t* runs, const int32_t* seq_runs, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                    int max_blocks_per_seq, int max_context, int ctas, cudaStream_t stream);
+cudaError_t launch_decode_planned_runs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const void* plan, void* workspace, float scale, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int block_size, int num_blocks,
+                                       int max_blocks_per_seq, int dtype, int ctas, bool early,
+                                       unsigned long long* timeline, cudaStream_t stream);
 void planned_plan_offsets(int num_seqs, int num_kv_heads, int block_size, int max_blocks_per_seq, int ctas,
                           bool adaptive, size_t* bounds_offset, size_t* rates_offset);
 cudaError_t launch_decode_plan(void* plan, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,

@@ -149,3 +149,81 @@ def test_compaction_then_block_table_decode(oracle, dtype):
     ref = oracle.decode_runs(q, kc, vc, runs, seq_runs, 0.088, Hkv, dtype == "bf16")
     assert max_abs_err(out, ref) <= TOL
     assert pa.read_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 37, 0])
+@pytest.mark.parametrize("B,dtype", [(16, "f16"), (32, "bf16"), (128, "f16")])
+def test_runs_plan_then_layers_with_early_reads(oracle, num_ctas, B, dtype):
+    """One runs plan serves three chained layers (each layer's q is the previous layer's output,
+    early reads from the second layer on); CTA counts from one to one per SM."""
+    lens = [3, 64, 65, 1, 700, 0, 129, 2000, 31]
+    Hkv, G, NB, layers = 2, 6, 200, 3
+    runs, seq_runs = _slotted(lens, B, NB, seed=11 * B + num_ctas)
+    dev = torch.device("cuda")
+    pools = [_pools(NB, Hkv, B, dtype, seed=500 + l) for l in range(layers)]
+    g = torch.Generator().manual_seed(3)
+    q0 = torch.randn((len(lens), Hkv * G, 128), generator=g).to(DT[dtype])
+    runs_d, seq_d = torch.from_numpy(runs).to(dev), torch.from_numpy(seq_runs).to(dev)
+    plan = pa.decode_plan_runs(runs_d, seq_d, Hkv * G, Hkv, B, NB, max(lens), num_ctas=num_ctas)
+    outs = [torch.full_like(q0.to(dev), float("nan")) for _ in range(layers)]
+    q = q0.to(dev)
+    for l in range(layers):
+        pa.decode_planned(q, pools[l][0].to(dev), pools[l][1].to(dev), plan, 0.09, out=outs[l], early_reads=l > 0)
+        q = outs[l]
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) == 0
+    oq = q0
+    for l in range(layers):
+        ref = oracle.decode_runs(oq, pools[l][0], pools[l][1], runs, seq_runs, 0.09, Hkv, dtype == "bf16")
+        err = max_abs_err(outs[l], ref)
+        assert err <= TOL, f"layer {l}: max abs error {err:.3e}"
+        oq = torch.from_numpy(ref).to(DT[dtype])
+
+
+def test_many_one_token_runs(oracle):
+    """Contexts made of runs of one or two tokens scattered over the pool (every row its own copy)."""
+    g = torch.Generator().manual_seed(21)
+    lens = [int(x) for x in torch.randint(1, 400, (40,), generator=g)]
+    B, NB, Hkv, G = 16, 64, 4, 2
+    runs, seq_runs = [], [0]
+    for L in lens:
+        t = 0
+        while t < L:
+            ln = min(int(torch.randint(1, 3, (1,), generator=g)), L - t)
+            off = int(torch.randint(0, B - ln + 1, (1,), generator=g))
+            runs.append((int(torch.randint(0, NB, (1,), generator=g)), off, ln))
+            t += ln
+        seq_runs.append(len(runs))
+    runs = np.array(runs, np.int32).reshape(-1, 3)
+    seq_runs = np.array(seq_runs, np.int32)
+    kc, vc = _pools(NB, Hkv, B, "f16", seed=22)
+    q = torch.randn((len(lens), Hkv * G, 128), generator=g).to(torch.float16)
+    dev = torch.device("cuda")
+    out = pa.decode_runs(q.to(dev), kc.to(dev), vc.to(dev), torch.from_numpy(runs).to(dev),
+                         torch.from_numpy(seq_runs).to(dev), 0.1, Hkv, max(lens))
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) == 0
+    ref = oracle.decode_runs(q, kc, vc, runs, seq_runs, 0.1, Hkv, False)
+    assert max_abs_err(out, ref) <= TOL
+
+
+def test_runs_plan_refuses_new_rows_and_block_table_launches():
+    """A runs plan carries no block ids: decode_planned with new rows is refused on the host, and
+    a launch that does not name PA_PLAN_RUNS flags PA_DEV_BAD_PLAN and writes nothing."""
+    lens = [40, 90]
+    B, NB, Hkv = 16, 32, 2
+    runs, seq_runs = _slotted(lens, B, NB, seed=5)
+    kc, vc = _pools(NB, Hkv, B, "f16", seed=6)
+    dev = torch.device("cuda")
+    q = torch.randn((2, 4, 128)).to(torch.float16).to(dev)
+    plan = pa.decode_plan_runs(torch.from_numpy(runs).to(dev), torch.from_numpy(seq_runs).to(dev), 4, Hkv, B, NB,
+                               max(lens))
+    with pytest.raises(pa.PAError):
+        pa.decode_planned(q, kc.to(dev), vc.to(dev), plan, 0.1, k_new=q[:, :Hkv].contiguous(),
+                          v_new=q[:, :Hkv].contiguous())
+    plan.runs = False
+    out = torch.full_like(q, 7.0)
+    pa.decode_planned(q, kc.to(dev), vc.to(dev), plan, 0.1, out=out)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) == pa._native.DEV_BAD_PLAN
+    assert torch.all(out == 7.0)
