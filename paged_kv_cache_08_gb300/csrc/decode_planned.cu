@@ -1474,22 +1474,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 float* red_o = reinterpret_cast<float*>(stage_p);                                  // [4][8][kRedStride]
                 float2* red_ml = reinterpret_cast<float2*>(red_o + kGroupWarps * 8 * kRedStride);  // [4][8]
                 group_sync(grp);   // every warp is past its reads of the stage
+                // rows past the GQA group carry nothing: only the group's rows go through shared
+                // memory, the others fold to a neutral (m 0, l 1, o 0) partial
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int row = tig * 2 + j;
-                    float* dst = &red_o[(wq * 8 + row) * kRedStride + gid];
+                    if (row < G) {
+                        float* dst = &red_o[(wq * 8 + row) * kRedStride + gid];
 #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        dst[mt * 16] = o[mt][j];
-                        dst[mt * 16 + 8] = o[mt][2 + j];
+                        for (int mt = 0; mt < 8; ++mt) {
+                            dst[mt * 16] = o[mt][j];
+                            dst[mt * 16 + 8] = o[mt][2 + j];
+                        }
+                        if (gid == 0) red_ml[wq * 8 + row] = make_float2(m_run[j], lr[j]);
                     }
-                    if (gid == 0) red_ml[wq * 8 + row] = make_float2(m_run[j], lr[j]);
                 }
                 group_sync(grp);
                 const int r = tg >> 4, d0 = (tg & 15) * 8;
                 Fold8 f;
                 f.init();
-                {
+                if (r >= G) {
+                    f.M = 0.f;
+                    f.den = 1.f;
+                } else {
                     float M = -INFINITY;
 #pragma unroll
                     for (int w2 = 0; w2 < kGroupWarps; ++w2) M = fmaxf(M, red_ml[w2 * 8 + r].x);
