@@ -391,7 +391,7 @@ def run_ours(args):
             for cfg, B in PER_CONFIG:
                 key = f"config{cfg}" + (f"_B{B}" if B else "")
                 per_config[key] = time_config(cfg, B, dev, 30, 3, args.num_ctas, errors=not args.no_cpu_baseline,
-                                               adaptive=args.adaptive)
+                                               adaptive=args.adaptive, with_adaptive=cfg != 1)
         per_config["clocks"] = clk_pc.summary()
 
     cpu = None
@@ -406,8 +406,10 @@ def run_ours(args):
             "config": {"workload": wl.name, "seqs": wl.num_seqs, "layers": wl.layers,
                        "context": "uniform [16, 2048]", "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
                        "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_blocks": wl.num_blocks,
-                       "decode_kernel": {1: "split grid, CUDA cores", 2: "persistent, tensor cores",
-                                         3: "split grid, tensor cores"}[kind],
+                       "decode_kernel": ("planned: one CTA per SM, two ranges streamed from both ends, "
+                                         "mma.sync tensor cores" if planned else
+                                         {1: "split grid, CUDA cores", 2: "persistent, tensor cores",
+                                          3: "split grid, tensor cores"}[kind]),
                        "step": ("pa_decode_plan once, then pa_decode_planned with the cache write per layer"
                                 if planned else "pa_decode_append per layer (cache write fused)" if fused
                                 else "pa_cache_write + pa_decode per layer"),
@@ -792,7 +794,7 @@ def _half_ulp(t: torch.Tensor):
 
 
 def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: int = 0, errors: bool = True,
-                adaptive: bool = False):
+                adaptive: bool = False, with_adaptive: bool = False):
     """One decode layer (the cache write of each sequence's new token plus attention) of a seeded
     configuration, timed alone: the step's plan built first (pa_decode_plan, timed separately),
     then ``steps`` pa_decode_planned launches, each after a 512 MB write that flushes the L2, by
@@ -858,6 +860,23 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
     if status:
         print(f"bench: device status {status:#x} after timing config {cfg}: not valid", file=sys.stderr)
     ms_p, _ = timed(replan, max(10, steps // 3))
+    ms_a = None
+    if with_adaptive and not adaptive:
+        # the same launches through an adaptive plan, after rebuilds that let its shares settle
+        aplan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks,
+                               num_ctas=num_ctas, adaptive=True)
+
+        def aplanned():
+            pa.decode_planned(q, kc, vc, aplan, wl.scale, k_new=kn, v_new=vn, out=out, workspace=ws)
+        for _ in range(max(24, warmup)):
+            flush.zero_()
+            aplanned()
+            pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, plan=aplan,
+                           num_ctas=num_ctas, adaptive=True)
+        torch.cuda.synchronize()
+        pa.read_device_status(clear=True)
+        ms_a, _ = timed(aplanned, steps)
+        status |= pa.read_device_status(clear=True)
     nbytes = decode_bytes(wl) + cache_write_bytes(wl)
     peak, peak_kind = measured_peak_gbs()
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -872,6 +891,10 @@ def time_config(cfg: int, block_size, dev, steps: int, warmup: int, num_ctas: in
                 "per_layer_persistent_gbs": round(nbytes / (ms_u * 1e-3) / 1e9, 1),
                 "peak": peak, "peak_source": f"{peak_kind} copy bandwidth", "adaptive_plan": adaptive,
                 "device_status": status, "l2": "flushed (512 MB write) before every timed launch"})
+    if ms_a is not None:
+        res.update({"adaptive_us": round(ms_a * 1e3, 2), "adaptive_gbs": round(nbytes / (ms_a * 1e-3) / 1e9, 1),
+                    "adaptive_frac": round(nbytes / (ms_a * 1e-3) / 1e9 / peak, 4),
+                    "adaptive_frac_of_8TBs_spec": round(nbytes / (ms_a * 1e-3) / 1e9 / SPEC_PEAK_GBS, 4)})
     if errors:
         import oracle as oracle_pkg
         o = oracle_pkg.get()
@@ -910,7 +933,7 @@ def run_config(args):
     torch.cuda.set_device(dev)
     with ClockSampler(0) as clk:
         r = time_config(args.config, args.block_size, dev, args.steps, args.warmup, args.num_ctas,
-                        errors=not args.no_cpu_baseline, adaptive=args.adaptive)
+                        errors=not args.no_cpu_baseline, adaptive=args.adaptive, with_adaptive=args.config != 1)
     line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(r["us"] / 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
