@@ -233,3 +233,45 @@ def test_adaptive_plan_used_without_the_flag_is_refused_on_the_device():
     torch.cuda.synchronize()
     assert pa.read_device_status(clear=True) == pa._native.DEV_BAD_PLAN
     assert torch.all(out == 7.0)
+
+
+def test_adaptive_chain_in_a_graph_never_gives_up_a_wait(oracle):
+    """Adaptive plans rebuilt every step change the cut from step to step; in a chained graph the
+    cross-CTA folds then race with the words they clear (a fold must not clear a row's (m, l)
+    while another thread of the row still polls it).  480 chained launches must leave the
+    status word clean, and the last step must match the oracle."""
+    layers, steps = 6, 80
+    wl = workloads.config(2, layers=layers)
+    dev = torch.device("cuda")
+    bt, lens = wl.block_tables.to(dev), wl.context_lens.to(dev)
+    kcs = [wl.k_cache[i].to(dev) for i in range(layers)]
+    vcs = [wl.v_cache[i].to(dev) for i in range(layers)]
+    qs = [wl.q[i].to(dev) for i in range(layers)]
+    outs = [torch.empty_like(qs[0]) for _ in range(layers)]
+    ws = pa.new_planned_workspace(0, dev)
+    plan = pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, adaptive=True)
+
+    def step():
+        pa.decode_plan(bt, lens, wl.num_q_heads, wl.num_kv_heads, wl.block_size, wl.num_blocks, plan=plan,
+                       adaptive=True)
+        q = qs[0]
+        for i in range(layers):
+            pa.decode_planned(q, kcs[i], vcs[i], plan, wl.scale, out=outs[i], workspace=ws, early_reads=i > 0)
+            q = outs[i]
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    pa.read_device_status(clear=True)
+    for _ in range(steps):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pa.read_device_status(clear=True) == 0
+    oq = wl.q[0]
+    for i in range(layers):
+        ref = oracle.decode(oq, oracle_pkg.as_u16(wl.k_cache[i]), oracle_pkg.as_u16(wl.v_cache[i]),
+                            wl.block_tables, wl.context_lens, wl.scale, wl.num_kv_heads, False)
+        err = max_abs_err(outs[i], ref)
+        assert err <= TOL, f"layer {i}: max abs error {err:.3e}"
+        oq = torch.from_numpy(ref).to(torch.float16)
