@@ -192,8 +192,9 @@ PlanLayout plan_layout(int num_seqs, int num_kv_heads, int block_size, int max_b
     PlanLayout L;
     const long long maxc = plan_max_chunks(num_seqs, num_kv_heads, block_size, max_blocks_per_seq);
     // A group gets at most (its share of the weight + one chunk) / the lightest chunk's weight.
-    // Chunks weigh 64 to 112 (at most 1.75x their mean): equal shares need fewer than two equal
-    // shares of chunks, adaptive ones (at most 1.5x the equal share) fewer than three.
+    // Chunks weigh 64 to 112 (at most 1.75x the lightest; with one row per kv head 336 to 500,
+    // 1.5x): equal shares need fewer than two equal shares of chunks, adaptive ones (at most 1.5x
+    // the equal share) fewer than three.
     const int eq = (int)((maxc + 2 * ctas - 1) / (2 * ctas));
     L.cap = adaptive ? 3 * eq + 6 : 2 * eq + 4;
     L.lens = 256;
@@ -228,17 +229,25 @@ constexpr int kPlanThreads = 256;
 // the K/V rows its boxes fetch (a partly valid last block still costs its whole box), a fixed
 // share for the consumers' per-chunk work and, at a segment's last chunk, the four warps' merge
 // and output (row units).  Ranges of many short contexts then get fewer chunks than ranges of
-// long ones.
-constexpr int kWChunk = 16;
-constexpr int kWEnd = 32;
+// long ones.  With one query row per kv head the fixed shares are a fit of the groups' end times
+// on 256 sequences x 32 kv heads of short contexts (about 2.6 ns per row fetched, 0.87 us per
+// chunk, 0.43 us per segment end); with groups of 4-6 rows the smaller shares measured better
+// (128 sequences of 6 rows per kv head, 16-token blocks: 2 % faster).
+struct ChunkWeights {
+    int chunk;   // fixed share per chunk (rows)
+    int end;     // extra at a segment's last chunk (rows)
+};
+__host__ __device__ inline ChunkWeights chunk_weights(int group_rows) {
+    return group_rows == 1 ? ChunkWeights{272, 164} : ChunkWeights{16, 32};
+}
 
 // Weight of one (sequence, kv head) segment of L tokens with boxes of R rows.
-__device__ __forceinline__ long long segment_weight(int L, int R) {
+__device__ __forceinline__ long long segment_weight(int L, int R, ChunkWeights w) {
     if (L <= 0) return 0;
     const int n = (L + kStageTokens - 1) / kStageTokens;
     const int last = L - (n - 1) * kStageTokens;                  // valid rows of the last chunk
     const int last_rows = ((last + R - 1) / R) * R;
-    return (long long)(n - 1) * (kStageTokens + kWChunk) + last_rows + kWChunk + kWEnd;
+    return (long long)(n - 1) * (kStageTokens + w.chunk) + last_rows + w.chunk + w.end;
 }
 
 // The group holding chunk x: the largest g with bnd[g] <= x (bnd ascending, bnd[G2] = N).
@@ -316,6 +325,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
     extern __shared__ long long plan_smem[];
     const int S = a.num_seqs, Hkv = a.num_kv_heads, B = a.block_size;
     const int G2 = 2 * a.ctas;
+    const ChunkWeights cw = chunk_weights(a.num_q_heads / Hkv);
     long long* PW = plan_smem;                                     // [S + 1] exclusive prefix of weights
     int* nch = reinterpret_cast<int*>(PW + S + 1);                 // [S] chunks per kv head of each sequence
     int* P = nch + S;                                              // [S + 1] exclusive prefix of nch
@@ -345,7 +355,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         Ls[s] = L;
         nch[s] = (L + kStageTokens - 1) / kStageTokens;
         local += nch[s];
-        local_w += (long long)Hkv * segment_weight(L, R);
+        local_w += (long long)Hkv * segment_weight(L, R, cw);
     }
     int incl = local;
     long long incl_w = local_w;
@@ -377,7 +387,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         P[s] = run;
         PW[s] = run_w;
         run += nch[s];
-        run_w += (long long)Hkv * segment_weight(Ls[s], R);
+        run_w += (long long)Hkv * segment_weight(Ls[s], R, cw);
     }
     if (tid == 0) {
         P[S] = tot;
@@ -460,10 +470,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
                 else h2 = mid - 1;
             }
             const int n = nch[l2];
-            const long long ws = segment_weight(Ls[l2], R);
+            const long long ws = segment_weight(Ls[l2], R, cw);
             const long long o = T - PW[l2];
             const long long h = o / ws, rem = o - h * ws;
-            const long long k = (rem + kStageTokens + kWChunk - 1) / (kStageTokens + kWChunk);   // ceil
+            const long long k = (rem + kStageTokens + cw.chunk - 1) / (kStageTokens + cw.chunk);   // ceil
             b = (long long)Hkv * P[l2] + h * n + (k < n ? k : n);
         }
         bnd[g] = (int32_t)b;
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const PlanArg
         const int n = nch[l2];
         const long long o = x - (long long)Hkv * P[l2];
         const long long h = o / n, k = o - h * n;
-        return PW[l2] + h * segment_weight(Ls[l2], R) + k * (kStageTokens + kWChunk);
+        return PW[l2] + h * segment_weight(Ls[l2], R, cw) + k * (kStageTokens + cw.chunk);
     };
     if (blockIdx.x == 0) {
         for (int s = tid; s < S; s += kPlanThreads) lens[s] = Ls[s];
