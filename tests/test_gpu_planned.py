@@ -110,6 +110,18 @@ def test_planned_many_short_segments(oracle):
     _check(oracle, wl, rounds=2)
 
 
+@pytest.mark.parametrize("num_ctas", [0, 37])
+def test_planned_many_short_segments_one_row_per_head(oracle, num_ctas):
+    """128 sequences x 8 kv heads with one query row each (the plan's weights fitted for that
+    case), contexts of 1..300 tokens: many segment ends per group, segments cut between CTAs."""
+    gen = torch.Generator().manual_seed(91)
+    lens = torch.randint(1, 300, (128,), generator=gen).tolist()
+    lens[7] = 0
+    wl = workloads.make_workload("plan_short_g1", context_lens=lens, num_q_heads=8, num_kv_heads=8, block_size=32,
+                                 seed=92, max_context=320)
+    _check(oracle, wl, num_ctas=num_ctas, rounds=2)
+
+
 def test_planned_layer_chain_with_early_reads(oracle):
     """Layer l + 1's query is layer l's output and every launch after the first asks for early
     reads: the plan and cached rows may be read while the previous layer runs, q only after it.
